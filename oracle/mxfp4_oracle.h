@@ -1,0 +1,98 @@
+/*
+ * mxfp4_oracle.h -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow CPU restatement of the MXFP4 training hot path: 32-point block
+ * Walsh-Hadamard rotation, E8M0 block scale, E2M1 rounding (nearest-even or
+ * stochastic), nibble packing, dequantization. It exists so that tests, the
+ * package smoke check and the benchmark's CPU-baseline leg can check and time
+ * the CUDA library against an independent definition. Nothing in the product
+ * path may call it, and it shares no code with the CUDA sources.
+ *
+ * Every floating-point step that the method fixes in IEEE fp32 is done here in
+ * fp32 C arithmetic compiled with -ffp-contract=off (no fused multiply-add,
+ * no fast-math); decisions that are definitions (nearest grid point, scale
+ * exponent) are made by direct search or exact fp64 arithmetic.
+ */
+#ifndef MXFP4_ORACLE_H
+#define MXFP4_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_BLOCK_1X32 = 0, ORC_BLOCK_32X32 = 1 };
+enum { ORC_SCALE_FLOOR = 0, ORC_SCALE_ROUNDUP = 1 };
+enum { ORC_ROUND_RTN = 0, ORC_ROUND_SR = 1 };
+enum { ORC_LAYOUT_ROWMAJOR = 0, ORC_LAYOUT_MMA = 1 };
+enum { ORC_DTYPE_BF16 = 0, ORC_DTYPE_F32 = 1 };
+
+typedef struct {
+  int block;              /* ORC_BLOCK_* */
+  int scale_mode;         /* ORC_SCALE_* */
+  int rounding;           /* ORC_ROUND_* */
+  int scale_layout;       /* ORC_LAYOUT_* (quantize_* write row-major only) */
+  int wht;                /* 1: rotate each 32-block along K before scaling */
+  uint32_t wht_sign_mask; /* bit i set => sign -1 on element i of a block */
+  uint64_t seed;          /* Philox key */
+  uint32_t sr_stream;     /* Philox counter word 2 */
+} orc_params;
+
+/* E2M1 code (4 bits, bit 3 = sign) -> value. */
+float orc_e2m1_value(int code);
+
+/* Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, SC'11). */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+
+/* 16 random bits for source element index i (row-major index of the input). */
+uint32_t orc_sr_bits(uint64_t seed, uint32_t stream, uint64_t i);
+
+/* One 32-point block rotation: forward c*H*diag(s)*x, inverse diag(s)*c*H*y. */
+void orc_wht32(const float in[32], uint32_t sign_mask, int inverse, float out[32]);
+
+/* Shared scale exponent e (scale 2^e) for block max-abs M >= 0. */
+int orc_scale_exponent(float M, int scale_mode);
+
+/* E2M1 codes for an already-scaled value v. */
+int orc_round_rtn(float v);
+int orc_round_sr(float v, uint32_t r16);
+
+/* Row-wise quantization of rows [r0, r1) of x [rows, cols] (leading dim ld,
+ * elements), along cols. q: [(r1-r0), cols/2] bytes, s: [(r1-r0), cols/32]
+ * bytes, both row-major. Returns 0 on success, nonzero on bad arguments. */
+int orc_quantize_rows(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                      const orc_params* p, int64_t r0, int64_t r1, uint8_t* q, uint8_t* s);
+
+/* Column-wise quantization (the quantization of x^T along the rows of x) for
+ * columns [c0, c1) of x. q: [(c1-c0), rows/2], s: [(c1-c0), rows/32]. Random
+ * bits are keyed by the element's index in x as passed. */
+int orc_quantize_cols(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                      const orc_params* p, int64_t c0, int64_t c1, uint8_t* q, uint8_t* s);
+
+/* Byte offset of scale (r, kb) in the tensor-core scale layout for a scale
+ * matrix of `rows` rows and `nkb` scale columns. */
+int64_t orc_mma_scale_offset(int64_t r, int64_t kb, int64_t rows, int64_t nkb);
+
+/* Row-major [rows, nkb] -> tensor-core layout (rows % 128 == 0, nkb % 4 == 0). */
+int orc_scales_to_mma(const uint8_t* s, int64_t rows, int64_t nkb, uint8_t* out);
+
+/* Dequantize q [rows, cols/2] with scales s (layout as given) to fp32 / fp64. */
+int orc_dequantize_f32(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
+                       int64_t cols, float* out);
+int orc_dequantize_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
+                       int64_t cols, double* out);
+
+/* Stand-alone rotation along cols of x; y [rows, cols] fp32 row-major. */
+int orc_hadamard32(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                   uint32_t sign_mask, int inverse, float* y);
+
+/* Brute-force fp64 product C[m,n] = sum_k A[m,k]*B[n,k] of dequantized
+ * operands for the listed (m, n) pairs; also returns sum_k |A[m,k]*B[n,k]|. */
+int orc_gemm_pairs(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb, const uint8_t* sb,
+                   int layout, int64_t M, int64_t N, int64_t K, int64_t npairs,
+                   const int64_t* ms, const int64_t* ns, double* c, double* abs_sum);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

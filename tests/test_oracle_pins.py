@@ -1,0 +1,421 @@
+"""Pins for the CPU oracle: checks against what the pages and mathematics fix.
+
+Each test compares the oracle with something other than itself: printed or
+published values (golden files), closed forms, exact rational arithmetic,
+brute force on tiny inputs, and invariants the pages state. A plausible slip in
+the oracle (a dropped butterfly stage, a flipped sign, a transposed index, a
+wrong tie rule or scale exponent) fails at least one of them.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+GRID = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3),
+        Fraction(4), Fraction(6)]
+C_BITS = 0x3E3504F3
+
+
+def _f32_from_bits(u: int) -> float:
+    return float(np.array([u], dtype=np.uint32).view(np.float32)[0])
+
+
+def _read_rows(name):
+    rows = []
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# --------------------------------------------------------------- formats ---
+
+def test_e2m1_codes_match_golden():
+    """E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6} with sign bit 3 (golden file)."""
+    rows = _read_rows("e2m1_codes.txt")
+    assert len(rows) == 16
+    for code, val in rows:
+        got = oracle.e2m1_value(int(code))
+        assert got == float(val) and math.copysign(1, got) == math.copysign(1, float(val))
+
+
+def test_philox_known_answers():
+    """Philox4x32-10 against the published known-answer vectors."""
+    for r in _read_rows("philox4x32_10_kat.txt"):
+        w = [int(v, 16) for v in r]
+        assert oracle.philox4x32_10(w[0:4], w[4:6]) == w[6:10]
+
+
+def test_sr_bits_mapping_slices_philox_output():
+    """Element i draws 16 bits from Philox(counter=(i>>3, stream), key=seed)."""
+    seed, stream = 0x0123456789ABCDEF, 7
+    for i in [0, 1, 2, 7, 8, 9, 15, 16, 1023, (1 << 35) + 13]:
+        g = i >> 3
+        out = oracle.philox4x32_10([g & 0xFFFFFFFF, g >> 32, stream, 0],
+                                   [seed & 0xFFFFFFFF, seed >> 32])
+        w = out[(i >> 1) & 3]
+        want = (w >> 16) if (i & 1) else (w & 0xFFFF)
+        assert oracle.sr_bits(seed, stream, i) == want
+
+
+def test_mma_scale_offsets_golden():
+    for r, kb, off in _read_rows("mma_scale_offsets.txt"):
+        assert oracle.mma_scale_offset(int(r), int(kb), 256, 8) == int(off)
+
+
+def test_mma_scale_layout_is_a_permutation():
+    rows, nkb = 384, 12
+    s = np.arange(rows * nkb, dtype=np.int64)
+    offs = np.array([[oracle.mma_scale_offset(r, k, rows, nkb) for k in range(nkb)]
+                     for r in range(rows)])
+    assert sorted(offs.reshape(-1).tolist()) == list(range(rows * nkb))
+    sb = (s % 251).astype(np.uint8).reshape(rows, nkb)
+    out = oracle.scales_to_mma(sb)
+    assert np.array_equal(out[offs.reshape(-1)], sb.reshape(-1))
+
+
+# ------------------------------------------------------------------- WHT ---
+
+def _sylvester(n=32):
+    return np.array([[(-1) ** bin(i & j).count("1") for j in range(n)] for i in range(n)])
+
+
+def test_wht_unit_vectors_give_closed_form_hadamard():
+    """Butterflies on e_j give column j of c*H*diag(s), H[i][j] = (-1)^popcount(i&j)."""
+    c = _f32_from_bits(C_BITS)
+    H = _sylvester()
+    for mask in [0, 0x80000001, 0xDEADBEEF]:
+        s = np.array([-1 if (mask >> i) & 1 else 1 for i in range(32)])
+        for j in range(32):
+            e = np.zeros(32, dtype=np.float32)
+            e[j] = 1.0
+            col = oracle.wht32(e, mask)
+            assert np.array_equal(col, (c * H[:, j] * s[j]).astype(np.float32)), (mask, j)
+
+
+def test_wht_hht_is_32_identity():
+    c = _f32_from_bits(C_BITS)
+    cols = []
+    for j in range(32):
+        e = np.zeros(32, dtype=np.float32)
+        e[j] = 1.0
+        cols.append(oracle.wht32(e, 0) / np.float32(c))
+    Hm = np.stack(cols, axis=1).astype(np.int64)
+    assert np.array_equal(Hm @ Hm.T, 32 * np.eye(32, dtype=np.int64))
+    assert abs(float(c) - 1 / math.sqrt(32)) < 2 ** -27
+
+
+def test_wht_random_vectors_match_fp64_product():
+    rng = np.random.default_rng(5)
+    H = _sylvester().astype(np.float64)
+    for t in range(200):
+        x = rng.standard_t(3, size=32).astype(np.float32)
+        mask = int(rng.integers(0, 2 ** 32))
+        s = np.array([-1.0 if (mask >> i) & 1 else 1.0 for i in range(32)])
+        want = (H @ (s * x.astype(np.float64))) / math.sqrt(32)
+        got = oracle.wht32(x, mask).astype(np.float64)
+        # 5 rounded adds + 1 rounded multiply per output: |err| <= 6 u sum|x| / sqrt(32)
+        bound = 6 * 2 ** -24 * np.abs(x).astype(np.float64).sum() / math.sqrt(32) + 1e-30
+        assert np.all(np.abs(got - want) <= bound), t
+        back = oracle.wht32(got.astype(np.float32), mask, inverse=True)
+        assert np.allclose(back, x, rtol=1e-5, atol=1e-6 * np.abs(x).max())
+        assert abs(np.linalg.norm(got) - np.linalg.norm(x)) <= 1e-5 * np.linalg.norm(x)
+
+
+# ----------------------------------------------------------- scale exponent ---
+
+def _all_positive_bf16_f32():
+    u = np.arange(1, 0x7F80, dtype=np.uint32) << 16    # +min subnormal .. max finite
+    return u.view(np.float32)
+
+
+def test_scale_exponent_floor_and_roundup_definitions():
+    """Floor: 4*2^e <= M < 8*2^e. Round-up: smallest e with 6*2^e >= M (nothing clips)."""
+    rng = np.random.default_rng(11)
+    Ms = list(_all_positive_bf16_f32()[::7]) + list(
+        (rng.uniform(0.5, 1.0, 4000) * 2.0 ** rng.integers(-140, 127, 4000)).astype(np.float32))
+    Ms += [np.float32(6.0), np.float32(6.0 * 2 ** 10), np.float32(3.0000002), np.float32(1.5)]
+    for M in Ms:
+        M = float(np.float32(M))
+        fM = Fraction(M)
+        ef = oracle.scale_exponent(M, oracle.SCALE_FLOOR)
+        er = oracle.scale_exponent(M, oracle.SCALE_ROUNDUP)
+        if -127 < ef < 127:
+            assert 4 * Fraction(2) ** ef <= fM < 8 * Fraction(2) ** ef, M
+        else:
+            assert ef == -127 and fM < 4 * Fraction(2) ** -126
+        if -127 < er < 127:
+            assert 6 * Fraction(2) ** er >= fM > 6 * Fraction(2) ** (er - 1), M
+            assert 3 < fM / Fraction(2) ** er <= 6
+        else:
+            assert er == -127 and 6 * Fraction(2) ** -127 >= fM
+    assert oracle.scale_exponent(0.0, oracle.SCALE_FLOOR) == -127
+    assert oracle.scale_exponent(0.0, oracle.SCALE_ROUNDUP) == -127
+
+
+# -------------------------------------------------------------- rounding ---
+
+def _nearest_even(v: float) -> int:
+    """Nearest E2M1 magnitude code by exact rational search; ties -> even code."""
+    a = min(abs(Fraction(v)), Fraction(6))
+    d = [abs(a - g) for g in GRID]
+    best = min(d)
+    cands = [k for k in range(8) if d[k] == best]
+    k = cands[0] if len(cands) == 1 else [c for c in cands if c % 2 == 0][0]
+    return (8 if math.copysign(1.0, v) < 0 else 0) | k
+
+
+def test_rtn_exhaustive_bf16_and_midpoints():
+    u = np.arange(0, 1 << 16, dtype=np.uint32)
+    finite = ((u >> 7) & 0xFF) != 0xFF
+    vals = (u[finite] << 16).view(np.float32)
+    for v in vals:
+        assert oracle.round_rtn(float(v)) == _nearest_even(float(v)), v
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    for m in mids:
+        for v in [m, float(np.nextafter(np.float32(m), np.float32(0))),
+                  float(np.nextafter(np.float32(m), np.float32(10)))]:
+            for sgn in (1, -1):
+                assert oracle.round_rtn(sgn * v) == _nearest_even(sgn * v)
+    # ties to the even code, spelled out
+    assert [oracle.round_rtn(m) for m in mids] == [0, 2, 2, 4, 4, 6, 6]
+    assert oracle.round_rtn(-0.0) == 8 and oracle.round_rtn(-0.1) == 8
+    assert oracle.round_rtn(7.9) == 7 and oracle.round_rtn(-100.0) == 15
+
+
+def test_sr_exact_probability_over_all_draws():
+    """P(up) = ceil(p * 2^16) / 2^16 exactly, outputs only lo/hi, grid never moves."""
+    for v in [0.0, 0.5, 0.1, 0.3, 0.74, 1.2, 1.6, 2.2, 2.9, 3.3, 4.0, 4.5, 5.99, 6.0, 7.5]:
+        a = min(Fraction(v), Fraction(6))
+        lo = max(k for k in range(8) if GRID[k] <= a)
+        codes = [oracle.round_sr(v, r) for r in range(0, 1 << 16)]
+        ups = sum(1 for c in codes if c == lo + 1)
+        assert all(c in (lo, lo + 1) for c in codes)
+        if lo == 7:
+            assert ups == 0
+            continue
+        p = (a - GRID[lo]) / (GRID[lo + 1] - GRID[lo])
+        assert ups == math.ceil(p * 65536), v
+        if a in GRID:
+            assert ups == 0
+
+
+def test_sr_unbiased_over_draws():
+    """E[deq(SR(v))] = v within 4 sigma / sqrt(n) + step * 2^-16 (seeded draws)."""
+    rows, cols = 64, 1024
+    for val in [0.37, 1.1, 2.6, 4.9]:
+        x = np.full((rows, cols), np.float32(val), dtype=np.float32)
+        x[:, ::32] = np.float32(6.0)    # pin every block scale to 2^0 (round-up mode)
+        p = oracle.Params(scale_mode=oracle.SCALE_ROUNDUP, rounding=oracle.ROUND_SR,
+                          seed=12345, sr_stream=3)
+        q, s = oracle.quantize_rows(x, p)
+        assert np.all(s == 127)
+        d = oracle.dequantize(q, s, rows, cols).astype(np.float64)
+        mask = np.ones_like(d, dtype=bool)
+        mask[:, ::32] = False
+        vals = d[mask]
+        a = Fraction(float(np.float32(val)))
+        lo = max(k for k in range(8) if GRID[k] <= a)
+        step = float(GRID[lo + 1] - GRID[lo])
+        sigma = step / 2
+        assert abs(vals.mean() - float(np.float32(val))) <= 4 * sigma / math.sqrt(vals.size) + step * 2 ** -16
+
+
+# ------------------------------------------------------------- quantizer ---
+
+def _bf16(x):
+    return synth.bf16_bits(x)
+
+
+@pytest.mark.parametrize("mode", [oracle.SCALE_FLOOR, oracle.SCALE_ROUNDUP])
+def test_quantize_block_ratio_and_error(mode):
+    x = _bf16(synth.student_t(64, 256, 3.0, seed=21))
+    xf = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    q, s = oracle.quantize_rows(x, oracle.Params(scale_mode=mode))
+    d = oracle.dequantize(q, s, 64, 256).astype(np.float64)
+    for r in range(64):
+        for kb in range(8):
+            blk = xf[r, kb * 32:(kb + 1) * 32]
+            M = np.abs(blk).max()
+            S = 2.0 ** (int(s[r, kb]) - 127)
+            if mode == oracle.SCALE_FLOOR:
+                assert 4 <= M / S < 8
+            else:
+                assert 3 < M / S <= 6      # nothing clips
+            err = np.abs(d[r, kb * 32:(kb + 1) * 32] - blk)
+            half_step = np.where(np.abs(blk) / S < 2, 0.25, np.where(np.abs(blk) / S < 4, 0.5, 1.0)) * S
+            if mode == oracle.SCALE_ROUNDUP:
+                assert np.all(err <= half_step)
+            else:
+                sat = np.abs(blk) / S > 6
+                assert np.all(err[~sat] <= half_step[~sat])
+                assert np.all(np.abs(d[r, kb * 32:(kb + 1) * 32][sat]) == 6 * S)
+
+
+def test_dequantize_exhaustive_codes_and_bytes():
+    rows, cols = 16, 32
+    for sb in range(0, 256):
+        q = np.zeros((rows, cols // 2), dtype=np.uint8)
+        for code in range(16):
+            q[code, :] = code | (code << 4)
+        s = np.full((rows, 1), sb, dtype=np.uint8)
+        d = oracle.dequantize(q, s, rows, cols)
+        for code in range(16):
+            g = float(GRID[code & 7]) * (-1 if code & 8 else 1)
+            if sb == 255:
+                assert np.all(np.isnan(d[code]))
+            else:
+                with np.errstate(over="ignore"):     # 6 * 2^127 overflows fp32 to inf
+                    want = np.float32(math.ldexp(g, sb - 127))
+                assert np.all(d[code] == want)
+
+
+def test_floor_rtn_requantization_keeps_values():
+    """quantize(dequantize(q)) reproduces the dequantized values (floor, RTN)."""
+    rows, cols = 32, 256
+    q0 = synth.random_codes(rows, cols, seed=3)
+    s0 = synth.random_scales(rows, cols, seed=4).reshape(rows, cols // 32)
+    d0 = oracle.dequantize(q0, s0, rows, cols)
+    q1, s1 = oracle.quantize_rows(d0, oracle.Params())
+    d1 = oracle.dequantize(q1, s1, rows, cols)
+    assert np.array_equal(d0, d1)
+
+
+def test_32x32_blocks_are_transposition_invariant():
+    """2D blocks: block (i, j) of X and block (j, i) of X^T share values and scale."""
+    x = synth.normal(128, 96, 0.02, seed=31)
+    xb = _bf16(x)
+    for mode in [oracle.SCALE_FLOOR, oracle.SCALE_ROUNDUP]:
+        p = oracle.Params(block=oracle.BLOCK_32X32, scale_mode=mode)
+        qr, sr = oracle.quantize_rows(xb, p)
+        qc, sc = oracle.quantize_cols(xb, p)
+        qt, st = oracle.quantize_rows(np.ascontiguousarray(xb.T), p)
+        assert np.array_equal(qc, qt) and np.array_equal(sc, st)
+        dr = oracle.dequantize(qr, sr, 128, 96)
+        dc = oracle.dequantize(qc, sc, 96, 128)
+        assert np.array_equal(dr, dc.T)
+        assert np.array_equal(sr[::32, :], sc[::32, :].T)
+        # one scale per 32x32 tile
+        assert np.all(sr.reshape(4, 32, 3) == sr.reshape(4, 32, 3)[:, :1, :])
+
+
+def test_1x32_blocks_disagree_under_transposition():
+    """1D blocks: the same element gets different scales in the two orientations."""
+    x = _bf16(synth.student_t(128, 128, 4.0, seed=41))
+    p = oracle.Params()
+    qr, sr = oracle.quantize_rows(x, p)
+    qc, sc = oracle.quantize_cols(x, p)
+    srow = np.repeat(sr, 32, axis=1)            # scale of (r, c) row-wise
+    scol = np.repeat(sc, 32, axis=1).T          # scale of (r, c) column-wise
+    frac = float(np.mean(srow != scol))
+    assert frac > 0.3
+    dr = oracle.dequantize(qr, sr, 128, 128)
+    dc = oracle.dequantize(qc, sc, 128, 128).T
+    assert np.mean(dr != dc) > 0.05
+
+
+def test_fused_rotation_equals_rotation_then_quantize():
+    x = _bf16(synth.normal_outlier_cols(64, 128, 1.0, 4, 50.0, seed=51))
+    mask = synth.sign_mask(51)
+    y = oracle.hadamard32(x, mask)
+    for rnd in [oracle.ROUND_RTN, oracle.ROUND_SR]:
+        p_f = oracle.Params(rounding=rnd, wht=True, wht_sign_mask=mask, seed=9)
+        p_n = oracle.Params(rounding=rnd, wht=False, seed=9)
+        assert all(np.array_equal(a, b) for a, b in zip(oracle.quantize_rows(x, p_f),
+                                                        oracle.quantize_rows(y, p_n)))
+
+
+def test_rotation_spreads_outlier_channel():
+    """A single large channel inside a block no longer dominates after rotation."""
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, 5] = 50.0
+    x[0, :5] = 0.1
+    y = oracle.hadamard32(x, 0)
+    assert np.abs(y).max() < 50.0 / math.sqrt(32) * 1.1
+
+
+def test_row_subrange_matches_full_tensor():
+    x = _bf16(synth.laplace(96, 64, 1e-3, seed=61))
+    for p in [oracle.Params(rounding=oracle.ROUND_SR, seed=3, sr_stream=1),
+              oracle.Params(block=oracle.BLOCK_32X32, scale_mode=oracle.SCALE_ROUNDUP,
+                            rounding=oracle.ROUND_SR, seed=4, wht=True, wht_sign_mask=77)]:
+        qf, sf = oracle.quantize_rows(x, p)
+        q, s = oracle.quantize_rows(x, p, 32, 64)
+        assert np.array_equal(q, qf[32:64]) and np.array_equal(s, sf[32:64])
+        qf, sf = oracle.quantize_cols(x, p)
+        q, s = oracle.quantize_cols(x, p, 32, 64)
+        assert np.array_equal(q, qf[32:64]) and np.array_equal(s, sf[32:64])
+
+
+def test_quantize_rejects_non_finite():
+    x = np.ones((1, 32), dtype=np.float32)
+    x[0, 3] = np.inf
+    with pytest.raises(ValueError):
+        oracle.quantize_rows(x, oracle.Params())
+
+
+# ------------------------------------------------------------------ GEMM ---
+
+def test_gemm_pairs_exact_rational():
+    """Brute force on tiny inputs against exact rational arithmetic."""
+    M = N = 128
+    K = 128
+    qa = synth.random_codes(M, K, 71)
+    qb = synth.random_codes(N, K, 72)
+    sa = synth.random_scales(M, K, 73)
+    sb = synth.random_scales(N, K, 74)
+
+    def val(q, s, r, k):
+        b = int(q[r, k // 2])
+        code = (b >> 4) if k & 1 else (b & 15)
+        sc = int(s[oracle.mma_scale_offset(r, k // 32, 128, K // 32)])
+        g = GRID[code & 7] * (-1 if code & 8 else 1)
+        return g * Fraction(2) ** (sc - 127)
+
+    ms = [0, 1, 37, 127, 64]
+    ns = [0, 100, 5, 127, 64]
+    c, a = oracle.gemm_pairs(qa, sa, qb, sb, M, N, K, ms, ns)
+    for t, (m, n) in enumerate(zip(ms, ns)):
+        exact = sum(val(qa, sa, m, k) * val(qb, sb, n, k) for k in range(K))
+        exact_abs = sum(abs(val(qa, sa, m, k) * val(qb, sb, n, k)) for k in range(K))
+        assert Fraction(c[t]) == exact and Fraction(a[t]) == exact_abs
+
+
+def test_gemm_closed_forms():
+    M, N, K = 128, 128, 256
+    ones = np.full((M, K // 2), 0x22, dtype=np.uint8)           # every element 1.0
+    s127 = np.full(M * K // 32, 127, dtype=np.uint8)
+    C, A = oracle.gemm_ref(ones, s127, ones, s127, M, N, K)
+    assert np.all(C == K) and np.all(A == K)
+    # one nonzero code per row of A: C row m = that code * column k(m) of B
+    qa = np.zeros((M, K // 2), dtype=np.uint8)
+    ks = np.arange(M) * 2 % K
+    for m in range(M):
+        qa[m, ks[m] // 2] = 0x06                              # 4.0 at even k
+    qb = synth.random_codes(N, K, 81)
+    sb = synth.random_scales(N, K, 82)
+    C, _ = oracle.gemm_ref(qa, s127, qb, sb, M, N, K)
+    B = oracle.dequantize(qb, sb, N, K, oracle.LAYOUT_MMA, f64=True)
+    assert np.array_equal(C, 4.0 * B[:, ks].T)
+
+
+def test_gemm_ref_agrees_with_pairs():
+    M, N, K = 256, 128, 512
+    qa, qb = synth.random_codes(M, K, 91), synth.random_codes(N, K, 92)
+    sa, sb = synth.random_scales(M, K, 93), synth.random_scales(N, K, 94)
+    C, A = oracle.gemm_ref(qa, sa, qb, sb, M, N, K)
+    ms = np.arange(0, M, 17)
+    ns = (ms * 7) % N
+    c, a = oracle.gemm_pairs(qa, sa, qb, sb, M, N, K, ms, ns)
+    assert np.allclose(C[ms, ns], c, rtol=0, atol=1e-12 * a.max())
+    assert np.allclose(A[ms, ns], a, rtol=1e-14)
