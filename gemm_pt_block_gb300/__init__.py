@@ -1,0 +1,37 @@
+"""GB300-native MXFP4 training hot path.
+
+A thin Python binding over the C ABI of ``libmxfp4.so`` (declared in
+``include/mxfp4.h``). PyTorch supplies device memory and streams; every step
+of the computation runs in the library's sm_103a kernels. There is no CPU or
+PyTorch fallback: if the library is missing or fails to load, every call
+raises.
+
+Calls (same names as the C ABI):
+  mxfp4_quantize    fused rotation + E8M0 scale + E2M1 rounding + packing,
+                    row-wise and/or column-wise in one pass
+  mxfp4_dequantize  codes * 2^(scale - 127) -> fp32
+  mxfp4_gemm        block-scaled MXFP4 GEMM on tcgen05 tensor cores
+  hadamard32        stand-alone 32-point block rotation
+"""
+from .binding import (  # noqa: F401
+    BLOCK_1X32,
+    BLOCK_32X32,
+    DTYPE_BF16,
+    DTYPE_F32,
+    LAYOUT_MMA,
+    LAYOUT_ROWMAJOR,
+    ROUND_RTN,
+    ROUND_SR,
+    SCALE_FLOOR,
+    SCALE_ROUNDUP,
+    Mxfp4Error,
+    QuantParams,
+    device_status,
+    hadamard32,
+    lib,
+    lib_path,
+    mxfp4_dequantize,
+    mxfp4_gemm,
+    mxfp4_quantize,
+    scale_numel,
+)

@@ -1,0 +1,212 @@
+"""ctypes marshalling for libmxfp4.so: torch tensors in, pointers and sizes out.
+
+Nothing here computes: each function checks that tensors live on a CUDA
+device with the expected dtype and contiguity, allocates outputs the caller did
+not pass, and forwards raw pointers plus the current CUDA stream to the C ABI.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libmxfp4.so"
+
+BLOCK_1X32, BLOCK_32X32 = 0, 1
+SCALE_FLOOR, SCALE_ROUNDUP = 0, 1
+ROUND_RTN, ROUND_SR = 0, 1
+LAYOUT_ROWMAJOR, LAYOUT_MMA = 0, 1
+DTYPE_BF16, DTYPE_F32 = 0, 1
+
+_STATUS = {
+    0: "MXFP4_OK", 1: "MXFP4_ERR_INVALID_ARG", 2: "MXFP4_ERR_SHAPE", 3: "MXFP4_ERR_ALIGN",
+    4: "MXFP4_ERR_UNSUPPORTED", 5: "MXFP4_ERR_CUDA", 6: "MXFP4_ERR_TIMEOUT",
+}
+
+
+class Mxfp4Error(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {detail}")
+        self.status = status
+
+
+class _CParams(ctypes.Structure):
+    _fields_ = [
+        ("block", ctypes.c_int32),
+        ("scale_mode", ctypes.c_int32),
+        ("rounding", ctypes.c_int32),
+        ("scale_layout", ctypes.c_int32),
+        ("wht", ctypes.c_int32),
+        ("wht_sign_mask", ctypes.c_uint32),
+        ("seed", ctypes.c_uint64),
+        ("sr_stream", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
+    ]
+
+
+@dataclass(frozen=True)
+class QuantParams:
+    """Parameters of one quantizer output orientation (see mxfp4_quant_params)."""
+    block: int = BLOCK_1X32
+    scale_mode: int = SCALE_FLOOR
+    rounding: int = ROUND_RTN
+    scale_layout: int = LAYOUT_ROWMAJOR
+    wht: bool = False
+    wht_sign_mask: int = 0
+    seed: int = 0
+    sr_stream: int = 0
+
+    def _c(self) -> _CParams:
+        return _CParams(self.block, self.scale_mode, self.rounding, self.scale_layout,
+                        int(bool(self.wht)), self.wht_sign_mask & 0xFFFFFFFF,
+                        self.seed & 0xFFFFFFFFFFFFFFFF, self.sr_stream & 0xFFFFFFFF, 0)
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return os.path.join(HERE, _LIB_NAME)
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libmxfp4.so (built by gemm_pt_block_gb300.build). Raises if absent."""
+    global _lib
+    if _lib is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is not built; run gemm_pt_block_gb300.build.build() "
+                               "(there is no fallback implementation)")
+        L = ctypes.CDLL(path)
+        P, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        L.mxfp4_quantize.restype = i32
+        L.mxfp4_quantize.argtypes = [P, i32, i64, i64, i64, ctypes.POINTER(_CParams), P, P,
+                                     ctypes.POINTER(_CParams), P, P, P]
+        L.mxfp4_dequantize.restype = i32
+        L.mxfp4_dequantize.argtypes = [P, P, i32, i64, i64, P, P]
+        L.mxfp4_gemm.restype = i32
+        L.mxfp4_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
+        L.hadamard32.restype = i32
+        L.hadamard32.argtypes = [P, i32, i64, i64, i64, ctypes.c_uint32, i32, P, P]
+        L.mxfp4_status_string.restype = ctypes.c_char_p
+        L.mxfp4_status_string.argtypes = [i32]
+        L.mxfp4_last_error.restype = ctypes.c_char_p
+        L.mxfp4_last_error.argtypes = []
+        L.mxfp4_device_status.restype = i32
+        L.mxfp4_device_status.argtypes = [P]
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise Mxfp4Error(status, lib().mxfp4_last_error().decode())
+
+
+def _stream(t: torch.Tensor, stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream(t.device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _cuda2d(x: torch.Tensor, name: str) -> None:
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dim() != 2 or (x.shape[1] > 1 and x.stride(1) != 1):
+        raise ValueError(f"{name} must be 2-D with unit column stride")
+
+
+def scale_numel(rows: int, k: int) -> int:
+    return rows * (k // 32)
+
+
+def _scales_out(rows: int, k: int, p: QuantParams, dev) -> torch.Tensor:
+    if p.scale_layout == LAYOUT_MMA:
+        return torch.empty(scale_numel(rows, k), dtype=torch.uint8, device=dev)
+    return torch.empty((rows, k // 32), dtype=torch.uint8, device=dev)
+
+
+def mxfp4_quantize(x: torch.Tensor, row: QuantParams | None = None, col: QuantParams | None = None,
+                   *, q_row=None, s_row=None, q_col=None, s_col=None, stream=None):
+    """Quantize x [rows, cols] (bf16 or fp32) row-wise and/or column-wise.
+
+    Returns (q_row, s_row, q_col, s_col); entries for an orientation not asked
+    for are None. Codes are [rows, cols/2] (row-wise) / [cols, rows/2]
+    (column-wise) uint8; scales are [out_rows, K/32] (row-major layout) or flat
+    (tensor-core layout).
+    """
+    _cuda2d(x, "x")
+    if x.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif x.dtype == torch.float32:
+        dt = DTYPE_F32
+    else:
+        raise TypeError("x must be bfloat16 or float32")
+    rows, cols = x.shape
+    ld = x.stride(0) if rows > 1 else cols
+    dev = x.device
+    if row is not None:
+        q_row = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev) if q_row is None else q_row
+        s_row = _scales_out(rows, cols, row, dev) if s_row is None else s_row
+    if col is not None:
+        q_col = torch.empty((cols, rows // 2), dtype=torch.uint8, device=dev) if q_col is None else q_col
+        s_col = _scales_out(cols, rows, col, dev) if s_col is None else s_col
+    rp = row._c() if row is not None else None
+    cp = col._c() if col is not None else None
+    _check(lib().mxfp4_quantize(
+        _ptr(x), dt, rows, cols, ld,
+        ctypes.byref(rp) if rp is not None else None, _ptr(q_row if row else None),
+        _ptr(s_row if row else None),
+        ctypes.byref(cp) if cp is not None else None, _ptr(q_col if col else None),
+        _ptr(s_col if col else None), _stream(x, stream)))
+    return (q_row if row else None, s_row if row else None,
+            q_col if col else None, s_col if col else None)
+
+
+def mxfp4_dequantize(q: torch.Tensor, s: torch.Tensor, rows: int, cols: int,
+                     scale_layout: int = LAYOUT_ROWMAJOR, *, out=None, stream=None):
+    if not q.is_cuda or not s.is_cuda:
+        raise ValueError("q and s must be CUDA tensors")
+    out = torch.empty((rows, cols), dtype=torch.float32, device=q.device) if out is None else out
+    _check(lib().mxfp4_dequantize(_ptr(q), _ptr(s), scale_layout, rows, cols, _ptr(out),
+                                  _stream(q, stream)))
+    return out
+
+
+def mxfp4_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
+               M: int, N: int, K: int, *, c=None, ldc: int | None = None, stream=None):
+    """C[M, N] fp32 = deq(A) deq(B)^T; A, B K-major packed codes, scales in tensor-core layout."""
+    for t, n in ((qa, "qa"), (sa, "sa"), (qb, "qb"), (sb, "sb")):
+        if not t.is_cuda or t.dtype != torch.uint8:
+            raise ValueError(f"{n} must be a CUDA uint8 tensor")
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=qa.device)
+    ldc = c.stride(0) if ldc is None else ldc
+    _check(lib().mxfp4_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), ldc,
+                            _stream(qa, stream)))
+    return c
+
+
+def hadamard32(x: torch.Tensor, sign_mask: int = 0, inverse: bool = False, *, y=None, stream=None):
+    _cuda2d(x, "x")
+    dt = DTYPE_BF16 if x.dtype == torch.bfloat16 else DTYPE_F32
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("x must be bfloat16 or float32")
+    rows, cols = x.shape
+    ld = x.stride(0) if rows > 1 else cols
+    y = torch.empty((rows, cols), dtype=torch.float32, device=x.device) if y is None else y
+    _check(lib().hadamard32(_ptr(x), dt, rows, cols, ld, sign_mask & 0xFFFFFFFF, int(bool(inverse)),
+                            _ptr(y), _stream(x, stream)))
+    return y
+
+
+def device_status(stream=None) -> int:
+    """Synchronizes the stream and returns (and clears) the GEMM's device error word."""
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(lib().mxfp4_device_status(ctypes.c_void_p(s.cuda_stream)))

@@ -1,0 +1,169 @@
+// api.cu -- the extern "C" entry points declared in include/mxfp4.h:
+// argument validation, status codes and the thread-local error detail; the
+// work itself is enqueued by the launchers in quant.cu and gemm.cu.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+
+#include "../../include/mxfp4.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+mxfp4_status fail(mxfp4_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mxfp4_status from_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return MXFP4_OK;
+  return fail(MXFP4_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Validates one orientation's parameters and fills the launcher's view.
+mxfp4_status check_params(const mxfp4_quant_params* p, uint8_t* q, uint8_t* s, int64_t out_rows,
+                          int64_t k, const char* name, mx::OrientArgs* o) {
+  if (!q || !s) return fail(MXFP4_ERR_INVALID_ARG, "%s: output pointers must be non-NULL", name);
+  if (!aligned16(q)) return fail(MXFP4_ERR_ALIGN, "%s: codes pointer not 16-byte aligned", name);
+  if (p->block != MXFP4_BLOCK_1X32 && p->block != MXFP4_BLOCK_32X32)
+    return fail(MXFP4_ERR_INVALID_ARG, "%s: bad block %d", name, p->block);
+  if (p->scale_mode != MXFP4_SCALE_FLOOR && p->scale_mode != MXFP4_SCALE_ROUNDUP)
+    return fail(MXFP4_ERR_INVALID_ARG, "%s: bad scale_mode %d", name, p->scale_mode);
+  if (p->rounding != MXFP4_ROUND_RTN && p->rounding != MXFP4_ROUND_SR)
+    return fail(MXFP4_ERR_INVALID_ARG, "%s: bad rounding %d", name, p->rounding);
+  if (p->scale_layout != MXFP4_LAYOUT_ROWMAJOR && p->scale_layout != MXFP4_LAYOUT_MMA)
+    return fail(MXFP4_ERR_INVALID_ARG, "%s: bad scale_layout %d", name, p->scale_layout);
+  if (p->wht != 0 && p->wht != 1) return fail(MXFP4_ERR_INVALID_ARG, "%s: wht must be 0/1", name);
+  if (p->reserved != 0) return fail(MXFP4_ERR_INVALID_ARG, "%s: reserved field must be 0", name);
+  if (p->scale_layout == MXFP4_LAYOUT_MMA && (out_rows % 128 != 0 || k % 128 != 0))
+    return fail(MXFP4_ERR_SHAPE,
+                "%s: tensor-core scale layout needs rows %% 128 == 0 and K %% 128 == 0 (got %lld x %lld)",
+                name, (long long)out_rows, (long long)k);
+  o->block = p->block;
+  o->roundup = p->scale_mode == MXFP4_SCALE_ROUNDUP;
+  o->sr = p->rounding == MXFP4_ROUND_SR;
+  o->mma_layout = p->scale_layout == MXFP4_LAYOUT_MMA;
+  o->wht = p->wht;
+  o->sign_mask = p->wht_sign_mask;
+  o->seed = p->seed;
+  o->stream = p->sr_stream;
+  o->q = q;
+  o->s = s;
+  return MXFP4_OK;
+}
+
+mxfp4_status check_input(const void* x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld) {
+  if (!x && rows * cols > 0) return fail(MXFP4_ERR_INVALID_ARG, "x is NULL");
+  if (dtype != MXFP4_DTYPE_BF16 && dtype != MXFP4_DTYPE_F32)
+    return fail(MXFP4_ERR_INVALID_ARG, "bad x_dtype %d", dtype);
+  if (rows < 0 || cols < 0) return fail(MXFP4_ERR_SHAPE, "negative dimension");
+  if (cols % 32 != 0) return fail(MXFP4_ERR_SHAPE, "cols (%lld) must be a multiple of 32", (long long)cols);
+  if (ld < cols) return fail(MXFP4_ERR_SHAPE, "ld_x (%lld) < cols (%lld)", (long long)ld, (long long)cols);
+  if (!aligned16(x) || ld % 8 != 0)
+    return fail(MXFP4_ERR_ALIGN, "x must be 16-byte aligned with ld_x %% 8 == 0");
+  return MXFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mxfp4_status_string(mxfp4_status s) {
+  switch (s) {
+    case MXFP4_OK: return "MXFP4_OK";
+    case MXFP4_ERR_INVALID_ARG: return "MXFP4_ERR_INVALID_ARG";
+    case MXFP4_ERR_SHAPE: return "MXFP4_ERR_SHAPE";
+    case MXFP4_ERR_ALIGN: return "MXFP4_ERR_ALIGN";
+    case MXFP4_ERR_UNSUPPORTED: return "MXFP4_ERR_UNSUPPORTED";
+    case MXFP4_ERR_CUDA: return "MXFP4_ERR_CUDA";
+    case MXFP4_ERR_TIMEOUT: return "MXFP4_ERR_TIMEOUT";
+  }
+  return "MXFP4_ERR_UNKNOWN";
+}
+
+const char* mxfp4_last_error(void) { return g_last_error; }
+
+mxfp4_status mxfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
+                            int64_t ld_x, const mxfp4_quant_params* row, uint8_t* q_row,
+                            uint8_t* s_row, const mxfp4_quant_params* col, uint8_t* q_col,
+                            uint8_t* s_col, void* stream) {
+  if (!row && !col) return fail(MXFP4_ERR_INVALID_ARG, "at least one of row / col params is required");
+  mxfp4_status st = check_input(x, x_dtype, rows, cols, ld_x);
+  if (st) return st;
+  const bool need_rows32 = col || (row && row->block == MXFP4_BLOCK_32X32);
+  if (need_rows32 && rows % 32 != 0)
+    return fail(MXFP4_ERR_SHAPE, "rows (%lld) must be a multiple of 32 for column-wise or 32x32 output",
+                (long long)rows);
+  mx::OrientArgs ro{}, co{};
+  if (row && (st = check_params(row, q_row, s_row, rows, cols, "row", &ro))) return st;
+  if (col && (st = check_params(col, q_col, s_col, cols, rows, "col", &co))) return st;
+  return from_cuda(mx::launch_quantize(x, x_dtype == MXFP4_DTYPE_F32, rows, cols, ld_x,
+                                       row ? &ro : nullptr, col ? &co : nullptr,
+                                       static_cast<cudaStream_t>(stream)),
+                   "mxfp4_quantize launch");
+}
+
+mxfp4_status mxfp4_dequantize(const uint8_t* q, const uint8_t* s, int32_t scale_layout,
+                              int64_t rows, int64_t cols, float* out, void* stream) {
+  if ((!q || !s || !out) && rows * cols > 0) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
+  if (scale_layout != MXFP4_LAYOUT_ROWMAJOR && scale_layout != MXFP4_LAYOUT_MMA)
+    return fail(MXFP4_ERR_INVALID_ARG, "bad scale_layout %d", scale_layout);
+  if (rows < 0 || cols < 0 || cols % 32 != 0)
+    return fail(MXFP4_ERR_SHAPE, "cols (%lld) must be a non-negative multiple of 32", (long long)cols);
+  if (scale_layout == MXFP4_LAYOUT_MMA && (rows % 128 != 0 || cols % 128 != 0))
+    return fail(MXFP4_ERR_SHAPE, "tensor-core scale layout needs rows and cols %% 128 == 0");
+  if (!aligned16(q) || !aligned16(out)) return fail(MXFP4_ERR_ALIGN, "q / out must be 16-byte aligned");
+  return from_cuda(mx::launch_dequantize(q, s, scale_layout == MXFP4_LAYOUT_MMA, rows, cols, out,
+                                         static_cast<cudaStream_t>(stream)),
+                   "mxfp4_dequantize launch");
+}
+
+mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
+                        int64_t ldc, void* stream) {
+  if (!qa || !sa || !qb || !sb || !c) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0)
+    return fail(MXFP4_ERR_SHAPE, "mxfp4_gemm needs M %% 128 == 0, N %% 256 == 0, K %% 256 == 0 (got %lld, %lld, %lld)",
+                (long long)M, (long long)N, (long long)K);
+  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30) || (M / 128) * (N / 256) > (1ll << 30))
+    return fail(MXFP4_ERR_SHAPE, "mxfp4_gemm dimensions too large");
+  if (ldc < N) return fail(MXFP4_ERR_SHAPE, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
+  if (!aligned16(qa) || !aligned16(qb) || !aligned16(sa) || !aligned16(sb) || !aligned16(c) || ldc % 8 != 0)
+    return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");
+  const char* why = "";
+  cudaError_t e = mx::launch_gemm(qa, sa, qb, sb, M, N, K, c, ldc, static_cast<cudaStream_t>(stream), &why);
+  if (e == cudaErrorNotSupported) return fail(MXFP4_ERR_UNSUPPORTED, "%s", why);
+  if (e == cudaErrorInvalidValue && why[0]) return fail(MXFP4_ERR_ALIGN, "%s", why);
+  return from_cuda(e, "mxfp4_gemm launch");
+}
+
+mxfp4_status hadamard32(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
+                        int64_t ld_x, uint32_t sign_mask, int32_t inverse, float* y,
+                        void* stream) {
+  mxfp4_status st = check_input(x, x_dtype, rows, cols, ld_x);
+  if (st) return st;
+  if (!y && rows * cols > 0) return fail(MXFP4_ERR_INVALID_ARG, "y is NULL");
+  if (!aligned16(y)) return fail(MXFP4_ERR_ALIGN, "y must be 16-byte aligned");
+  if (inverse != 0 && inverse != 1) return fail(MXFP4_ERR_INVALID_ARG, "inverse must be 0/1");
+  return from_cuda(mx::launch_hadamard32(x, x_dtype == MXFP4_DTYPE_F32, rows, cols, ld_x, sign_mask,
+                                         inverse != 0, y, static_cast<cudaStream_t>(stream)),
+                   "hadamard32 launch");
+}
+
+mxfp4_status mxfp4_device_status(void* stream) {
+  uint32_t err = 0;
+  cudaError_t e = mx::read_device_error(static_cast<cudaStream_t>(stream), &err);
+  if (e != cudaSuccess) return from_cuda(e, "mxfp4_device_status");
+  if (err == MXFP4_ERR_TIMEOUT)
+    return fail(MXFP4_ERR_TIMEOUT, "a bounded device-side wait in the GEMM ran out");
+  return err ? fail(static_cast<mxfp4_status>(err), "device error word %u", err) : MXFP4_OK;
+}
+
+}  // extern "C"

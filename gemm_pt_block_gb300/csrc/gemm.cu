@@ -1,0 +1,371 @@
+// gemm.cu -- block-scaled MXFP4 GEMM on the 5th-generation tensor cores
+// (sm_103a: tcgen05.mma kind::mxf4 with E8M0 block scales).
+//
+//   C[m, n] = sum_k (a[m,k] * 2^(sa[m,k/32]-127)) * (b[n,k] * 2^(sb[n,k/32]-127))
+//
+// for packed E2M1 operands, both K-major, fp32 accumulation in tensor memory.
+// This is the "MXFP4 GEMM" of "Training LLMs with MXFP4" (Abstract) that all
+// three training products -- Fprop, Dgrad, Wgrad of "Pretraining large
+// language models with MXFP4" (Abstract) -- reduce to.
+//
+// Design (one CTA per SM, persistent over output tiles):
+//  * tile 128 x 256 x 256 (M x N x K), 4-stage shared-memory ring;
+//  * warp 0: TMA producer -- 128-byte-swizzled tensor loads of the A and B
+//    code tiles, plus bulk copies of the matching 512-byte scale tiles (the
+//    scales are stored in the tensor-core scale layout, so each is one
+//    contiguous copy);
+//  * warp 1: allocates tensor memory, moves each stage's scales into it with
+//    tcgen05.cp, and issues 4 tcgen05.mma (K = 64 each) per stage from one
+//    thread; tcgen05.commit releases the stage and, after the last k-block,
+//    hands the accumulator to the epilogue;
+//  * warps 2..9: epilogue -- drain the 128 x 256 fp32 accumulator from tensor
+//    memory into registers, release it so the next tile's MMAs can start, then
+//    store to global memory.
+// Every mbarrier wait is bounded (about 2 s): on expiry the CTA sets the
+// library's device error word, stops issuing work, and still frees its tensor
+// memory before exiting.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mx {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 256;
+constexpr int BKB = BK / 2;                    // bytes of packed codes per row per stage
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BKB;              // 16 KB
+constexpr int B_BYTES = BN * BKB;              // 32 KB
+constexpr int SFA_BYTES = BM * (BK / 32);      // 1 KB: two 512-byte scale tiles
+constexpr int SFB_BYTES = BN * (BK / 32);      // 2 KB: four 512-byte scale tiles
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COL = 0;                // 256 fp32 columns
+constexpr uint32_t SFA_COL = 256;              // 2 k-chunks x 4 columns
+constexpr uint32_t SFB_COL = 264;              // 2 k-chunks x 8 columns
+constexpr int CTL_BYTES = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + CTL_BYTES + 1024;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kGroupM = 8;                     // tile raster: 8 M-tiles share each N sweep
+
+static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
+
+__device__ uint32_t g_gemm_error;
+
+struct Ctl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t acc_full;
+  uint64_t acc_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+static_assert(sizeof(Ctl) <= CTL_BYTES, "control block");
+
+// Instruction descriptor, kind::mxf4 block-scaled: E2M1 A and B (format 1 at
+// bits 7-9 and 10-12), both K-major, N >> 3 at bits 17-22, E8M0 scales (bit
+// 23), M >> 4 at bits 24-28, scale-factor byte selectors for B (bits 4-5) and
+// A (bits 29-30).
+__device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
+  return (sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl* ctl) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*reinterpret_cast<volatile uint32_t*>(&ctl->abort)) return false;
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+        *reinterpret_cast<volatile uint32_t*>(&ctl->abort) = 1u;
+        atomicExch(&g_gemm_error, 6u);  // MXFP4_ERR_TIMEOUT
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait used only while shutting down after an abort.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity))
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs / 8) return;
+}
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
+  const int per_group = kGroupM * num_n;
+  const int g = tile / per_group;
+  const int first_m = g * kGroupM;
+  const int gm = min(kGroupM, num_m - first_m);
+  const int w = tile - g * per_group;
+  mb = first_m + w % gm;
+  nb = w / gm;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const uint8_t* __restrict__ sa, const uint8_t* __restrict__ sb,
+                 float* __restrict__ C, int64_t ldc, int M, int N, int K) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = M / BM, num_n = N / BN, num_k = K / BK;
+  const int num_tiles = num_m * num_n;
+  const int64_t ktiles = K / 128;  // 512-byte scale tiles per 128-row band
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&ctl->full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&ctl->empty[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&ctl->acc_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&ctl->acc_empty), NUM_EPI_WARPS);
+    ptx::mbar_init(ptx::smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&ctl->tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued = 0, issued_parity = 0;  // per-stage bit masks of the last issue
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, mb, nb);
+        for (int kb = 0; kb < num_k; ++kb) {
+          const uint32_t empty = ptx::smem_u32(&ctl->empty[stage]);
+          const uint32_t full = ptx::smem_u32(&ctl->full[stage]);
+          if (!(ok = wait_bar(empty, phase ^ 1u, ctl))) break;
+          const uint32_t st = ptx::smem_u32(smem + stage * STAGE_BYTES);
+          ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+          ptx::tma_load_2d(st, &tmA, kb * BKB, mb * BM, full);
+          ptx::tma_load_2d(st + A_BYTES, &tmB, kb * BKB, nb * BN, full);
+          ptx::bulk_load(st + A_BYTES + B_BYTES, sa + ((int64_t)mb * ktiles + 2 * kb) * 512,
+                         SFA_BYTES, full);
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            ptx::bulk_load(st + A_BYTES + B_BYTES + SFA_BYTES + t * 1024,
+                           sb + ((int64_t)(2 * nb + t) * ktiles + 2 * kb) * 512, 1024, full);
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // After an abort, wait (bounded) for the last load issued into each
+      // stage to land before the CTA's shared memory is released.
+      if (!ok) {
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1u) drain_wait(ptx::smem_u32(&ctl->full[s]), (issued_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!(ok = wait_bar(ptx::smem_u32(&ctl->acc_empty), acc_phase ^ 1u, ctl))) break;
+        ptx::tc_fence_after();
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!(ok = wait_bar(ptx::smem_u32(&ctl->full[stage]), phase, ctl))) break;
+          ptx::tc_fence_after();
+          const uint32_t st = ptx::smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sfa_s = st + A_BYTES + B_BYTES;
+          const uint32_t sfb_s = sfa_s + SFA_BYTES;
+          // Scales to tensor memory: each 512-byte tile (128 rows x 4 scale
+          // columns) fills 4 columns; row r's scales land in column r / 32.
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            ptx::tc_cp_32x128b_warpx4(tmem + SFA_COL + 4 * c,
+                                      ptx::smem_desc(sfa_s + c * 512, 0, 128, 0));
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+              ptx::tc_cp_32x128b_warpx4(tmem + SFB_COL + 8 * c + 4 * t,
+                                        ptx::smem_desc(sfb_s + t * 1024 + c * 512, 0, 128, 0));
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
+            const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
+            ptx::mma_mxf4(tmem + ACC_COL, ad, bd, make_idesc((k & 1) * 2),
+                          tmem + SFA_COL + 4 * (k >> 1), tmem + SFB_COL + 8 * (k >> 1),
+                          (kb | k) != 0);
+          }
+          ptx::tc_commit(ptx::smem_u32(&ctl->empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::tc_commit(ptx::smem_u32(&ctl->acc_full));
+        acc_phase ^= 1u;
+      }
+      // No MMA may still be reading shared or tensor memory at teardown.
+      ptx::tc_commit(ptx::smem_u32(&ctl->drain));
+      drain_wait(ptx::smem_u32(&ctl->drain), 0);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int q = warp & 3;            // tensor-memory lane quarter this warp may access
+    const int h = (warp - 2) >> 2;     // column half of the 256-wide tile
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, num_m, num_n, mb, nb);
+      // One lane waits; the verdict is broadcast so the warp stays converged
+      // for the .sync.aligned tensor-memory loads.
+      int ok = 0;
+      if (lane == 0) ok = wait_bar(ptx::smem_u32(&ctl->acc_full), acc_phase, ctl);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      ptx::tc_fence_after();
+      uint32_t r0[64], r1[64];
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + ACC_COL + h * 128;
+      ptx::tmem_ld_32x32b_x64(taddr, r0);
+      ptx::tmem_ld_32x32b_x64(taddr + 64, r1);
+      ptx::tc_wait_ld();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctl->acc_empty));
+      acc_phase ^= 1u;
+      const int64_t row = (int64_t)mb * BM + q * 32 + lane;
+      float4* dst = reinterpret_cast<float4*>(C + row * ldc + (int64_t)nb * BN + h * 128);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        dst[j] = make_float4(__uint_as_float(r0[4 * j]), __uint_as_float(r0[4 * j + 1]),
+                             __uint_as_float(r0[4 * j + 2]), __uint_as_float(r0[4 * j + 3]));
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        dst[16 + j] = make_float4(__uint_as_float(r1[4 * j]), __uint_as_float(r1[4 * j + 1]),
+                                  __uint_as_float(r1[4 * j + 2]), __uint_as_float(r1[4 * j + 3]));
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host ---
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_code_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t kbytes,
+                   uint32_t box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)kbytes, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kbytes};
+  const cuuint32_t box[2] = {(cuuint32_t)BKB, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DevInfo {
+  int sms = 0;
+  int major = 0;
+  bool attr_set = false;
+};
+
+DevInfo& dev_info(int dev) {
+  static DevInfo info[64];
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  DevInfo& d = info[dev & 63];
+  if (!d.attr_set) {
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (d.major == 10)
+      cudaFuncSetAttribute(mxf4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SMEM_BYTES);
+    d.attr_set = true;
+  }
+  return d;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
+                        int64_t ldc, cudaStream_t st, const char** why) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  DevInfo& d = dev_info(dev);
+  if (d.major != 10) {
+    *why = "tcgen05 block-scaled MMA needs an sm_100-family (GB300 sm_103) device";
+    return cudaErrorNotSupported;
+  }
+  if (!encode_fn()) {
+    *why = "driver entry point cuTensorMapEncodeTiled not available";
+    return cudaErrorNotSupported;
+  }
+  CUtensorMap ta, tb;
+  if (!make_code_map(&ta, qa, M, K / 2, BM) || !make_code_map(&tb, qb, N, K / 2, BN)) {
+    *why = "cuTensorMapEncodeTiled rejected the operand layout";
+    return cudaErrorInvalidValue;
+  }
+  const int num_tiles = (int)((M / BM) * (N / BN));
+  const int grid = num_tiles < d.sms ? num_tiles : d.sms;
+  mxf4_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sa, sb, c, ldc, (int)M, (int)N,
+                                                      (int)K);
+  return cudaGetLastError();
+}
+
+cudaError_t read_device_error(cudaStream_t st, uint32_t* err) {
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(err, g_gemm_error, sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  if (*err) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(uint32_t));
+  }
+  return e;
+}
+
+}  // namespace mx

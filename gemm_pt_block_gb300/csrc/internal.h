@@ -1,0 +1,35 @@
+// internal.h -- launchers shared between the C-ABI layer and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mx {
+
+// One output orientation of the quantizer, already validated.
+struct OrientArgs {
+  int32_t block;        // 0: 1x32, 1: 32x32
+  int32_t roundup;      // scale mode: 0 floor, 1 round-up
+  int32_t sr;           // 0: nearest-even, 1: stochastic
+  int32_t mma_layout;   // scale array layout: 0 row-major, 1 tensor-core tiles
+  int32_t wht;          // rotate 32-runs along the quantization axis first
+  uint32_t sign_mask;
+  uint64_t seed;
+  uint32_t stream;
+  uint8_t* q;           // packed codes [out_rows, K/2]
+  uint8_t* s;           // scales
+};
+
+// All launchers return the cudaError_t of the launch.
+cudaError_t launch_quantize(const void* x, bool f32_in, int64_t rows, int64_t cols, int64_t ld,
+                            const OrientArgs* row, const OrientArgs* col, cudaStream_t st);
+cudaError_t launch_dequantize(const uint8_t* q, const uint8_t* s, bool mma_layout, int64_t rows,
+                              int64_t cols, float* out, cudaStream_t st);
+cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t cols, int64_t ld,
+                              uint32_t sign_mask, bool inverse, float* y, cudaStream_t st);
+cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
+                        int64_t ldc, cudaStream_t st, const char** why);
+// Reads and clears the GEMM's device error word (synchronizes st).
+cudaError_t read_device_error(cudaStream_t st, uint32_t* err);
+
+}  // namespace mx

@@ -1,0 +1,171 @@
+/*
+ * mxfp4.h -- C ABI of the GB300 (sm_103a) MXFP4 training hot path.
+ *
+ * The library implements the two parts of the hot path that the following
+ * pages describe for MXFP4 training:
+ *   [News]  "Block-Scaled MXFP4 With Stochastic Hadamard Rounding Matches BF16
+ *           Convergence on 70B Pre-Training", paras. 1-2.
+ *   [Cim]   "Pretraining large language models with MXFP4", Abstract.
+ *   [TIBQ]  "Stable FP4 Training via Transposition-Invariant Block
+ *           Quantization", sections "Why FP4 training is the current
+ *           frontier of precision reduction", "The aha: transposition
+ *           scrambles the blocks", "The fix, and its supporting cast".
+ *   [Tseng] "Training LLMs with MXFP4", Abstract.
+ *
+ * Conventions for every call:
+ *  - Pointers named x, y, q_*, s_*, qa, sa, qb, sb, c, out are DEVICE pointers
+ *    (cudaMalloc / PyTorch CUDA memory) owned by the caller; params pointers
+ *    are HOST pointers read during the call only. The library allocates no
+ *    device memory and keeps no per-call state.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Work is enqueued asynchronously on it; the return value reports argument
+ *    validation and launch errors only. Calls are thread-safe.
+ *  - Tensors are row-major with a leading dimension in elements. Packed E2M1
+ *    codes hold two elements per byte: the even index in the low nibble, the
+ *    odd index in the high nibble; code = sign << 3 | magnitude index into
+ *    {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+ *  - Scales are E8M0 bytes (value 2^(byte - 127)), one per block of 32
+ *    elements along the quantization axis, stored in one of two layouts:
+ *      MXFP4_LAYOUT_ROWMAJOR: s[r * (K/32) + kb];
+ *      MXFP4_LAYOUT_MMA: the block-scaled tensor-core operand layout: 128-row
+ *        x 4-column tiles of 512 bytes, tiles in row-tile-major order, scale
+ *        (r, kb) at tile ((r/128) * (K/128) + kb/4), byte
+ *        (r % 32) * 16 + ((r % 128) / 32) * 4 + kb % 4 (needs rows % 128 == 0
+ *        and K % 128 == 0). mxfp4_gemm consumes this layout.
+ *  - Pointers must be 16-byte aligned and leading dimensions multiples of
+ *    8 elements, else MXFP4_ERR_ALIGN.
+ */
+#ifndef MXFP4_H
+#define MXFP4_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MXFP4_OK = 0,
+  MXFP4_ERR_INVALID_ARG = 1, /* null pointer, bad enum value */
+  MXFP4_ERR_SHAPE = 2,       /* dimension not supported (see each call) */
+  MXFP4_ERR_ALIGN = 3,       /* pointer or leading dimension misaligned */
+  MXFP4_ERR_UNSUPPORTED = 4, /* device is not sm_103 / sm_100 family */
+  MXFP4_ERR_CUDA = 5,        /* CUDA runtime / driver error at launch */
+  MXFP4_ERR_TIMEOUT = 6      /* a bounded device-side wait ran out */
+} mxfp4_status;
+
+enum { MXFP4_BLOCK_1X32 = 0, MXFP4_BLOCK_32X32 = 1 };
+enum { MXFP4_SCALE_FLOOR = 0, MXFP4_SCALE_ROUNDUP = 1 };
+enum { MXFP4_ROUND_RTN = 0, MXFP4_ROUND_SR = 1 };
+enum { MXFP4_LAYOUT_ROWMAJOR = 0, MXFP4_LAYOUT_MMA = 1 };
+enum { MXFP4_DTYPE_BF16 = 0, MXFP4_DTYPE_F32 = 1 };
+
+/* Quantization parameters of one output orientation.
+ *  block        MXFP4_BLOCK_1X32: 32 consecutive elements along the
+ *               quantization axis share a scale [News, para. 1].
+ *               MXFP4_BLOCK_32X32: the aligned 32 x 32 tile shares one scale,
+ *               written on each of its 32 rows of the scale array [TIBQ,
+ *               "The fix, and its supporting cast", 2D blocks].
+ *  scale_mode   MXFP4_SCALE_FLOOR: e = floor(log2 M) - 2 (OCP Microscaling
+ *               v1.0; the block max may saturate at 6).
+ *               MXFP4_SCALE_ROUNDUP: e = ceil(log2(M / 6)), nothing clips
+ *               [TIBQ, "Truncation-free scaling"]. M is the block max-abs
+ *               after the optional rotation; M == 0 gives e = -127; e is
+ *               clamped to [-127, 127].
+ *  rounding     MXFP4_ROUND_RTN: nearest grid point, ties to the even code,
+ *               saturating at 6. MXFP4_ROUND_SR: stochastic rounding [TIBQ,
+ *               "Stochastic rounding in the backward pass"; Tseng, Abstract]:
+ *               a 16-bit Philox4x32-10 draw r rounds |v| up from lo to hi iff
+ *               r / 2^16 < (|v| - lo) / (hi - lo). The draw for source element
+ *               i = row * cols + col (index in x as passed, for either
+ *               orientation) is 16-bit half (i & 1) of word ((i >> 1) & 3) of
+ *               Philox(counter = {i >> 3 (low, high word), sr_stream, 0},
+ *               key = {seed low word, seed high word}).
+ *  scale_layout MXFP4_LAYOUT_* for the scale array written.
+ *  wht          1: before scaling, rotate every run of 32 elements along the
+ *               quantization axis by c * H * diag(s) [News, para. 2; Tseng,
+ *               Abstract; Cim, Abstract] -- H the 32 x 32 Sylvester Hadamard
+ *               matrix, butterflies in the order h = 1, 2, 4, 8, 16 in fp32,
+ *               c = fp32(1/sqrt(32)) applied last as one rounded multiply.
+ *  wht_sign_mask bit i set => s_i = -1 (0 = the deterministic rotation).
+ *  seed, sr_stream  Philox key and counter word 2 (used by MXFP4_ROUND_SR).
+ * All arithmetic is IEEE fp32 without fused multiply-add or flush-to-zero, so
+ * results are bit-reproducible across calls and streams. */
+typedef struct {
+  int32_t block;
+  int32_t scale_mode;
+  int32_t rounding;
+  int32_t scale_layout;
+  int32_t wht;
+  uint32_t wht_sign_mask;
+  uint64_t seed;
+  uint32_t sr_stream;
+  uint32_t reserved; /* must be 0 */
+} mxfp4_quant_params;
+
+/* Fused MXFP4 quantizer ([News], paras. 1-2; [TIBQ] P_i = round(X_i / S)).
+ *  x      [rows, cols] bf16 or fp32 (x_dtype), leading dimension ld_x >= cols.
+ *  row    if non-NULL, quantize along cols:  q_row [rows, cols/2] bytes,
+ *         s_row [rows, cols/32] scale bytes (row->scale_layout).
+ *  col    if non-NULL, quantize x^T, i.e. along rows, in the same pass [TIBQ,
+ *         "The aha: transposition scrambles the blocks"]: q_col [cols, rows/2],
+ *         s_col [cols, rows/32]. Stochastic-rounding draws are keyed by the
+ *         source index, so 32x32 blocks without rotation stay transposition
+ *         invariant under stochastic rounding too.
+ *  At least one of row / col must be non-NULL.
+ *  Shapes: cols % 32 == 0; rows % 32 == 0 when col != NULL or either
+ *  orientation uses 32x32 blocks; MMA scale layout needs the output's row
+ *  count % 128 == 0 and its K % 128 == 0. Else MXFP4_ERR_SHAPE.
+ *  Inputs must be finite (non-finite inputs give unspecified codes). */
+mxfp4_status mxfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
+                            int64_t ld_x, const mxfp4_quant_params* row, uint8_t* q_row,
+                            uint8_t* s_row, const mxfp4_quant_params* col, uint8_t* q_col,
+                            uint8_t* s_col, void* stream);
+
+/* Reconstruction P_i * S ([TIBQ], "Why FP4 training is the current frontier
+ * of precision reduction"): out[r, c] = E2M1(code) * 2^(byte - 127) in fp32;
+ * scale byte 0xFF (E8M0 NaN) gives NaN.
+ *  q [rows, cols/2], s in scale_layout, out [rows, cols] fp32 (dense).
+ *  cols % 32 == 0 (MMA layout: rows % 128 == 0, cols % 128 == 0). */
+mxfp4_status mxfp4_dequantize(const uint8_t* q, const uint8_t* s, int32_t scale_layout,
+                              int64_t rows, int64_t cols, float* out, void* stream);
+
+/* Block-scaled MXFP4 GEMM ([Tseng], Abstract: "MXFP4 GEMMs"; [Cim], Abstract:
+ * Fprop, Dgrad and Wgrad all take this form):
+ *   C[m, n] = sum_k deqA[m, k] * deqB[n, k]   (fp32 accumulation)
+ * with both operands K-major (the "TN" form): qa [M, K/2], qb [N, K/2] packed
+ * codes, sa / sb scales in MXFP4_LAYOUT_MMA. C fp32 [M, N] with leading
+ * dimension ldc >= N. Fprop Y = X W^T is (A = X row-wise, B = W row-wise);
+ * Dgrad dX = dY W is (A = dY row-wise, B = W column-wise); Wgrad dW = dY^T X is
+ * (A = dY column-wise, B = X column-wise).
+ *  Shapes: M % 128 == 0, N % 256 == 0, K % 256 == 0, all > 0.
+ *  Runs on tcgen05 tensor cores (sm_103a); returns MXFP4_ERR_UNSUPPORTED on
+ *  other devices. */
+mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
+                        int64_t ldc, void* stream);
+
+/* Stand-alone 32-point block rotation along cols ([News], para. 2):
+ *  forward (inverse == 0): y = c * H * diag(s) * x per 32-block;
+ *  inverse (inverse == 1): y = diag(s) * c * H * x.
+ *  x [rows, cols] bf16/fp32 with ld_x; y [rows, cols] fp32 dense; cols % 32 == 0.
+ *  The forward rotation is bit-identical to the one mxfp4_quantize fuses. */
+mxfp4_status hadamard32(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
+                        int64_t ld_x, uint32_t sign_mask, int32_t inverse, float* y,
+                        void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* mxfp4_status_string(mxfp4_status s);
+
+/* Detail of the last non-OK status returned on the calling thread. */
+const char* mxfp4_last_error(void);
+
+/* Reads and clears the device-side error word that bounded waits inside the
+ * GEMM kernel set when they run out (MXFP4_OK if none). Synchronizes `stream`
+ * first. */
+mxfp4_status mxfp4_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MXFP4_H */

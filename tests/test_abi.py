@@ -1,0 +1,109 @@
+"""The C ABI library loads, exports every function include/mxfp4.h declares,
+and rejects bad arguments on the host (no GPU needed for these paths)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxfp4.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from gemm_pt_block_gb300 import build as b
+
+    b.build()
+    import gemm_pt_block_gb300 as mx
+
+    return mx.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_four_hot_path_calls():
+    names = _declared_functions()
+    for n in ["mxfp4_quantize", "mxfp4_dequantize", "mxfp4_gemm", "hadamard32"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", L._name], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (\S+)", out))
+    for name in _declared_functions():
+        assert name in exported, name
+
+
+def test_header_compiles_as_c():
+    src = '#include "mxfp4.h"\nint main(void){ mxfp4_quant_params p = {0}; (void)p; return 0; }\n'
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-x", "c", "-", "-fsyntax-only"], input=src, text=True, capture_output=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_status_strings(L):
+    names = [L.mxfp4_status_string(i).decode() for i in range(7)]
+    assert names == ["MXFP4_OK", "MXFP4_ERR_INVALID_ARG", "MXFP4_ERR_SHAPE", "MXFP4_ERR_ALIGN",
+                     "MXFP4_ERR_UNSUPPORTED", "MXFP4_ERR_CUDA", "MXFP4_ERR_TIMEOUT"]
+
+
+def test_host_side_validation(L):
+    import gemm_pt_block_gb300 as mx
+    from gemm_pt_block_gb300.binding import _CParams
+
+    P = ctypes.c_void_p
+    good = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails validation
+    p = mx.QuantParams()._c()
+    # no orientation requested
+    assert L.mxfp4_quantize(good, 0, 32, 32, 32, None, None, None, None, None, None, None) == 1
+    # cols not a multiple of 32
+    assert L.mxfp4_quantize(good, 0, 32, 48, 48, ctypes.byref(p), good, good, None, None, None, None) == 2
+    # ld < cols
+    assert L.mxfp4_quantize(good, 0, 32, 64, 32, ctypes.byref(p), good, good, None, None, None, None) == 2
+    # misaligned x
+    assert L.mxfp4_quantize(P((1 << 20) + 2), 0, 32, 32, 32, ctypes.byref(p), good, good,
+                            None, None, None, None) == 3
+    # bad enum
+    bad = _CParams(5, 0, 0, 0, 0, 0, 0, 0, 0)
+    assert L.mxfp4_quantize(good, 0, 32, 32, 32, ctypes.byref(bad), good, good, None, None, None, None) == 1
+    # reserved field
+    bad = _CParams(0, 0, 0, 0, 0, 0, 0, 0, 7)
+    assert L.mxfp4_quantize(good, 0, 32, 32, 32, ctypes.byref(bad), good, good, None, None, None, None) == 1
+    # column output needs rows % 32
+    assert L.mxfp4_quantize(good, 0, 48, 32, 32, None, None, None, ctypes.byref(p), good, good, None) == 2
+    # tensor-core scale layout needs 128-row tiles
+    pm = mx.QuantParams(scale_layout=mx.LAYOUT_MMA)._c()
+    assert L.mxfp4_quantize(good, 0, 64, 128, 128, ctypes.byref(pm), good, good, None, None, None, None) == 2
+    # GEMM shapes
+    assert L.mxfp4_gemm(good, good, good, good, 100, 256, 256, good, 256, None) == 2
+    assert L.mxfp4_gemm(good, good, good, good, 128, 128, 256, good, 128, None) == 2
+    assert L.mxfp4_gemm(good, good, good, good, 128, 256, 128, good, 256, None) == 2
+    assert L.mxfp4_gemm(good, good, good, good, 128, 256, 256, good, 100, None) == 2
+    assert L.mxfp4_gemm(None, good, good, good, 128, 256, 256, good, 256, None) == 1
+    assert L.mxfp4_gemm(good, good, good, good, 128, 256, 256, P((1 << 20) + 4), 256, None) == 3
+    # dequantize / hadamard32
+    assert L.mxfp4_dequantize(good, good, 1, 64, 128, good, None) == 2
+    assert L.mxfp4_dequantize(good, good, 2, 64, 128, good, None) == 1
+    assert L.hadamard32(good, 0, 4, 40, 40, 0, 0, good, None) == 2
+    assert L.hadamard32(good, 0, 4, 32, 32, 0, 2, good, None) == 1
+    assert b"multiple of 32" in L.mxfp4_last_error() or len(L.mxfp4_last_error()) > 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+
+    import gemm_pt_block_gb300 as mx
+
+    with pytest.raises(ValueError):
+        mx.mxfp4_quantize(torch.zeros(32, 32, dtype=torch.bfloat16), mx.QuantParams())
