@@ -1,0 +1,554 @@
+"""Benchmark of the MXFP4 training hot path on GB300.
+
+A step is one pass of the whole hot path for one linear layer of a training
+step: the fused quantization of the activation X, the weight W and the output
+gradient dY (each in both orientations in one pass), then the three
+block-scaled MXFP4 GEMMs Fprop Y = X W^T, Dgrad dX = dY W, Wgrad dW = dY^T X.
+
+Default workload (N = 1): the 70B-dense-shaped layer (tokens 16384, d 8192,
+ffn 28672): X ~ Student-t(4), W ~ N(0, 0.02), dY ~ Laplace(0, 1e-3) with 0.1% of
+entries x100, all bf16; W and dY in 32x32 blocks, X in 1x32 blocks; round-up
+scales; Fprop operands nearest-even without rotation; Dgrad's dY by stochastic
+rounding; the Wgrad operands (dY and X column-wise) with the random-sign
+32-point rotation and stochastic rounding.
+
+Prints one JSON line. `value` = GEMM FLOPs of the step / step time (the
+quantization time included), TFLOP/s summed over ranks; the parts (GEMM
+TFLOP/s against the dense FP4 peak, quantizer GB/s against the HBM peak) are
+reported alongside, with the roofline of the dominant kernel.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+       [--workload NAME] [--no-cpu-baseline] [--no-e2e]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from dataclasses import dataclass, field
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP4 GEMM TFLOPS (% FP4 peak); fused RHT+quantize GB/s (% HBM peak)"
+FP4_OVER_BF16 = 13.5 / 2.25        # nominal dense FP4 : BF16 tensor rate
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# Training-step workloads: name -> (tokens T, d D, ffn F, data seed, description).
+LAYERS = {
+    "70b-layer": (16384, 8192, 28672, 1003,
+                  "70B-dense-shaped layer training step: tokens 16384, d 8192, ffn 28672"),
+    "8b-mlp-up": (8192, 4096, 14336, 1002,
+                  "Llama-3.1-8B-shaped MLP up-proj training step: tokens 8192, d 4096, ffn 14336"),
+}
+# Square sweep points: quantize A and B (1x32 floor nearest-even) + one n^3 GEMM.
+SQUARES = {f"sq{n}": n for n in (1024, 2048, 4096, 8192, 16384)}
+WORKLOADS = sorted(LAYERS) + ["tiny"] + sorted(SQUARES, key=lambda k: SQUARES[k])
+
+
+# ------------------------------------------------------------ workloads ---
+
+@dataclass
+class QuantOp:
+    name: str
+    rows: int
+    cols: int
+    dist: tuple           # ("t", df) | ("normal", std) | ("laplace", b, outlier_frac) | ("outcols", n, mult)
+    seed: int
+    prow: object          # gemm_pt_block_gb300.QuantParams or None
+    pcol: object
+
+
+@dataclass
+class GemmOp:
+    label: str
+    a: tuple              # (input name, "row" | "col")
+    b: tuple
+    M: int
+    N: int
+    K: int
+
+
+@dataclass
+class Spec:
+    name: str
+    desc: str
+    quants: list = field(default_factory=list)
+    gemms: list = field(default_factory=list)
+
+    def quant_bytes(self):
+        """Algorithmic bytes per quantize launch: read the bf16 input once, write
+        each requested orientation's codes (0.5 B/elem) and scales (1/32 B/elem)."""
+        return [q.rows * q.cols * (2 + ((q.prow is not None) + (q.pcol is not None)) * (0.5 + 1 / 32))
+                for q in self.quants]
+
+    def gemm_flops(self):
+        return [2.0 * g.M * g.N * g.K for g in self.gemms]
+
+    def labels(self):
+        return [f"quantize {q.name}" for q in self.quants] + [f"gemm {g.label}" for g in self.gemms]
+
+
+def make_spec(name: str) -> Spec:
+    import gemm_pt_block_gb300 as mx
+    import synth
+
+    P, mma = mx.QuantParams, mx.LAYOUT_MMA
+    if name in LAYERS:
+        T, D, F, seed, desc = LAYERS[name]
+        big = name == "70b-layer"
+        mask = synth.sign_mask(seed)
+        # 70B step: W, dY in 32x32 blocks, round-up scales, random-sign rotation
+        # for Wgrad, SR on Dgrad's dY. 8B step: 1x32 floor, deterministic
+        # rotation + SR for the Wgrad operands only.
+        wblk = mx.BLOCK_32X32 if big else mx.BLOCK_1X32
+        smode = mx.SCALE_ROUNDUP if big else mx.SCALE_FLOOR
+        wmask = mask if big else 0
+        dgrad = mx.ROUND_SR if big else mx.ROUND_RTN
+        s = Spec(name, desc)
+        s.quants = [
+            QuantOp("X", T, D, ("t", 4.0), seed,
+                    P(mx.BLOCK_1X32, smode, mx.ROUND_RTN, mma),
+                    P(mx.BLOCK_1X32, smode, mx.ROUND_SR, mma, True, wmask, 1, 0)),
+            QuantOp("W", F, D, ("normal", 0.02), seed + 100,
+                    P(wblk, smode, mx.ROUND_RTN, mma), P(wblk, smode, mx.ROUND_RTN, mma)),
+            QuantOp("dY", T, F, ("laplace", 1e-3, 0.001 if big else 0.0), seed + 200,
+                    P(wblk, smode, dgrad, mma, False, 0, 1, 2),
+                    P(wblk, smode, mx.ROUND_SR, mma, True, wmask, 1, 1)),
+        ]
+        s.gemms = [GemmOp("Fprop", ("X", "row"), ("W", "row"), T, F, D),
+                   GemmOp("Dgrad", ("dY", "row"), ("W", "col"), T, D, F),
+                   GemmOp("Wgrad", ("dY", "col"), ("X", "col"), F, D, T)]
+        return s
+    if name == "tiny":
+        mask = synth.sign_mask(1000)
+        s = Spec(name, "tiny: X [512,1024] N(0,1) with 8 outlier columns x50, W [512,1024] N(0,0.02); "
+                       "random-sign rotation, 1x32 floor; W nearest-even, X SR seed 0; Y = Xq Wq^T")
+        s.quants = [
+            QuantOp("X", 512, 1024, ("outcols", 8, 50.0), 1000,
+                    P(mx.BLOCK_1X32, mx.SCALE_FLOOR, mx.ROUND_SR, mma, True, mask, 0, 0), None),
+            QuantOp("W", 512, 1024, ("normal", 0.02), 1100,
+                    P(mx.BLOCK_1X32, mx.SCALE_FLOOR, mx.ROUND_RTN, mma, True, mask), None)]
+        s.gemms = [GemmOp("Fprop", ("X", "row"), ("W", "row"), 512, 512, 1024)]
+        return s
+    n = SQUARES[name]
+    s = Spec(name, f"square sweep point n={n}: A, B [{n},{n}] ~ t(3) bf16, 1x32 floor nearest-even; C = A B^T")
+    p = P(mx.BLOCK_1X32, mx.SCALE_FLOOR, mx.ROUND_RTN, mma)
+    s.quants = [QuantOp("A", n, n, ("t", 3.0), 1004, p, None),
+                QuantOp("B", n, n, ("t", 3.0), 1104, p, None)]
+    s.gemms = [GemmOp("C", ("A", "row"), ("B", "row"), n, n, n)]
+    return s
+
+
+def gen_input(q: QuantOp, device, rows=None, cols=None, seed_offset=0):
+    """Seeded bf16 input of the op's distribution (device tensor, or CPU for the oracle)."""
+    import synth
+
+    r = q.rows if rows is None else rows
+    c = q.cols if cols is None else cols
+    seed = q.seed + seed_offset
+    kind = q.dist[0]
+    if str(device) == "cpu":
+        if kind == "t":
+            return synth.student_t(r, c, q.dist[1], seed)
+        if kind == "normal":
+            return synth.normal(r, c, q.dist[1], seed)
+        if kind == "laplace":
+            return synth.laplace(r, c, q.dist[1], seed, outlier_frac=q.dist[2])
+        return synth.normal_outlier_cols(r, c, 1.0, q.dist[1], q.dist[2], seed)
+    if kind == "t":
+        return synth.dev_student_t(r, c, q.dist[1], seed, device)
+    if kind == "normal":
+        return synth.dev_normal(r, c, q.dist[1], seed, device)
+    if kind == "laplace":
+        return synth.dev_laplace(r, c, q.dist[1], seed, device, outlier_frac=q.dist[2])
+    return synth.normal_outlier_cols(r, c, 1.0, q.dist[1], q.dist[2], seed).to(device)
+
+
+class Step:
+    """Device inputs, preallocated outputs and the launch sequence of one step."""
+
+    def __init__(self, spec: Spec, device):
+        import torch
+
+        self.spec = spec
+        u8 = torch.uint8
+        self.inputs, self.bufs, self.outs = {}, {}, {}
+        for q in spec.quants:
+            self.inputs[q.name] = gen_input(q, device)
+            r, c = q.rows, q.cols
+            self.bufs[q.name] = (
+                torch.empty(r, c // 2, dtype=u8, device=device) if q.prow else None,
+                torch.empty(r * c // 32, dtype=u8, device=device) if q.prow else None,
+                torch.empty(c, r // 2, dtype=u8, device=device) if q.pcol else None,
+                torch.empty(r * c // 32, dtype=u8, device=device) if q.pcol else None)
+        for g in spec.gemms:
+            self.outs[g.label] = torch.empty(g.M, g.N, device=device)
+        torch.cuda.empty_cache()
+
+    @property
+    def launches(self):
+        return len(self.spec.quants) + len(self.spec.gemms)
+
+    def operand(self, ref):
+        q, s, qc, sc = self.bufs[ref[0]]
+        return (q, s) if ref[1] == "row" else (qc, sc)
+
+    def run(self, inputs=None, events=None):
+        """Enqueue the step on the current stream; events[i], events[i+1] bracket launch i."""
+        import gemm_pt_block_gb300 as mx
+
+        inp = self.inputs if inputs is None else inputs
+        k = 0
+        if events is not None:
+            events[0].record()
+        for q in self.spec.quants:
+            qr, sr, qc, sc = self.bufs[q.name]
+            mx.mxfp4_quantize(inp[q.name], q.prow, q.pcol, q_row=qr, s_row=sr, q_col=qc, s_col=sc)
+            k += 1
+            if events is not None:
+                events[k].record()
+        for g in self.spec.gemms:
+            qa, sa = self.operand(g.a)
+            qb, sb = self.operand(g.b)
+            mx.mxfp4_gemm(qa, sa, qb, sb, g.M, g.N, g.K, c=self.outs[g.label])
+            k += 1
+            if events is not None:
+                events[k].record()
+
+
+# ------------------------------------------------------------ utilities ---
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return FALLBACK, "fallback"
+
+
+def _dist():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while the block runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, power, reasons = [], None, [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(self.NAMES, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def _traffic_record():
+    """DRAM traffic per GEMM launch from the committed ncu summary, if it was
+    taken on the current GEMM source (else None)."""
+    path = os.path.join(ROOT, "profiles", "gemm_traffic.txt")
+    src = os.path.join(ROOT, "gemm_pt_block_gb300", "csrc", "gemm.cu")
+    try:
+        rec = {}
+        with open(path) as f:
+            for ln in f:
+                if ":" in ln and not ln.startswith("#"):
+                    k, v = ln.split(":", 1)
+                    rec[k.strip()] = v.strip()
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+        return rec if rec.get("gemm_cu_sha256_16") == digest else None
+    except OSError:
+        return None
+
+
+# ------------------------------------------------------------ CPU oracle ---
+
+def cpu_oracle_sample(spec: Spec, r: int = 128):
+    """Times the oracle on a bounded sample of the same step: for every quantize
+    op an r-row band (row-wise output) and an r-column band (column-wise output),
+    and for every GEMM r output rows (dequantize + fp64 product). Inputs are
+    generated before the clock starts. Returns (seconds, sampled GEMM FLOPs,
+    sampled quantize bytes, threads, description)."""
+    import oracle
+    import synth
+
+    def op(p):
+        return None if p is None else oracle.Params(p.block, p.scale_mode, p.rounding, p.wht,
+                                                     p.wht_sign_mask, p.seed, p.sr_stream)
+
+    jobs, qbytes, flops = [], 0.0, 0.0
+    for q in spec.quants:
+        rr = min(r, q.rows)
+        if q.prow is not None:
+            band = synth.bf16_bits(gen_input(q, "cpu", rows=rr))
+            jobs.append(("rows", band, op(q.prow)))
+            qbytes += band.size * (2 + 0.5 + 1 / 32)
+        if q.pcol is not None:
+            cc = min(r, q.cols)
+            band = synth.bf16_bits(gen_input(q, "cpu", cols=cc, seed_offset=1))
+            jobs.append(("cols", band, op(q.pcol)))
+            qbytes += band.size * (2 + 0.5 + 1 / 32)
+    gem = []
+    for g in spec.gemms:
+        m = min(r, g.M)
+        gem.append((synth.random_codes(m, g.K, 1), synth.random_scales(m, g.K, 2),
+                    synth.random_codes(g.N, g.K, 3), synth.random_scales(g.N, g.K, 4), m, g.N, g.K))
+        flops += 2.0 * m * g.N * g.K
+    t0 = time.perf_counter()
+    for kind, band, p in jobs:
+        (oracle.quantize_rows if kind == "rows" else oracle.quantize_cols)(band, p)
+    for qa, sa, qb, sb, m, N, K in gem:
+        A = oracle.dequantize(qa, sa.reshape(m, K // 32), m, K, f64=True)
+        B = oracle.dequantize(qb, sb.reshape(N, K // 32), N, K, f64=True)
+        _ = A @ B.T
+    dt = time.perf_counter() - t0
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    desc = (f"{r}-row / {r}-column bands of every quantized tensor (oracle quantize, both "
+            f"orientations as the step asks) and {r} output rows of every GEMM (oracle dequantize + "
+            f"fp64 product); value = sampled GEMM FLOPs / oracle seconds")
+    return dt, flops, qbytes, threads, desc
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    spec = make_spec(args.workload)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, flops, qb, threads, sdesc = cpu_oracle_sample(spec)
+        if i >= args.warmup:
+            times.append(dt)
+    ms = 1000.0 * statistics.mean(times)
+    value = flops / (ms / 1000.0) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.desc, "sample": sdesc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sdesc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ main ---
+
+def measure_e2e(st: Step, steps: int, ws: int):
+    """The same metric through the public API with host buffers: every step
+    copies the bf16 inputs from pinned host memory, runs the step and reads the
+    fp32 GEMM results back to pinned host memory."""
+    import torch
+
+    host_in = {k: v.cpu().pin_memory() for k, v in st.inputs.items()}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in st.outs.items()}
+    dev_in = {k: torch.empty_like(v) for k, v in st.inputs.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def one():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        st.run(inputs=dev_in)
+        for k in host_out:
+            host_out[k].copy_(st.outs[k], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    if ws > 1:
+        t = torch.tensor([ms], device=next(iter(st.outs.values())).device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    flops = sum(st.spec.gemm_flops())
+    return {"value": ws * flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="70b-layer", choices=WORKLOADS)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    import gemm_pt_block_gb300 as mx
+    from gemm_pt_block_gb300 import build as mxbuild
+
+    if not os.path.exists(mx.lib_path()):
+        mxbuild.build()
+    mx.lib()
+
+    spec = make_spec(args.workload)
+    st = Step(spec, device)
+    qwork, gwork = spec.quant_bytes(), spec.gemm_flops()
+    nq = len(qwork)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        st.run()
+    barrier()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(st.launches + 1)]
+           for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(args.steps):
+            st.run(events=evs[i])
+        t1.record()
+        barrier()
+    total_ms = t0.elapsed_time(t1)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    per_launch = [statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+                  for j in range(st.launches)]
+    if mx.device_status() != 0:
+        raise RuntimeError("a bounded device-side wait ran out during the benchmark")
+
+    peaks, peak_src = _peaks()
+    fp4_peak = peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]) * FP4_OVER_BF16
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    q_ms, g_ms = per_launch[:nq], per_launch[nq:]
+    labels = spec.labels()
+    gemm_tflops = sum(gwork) / (sum(g_ms) / 1e3) / 1e12
+    quant_gbs = sum(qwork) / (sum(q_ms) / 1e3) / 1e9
+    value = ws * sum(gwork) / (ms_step / 1e3) / 1e12
+
+    # Dominant kernel by share of the step: the GEMM (per-launch average).
+    achieved = statistics.mean(f / (m / 1e3) / 1e12 for f, m in zip(gwork, g_ms))
+    tr = _traffic_record()
+    traffic = None
+    if tr is not None and tr.get("workload") == args.workload:
+        traffic = float(tr["dram_bytes_per_launch"])
+    roofline = {"bound": "tensor", "kernel": "mxf4_gemm_kernel", "achieved": achieved,
+                "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak, "traffic": traffic,
+                "peak_source": f"{peak_src}: bf16_tflops_sustained x {FP4_OVER_BF16:g} (nominal dense FP4:BF16)"}
+    share = {lab: m / ms_step for lab, m in zip(labels, per_launch)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1", "data": "synthetic",
+        "config": {"workload": spec.desc,
+                   "parallelism": f"{ws} independent replicas" if ws > 1 else "1 GPU",
+                   "l2": "no flush: every input tensor and operand of the default workload is larger "
+                         "than the 129 MB L2 (X 268 MB, W 470 MB, dY 940 MB bf16; codes 67-235 MB)"},
+        "parts": {
+            "gemm": {"tflops": gemm_tflops, "frac_of_fp4_peak": gemm_tflops / fp4_peak,
+                     "ms": dict(zip(labels[nq:], g_ms))},
+            "quantize": {"gbs": quant_gbs, "frac_of_hbm": quant_gbs / hbm_peak,
+                         "ms": dict(zip(labels[:nq], q_ms)),
+                         "gbs_each": {lab: b / (m / 1e3) / 1e9 for lab, b, m in zip(labels[:nq], qwork, q_ms)},
+                         "bytes_model": "bf16 read + per orientation 0.5 B codes + 1/32 B scales per element"},
+            "share_of_step": share,
+            "peaks": {"fp4_tflops": fp4_peak, "hbm_gbs": hbm_peak, "source": peak_src},
+        },
+        "roofline": roofline,
+        "gpu_launches": st.launches * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        line["e2e"] = measure_e2e(st, max(1, min(args.steps, 5)), ws)
+    if not args.no_cpu_baseline and rank == 0 and ws == 1:
+        dt, flops, qb, threads, sdesc = cpu_oracle_sample(spec)
+        line["cpu_baseline"] = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle", "sample": sdesc, "seconds": dt,
+                                "quantize_gbs": qb / dt / 1e9}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

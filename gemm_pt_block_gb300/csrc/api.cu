@@ -30,7 +30,8 @@ mxfp4_status from_cuda(cudaError_t e, const char* what) {
 // Validates one orientation's parameters and fills the launcher's view.
 mxfp4_status check_params(const mxfp4_quant_params* p, uint8_t* q, uint8_t* s, int64_t out_rows,
                           int64_t k, const char* name, mx::OrientArgs* o) {
-  if (!q || !s) return fail(MXFP4_ERR_INVALID_ARG, "%s: output pointers must be non-NULL", name);
+  if ((!q || !s) && out_rows * k > 0)
+    return fail(MXFP4_ERR_INVALID_ARG, "%s: output pointers must be non-NULL", name);
   if (!aligned16(q)) return fail(MXFP4_ERR_ALIGN, "%s: codes pointer not 16-byte aligned", name);
   if (p->block != MXFP4_BLOCK_1X32 && p->block != MXFP4_BLOCK_32X32)
     return fail(MXFP4_ERR_INVALID_ARG, "%s: bad block %d", name, p->block);

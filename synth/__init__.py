@@ -82,3 +82,43 @@ def random_scales(rows: int, k: int, seed: int, lo: int = 120, hi: int = 134) ->
 def uniform_f32(rows: int, cols: int, lo: float, hi: float, seed: int) -> np.ndarray:
     rng = np.random.default_rng(seed)
     return rng.uniform(lo, hi, size=(rows, cols)).astype(np.float32)
+
+
+# ----------------------------------------------------------------------------
+# Device-side generators for workload-sized inputs (the benchmark). Same
+# distributions, drawn with torch's seeded CUDA generator, rounded to bf16 RNE.
+# ----------------------------------------------------------------------------
+
+def _gen(device, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def dev_normal(rows: int, cols: int, std: float, seed: int, device) -> torch.Tensor:
+    g = _gen(device, seed)
+    return (torch.randn(rows, cols, generator=g, device=device) * std).to(torch.bfloat16)
+
+
+def dev_student_t(rows: int, cols: int, df: float, seed: int, device) -> torch.Tensor:
+    """t(df) = Z / sqrt(V / df), Z ~ N(0,1), V ~ chi^2(df) = 2 * Gamma(df/2)."""
+    g = _gen(device, seed)
+    z = torch.randn(rows, cols, generator=g, device=device)
+    # chi^2 with integer df as a sum of df squared normals (df is 3 or 4 here)
+    v = torch.zeros(rows, cols, device=device)
+    for _ in range(int(df)):
+        v.addcmul_(t1 := torch.randn(rows, cols, generator=g, device=device), t1)
+    return (z / torch.sqrt(v / df)).to(torch.bfloat16)
+
+
+def dev_laplace(rows: int, cols: int, b: float, seed: int, device, outlier_frac: float = 0.0,
+                outlier_mult: float = 100.0) -> torch.Tensor:
+    """Laplace(0, b) by inverse CDF; round(outlier_frac * n) distinct entries x outlier_mult."""
+    g = _gen(device, seed)
+    u = torch.rand(rows, cols, generator=g, device=device) - 0.5
+    a = -b * torch.sign(u) * torch.log1p(-2.0 * u.abs())
+    n = int(round(outlier_frac * rows * cols))
+    if n:
+        idx = torch.randperm(rows * cols, generator=g, device=device)[:n]
+        a.view(-1)[idx] *= outlier_mult
+    return a.to(torch.bfloat16)

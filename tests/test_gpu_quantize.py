@@ -89,9 +89,14 @@ def test_quantize_every_bf16_pattern():
     x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
     for p in [oracle.Params(), oracle.Params(scale_mode=oracle.SCALE_ROUNDUP),
               oracle.Params(rounding=oracle.ROUND_SR, seed=3),
-              oracle.Params(block=oracle.BLOCK_32X32, rounding=oracle.ROUND_SR, seed=4),
-              oracle.Params(wht=True, wht_sign_mask=0xF0F0F0F0)]:
+              oracle.Params(block=oracle.BLOCK_32X32, rounding=oracle.ROUND_SR, seed=4)]:
         assert_same(gpu_quantize(x.to(DEV), p, p), oracle_quantize(bits, p, p), "bf16 sweep")
+    # With the rotation on, a block sum must stay finite: magnitudes >= 2^122 are zeroed.
+    small = bits.copy()
+    small[(small & 0x7FFF) >= 0x7C80] = 0
+    xs = torch.from_numpy(small.view(np.int16)).view(torch.bfloat16)
+    p = oracle.Params(wht=True, wht_sign_mask=0xF0F0F0F0)
+    assert_same(gpu_quantize(xs.to(DEV), p, p), oracle_quantize(small, p, p), "bf16 sweep, rotated")
 
 
 def test_quantize_rtn_midpoints_and_special_values():
