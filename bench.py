@@ -106,7 +106,9 @@ def make_spec(name: str) -> Spec:
         mask = synth.sign_mask(seed)
         # 70B step: W, dY in 32x32 blocks, round-up scales, random-sign rotation
         # for Wgrad, SR on Dgrad's dY. 8B step: 1x32 floor, deterministic
-        # rotation + SR for the Wgrad operands only.
+        # rotation + SR for the Wgrad operands only. Each tensor has its own
+        # Philox stream (X: 0, dY: 1); both orientations of dY share it, so a
+        # source element draws the same bits for Dgrad and Wgrad.
         wblk = mx.BLOCK_32X32 if big else mx.BLOCK_1X32
         smode = mx.SCALE_ROUNDUP if big else mx.SCALE_FLOOR
         wmask = mask if big else 0
@@ -119,7 +121,7 @@ def make_spec(name: str) -> Spec:
             QuantOp("W", F, D, ("normal", 0.02), seed + 100,
                     P(wblk, smode, mx.ROUND_RTN, mma), P(wblk, smode, mx.ROUND_RTN, mma)),
             QuantOp("dY", T, F, ("laplace", 1e-3, 0.001 if big else 0.0), seed + 200,
-                    P(wblk, smode, dgrad, mma, False, 0, 1, 2),
+                    P(wblk, smode, dgrad, mma, False, 0, 1, 1),
                     P(wblk, smode, mx.ROUND_SR, mma, True, wmask, 1, 1)),
         ]
         s.gemms = [GemmOp("Fprop", ("X", "row"), ("W", "row"), T, F, D),

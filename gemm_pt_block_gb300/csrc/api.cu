@@ -57,6 +57,7 @@ mxfp4_status check_params(const mxfp4_quant_params* p, uint8_t* q, uint8_t* s, i
   o->stream = p->sr_stream;
   o->q = q;
   o->s = s;
+  mx::prepare_orient(o);
   return MXFP4_OK;
 }
 
@@ -98,6 +99,8 @@ mxfp4_status mxfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int64_
   if (!row && !col) return fail(MXFP4_ERR_INVALID_ARG, "at least one of row / col params is required");
   mxfp4_status st = check_input(x, x_dtype, rows, cols, ld_x);
   if (st) return st;
+  if (rows > 0 && cols / 16 > (int64_t)0xFFFFFFFF / rows)
+    return fail(MXFP4_ERR_SHAPE, "tensor too large: rows * cols / 16 must be below 2^32");
   const bool need_rows32 = col || (row && row->block == MXFP4_BLOCK_32X32);
   if (need_rows32 && rows % 32 != 0)
     return fail(MXFP4_ERR_SHAPE, "rows (%lld) must be a multiple of 32 for column-wise or 32x32 output",

@@ -53,7 +53,11 @@ constexpr uint32_t SFB_COL = 264;              // 2 k-chunks x 8 columns
 constexpr int CTL_BYTES = 256;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + CTL_BYTES + 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr int kGroupM = 8;                     // tile raster: 8 M-tiles share each N sweep
+// Tile raster: a group of G consecutive M-tiles sweeps all N-tiles before the
+// next group starts, so a group's A rows (G * 128 * K/2 bytes) stay in L2 while
+// B streams through once per group. G is chosen on the host so that this
+// footprint is about 48 MB (8 <= G <= 64).
+constexpr int64_t kGroupBytes = 48ll << 20;
 
 static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
 
@@ -102,11 +106,12 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (ptx::globaltimer_ns() - t0 > kWaitLimitNs / 8) return;
 }
 
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
-  const int per_group = kGroupM * num_n;
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group_m, int& mb,
+                                            int& nb) {
+  const int per_group = group_m * num_n;
   const int g = tile / per_group;
-  const int first_m = g * kGroupM;
-  const int gm = min(kGroupM, num_m - first_m);
+  const int first_m = g * group_m;
+  const int gm = min(group_m, num_m - first_m);
   const int w = tile - g * per_group;
   mb = first_m + w % gm;
   nb = w / gm;
@@ -115,7 +120,7 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
 __global__ void __launch_bounds__(THREADS, 1)
 mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const uint8_t* __restrict__ sa, const uint8_t* __restrict__ sb,
-                 float* __restrict__ C, int64_t ldc, int M, int N, int K) {
+                 float* __restrict__ C, int64_t ldc, int M, int N, int K, int group_m) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -157,7 +162,7 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         int mb, nb;
-        tile_coords(tile, num_m, num_n, mb, nb);
+        tile_coords(tile, num_m, num_n, group_m, mb, nb);
         for (int kb = 0; kb < num_k; ++kb) {
           const uint32_t empty = ptx::smem_u32(&ctl->empty[stage]);
           const uint32_t full = ptx::smem_u32(&ctl->full[stage]);
@@ -241,7 +246,7 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       int mb, nb;
-      tile_coords(tile, num_m, num_n, mb, nb);
+      tile_coords(tile, num_m, num_n, group_m, mb, nb);
       // One lane waits; the verdict is broadcast so the warp stays converged
       // for the .sync.aligned tensor-memory loads.
       int ok = 0;
@@ -351,8 +356,10 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   }
   const int num_tiles = (int)((M / BM) * (N / BN));
   const int grid = num_tiles < d.sms ? num_tiles : d.sms;
+  int64_t gm = kGroupBytes / (BM * (K / 2));
+  gm = gm < 8 ? 8 : (gm > 64 ? 64 : gm);
   mxf4_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sa, sb, c, ldc, (int)M, (int)N,
-                                                      (int)K);
+                                                      (int)K, (int)gm);
   return cudaGetLastError();
 }
 
@@ -364,7 +371,11 @@ cudaError_t read_device_error(cudaStream_t st, uint32_t* err) {
   if (*err) {
     const uint32_t zero = 0;
     e = cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
   }
+  uint32_t qerr = 0;
+  e = read_quant_error(&qerr);
+  if (!*err) *err = qerr;
   return e;
 }
 

@@ -3,9 +3,12 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "mx_device.cuh"
+
 namespace mx {
 
-// One output orientation of the quantizer, already validated.
+// One output orientation of the quantizer, already validated. The Philox round
+// keys and per-lane sign words are precomputed on the host (see api.cu).
 struct OrientArgs {
   int32_t block;        // 0: 1x32, 1: 32x32
   int32_t roundup;      // scale mode: 0 floor, 1 round-up
@@ -17,7 +20,14 @@ struct OrientArgs {
   uint32_t stream;
   uint8_t* q;           // packed codes [out_rows, K/2]
   uint8_t* s;           // scales
+  PhiloxKeys keys;      // the ten round keys of `seed`
+  uint32_t sm_half[2];  // sign bits of local elements, lane holding block half 0 / 1
+  uint32_t sm_inter[2]; // sign bits of local elements, lane holding even / odd block elements
+  uint32_t xw[2][8];    // sign bits placed on bf16 word pairs (bits 15 and 31), per half
 };
+
+// Fills keys, sm_* and xw from seed and sign_mask.
+void prepare_orient(OrientArgs* o);
 
 // All launchers return the cudaError_t of the launch.
 cudaError_t launch_quantize(const void* x, bool f32_in, int64_t rows, int64_t cols, int64_t ld,
@@ -29,7 +39,9 @@ cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t 
 cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
                         int64_t ldc, cudaStream_t st, const char** why);
-// Reads and clears the GEMM's device error word (synchronizes st).
+// Reads and clears the quantizer's device error word.
+cudaError_t read_quant_error(uint32_t* err);
+// Reads and clears the device error words (synchronizes st).
 cudaError_t read_device_error(cudaStream_t st, uint32_t* err);
 
 }  // namespace mx

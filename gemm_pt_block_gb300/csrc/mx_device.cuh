@@ -1,10 +1,11 @@
 // mx_device.cuh -- per-element MXFP4 arithmetic shared by the quantizer,
 // rotation and dequantization kernels (sm_103a).
 //
-// Every floating-point step uses explicit round-to-nearest intrinsics
-// (__fadd_rn / __fsub_rn / __fmul_rn), which the compiler never contracts into
-// FMAs, and the library is built without flush-to-zero, so results are the
-// IEEE fp32 results the method's definition fixes.
+// Every floating-point step is an explicitly rounded IEEE operation: scalar
+// __fadd_rn / __fmul_rn, or the packed two-lane forms add/sub/mul.rn.f32x2,
+// which round each lane exactly like the scalar instruction. Nothing is
+// contracted into an FMA and the library is built without flush-to-zero, so
+// results are the fp32 results the method's definition fixes.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -18,89 +19,208 @@ constexpr uint32_t kWhtNormBits = 0x3E3504F3u;
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy
 // as 1, 2, 3", SC'11), written from the published round function: words 0 and
 // 2 are multiplied by the round multipliers, the high halves are mixed with
-// words 1 and 3 and the key, and the key advances by the Weyl increments
-// between rounds.
+// words 1 and 3 and the round key. The ten round keys (the key advanced by the
+// Weyl increments) are computed once on the host and passed in.
 struct U4 {
   uint32_t x, y, z, w;
 };
 
-__device__ __forceinline__ U4 philox4x32_10(U4 c, uint32_t k0, uint32_t k1) {
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ U4 philox4x32_10(U4 c, const PhiloxKeys& k) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    if (r) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
     const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
     const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = U4{hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0};
+    c = U4{hi1 ^ c.y ^ k.k0[r], lo1, hi0 ^ c.w ^ k.k1[r], lo0};
   }
   return c;
 }
 
-// The 128 random bits that serve source elements 8g .. 8g+7: element 8g + j
-// takes 16-bit half (j & 1) of word (j >> 1).
-__device__ __forceinline__ U4 sr_group_bits(uint64_t seed, uint32_t stream, uint64_t g) {
-  return philox4x32_10(U4{(uint32_t)g, (uint32_t)(g >> 32), stream, 0u}, (uint32_t)seed,
-                       (uint32_t)(seed >> 32));
+// Random words for source elements 16 h .. 16 h + 15 (two Philox calls, one
+// per 8 elements). Word j of the result holds the draws of elements 2j (low
+// 16 bits) and 2j + 1 (high 16 bits).
+__device__ __forceinline__ void draws16(const PhiloxKeys& k, uint32_t stream, uint64_t i0,
+                                        uint32_t (&w)[8]) {
+  const uint64_t g = i0 >> 3;
+  const U4 a = philox4x32_10(U4{(uint32_t)g, (uint32_t)(g >> 32), stream, 0u}, k);
+  const U4 b = philox4x32_10(U4{(uint32_t)(g + 1), (uint32_t)((g + 1) >> 32), stream, 0u}, k);
+  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
 }
 
-__device__ __forceinline__ uint32_t u4_word(const U4& u, int w) {
-  return w == 0 ? u.x : w == 1 ? u.y : w == 2 ? u.z : u.w;
+// ------------------------------------------------------- packed fp32 ops ---
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) {
+  float2 r;
+  asm("{.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+__device__ __forceinline__ float2 f2sub(float2 a, float2 b) {
+  float2 r;
+  asm("{.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+__device__ __forceinline__ float2 f2mul(float2 a, float2 b) {
+  float2 r;
+  asm("{.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+// a + b rounded toward -infinity, per lane.
+__device__ __forceinline__ float2 f2add_rm(float2 a, float2 b) {
+  float2 r;
+  asm("{.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rm.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // ------------------------------------------------------------- rotation ---
-// In-register part of the 32-point butterfly for the 16 elements a thread
-// holds (block positions half*16 .. half*16+15): stages h = 1, 2, 4, 8, each
-// pair (a, b) = (y[i], y[i+h]) becoming (a + b, a - b).
-__device__ __forceinline__ void butterfly16(float (&y)[16]) {
+// A lane pair holds one 32-element block, 16 elements per lane as 8 pairs
+// R[k] = (y[2k], y[2k+1]) of the lane's local index. Local butterfly stages
+// pair local indices (i, i + h), h = 1, 2, 4, 8: h = 1 is within a pair
+// (scalar), the others combine whole pairs (packed f32x2).
+__device__ __forceinline__ void local_stage(float2 (&R)[8], int h) {
+  if (h == 1) {
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
+    for (int k = 0; k < 8; ++k) {
+      const float a = R[k].x, b = R[k].y;
+      R[k] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
+    }
+  } else {
+    const int hp = h >> 1;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i & h) continue;
-      const float a = y[i], b = y[i + h];
-      y[i] = __fadd_rn(a, b);
-      y[i + h] = __fsub_rn(a, b);
+    for (int k = 0; k < 8; ++k) {
+      if (k & hp) continue;
+      const float2 a = R[k], b = R[k + hp];
+      R[k] = f2add(a, b);
+      R[k + hp] = f2sub(a, b);
     }
   }
 }
 
-// Last stage (h = 16) across the lane pair (lane, lane ^ 1) that holds the
-// two halves of one block: the lower half becomes a + b, the upper a - b,
-// with a from the lower and b from the upper half.
-__device__ __forceinline__ void butterfly_pair(float (&y)[16], int half) {
+// The stage across the lane pair (lane, lane ^ 1): the lower lane's element
+// (a) and the upper lane's element (b) with the same local index become
+// a + b (lower) and a - b (upper).
+__device__ __forceinline__ void cross_stage(float2 (&R)[8], int upper) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float o = __shfl_xor_sync(0xffffffffu, y[i], 1);
-    y[i] = half ? __fsub_rn(o, y[i]) : __fadd_rn(y[i], o);
+  for (int k = 0; k < 8; ++k) {
+    float2 o;
+    o.x = __shfl_xor_sync(0xffffffffu, R[k].x, 1);
+    o.y = __shfl_xor_sync(0xffffffffu, R[k].y, 1);
+    R[k] = upper ? f2sub(o, R[k]) : f2add(R[k], o);
   }
 }
 
-// Forward rotation c * H * diag(s) of one 32-block held by a lane pair.
-__device__ __forceinline__ void wht_forward(float (&y)[16], int half, uint32_t sign_mask) {
-  const uint32_t m = sign_mask >> (half * 16);
+__device__ __forceinline__ void scale_all(float2 (&R)[8], float s) {
+  const float2 s2 = make_float2(s, s);
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
-    if ((m >> i) & 1u) y[i] = -y[i];
-  butterfly16(y);
-  butterfly_pair(y, half);
-  const float c = __uint_as_float(kWhtNormBits);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(y[i], c);
+  for (int k = 0; k < 8; ++k) R[k] = f2mul(R[k], s2);
 }
 
-// Inverse rotation diag(s) * c * H.
-__device__ __forceinline__ void wht_inverse(float (&y)[16], int half, uint32_t sign_mask) {
-  butterfly16(y);
-  butterfly_pair(y, half);
-  const float c = __uint_as_float(kWhtNormBits);
-  const uint32_t m = sign_mask >> (half * 16);
+// Butterflies of c * H in the order h = 1, 2, 4, 8, 16 of the block index, for
+// a lane holding block elements 16 * upper + local (contiguous halves): the
+// four local stages come first, then the cross-lane stage (h = 16).
+__device__ __forceinline__ void hadamard_halves(float2 (&R)[8], int upper) {
+  local_stage(R, 1);
+  local_stage(R, 2);
+  local_stage(R, 4);
+  local_stage(R, 8);
+  cross_stage(R, upper);
+  scale_all(R, __uint_as_float(kWhtNormBits));
+}
+
+// The same transform for a lane holding block elements 2 * local + upper
+// (interleaved): block stage h = 1 is the cross-lane one, block stages
+// 2, 4, 8, 16 are local stages 1, 2, 4, 8.
+__device__ __forceinline__ void hadamard_interleaved(float2 (&R)[8], int upper) {
+  cross_stage(R, upper);
+  local_stage(R, 1);
+  local_stage(R, 2);
+  local_stage(R, 4);
+  local_stage(R, 8);
+  scale_all(R, __uint_as_float(kWhtNormBits));
+}
+
+// Multiply element i by -1 where bit i of m is set (exact sign flips).
+__device__ __forceinline__ void apply_signs(float2 (&R)[8], uint32_t m) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    y[i] = __fmul_rn(y[i], c);
-    if ((m >> i) & 1u) y[i] = -y[i];
+  for (int k = 0; k < 8; ++k) {
+    R[k].x = __uint_as_float(__float_as_uint(R[k].x) ^ ((m >> (2 * k)) << 31));
+    R[k].y = __uint_as_float(__float_as_uint(R[k].y) ^ ((m >> (2 * k + 1)) << 31));
   }
+}
+
+// ------------------------------------------------ whole block in-thread ---
+// A lane holding all 32 elements of a block as 16 pairs R[k] = (y[2k], y[2k+1]).
+// Butterfly stage h pairs elements (i, i + h): h = 1 within a pair (scalar),
+// h = 2, 4, 8, 16 between pairs k and k + h/2 (packed f32x2).
+__device__ __forceinline__ void stage32(float2 (&R)[16], int h) {
+  if (h == 1) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float a = R[k].x, b = R[k].y;
+      R[k] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
+    }
+  } else {
+    const int hp = h >> 1;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      if (k & hp) continue;
+      const float2 a = R[k], b = R[k + hp];
+      R[k] = f2add(a, b);
+      R[k + hp] = f2sub(a, b);
+    }
+  }
+}
+
+// y = c * H * diag(s) * x for one block held by one lane, butterflies in the
+// order h = 1, 2, 4, 8, 16, c applied last.
+__device__ __forceinline__ void hadamard32_lane(float2 (&R)[16], uint32_t sign_mask) {
+  if (sign_mask) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      R[k].x = __uint_as_float(__float_as_uint(R[k].x) ^ ((sign_mask >> (2 * k)) << 31));
+      R[k].y = __uint_as_float(__float_as_uint(R[k].y) ^ ((sign_mask >> (2 * k + 1)) << 31));
+    }
+  }
+  stage32(R, 1);
+  stage32(R, 2);
+  stage32(R, 4);
+  stage32(R, 8);
+  stage32(R, 16);
+  const float2 c = make_float2(__uint_as_float(kWhtNormBits), __uint_as_float(kWhtNormBits));
+#pragma unroll
+  for (int k = 0; k < 16; ++k) R[k] = f2mul(R[k], c);
+}
+
+__device__ __forceinline__ float absmax32(const float2 (&R)[16]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) m = max3(m, fabsf(R[k].x), fabsf(R[k].y));
+  return m;
+}
+
+__device__ __forceinline__ float warp_max(float m) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
 }
 
 // ----------------------------------------------------------------- scale ---
@@ -121,46 +241,96 @@ __device__ __forceinline__ int scale_exponent(float M, bool roundup) {
 // 2^-e as an fp32 (normal for every e in [-127, 126]).
 __device__ __forceinline__ float inv_scale(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
 
-// -------------------------------------------------------------- rounding ---
-// Nearest E2M1 code, ties to the even code, saturating at 6; sign from v.
-// Thresholds are the grid midpoints 0.25 0.75 1.25 1.75 2.5 3.5 5; a midpoint
-// whose lower neighbour has an even code rounds down (strict >), else up (>=).
-__device__ __forceinline__ uint32_t round_rtn(float v) {
-  const float a = fabsf(v);
-  uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
-               (a >= 3.5f) + (a > 5.0f);
-  return m | ((__float_as_uint(v) >> 28) & 8u);
+__device__ __forceinline__ float pair_absmax(const float2 (&R)[8]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m = max3(m, fabsf(R[k].x), fabsf(R[k].y));
+  return fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
 }
 
-// Stochastic rounding with a 16-bit draw r: a = min(|v|, 6) in [lo, hi) goes to
-// hi iff r < 2^16 * (a - lo) / (hi - lo). Every step is exact in fp32: a - lo
-// is exact (lo <= a < 2 lo or lo = 0) and the step is a power of two.
-__device__ __forceinline__ uint32_t round_sr(float v, uint32_t r16) {
-  const float a = fminf(fabsf(v), 6.0f);
-  float lo, inv_step;
-  uint32_t c0;
-  if (a < 2.0f) {
-    const float t = floorf(__fmul_rn(a, 2.0f));
-    c0 = (uint32_t)t;
-    lo = __fmul_rn(t, 0.5f);
-    inv_step = 2.0f;
-  } else if (a < 4.0f) {
-    const float t = floorf(a);
-    c0 = (uint32_t)t + 2u;
-    lo = t;
-    inv_step = 1.0f;
-  } else if (a < 6.0f) {
-    c0 = 6u;
-    lo = 4.0f;
-    inv_step = 0.5f;
-  } else {
-    c0 = 7u;
-    lo = 6.0f;
-    inv_step = 0.0f;
-  }
-  const float p = __fmul_rn(__fsub_rn(a, lo), inv_step);
-  const uint32_t up = ((float)r16 < __fmul_rn(p, 65536.0f)) ? 1u : 0u;
-  return (c0 + up) | ((__float_as_uint(v) >> 28) & 8u);
+// -------------------------------------------------------------- rounding ---
+// Round-to-nearest, ties to the even code, saturating at 6, sign kept: the
+// IEEE conversion to E2M1 (cvt.rn.satfinite), two values per instruction.
+// Returns 8 codes packed little-nibble-first (element 0 in bits 0-3).
+__device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v3, float v4,
+                                           float v5, float v6, float v7) {
+  uint32_t r;
+  asm("{.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};}"
+      : "=r"(r)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+  return r;
+}
+
+__device__ __forceinline__ uint4 encode32(const float2 (&V)[16]) {
+  return make_uint4(e2m1x8(V[0].x, V[0].y, V[1].x, V[1].y, V[2].x, V[2].y, V[3].x, V[3].y),
+                    e2m1x8(V[4].x, V[4].y, V[5].x, V[5].y, V[6].x, V[6].y, V[7].x, V[7].y),
+                    e2m1x8(V[8].x, V[8].y, V[9].x, V[9].y, V[10].x, V[10].y, V[11].x, V[11].y),
+                    e2m1x8(V[12].x, V[12].y, V[13].x, V[13].y, V[14].x, V[14].y, V[15].x, V[15].y));
+}
+
+__device__ __forceinline__ uint2 encode16(const float2 (&V)[8]) {
+  return make_uint2(e2m1x8(V[0].x, V[0].y, V[1].x, V[1].y, V[2].x, V[2].y, V[3].x, V[3].y),
+                    e2m1x8(V[4].x, V[4].y, V[5].x, V[5].y, V[6].x, V[6].y, V[7].x, V[7].y));
+}
+
+// Stochastic rounding of two scaled values with draws rf = r * 2^-16 (r a
+// 16-bit integer): a = min(|v|, 6) lies in [lo, lo + step) on the E2M1 grid;
+// it goes up iff r < 2^16 (a - lo) / step, i.e. iff a - lo > rf * step. Every
+// step is exact in fp32:
+//   step = max(1/2, 2^(E(a) - 1))  (E = unbiased exponent; 1/2 below 1),
+//   lo   = (a + C, rounded down) - C  with C = step * 2^23 (ulp of C = step),
+//   a - lo and rf * step are exact (Sterbenz; power-of-two scaling).
+// Returns the chosen grid values with v's signs; their E2M1 conversion is then
+// exact.
+__device__ __forceinline__ float2 sr_pair(float2 v, float2 rf) {
+  const float2 a = make_float2(fminf(fabsf(v.x), 6.0f), fminf(fabsf(v.y), 6.0f));
+  const float2 p2 = make_float2(__uint_as_float(__float_as_uint(a.x) & 0x7F800000u),
+                                __uint_as_float(__float_as_uint(a.y) & 0x7F800000u));
+  float2 st = f2mul(p2, make_float2(0.5f, 0.5f));
+  st = make_float2(fmaxf(st.x, 0.5f), fmaxf(st.y, 0.5f));
+  const float2 C = f2mul(st, make_float2(8388608.0f, 8388608.0f));
+  const float2 lo = f2sub(f2add_rm(a, C), C);
+  const float2 d = f2sub(a, lo);
+  const float2 th = f2mul(rf, st);
+  const float2 q = f2add(lo, make_float2(d.x > th.x ? st.x : 0.0f, d.y > th.y ? st.y : 0.0f));
+  return make_float2(__uint_as_float(__float_as_uint(q.x) | (__float_as_uint(v.x) & 0x80000000u)),
+                     __uint_as_float(__float_as_uint(q.y) | (__float_as_uint(v.y) & 0x80000000u)));
+}
+
+// The draws of a word holding two 16-bit values, as r * 2^-16 (exact).
+__device__ __forceinline__ float2 draw_pair(uint32_t w) {
+  return f2mul(make_float2((float)(w & 0xFFFFu), (float)(w >> 16)),
+               make_float2(1.0f / 65536.0f, 1.0f / 65536.0f));
+}
+
+// SR of 16 scaled values; word k of w holds the draws of pair R[k].
+__device__ __forceinline__ void sr16(float2 (&V)[8], const uint32_t (&w)[8]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) V[k] = sr_pair(V[k], draw_pair(w[k]));
+}
+
+// ------------------------------------------------------- fast division ---
+// Unsigned 32-bit division by a run-time constant d >= 1 (Granlund and
+// Montgomery, "Division by Invariant Integers using Multiplication", PLDI'94):
+// l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1, n / d = (mulhi(m, n) + n) >> l.
+struct FastDiv {
+  uint32_t d, m, l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while (l < 32 && (1ull << l) < d) ++l;
+  const uint64_t m = (((1ull << 32) * ((1ull << l) - d)) / d) + 1;
+  return FastDiv{d, (uint32_t)m, l};
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  return (uint32_t)(((uint64_t)__umulhi(f.m, n) + n) >> f.l);
 }
 
 // ------------------------------------------------------------ layouts ---
@@ -170,8 +340,6 @@ __device__ __forceinline__ int64_t mma_scale_offset(int64_t r, int64_t kb, int64
   return (((r >> 7) * (nkb >> 2) + (kb >> 2)) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2) +
          (kb & 3);
 }
-
-__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
 // E2M1 magnitude code 0..7 -> value.
 __device__ __forceinline__ float e2m1_magnitude(uint32_t m) {

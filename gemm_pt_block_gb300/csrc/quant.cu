@@ -1,8 +1,10 @@
 // quant.cu -- the fused MXFP4 quantizer, the stand-alone 32-point rotation and
-// dequantization (sm_103a). All three are HBM-bound streaming kernels: 128-bit
-// coalesced loads, the rotation's butterflies in registers with one warp
-// shuffle stage, Philox4x32-10 draws for stochastic rounding computed once per
-// 8 consecutive source elements, packed 64-bit code stores.
+// dequantization (sm_103a). All are streaming kernels bound by HBM traffic
+// once the per-element instruction count is low: 128-bit coalesced loads,
+// the rotation's butterflies in registers (packed f32x2) with one warp-shuffle
+// stage, Philox4x32-10 draws for stochastic rounding once per 8 consecutive
+// source elements with host-precomputed round keys, and the hardware E2M1
+// conversion for nearest-even rounding and for encoding.
 //
 // Method: "Block-Scaled MXFP4 With Stochastic Hadamard Rounding Matches BF16
 // Convergence on 70B Pre-Training" (paras. 1-2: E8M0 scale per 32 E2M1
@@ -15,73 +17,122 @@
 
 #include "internal.h"
 #include "mx_device.cuh"
+#include "ptx.cuh"
+#include "tma_host.h"
 
 namespace mx {
+
+void prepare_orient(OrientArgs* o) {
+  uint32_t k0 = (uint32_t)o->seed, k1 = (uint32_t)(o->seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    o->keys.k0[r] = k0;
+    o->keys.k1[r] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  const uint32_t m = o->wht ? o->sign_mask : 0u;
+  for (int u = 0; u < 2; ++u) {
+    o->sm_half[u] = (m >> (16 * u)) & 0xFFFFu;
+    // Column-orientation lanes hold block elements 4 (j / 2) + 2 u + (j % 2).
+    uint32_t inter = 0;
+    for (int j = 0; j < 16; ++j) inter |= ((m >> (4 * (j >> 1) + 2 * u + (j & 1))) & 1u) << j;
+    o->sm_inter[u] = inter;
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t b0 = (o->sm_half[u] >> (2 * k)) & 1u, b1 = (o->sm_half[u] >> (2 * k + 1)) & 1u;
+      o->xw[u][k] = (b0 << 15) | (b1 << 31);
+    }
+  }
+}
+
 namespace {
 
 constexpr int kThreads = 256;
 
 // ------------------------------------------------------------ loading ---
-// 16 consecutive elements starting at p (16-byte aligned) widened to fp32.
-__device__ __forceinline__ void load16(const uint16_t* p, float (&v)[16]) {
-  const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
-  const uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
+// The 16 consecutive inputs a lane processes, as loaded (two 128-bit loads of
+// bf16, four of fp32), so the next unit can be prefetched into registers while
+// the current one is processed.
+template <typename InT>
+struct Raw;
+template <>
+struct Raw<uint16_t> {
+  uint4 a, b;
+};
+template <>
+struct Raw<float> {
+  float4 a, b, c, d;
+};
+
+__device__ __forceinline__ void load_raw(const uint16_t* p, Raw<uint16_t>& r) {
+  r.a = __ldg(reinterpret_cast<const uint4*>(p));
+  r.b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
 }
 
-__device__ __forceinline__ void load16(const float* p, float (&v)[16]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(p) + i);
-    v[4 * i] = a.x;
-    v[4 * i + 1] = a.y;
-    v[4 * i + 2] = a.z;
-    v[4 * i + 3] = a.w;
-  }
+__device__ __forceinline__ void load_raw(const float* p, Raw<float>& r) {
+  const float4* q = reinterpret_cast<const float4*>(p);
+  r.a = __ldg(q);
+  r.b = __ldg(q + 1);
+  r.c = __ldg(q + 2);
+  r.d = __ldg(q + 3);
 }
 
-// ------------------------------------------------------- quantize core ---
-// Max-abs of a lane pair's 32-block.
-__device__ __forceinline__ float pair_max(const float (&y)[16]) {
-  float m = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(y[i]));
-  return fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+__device__ __forceinline__ void zero_raw(Raw<uint16_t>& r) { r.a = r.b = make_uint4(0, 0, 0, 0); }
+__device__ __forceinline__ void zero_raw(Raw<float>& r) {
+  r.a = r.b = r.c = r.d = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 }
 
-// Codes of 16 scaled elements, packed little-nibble-first into two words.
-// bits[j] holds element j's 16-bit draw when stochastic rounding is on.
-__device__ __forceinline__ uint2 encode16(const float (&y)[16], float is, bool sr,
-                                          const uint32_t (&bits)[16]) {
-  uint32_t lo = 0, hi = 0;
+// Widen to fp32 pairs; for bf16 the lane's sign words xw are applied to the
+// packed words first (exact sign flips of the rotation's diag(s)).
+__device__ __forceinline__ void unpack(const Raw<uint16_t>& r, float2 (&R)[8], const uint32_t* xw,
+                                       bool signs) {
+  uint32_t w[8] = {r.a.x, r.a.y, r.a.z, r.a.w, r.b.x, r.b.y, r.b.z, r.b.w};
+  if (signs) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float v = __fmul_rn(y[j], is);
-    const uint32_t code = sr ? round_sr(v, bits[j]) : round_rtn(v);
-    if (j < 8)
-      lo |= code << (4 * j);
-    else
-      hi |= code << (4 * (j - 8));
+    for (int k = 0; k < 8; ++k) w[k] ^= xw[k];
   }
-  return make_uint2(lo, hi);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    R[k] = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
 }
 
-// Draws for source elements i0 .. i0+15 (i0 % 16 == 0): two Philox calls.
-__device__ __forceinline__ void draws16(uint64_t seed, uint32_t stream, uint64_t i0,
-                                        uint32_t (&bits)[16]) {
-  const U4 a = sr_group_bits(seed, stream, i0 >> 3);
-  const U4 b = sr_group_bits(seed, stream, (i0 >> 3) + 1);
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    bits[2 * j] = w[j] & 0xFFFFu;
-    bits[2 * j + 1] = w[j] >> 16;
+__device__ __forceinline__ void unpack(const Raw<float>& r, float2 (&R)[8], const uint32_t*, bool) {
+  R[0] = make_float2(r.a.x, r.a.y); R[1] = make_float2(r.a.z, r.a.w);
+  R[2] = make_float2(r.b.x, r.b.y); R[3] = make_float2(r.b.z, r.b.w);
+  R[4] = make_float2(r.c.x, r.c.y); R[5] = make_float2(r.c.z, r.c.w);
+  R[6] = make_float2(r.d.x, r.d.y); R[7] = make_float2(r.d.z, r.d.w);
+}
+
+template <typename InT>
+__device__ __forceinline__ void load16(const InT* p, float2 (&R)[8]) {
+  Raw<InT> r;
+  load_raw(p, r);
+  unpack(r, R, nullptr, false);
+}
+
+template <typename InT>
+__device__ __forceinline__ constexpr bool is_bf16() { return sizeof(InT) == 2; }
+
+// Row-orientation processing of the 16 elements a lane holds (block half
+// `upper` of a 1x32 run): rotation, block max (optionally reduced further by
+// `reduce`), scale, rounding. Returns the packed codes; *e receives the
+// exponent. i0 = source index of the first element (for the random draws).
+template <typename InT, typename Reduce>
+__device__ __forceinline__ uint2 quantize_halves(float2 (&R)[8], int upper, const OrientArgs& o,
+                                                 uint64_t i0, Reduce reduce, int* e_out) {
+  if (o.wht) {
+    if (!is_bf16<InT>() && o.sm_half[upper]) apply_signs(R, o.sm_half[upper]);
+    hadamard_halves(R, upper);
   }
+  const float M = reduce(pair_absmax(R));
+  const int e = scale_exponent(M, o.roundup);
+  scale_all(R, inv_scale(e));
+  if (o.sr) {
+    uint32_t w[8];
+    draws16(o.keys, o.stream, i0, w);
+    sr16(R, w);
+  }
+  *e_out = e;
+  return encode16(R);
 }
 
 __device__ __forceinline__ void store_scale(const OrientArgs& o, int64_t orow, int64_t kb,
@@ -91,140 +142,301 @@ __device__ __forceinline__ void store_scale(const OrientArgs& o, int64_t orow, i
 }
 
 // ------------------------------------------------- row-wise, 1x32 blocks ---
-// One thread per 16 consecutive elements of a row; lanes (2k, 2k+1) hold one
-// 32-element block. Grid covers rows * cols / 16 threads.
+// A unit is 16 consecutive elements of a row; lanes (2k, 2k+1) hold one
+// 32-element block. Persistent grid-stride loop over `total` units (warp-
+// uniform trip count, so the pair shuffles always see both lanes), with the
+// next unit's input prefetched into registers while the current one is
+// processed.
 template <typename InT>
 __global__ void __launch_bounds__(kThreads)
-quant_rows_1x32_kernel(const InT* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
-                       OrientArgs o) {
-  const int64_t halves = cols >> 4;
-  const int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-  const bool valid = t < rows * halves;
-  const int64_t r = valid ? t / halves : 0;
-  const int64_t c0 = valid ? (t - r * halves) << 4 : 0;
-  const int half = threadIdx.x & 1;
-
-  float y[16];
-  if (valid) {
-    load16(x + r * ld + c0, y);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) y[i] = 0.0f;
-  }
-  if (o.wht) wht_forward(y, half, o.sign_mask);
-  const float M = pair_max(y);
-  const int e = scale_exponent(M, o.roundup);
-  uint32_t bits[16];
-  if (o.sr) draws16(o.seed, o.stream, (uint64_t)(r * cols + c0), bits);
-  const uint2 packed = encode16(y, inv_scale(e), o.sr, bits);
-  if (valid) {
-    *reinterpret_cast<uint2*>(o.q + r * (cols >> 1) + (c0 >> 1)) = packed;
-    if (!half) store_scale(o, r, c0 >> 5, cols >> 5, e);
+quant_rows_1x32_kernel(const InT* __restrict__ x, uint32_t total, FastDiv halves, int64_t cols,
+                       int64_t ld, const __grid_constant__ OrientArgs o) {
+  const int lane = threadIdx.x & 31, upper = threadIdx.x & 1;
+  const uint32_t stride = gridDim.x * kThreads;
+  const bool signs = o.sm_half[upper] != 0;
+  uint32_t base = blockIdx.x * kThreads + (threadIdx.x & ~31u);
+  Raw<InT> nxt;
+  auto src = [&](uint32_t u) {
+    const uint32_t r = fdiv(u, halves);
+    return x + (int64_t)r * ld + (int64_t)(u - r * halves.d) * 16;
+  };
+  if (base + lane < total) load_raw(src(base + lane), nxt); else zero_raw(nxt);
+  for (; base < total; base += stride) {
+    const uint32_t u = base + lane;
+    const bool valid = u < total;
+    const Raw<InT> cur = nxt;
+    if (u + stride < total) load_raw(src(u + stride), nxt); else zero_raw(nxt);
+    const uint32_t r = fdiv(u, halves);
+    const int64_t c0 = (int64_t)(u - r * halves.d) * 16;
+    float2 R[8];
+    unpack(cur, R, o.xw[upper], signs);
+    int e;
+    const uint2 packed = quantize_halves<InT>(R, upper, o, (uint64_t)((int64_t)r * cols + c0),
+                                              [](float m) { return m; }, &e);
+    if (valid) {
+      *reinterpret_cast<uint2*>(o.q + (int64_t)r * (cols >> 1) + (c0 >> 1)) = packed;
+      if (!upper) store_scale(o, r, c0 >> 5, cols >> 5, e);
+    }
   }
 }
 
 // --------------------------------------- 64 x 64 tiles: both orientations ---
 // Used when the column-wise output is requested or a 32x32 block is in play.
-// Phase 1 (row-major ownership, thread t: tile row t/4, columns (t%4)*16..+16)
-// loads the tile, quantizes the row-wise output, and stages fp32 values (and
-// the column orientation's random draws, keyed by source index) in shared
-// memory. Phase 2 (column ownership, thread t: tile column (t/2)%64, rows
-// (t/128)*32 + (t%2)*16 .. +16) quantizes x^T from shared memory.
-template <typename InT>
-__global__ void __launch_bounds__(kThreads)
-quant_tile_kernel(const InT* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
-                  OrientArgs orow, OrientArgs ocol, int do_row, int do_col) {
-  __shared__ float tile[64][65];
-  __shared__ uint16_t tbits[64][66];
-  __shared__ float red_r[2][2][4];
-  __shared__ float red_c[2][2][2];
+// Persistent, warp-specialized CTAs walk the 64x64 tiles of x:
+//  * warp 4 (one lane) streams tiles with TMA (cp.async.bulk.tensor, 128-byte
+//    swizzle, zero fill past the tensor's edges) into a 3-stage shared ring,
+//    guarded by full / empty mbarriers;
+//  * warps 0-3 consume. Phase 1: warp w owns the 32 x 32 block (rows 32(w%2) +
+//    lane, columns 32(w/2) ..): each lane holds one whole 1x32 run of its row,
+//    so the rotation and the 1x32 max are in-thread and the 32x32 max is one
+//    warp reduction; it writes the row-wise output (16 bytes per lane) and,
+//    for stochastic rounding of the column orientation, the draws keyed by
+//    source index (computed once when both orientations share seed and stream).
+//    Phase 2: warp w owns columns 32(w%2) + lane of rows 32(w/2) ..: the same
+//    with a lane holding a whole column run; 16 bytes per lane.
+// Bank conflicts: row reads of 8 rows hit 8 different swizzled chunks; column
+// reads of 32 lanes read one 64-byte row segment.
+constexpr int kTile = 64;
+constexpr int kStages = 3;
+constexpr int kConsumers = 128;
+constexpr int kTileThreads = kConsumers + 32;
+constexpr uint64_t kQuantWaitNs = 2000000000ull;
 
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, half = t & 1;
-  const int64_t R0 = (int64_t)blockIdx.y * 64, C0 = (int64_t)blockIdx.x * 64;
+__device__ uint32_t g_quant_error;
 
-  // ---- phase 1 ----
-  {
-    const int lr = t >> 2, lc = (t & 3) * 16;
-    const int64_t r = R0 + lr, c = C0 + lc;
-    const bool valid = r < rows && c < cols;
-    float v[16];
-    if (valid) {
-      load16(x + r * ld + c, v);
-    } else {
+// Byte offset of element (r, c) in a 64 x 64 tile as TMA lays it out with the
+// 128-byte swizzle: 128-byte rows, 16-byte chunk j of row r at chunk j ^ (r % 8).
+// fp32 tiles are two 64 x 32 boxes, 8 KB apart.
+__device__ __forceinline__ uint32_t tile_off(int r, int c, uint16_t) {
+  return (uint32_t)(r * 128 + ((((c >> 3) ^ r) & 7) << 4) + ((c & 7) << 1));
+}
+__device__ __forceinline__ uint32_t tile_off(int r, int c, float) {
+  return (uint32_t)(((c >> 5) << 13) + r * 128 + (((((c & 31) >> 2) ^ r) & 7) << 4) + ((c & 3) << 2));
+}
+
+// 32 consecutive elements (c % 32 == 0) of row r of a staged tile.
+__device__ __forceinline__ void read_run(const uint8_t* st, int r, int c, float2 (&R)[16], uint16_t) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-    }
-    if (do_col) {
+  for (int i = 0; i < 4; ++i) {
+    const uint4 q = *reinterpret_cast<const uint4*>(st + tile_off(r, c + 8 * i, uint16_t()));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-      for (int i = 0; i < 16; ++i) tile[lr][lc + i] = v[i];
-      if (ocol.sr) {
-        uint32_t bits[16];
-        draws16(ocol.seed, ocol.stream, valid ? (uint64_t)(r * cols + c) : 0ull, bits);
+    for (int k = 0; k < 4; ++k)
+      R[4 * i + k] = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+  }
+}
+__device__ __forceinline__ void read_run(const uint8_t* st, int r, int c, float2 (&R)[16], float) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) tbits[lr][lc + i] = (uint16_t)bits[i];
-      }
-    }
-    if (do_row) {
-      if (orow.wht) wht_forward(v, half, orow.sign_mask);
-      float M = pair_max(v);
-      if (orow.block) {
-        // 32x32: max over the 8 rows of this warp (lane bits 2..4), then over
-        // the 4 warps of the 32-row group.
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 8));
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
-        if (lane == 0 || lane == 2) red_r[warp >> 2][lane >> 1][warp & 3] = M;
-        __syncthreads();
-        const float* rr = red_r[warp >> 2][(t & 3) >> 1];
-        M = fmaxf(fmaxf(rr[0], rr[1]), fmaxf(rr[2], rr[3]));
-      }
-      const int e = scale_exponent(M, orow.roundup);
-      uint32_t bits[16];
-      if (orow.sr) draws16(orow.seed, orow.stream, (uint64_t)(r * cols + c), bits);
-      const uint2 packed = encode16(v, inv_scale(e), orow.sr, bits);
-      if (valid) {
-        *reinterpret_cast<uint2*>(orow.q + r * (cols >> 1) + (c >> 1)) = packed;
-        if (!half) store_scale(orow, r, c >> 5, cols >> 5, e);
+  for (int i = 0; i < 8; ++i) {
+    const float4 q = *reinterpret_cast<const float4*>(st + tile_off(r, c + 4 * i, 0.0f));
+    R[2 * i] = make_float2(q.x, q.y);
+    R[2 * i + 1] = make_float2(q.z, q.w);
+  }
+}
+// 32 consecutive rows (r % 32 == 0) of column c of a staged tile.
+__device__ __forceinline__ void read_col(const uint8_t* st, int r, int c, float2 (&R)[16], uint16_t) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t a = *reinterpret_cast<const uint16_t*>(st + tile_off(r + 2 * k, c, uint16_t()));
+    const uint32_t b = *reinterpret_cast<const uint16_t*>(st + tile_off(r + 2 * k + 1, c, uint16_t()));
+    R[k] = make_float2(__uint_as_float(a << 16), __uint_as_float(b << 16));
+  }
+}
+__device__ __forceinline__ void read_col(const uint8_t* st, int r, int c, float2 (&R)[16], float) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k)
+    R[k] = make_float2(*reinterpret_cast<const float*>(st + tile_off(r + 2 * k, c, 0.0f)),
+                       *reinterpret_cast<const float*>(st + tile_off(r + 2 * k + 1, c, 0.0f)));
+}
+
+__device__ __forceinline__ bool same_draws(const OrientArgs& a, const OrientArgs& b) {
+  return a.sr && b.sr && a.seed == b.seed && a.stream == b.stream;
+}
+
+// Draw words for 32 consecutive source elements i0 .. i0 + 31 (i0 % 32 == 0).
+__device__ __forceinline__ void draws32(const PhiloxKeys& k, uint32_t stream, uint64_t i0,
+                                        uint32_t (&w)[16]) {
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const uint64_t g = (i0 >> 3) + h;
+    const U4 a = philox4x32_10(U4{(uint32_t)g, (uint32_t)(g >> 32), stream, 0u}, k);
+    w[4 * h] = a.x; w[4 * h + 1] = a.y; w[4 * h + 2] = a.z; w[4 * h + 3] = a.w;
+  }
+}
+
+// Scale, round and encode one 32-run whose max-abs is M.
+__device__ __forceinline__ uint4 finish32(float2 (&R)[16], const OrientArgs& o, float M,
+                                          const uint32_t (&w)[16], int* e_out) {
+  const int e = scale_exponent(M, o.roundup);
+  const float2 is = make_float2(inv_scale(e), inv_scale(e));
+#pragma unroll
+  for (int k = 0; k < 16; ++k) R[k] = f2mul(R[k], is);
+  if (o.sr) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) R[k] = sr_pair(R[k], draw_pair(w[k]));
+  }
+  *e_out = e;
+  return encode32(R);
+}
+
+__device__ __forceinline__ void named_sync_consumers() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+// Bounded wait; false on timeout (which also raises the CTA's abort flag and
+// the library error word) or when the CTA has already aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t par, uint32_t* abort_flag) {
+  if (ptx::mbar_try_wait(bar, par)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ptx::mbar_try_wait(bar, par)) return true;
+    if ((i & 63u) == 0) {
+      if (*reinterpret_cast<volatile uint32_t*>(abort_flag)) return false;
+      if (ptx::globaltimer_ns() - t0 > kQuantWaitNs) {
+        *reinterpret_cast<volatile uint32_t*>(abort_flag) = 1u;
+        atomicExch(&g_quant_error, 6u);  // MXFP4_ERR_TIMEOUT
+        return false;
       }
     }
   }
-  if (!do_col) return;
+}
+
+template <typename InT>
+__global__ void __launch_bounds__(kTileThreads, 4)
+quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols,
+                  uint32_t ntiles, FastDiv tiles_x, const __grid_constant__ OrientArgs orow,
+                  const __grid_constant__ OrientArgs ocol, int do_row, int do_col) {
+  constexpr uint32_t kStageBytes = kTile * kTile * sizeof(InT);
+  constexpr uint32_t kBitsBytes = kTile * kTile * 2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* tbits0 = sm + kStages * kStageBytes;   // two draw buffers, swizzled like bf16 tiles
+  uint64_t* full = reinterpret_cast<uint64_t*>(tbits0 + 2 * kBitsBytes);
+  uint64_t* empty = full + kStages;
+  uint32_t* abort_flag = reinterpret_cast<uint32_t*>(empty + kStages);
+
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  auto origin = [&](uint32_t tl, int64_t& R0, int64_t& C0) {
+    const uint32_t ty = fdiv(tl, tiles_x);
+    R0 = (int64_t)ty * kTile;
+    C0 = (int64_t)(tl - ty * tiles_x.d) * kTile;
+  };
+
+  if (t == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&empty[s]), kConsumers / 32);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
   __syncthreads();
 
-  // ---- phase 2: the column orientation (quantization along rows) ----
-  {
-    const int cc = (t >> 1) & 63, rb = t >> 7;
-    const int lr0 = rb * 32 + half * 16;
-    const int64_t oc = C0 + cc, k0 = R0 + lr0;
-    const bool valid = oc < cols && k0 < rows;
-    float v[16];
+  if (warp == kConsumers / 32) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tmx);
+      uint32_t j = 0;
+      for (uint32_t tl = blockIdx.x; tl < ntiles; tl += gridDim.x, ++j) {
+        const int s = (int)(j % kStages);
+        if (j >= kStages &&
+            !wait_or_abort(ptx::smem_u32(&empty[s]), ((j / kStages) - 1) & 1u, abort_flag))
+          break;
+        int64_t R0, C0;
+        origin(tl, R0, C0);
+        const uint32_t bar = ptx::smem_u32(&full[s]);
+        const uint32_t dst = ptx::smem_u32(sm + s * kStageBytes);
+        ptx::mbar_arrive_expect_tx(bar, kStageBytes);
+        ptx::tma_load_2d(dst, &tmx, (int32_t)C0, (int32_t)R0, bar);
+        if (sizeof(InT) == 4) ptx::tma_load_2d(dst + 8192, &tmx, (int32_t)C0 + 32, (int32_t)R0, bar);
+      }
+      // After an abort, wait (bounded) for the loads still in flight.
+      if (*reinterpret_cast<volatile uint32_t*>(abort_flag)) {
+        for (uint32_t q = (j > kStages ? j - kStages : 0); q < j; ++q) {
+          const uint32_t bar = ptx::smem_u32(&full[q % kStages]);
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (!ptx::mbar_try_wait(bar, (q / kStages) & 1u))
+            if (ptx::globaltimer_ns() - t0 > kQuantWaitNs / 8) break;
+        }
+      }
+    }
+    return;
+  }
+
+  // --------------------------------------------------------------- consumers
+  const bool share = do_row && do_col && same_draws(orow, ocol);
+  uint32_t j = 0;
+  for (uint32_t tl = blockIdx.x; tl < ntiles; tl += gridDim.x, ++j) {
+    const int s = (int)(j % kStages);
+    const uint8_t* st = sm + s * kStageBytes;
+    uint8_t* tb = tbits0 + (j & 1) * kBitsBytes;
+    int ok = 0;
+    if (lane == 0) ok = wait_or_abort(ptx::smem_u32(&full[s]), (j / kStages) & 1u, abort_flag);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    int64_t R0, C0;
+    origin(tl, R0, C0);
+
+    // ---- phase 1: rows ----
+    if (ok) {
+      const int rl = 32 * (warp & 1) + lane, cl = 32 * (warp >> 1);
+      const int64_t r = R0 + rl, c = C0 + cl;
+      const bool valid = r < rows && c < cols;
+      float2 R[16];
+      read_run(st, rl, cl, R, InT());
+      uint32_t w[16];
+      if (do_col && ocol.sr) {
+        draws32(ocol.keys, ocol.stream, (uint64_t)(r * cols + c), w);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = tile[lr0 + i][cc];
-    if (ocol.wht) wht_forward(v, half, ocol.sign_mask);
-    float M = pair_max(v);
-    if (ocol.block) {
-      // 32x32: max over the 16 columns of this warp (lane bits 1..4), then
-      // over the 2 warps holding the block's 32 columns.
-      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
-      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 8));
-      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
-      if (lane == 0) red_c[rb][(warp & 3) >> 1][warp & 1] = M;
-      __syncthreads();
-      const float* rc = red_c[rb][(warp & 3) >> 1];
-      M = fmaxf(rc[0], rc[1]);
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(tb + tile_off(rl, cl + 8 * i, uint16_t())) =
+              make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      }
+      if (do_row) {
+        if (orow.wht) hadamard32_lane(R, orow.sign_mask);
+        float M = absmax32(R);
+        if (orow.block) M = warp_max(M);
+        if (orow.sr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
+        int e;
+        const uint4 packed = finish32(R, orow, M, w, &e);
+        if (valid) {
+          *reinterpret_cast<uint4*>(orow.q + r * (cols >> 1) + (c >> 1)) = packed;
+          store_scale(orow, r, c >> 5, cols >> 5, e);
+        }
+      }
     }
-    const int e = scale_exponent(M, ocol.roundup);
-    uint32_t bits[16];
-    if (ocol.sr) {
+
+    // ---- phase 2: columns (quantization of x^T along rows) ----
+    if (do_col) {
+      if (ocol.sr) named_sync_consumers();   // the draws were written by other warps
+      if (ok) {
+        const int cl = 32 * (warp & 1) + lane, rl = 32 * (warp >> 1);
+        const int64_t oc = C0 + cl, k0 = R0 + rl;
+        const bool valid = oc < cols && k0 < rows;
+        float2 R[16];
+        read_col(st, rl, cl, R, InT());
+        if (ocol.wht) hadamard32_lane(R, ocol.sign_mask);
+        float M = absmax32(R);
+        if (ocol.block) M = warp_max(M);
+        uint32_t w[16];
+        if (ocol.sr) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) bits[i] = tbits[lr0 + i][cc];
+          for (int k = 0; k < 16; ++k) {
+            const uint32_t a = *reinterpret_cast<const uint16_t*>(tb + tile_off(rl + 2 * k, cl, uint16_t()));
+            const uint32_t b = *reinterpret_cast<const uint16_t*>(tb + tile_off(rl + 2 * k + 1, cl, uint16_t()));
+            w[k] = a | (b << 16);
+          }
+        }
+        int e;
+        const uint4 packed = finish32(R, ocol, M, w, &e);
+        if (valid) {
+          *reinterpret_cast<uint4*>(ocol.q + oc * (rows >> 1) + (k0 >> 1)) = packed;
+          store_scale(ocol, oc, k0 >> 5, rows >> 5, e);
+        }
+      }
     }
-    const uint2 packed = encode16(v, inv_scale(e), ocol.sr, bits);
-    if (valid) {
-      *reinterpret_cast<uint2*>(ocol.q + oc * (rows >> 1) + (k0 >> 1)) = packed;
-      if (!half) store_scale(ocol, oc, k0 >> 5, rows >> 5, e);
-    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[s]));
   }
 }
 
@@ -238,22 +450,22 @@ hadamard32_kernel(const InT* __restrict__ x, int64_t rows, int64_t cols, int64_t
   const bool valid = t < rows * halves;
   const int64_t r = valid ? t / halves : 0;
   const int64_t c0 = valid ? (t - r * halves) << 4 : 0;
-  const int half = threadIdx.x & 1;
-  float v[16];
+  const int upper = threadIdx.x & 1;
+  const uint32_t m = (sign_mask >> (16 * upper)) & 0xFFFFu;
+  float2 R[8];
   if (valid) {
-    load16(x + r * ld + c0, v);
+    load16(x + r * ld + c0, R);
   } else {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+    for (int k = 0; k < 8; ++k) R[k] = make_float2(0.0f, 0.0f);
   }
-  if (inverse)
-    wht_inverse(v, half, sign_mask);
-  else
-    wht_forward(v, half, sign_mask);
+  if (!inverse) apply_signs(R, m);
+  hadamard_halves(R, upper);
+  if (inverse) apply_signs(R, m);
   if (valid) {
     float4* out = reinterpret_cast<float4*>(y + r * cols + c0);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) out[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    for (int i = 0; i < 4; ++i) out[i] = make_float4(R[2 * i].x, R[2 * i].y, R[2 * i + 1].x, R[2 * i + 1].y);
   }
 }
 
@@ -286,21 +498,57 @@ dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int
 
 inline unsigned blocks_for(int64_t threads) { return (unsigned)((threads + kThreads - 1) / kThreads); }
 
+// Persistent grids: as many CTAs as can be resident (queried once per device
+// and kernel), never more than there are work items.
+template <typename K>
+unsigned resident_ctas(K kernel, int64_t items, int smem, int threads) {
+  static int per_sm[64] = {0};
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  dev &= 63;
+  if (!per_sm[dev]) {
+    cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    int n = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
+    per_sm[dev] = n > 0 ? n : 1;
+  }
+  const int64_t want = (int64_t)per_sm[dev] * sms[dev];
+  return (unsigned)(items < want ? items : want);
+}
+
 template <typename InT>
 cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
                           const OrientArgs* row, const OrientArgs* col, cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   const bool tile = col != nullptr || (row && row->block);
   if (!tile) {
-    quant_rows_1x32_kernel<InT><<<blocks_for(rows * (cols >> 4)), kThreads, 0, st>>>(
-        x, rows, cols, ld, *row);
-  } else {
-    OrientArgs dummy{};
-    dim3 grid((unsigned)((cols + 63) / 64), (unsigned)((rows + 63) / 64));
-    quant_tile_kernel<InT><<<grid, kThreads, 0, st>>>(x, rows, cols, ld, row ? *row : dummy,
-                                                      col ? *col : dummy, row != nullptr,
-                                                      col != nullptr);
+    const int64_t total = rows * (cols >> 4);
+    const unsigned grid =
+        resident_ctas(quant_rows_1x32_kernel<InT>, (total + kThreads - 1) / kThreads, 0, kThreads);
+    quant_rows_1x32_kernel<InT><<<grid, kThreads, 0, st>>>(
+        x, (uint32_t)total, make_fastdiv((uint32_t)(cols >> 4)), cols, ld, *row);
+    return cudaGetLastError();
   }
+  CUtensorMap tm;
+  const bool bf = sizeof(InT) == 2;
+  if (!make_tma_2d(&tm, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                   sizeof(InT), x, rows, cols, ld, kTile, bf ? 64 : 32))
+    return cudaErrorInvalidValue;
+  constexpr int smem = kStages * kTile * kTile * sizeof(InT) + 2 * kTile * kTile * 2 + 256 + 1024;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_set[dev & 63]) {
+    cudaFuncSetAttribute(quant_tile_kernel<InT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attr_set[dev & 63] = true;
+  }
+  OrientArgs dummy{};
+  const int64_t tx = (cols + kTile - 1) / kTile, ty = (rows + kTile - 1) / kTile;
+  const unsigned grid = resident_ctas(quant_tile_kernel<InT>, tx * ty, smem, kTileThreads);
+  quant_tile_kernel<InT><<<grid, kTileThreads, smem, st>>>(
+      tm, rows, cols, (uint32_t)(tx * ty), make_fastdiv((uint32_t)tx), row ? *row : dummy,
+      col ? *col : dummy, row != nullptr, col != nullptr);
   return cudaGetLastError();
 }
 
@@ -323,6 +571,15 @@ cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t 
     hadamard32_kernel<uint16_t><<<nb, kThreads, 0, st>>>(static_cast<const uint16_t*>(x), rows,
                                                          cols, ld, sign_mask, inverse, y);
   return cudaGetLastError();
+}
+
+cudaError_t read_quant_error(uint32_t* err) {
+  cudaError_t e = cudaMemcpyFromSymbol(err, g_quant_error, sizeof(uint32_t));
+  if (e == cudaSuccess && *err) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_quant_error, &zero, sizeof(uint32_t));
+  }
+  return e;
 }
 
 cudaError_t launch_dequantize(const uint8_t* q, const uint8_t* s, bool mma_layout, int64_t rows,

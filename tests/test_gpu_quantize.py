@@ -68,6 +68,13 @@ def test_quantize_mixed_orientation_params():
     for lr, lc in [(0, 0), (1, 1), (0, 1)]:
         assert_same(gpu_quantize(x.to(DEV), pr, pc, lr, lc),
                     oracle_quantize(synth.bf16_bits(x), pr, pc, lr, lc), "mixed")
+    # both orientations stochastic: separate draws (different streams or seeds) and shared draws
+    for pr2 in [oracle.Params(block=oracle.BLOCK_32X32, rounding=oracle.ROUND_SR, seed=1, sr_stream=2),
+                oracle.Params(rounding=oracle.ROUND_SR, seed=2, sr_stream=1),
+                oracle.Params(block=oracle.BLOCK_32X32, scale_mode=oracle.SCALE_ROUNDUP,
+                              rounding=oracle.ROUND_SR, seed=1, sr_stream=1)]:
+        assert_same(gpu_quantize(x.to(DEV), pr2, pc, 1, 1),
+                    oracle_quantize(synth.bf16_bits(x), pr2, pc, 1, 1), "both SR")
 
 
 @pytest.mark.parametrize("shape", [(32, 32), (64, 96), (96, 32), (32, 4096), (4128, 64)])
@@ -223,3 +230,32 @@ def test_quantize_is_deterministic_across_calls_and_streams():
     torch.cuda.synchronize()
     for u, v in zip(a, b):
         assert torch.equal(u, v)
+
+
+def test_nearest_even_dense_fp32_sweep():
+    """Scaled values v in (-8, 8): every 256th fp32 pattern, plus 2048 ulps either
+    side of every grid point and midpoint, both signs. A 4.0 in each block pins
+    the floor-mode scale to 2^0, so v = x and values above 6 saturate. Both
+    nearest-even and stochastic rounding must match the oracle exactly."""
+    coarse = np.arange(0, 0x41000000, 256, dtype=np.uint32)
+    pts = np.array([0, .25, .5, .75, 1, 1.25, 1.5, 1.75, 2, 2.5, 3, 3.5, 4, 5, 6, 7], dtype=np.float32)
+    fine = (pts.view(np.uint32)[:, None].astype(np.int64) + np.arange(-2048, 2049)[None, :]).reshape(-1)
+    fine = fine[(fine >= 0) & (fine < 0x41000000)].astype(np.uint32)
+    vals = np.concatenate([coarse, fine]).view(np.float32)
+    vals = np.concatenate([vals, -vals])
+    n_blk = (vals.size + 30) // 31
+    body = np.zeros(n_blk * 31, dtype=np.float32)
+    body[: vals.size] = vals
+    blocks = np.hstack([np.full((n_blk, 1), 4.0, np.float32), body.reshape(n_blk, 31)])
+    cols = 4096
+    n_rows = (blocks.size + cols - 1) // cols
+    n_rows = (n_rows + 31) // 32 * 32
+    flat = np.full(n_rows * cols, 4.0, dtype=np.float32)
+    flat[: blocks.size] = blocks.reshape(-1)
+    x = flat.reshape(n_rows, cols)
+    xt = torch.from_numpy(x).to(DEV)
+    for p in [oracle.Params(), oracle.Params(rounding=oracle.ROUND_SR, seed=5, sr_stream=9)]:
+        got = gpu_quantize(xt, p, None)
+        want = oracle_quantize(x, p, None)
+        assert np.all(want[1] == 127)
+        assert_same(got, want, "dense fp32 sweep")
