@@ -63,15 +63,18 @@ static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle align
 
 __device__ uint32_t g_gemm_error;
 
-struct Ctl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+// Barriers and flags of one CTA; S = pipeline depth of the kernel using it.
+template <int S>
+struct CtlT {
+  uint64_t full[S];
+  uint64_t empty[S];
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
 };
+using Ctl = CtlT<STAGES>;
 static_assert(sizeof(Ctl) <= CTL_BYTES, "control block");
 
 // Instruction descriptor, kind::mxf4 block-scaled: E2M1 A and B (format 1 at
@@ -83,7 +86,8 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
          ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
 }
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl* ctl) {
+template <int S>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, CtlT<S>* ctl) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
@@ -283,6 +287,206 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   }
 }
 
+// ============================================================ CTA pairs ===
+// The same GEMM on CTA pairs (a cluster of 2, tcgen05 cta_group::2): a pair
+// computes a 256 x 256 output tile. CTA r loads rows 128 r .. of the pair's A
+// rows and rows 128 r .. of its B rows, so each SM stages 128 + 128 rows per
+// K-step instead of 128 + 256; the leader (rank 0) issues M = 256 MMAs that
+// read both CTAs' shared memory, and each CTA's tensor memory receives its
+// 128 x 256 fp32 accumulator. Scales: each CTA stages its own 128 rows of A
+// scales and all 256 rows of B scales (tensor-memory columns as in the 1-CTA
+// kernel); the leader copies them to tensor memory with tcgen05.cp.cta_group::2.
+// All loads of a stage (both CTAs) are counted on the leader's full barrier;
+// the leader's commits are multicast to both CTAs' empty / accumulator-full
+// barriers; both CTAs' epilogues arrive on the leader's accumulator-empty
+// barrier.
+namespace pair {
+constexpr int BM = 128;                        // rows of A per CTA
+constexpr int BNP = 256;                       // N of the pair tile
+constexpr int BNH = 128;                       // rows of B per CTA
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BKB;              // 16 KB
+constexpr int B_BYTES = BNH * BKB;             // 16 KB
+constexpr int SFA_BYTES = BM * (BK / 32);      // 1 KB
+constexpr int SFB_BYTES = BNP * (BK / 32);     // 2 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr uint32_t TX_BYTES = 2 * STAGE_BYTES; // both CTAs' loads land on the leader's barrier
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + CTL_BYTES + 1024;
+static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
+using Ctl = CtlT<STAGES>;
+static_assert(sizeof(Ctl) <= CTL_BYTES, "control block");
+
+__device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
+  return (sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(256 >> 4) << 24) | (sf_id << 29);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                      float* __restrict__ C, int64_t ldc, int M, int N, int K, int group_m) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int num_m = M / (2 * BM), num_n = N / BNP, num_k = K / BK;
+  const int num_tiles = num_m * num_n;
+  const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&ctl->full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&ctl->empty[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&ctl->acc_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&ctl->acc_empty), 2 * NUM_EPI_WARPS);
+    ptx::mbar_init(ptx::smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB);
+    ptx::prefetch_tensormap(&tmSA);
+    ptx::prefetch_tensormap(&tmSB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(&ctl->tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();        // both CTAs' barriers initialised before any remote signal
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, issued_rounds = 0;
+      bool ok = true;
+      for (int tile = pair_id; ok && tile < num_tiles; tile += num_pairs) {
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, group_m, mb, nb);
+        const int a_row = mb * 2 * BM + (int)rank * BM;
+        const int b_row = nb * BNP + (int)rank * BNH;
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!(ok = wait_bar(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl))) break;
+          const uint32_t full_local = ptx::smem_u32(&ctl->full[stage]);
+          const uint32_t full_leader = ptx::mapa(full_local, 0);
+          if (leader) ptx::mbar_arrive_expect_tx(full_local, TX_BYTES);
+          const uint32_t st = ptx::smem_u32(smem + stage * STAGE_BYTES);
+          ptx::tma_load_2d_pair(st, &tmA, kb * BKB, a_row, full_leader);
+          ptx::tma_load_2d_pair(st + A_BYTES, &tmB, kb * BKB, b_row, full_leader);
+          ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES, &tmSA, 0, 2 * kb, a_row / 128, full_leader);
+          ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES + SFA_BYTES, &tmSB, 0, 2 * kb, nb * 2,
+                                full_leader);
+          ++issued_rounds;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Wait until the leader's commits have released every stage this CTA
+      // filled, so no remote arrive targets this CTA after it exits.
+      for (int s = 0; s < STAGES; ++s) {
+        const uint32_t n = issued_rounds / STAGES + ((uint32_t)s < issued_rounds % STAGES ? 1u : 0u);
+        if (n) drain_wait(ptx::smem_u32(&ctl->empty[s]), (n - 1) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (leader && lane == 0) {
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair_id; ok && tile < num_tiles; tile += num_pairs) {
+        if (!(ok = wait_bar(ptx::smem_u32(&ctl->acc_empty), acc_phase ^ 1u, ctl))) break;
+        ptx::tc_fence_after();
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!(ok = wait_bar(ptx::smem_u32(&ctl->full[stage]), phase, ctl))) break;
+          ptx::tc_fence_after();
+          const uint32_t st = ptx::smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sfa_s = st + A_BYTES + B_BYTES;
+          const uint32_t sfb_s = sfa_s + SFA_BYTES;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            ptx::tc_cp_pair_32x128b_warpx4(tmem + SFA_COL + 4 * c,
+                                           ptx::smem_desc(sfa_s + c * 512, 0, 128, 0));
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+              ptx::tc_cp_pair_32x128b_warpx4(tmem + SFB_COL + 8 * c + 4 * t,
+                                             ptx::smem_desc(sfb_s + t * 1024 + c * 512, 0, 128, 0));
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
+            const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
+            ptx::mma_mxf4_pair(tmem + ACC_COL, ad, bd, make_idesc((k & 1) * 2),
+                               tmem + SFA_COL + 4 * (k >> 1), tmem + SFB_COL + 8 * (k >> 1),
+                               (kb | k) != 0);
+          }
+          ptx::tc_commit_pair_multicast(ptx::smem_u32(&ctl->empty[stage]), 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::tc_commit_pair_multicast(ptx::smem_u32(&ctl->acc_full), 0x3);
+        acc_phase ^= 1u;
+      }
+      ptx::tc_commit_pair_multicast(ptx::smem_u32(&ctl->drain), 0x1);
+      drain_wait(ptx::smem_u32(&ctl->drain), 0);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const uint32_t acc_empty_leader = ptx::mapa(ptx::smem_u32(&ctl->acc_empty), 0);
+    uint32_t acc_phase = 0;
+    for (int tile = pair_id; tile < num_tiles; tile += num_pairs) {
+      int mb, nb;
+      tile_coords(tile, num_m, num_n, group_m, mb, nb);
+      int ok = 0;
+      if (lane == 0) ok = wait_bar(ptx::smem_u32(&ctl->acc_full), acc_phase, ctl);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      ptx::tc_fence_after();
+      uint32_t r0[64], r1[64];
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + ACC_COL + h * 128;
+      ptx::tmem_ld_32x32b_x64(taddr, r0);
+      ptx::tmem_ld_32x32b_x64(taddr + 64, r1);
+      ptx::tc_wait_ld();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(acc_empty_leader);
+      acc_phase ^= 1u;
+      const int64_t row = (int64_t)mb * 2 * BM + rank * BM + q * 32 + lane;
+      float4* dst = reinterpret_cast<float4*>(C + row * ldc + (int64_t)nb * BNP + h * 128);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        dst[j] = make_float4(__uint_as_float(r0[4 * j]), __uint_as_float(r0[4 * j + 1]),
+                             __uint_as_float(r0[4 * j + 2]), __uint_as_float(r0[4 * j + 3]));
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        dst[16 + j] = make_float4(__uint_as_float(r1[4 * j]), __uint_as_float(r1[4 * j + 1]),
+                                  __uint_as_float(r1[4 * j + 2]), __uint_as_float(r1[4 * j + 3]));
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();        // the leader's MMAs and the peer's epilogue are both done
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+  }
+}
+}  // namespace pair
+
 // ---------------------------------------------------------------- host ---
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -310,6 +514,20 @@ bool make_code_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t kb
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale array in the tensor-core layout as a 3-D tensor of 32-bit words:
+// [rows/128 bands][K/128 tiles][128 words (512 bytes)]; a box covers 2 tiles
+// (one 256-deep K stage) of `bands` consecutive bands.
+bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t K, uint32_t bands) {
+  const cuuint64_t dims[3] = {128, (cuuint64_t)(K / 128), (cuuint64_t)(rows / 128)};
+  const cuuint64_t strides[2] = {512, (cuuint64_t)(K / 128) * 512};
+  const cuuint32_t box[3] = {128, 2, bands};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct DevInfo {
   int sms = 0;
   int major = 0;
@@ -324,9 +542,12 @@ DevInfo& dev_info(int dev) {
   if (!d.attr_set) {
     cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
-    if (d.major == 10)
+    if (d.major == 10) {
       cudaFuncSetAttribute(mxf4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_BYTES);
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           pair::SMEM_BYTES);
+    }
     d.attr_set = true;
   }
   return d;
@@ -350,6 +571,23 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
     return cudaErrorNotSupported;
   }
   CUtensorMap ta, tb;
+  if (M % 256 == 0) {
+    // CTA pairs: 256 x 256 tiles.
+    CUtensorMap tsa, tsb;
+    if (!make_code_map(&ta, qa, M, K / 2, pair::BM) || !make_code_map(&tb, qb, N, K / 2, pair::BNH) ||
+        !make_scale_map(&tsa, sa, M, K, 1) || !make_scale_map(&tsb, sb, N, K, 2)) {
+      *why = "cuTensorMapEncodeTiled rejected the operand layout";
+      return cudaErrorInvalidValue;
+    }
+    const int num_tiles = (int)((M / 256) * (N / pair::BNP));
+    const int pairs = d.sms / 2;
+    const int grid = 2 * (num_tiles < pairs ? num_tiles : pairs);
+    int64_t gm = kGroupBytes / (256 * (K / 2));
+    gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
+    pair::mxf4_gemm_pair_kernel<<<grid, THREADS, pair::SMEM_BYTES, st>>>(
+        ta, tb, tsa, tsb, c, ldc, (int)M, (int)N, (int)K, (int)gm);
+    return cudaGetLastError();
+  }
   if (!make_code_map(&ta, qa, M, K / 2, BM) || !make_code_map(&tb, qb, N, K / 2, BN)) {
     *why = "cuTensorMapEncodeTiled rejected the operand layout";
     return cudaErrorInvalidValue;
