@@ -86,13 +86,19 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
          ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
 }
 
+// Bounded wait; after kWaitLimitNs in total the CTA aborts. With `sleep` each
+// try_wait may suspend the thread until the phase completes (used by the
+// epilogue, whose waits are off the critical path); the producer and MMA
+// threads poll, which wakes them with the least latency.
 template <int S>
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, CtlT<S>* ctl) {
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, CtlT<S>* ctl,
+                                         bool sleep = false) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
+    if (sleep ? ptx::mbar_try_wait_sleep(bar, parity, 200000u) : ptx::mbar_try_wait(bar, parity))
+      return true;
+    if (sleep || (i & 63u) == 0) {
       if (*reinterpret_cast<volatile uint32_t*>(&ctl->abort)) return false;
       if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
         *reinterpret_cast<volatile uint32_t*>(&ctl->abort) = 1u;
@@ -254,7 +260,7 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       // One lane waits; the verdict is broadcast so the warp stays converged
       // for the .sync.aligned tensor-memory loads.
       int ok = 0;
-      if (lane == 0) ok = wait_bar(ptx::smem_u32(&ctl->acc_full), acc_phase, ctl);
+      if (lane == 0) ok = wait_bar(ptx::smem_u32(&ctl->acc_full), acc_phase, ctl, true);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       ptx::tc_fence_after();
       uint32_t r0[64], r1[64];
@@ -452,7 +458,7 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       int mb, nb;
       tile_coords(tile, num_m, num_n, group_m, mb, nb);
       int ok = 0;
-      if (lane == 0) ok = wait_bar(ptx::smem_u32(&ctl->acc_full), acc_phase, ctl);
+      if (lane == 0) ok = wait_bar(ptx::smem_u32(&ctl->acc_full), acc_phase, ctl, true);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       ptx::tc_fence_after();
       uint32_t r0[64], r1[64];

@@ -233,20 +233,34 @@ __device__ __forceinline__ void read_run(const uint8_t* st, int r, int c, float2
     R[2 * i + 1] = make_float2(q.z, q.w);
   }
 }
-// 32 consecutive rows (r % 32 == 0) of column c of a staged tile.
-__device__ __forceinline__ void read_col(const uint8_t* st, int r, int c, float2 (&R)[16], uint16_t) {
+// Column reads: for rows r0 + 8 j + t (r0 % 8 == 0) of column c the swizzle
+// term depends on t only, so a lane keeps eight byte offsets o[t] (row r0 + t)
+// and reaches row r0 + 8 j + t at o[t] + 1024 j (an immediate).
+__device__ __forceinline__ void col_offsets(int r0, int c, uint32_t (&o)[8], uint16_t) {
+#pragma unroll
+  for (int t = 0; t < 8; ++t) o[t] = tile_off(r0 + t, c, uint16_t());
+}
+__device__ __forceinline__ void col_offsets(int r0, int c, uint32_t (&o)[8], float) {
+#pragma unroll
+  for (int t = 0; t < 8; ++t) o[t] = tile_off(r0 + t, c, 0.0f);
+}
+
+// 32 consecutive rows (o from col_offsets for the run's first row) of a column.
+__device__ __forceinline__ void read_col(const uint8_t* st, const uint32_t (&o)[8], float2 (&R)[16],
+                                         uint16_t) {
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
-    const uint32_t a = *reinterpret_cast<const uint16_t*>(st + tile_off(r + 2 * k, c, uint16_t()));
-    const uint32_t b = *reinterpret_cast<const uint16_t*>(st + tile_off(r + 2 * k + 1, c, uint16_t()));
+    const uint32_t a = *reinterpret_cast<const uint16_t*>(st + o[(2 * k) & 7] + 1024 * (k >> 2));
+    const uint32_t b = *reinterpret_cast<const uint16_t*>(st + o[(2 * k + 1) & 7] + 1024 * (k >> 2));
     R[k] = make_float2(__uint_as_float(a << 16), __uint_as_float(b << 16));
   }
 }
-__device__ __forceinline__ void read_col(const uint8_t* st, int r, int c, float2 (&R)[16], float) {
+__device__ __forceinline__ void read_col(const uint8_t* st, const uint32_t (&o)[8], float2 (&R)[16],
+                                         float) {
 #pragma unroll
   for (int k = 0; k < 16; ++k)
-    R[k] = make_float2(*reinterpret_cast<const float*>(st + tile_off(r + 2 * k, c, 0.0f)),
-                       *reinterpret_cast<const float*>(st + tile_off(r + 2 * k + 1, c, 0.0f)));
+    R[k] = make_float2(*reinterpret_cast<const float*>(st + o[(2 * k) & 7] + 1024 * (k >> 2)),
+                       *reinterpret_cast<const float*>(st + o[(2 * k + 1) & 7] + 1024 * (k >> 2)));
 }
 
 __device__ __forceinline__ bool same_draws(const OrientArgs& a, const OrientArgs& b) {
@@ -288,9 +302,9 @@ __device__ __forceinline__ void named_sync_consumers() {
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t par, uint32_t* abort_flag) {
   if (ptx::mbar_try_wait(bar, par)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (ptx::mbar_try_wait(bar, par)) return true;
-    if ((i & 63u) == 0) {
+  for (;;) {
+    if (ptx::mbar_try_wait_sleep(bar, par, 500000u)) return true;
+    {
       if (*reinterpret_cast<volatile uint32_t*>(abort_flag)) return false;
       if (ptx::globaltimer_ns() - t0 > kQuantWaitNs) {
         *reinterpret_cast<volatile uint32_t*>(abort_flag) = 1u;
@@ -414,16 +428,20 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
         const int64_t oc = C0 + cl, k0 = R0 + rl;
         const bool valid = oc < cols && k0 < rows;
         float2 R[16];
-        read_col(st, rl, cl, R, InT());
+        uint32_t o[8];
+        col_offsets(rl, cl, o, InT());
+        read_col(st, o, R, InT());
         if (ocol.wht) hadamard32_lane(R, ocol.sign_mask);
         float M = absmax32(R);
         if (ocol.block) M = warp_max(M);
         uint32_t w[16];
         if (ocol.sr) {
+          uint32_t ob[8];   // the draw buffer is laid out like a bf16 tile
+          col_offsets(rl, cl, ob, uint16_t());
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const uint32_t a = *reinterpret_cast<const uint16_t*>(tb + tile_off(rl + 2 * k, cl, uint16_t()));
-            const uint32_t b = *reinterpret_cast<const uint16_t*>(tb + tile_off(rl + 2 * k + 1, cl, uint16_t()));
+            const uint32_t a = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k) & 7] + 1024 * (k >> 2));
+            const uint32_t b = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k + 1) & 7] + 1024 * (k >> 2));
             w[k] = a | (b << 16);
           }
         }
