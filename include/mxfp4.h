@@ -116,7 +116,8 @@ typedef struct {
  *  Shapes: cols % 32 == 0; rows % 32 == 0 when col != NULL or either
  *  orientation uses 32x32 blocks; MMA scale layout needs the output's row
  *  count % 128 == 0 and its K % 128 == 0. Else MXFP4_ERR_SHAPE.
- *  Inputs must be finite (non-finite inputs give unspecified codes). */
+ *  Inputs must be finite, and with the rotation on every rotated value must
+ *  be finite too (|x| < 2^122 suffices); otherwise the codes are unspecified. */
 mxfp4_status mxfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
                             int64_t ld_x, const mxfp4_quant_params* row, uint8_t* q_row,
                             uint8_t* s_row, const mxfp4_quant_params* col, uint8_t* q_col,
