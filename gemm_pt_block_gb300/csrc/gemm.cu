@@ -71,9 +71,6 @@ struct CtlT {
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
-  uint64_t sf_full[3];    // CTA-pair kernel: scale sets in tensor memory
-  uint64_t sf_empty[3];
-  uint64_t sf_drain;
   uint32_t tmem_base;
   uint32_t abort;
 };
@@ -324,21 +321,13 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + CTL_BYTES + 1024;
 static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
 using Ctl = CtlT<STAGES>;
 static_assert(sizeof(Ctl) <= CTL_BYTES, "control block");
-// Warps: 0 TMA producer, 1 MMA issuer, 2-9 epilogue, 10 scale copier.
-constexpr int THREADS = 64 + NUM_EPI_WARPS * 32 + 32;
-constexpr int SF_WARP = 2 + NUM_EPI_WARPS;
-// Scale sets in tensor memory: set j holds one K-step's A scales at
-// SFA_COL + 24 j (8 columns) and B scales at SFB_COL + 24 j (16 columns).
-constexpr int SF_SETS = 3;
-constexpr uint32_t SF_SET_COLS = 24;
-static_assert(SFB_COL + (SF_SETS - 1) * SF_SET_COLS + 16 <= TMEM_COLS, "scale sets");
 
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
   return (sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) | (1u << 23) |
          ((uint32_t)(256 >> 4) << 24) | (sf_id << 29);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                       float* __restrict__ C, int64_t ldc, int M, int N, int K, int group_m) {
@@ -361,11 +350,6 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     ptx::mbar_init(ptx::smem_u32(&ctl->acc_full), 1);
     ptx::mbar_init(ptx::smem_u32(&ctl->acc_empty), 2 * NUM_EPI_WARPS);
     ptx::mbar_init(ptx::smem_u32(&ctl->drain), 1);
-    for (int j = 0; j < SF_SETS; ++j) {
-      ptx::mbar_init(ptx::smem_u32(&ctl->sf_full[j]), 1);
-      ptx::mbar_init(ptx::smem_u32(&ctl->sf_empty[j]), 1);
-    }
-    ptx::mbar_init(ptx::smem_u32(&ctl->sf_drain), 1);
     ctl->abort = 0;
     ptx::fence_mbar_init();
   }
@@ -422,38 +406,39 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    // The scale copies come from warp SF_WARP: tcgen05 operations issued by
-    // one thread run in issue order, so copies issued here would each hold
-    // the MMA stream for their full latency.
     if (leader && lane == 0) {
-      uint32_t stage = 0, phase = 0, acc_phase = 0, set = 0, set_phase = 0;
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = pair_id; ok && tile < num_tiles; tile += num_pairs) {
         if (!(ok = wait_bar(ptx::smem_u32(&ctl->acc_empty), acc_phase ^ 1u, ctl))) break;
         ptx::tc_fence_after();
         for (int kb = 0; kb < num_k; ++kb) {
           if (!(ok = wait_bar(ptx::smem_u32(&ctl->full[stage]), phase, ctl))) break;
-          if (!(ok = wait_bar(ptx::smem_u32(&ctl->sf_full[set]), set_phase, ctl))) break;
           ptx::tc_fence_after();
           const uint32_t st = ptx::smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t sfo = set * SF_SET_COLS;
+          const uint32_t sfa_s = st + A_BYTES + B_BYTES;
+          const uint32_t sfb_s = sfa_s + SFA_BYTES;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            ptx::tc_cp_pair_32x128b_warpx4(tmem + SFA_COL + 4 * c,
+                                           ptx::smem_desc(sfa_s + c * 512, 0, 128, 0));
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+              ptx::tc_cp_pair_32x128b_warpx4(tmem + SFB_COL + 8 * c + 4 * t,
+                                             ptx::smem_desc(sfb_s + t * 1024 + c * 512, 0, 128, 0));
+          }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
             const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
             ptx::mma_mxf4_pair(tmem + ACC_COL, ad, bd, make_idesc((k & 1) * 2),
-                               tmem + SFA_COL + sfo + 4 * (k >> 1),
-                               tmem + SFB_COL + sfo + 8 * (k >> 1), (kb | k) != 0);
+                               tmem + SFA_COL + 4 * (k >> 1), tmem + SFB_COL + 8 * (k >> 1),
+                               (kb | k) != 0);
           }
           ptx::tc_commit_pair_multicast(ptx::smem_u32(&ctl->empty[stage]), 0x3);
-          ptx::tc_commit_pair_multicast(ptx::smem_u32(&ctl->sf_empty[set]), 0x1);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
-          }
-          if (++set == SF_SETS) {
-            set = 0;
-            set_phase ^= 1u;
           }
         }
         if (!ok) break;
@@ -462,48 +447,6 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       }
       ptx::tc_commit_pair_multicast(ptx::smem_u32(&ctl->drain), 0x1);
       drain_wait(ptx::smem_u32(&ctl->drain), 0);
-    }
-  } else if (warp == SF_WARP) {
-    // ------------------------------------------------------ scale copier
-    // Per K-step: wait for the stage's loads and for the MMAs that last read
-    // scale set `set`, copy the stage's A and B scales into that set, and
-    // signal sf_full[set] when the copies have completed.
-    if (leader && lane == 0) {
-      uint32_t stage = 0, phase = 0, set = 0, set_phase = 0;
-      bool ok = true;
-      for (int tile = pair_id; ok && tile < num_tiles; tile += num_pairs) {
-        for (int kb = 0; kb < num_k; ++kb) {
-          if (!(ok = wait_bar(ptx::smem_u32(&ctl->full[stage]), phase, ctl))) break;
-          if (!(ok = wait_bar(ptx::smem_u32(&ctl->sf_empty[set]), set_phase ^ 1u, ctl))) break;
-          ptx::tc_fence_after();
-          const uint32_t sfa_s = ptx::smem_u32(smem + stage * STAGE_BYTES) + A_BYTES + B_BYTES;
-          const uint32_t sfb_s = sfa_s + SFA_BYTES;
-          const uint32_t sfo = set * SF_SET_COLS;
-          // Each 512-byte tile (128 rows x 4 scale columns) fills 4 columns
-          // in every lane quarter; row r's scales land in column r / 32.
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            ptx::tc_cp_pair_32x128b_warpx4(tmem + SFA_COL + sfo + 4 * c,
-                                           ptx::smem_desc(sfa_s + c * 512, 0, 128, 0));
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-              ptx::tc_cp_pair_32x128b_warpx4(tmem + SFB_COL + sfo + 8 * c + 4 * t,
-                                             ptx::smem_desc(sfb_s + t * 1024 + c * 512, 0, 128, 0));
-          }
-          ptx::tc_commit_pair_multicast(ptx::smem_u32(&ctl->sf_full[set]), 0x1);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          if (++set == SF_SETS) {
-            set = 0;
-            set_phase ^= 1u;
-          }
-        }
-      }
-      // No copy may still be writing tensor memory at teardown.
-      ptx::tc_commit_pair_multicast(ptx::smem_u32(&ctl->sf_drain), 0x1);
-      drain_wait(ptx::smem_u32(&ctl->sf_drain), 0);
     }
   } else {
     // --------------------------------------------------------- epilogue
@@ -647,7 +590,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
     const int grid = 2 * (num_tiles < pairs ? num_tiles : pairs);
     int64_t gm = kGroupBytes / (256 * (K / 2));
     gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
-    pair::mxf4_gemm_pair_kernel<<<grid, pair::THREADS, pair::SMEM_BYTES, st>>>(
+    pair::mxf4_gemm_pair_kernel<<<grid, THREADS, pair::SMEM_BYTES, st>>>(
         ta, tb, tsa, tsb, c, ldc, (int)M, (int)N, (int)K, (int)gm);
     return cudaGetLastError();
   }
