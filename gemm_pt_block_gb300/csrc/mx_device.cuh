@@ -2,10 +2,12 @@
 // rotation and dequantization kernels (sm_103a).
 //
 // Every floating-point step is an explicitly rounded IEEE operation: scalar
-// __fadd_rn / __fmul_rn, or the packed two-lane forms add/sub/mul.rn.f32x2,
+// __fadd_rn / __fmul_rn, or the packed two-lane forms add/sub/mul/fma.f32x2,
 // which round each lane exactly like the scalar instruction. Nothing is
-// contracted into an FMA and the library is built without flush-to-zero, so
-// results are the fp32 results the method's definition fixes.
+// contracted into an FMA by the compiler (the one explicit FMA, in stochastic
+// rounding, yields an exactly representable value) and the library is built
+// without flush-to-zero, so results are the fp32 results the method's
+// definition fixes.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -76,12 +78,22 @@ __device__ __forceinline__ float2 f2mul(float2 a, float2 b) {
   return r;
 }
 
-// a + b rounded toward -infinity, per lane.
-__device__ __forceinline__ float2 f2add_rm(float2 a, float2 b) {
+// a + b rounded toward +infinity, per lane.
+__device__ __forceinline__ float2 f2add_rp(float2 a, float2 b) {
   float2 r;
   asm("{.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-      "add.rm.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;}"
+      "add.rp.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;}"
       : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+// a * b + c with one rounding (to nearest), per lane.
+__device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return r;
 }
 
@@ -278,40 +290,46 @@ __device__ __forceinline__ uint2 encode16(const float2 (&V)[8]) {
                     e2m1x8(V[4].x, V[4].y, V[5].x, V[5].y, V[6].x, V[6].y, V[7].x, V[7].y));
 }
 
-// Stochastic rounding of two scaled values with draws rf = r * 2^-16 (r a
-// 16-bit integer): a = min(|v|, 6) lies in [lo, lo + step) on the E2M1 grid;
-// it goes up iff r < 2^16 (a - lo) / step, i.e. iff a - lo > rf * step. Every
-// step is exact in fp32:
-//   step = max(1/2, 2^(E(a) - 1))  (E = unbiased exponent; 1/2 below 1),
-//   lo   = (a + C, rounded down) - C  with C = step * 2^23 (ulp of C = step),
-//   a - lo and rf * step are exact (Sterbenz; power-of-two scaling).
-// Returns the chosen grid values with v's signs; their E2M1 conversion is then
-// exact.
-__device__ __forceinline__ float2 sr_pair(float2 v, float2 rf) {
-  const float2 a = make_float2(fminf(fabsf(v.x), 6.0f), fminf(fabsf(v.y), 6.0f));
-  const float2 p2 = make_float2(__uint_as_float(__float_as_uint(a.x) & 0x7F800000u),
-                                __uint_as_float(__float_as_uint(a.y) & 0x7F800000u));
-  float2 st = f2mul(p2, make_float2(0.5f, 0.5f));
-  st = make_float2(fmaxf(st.x, 0.5f), fmaxf(st.y, 0.5f));
-  const float2 C = f2mul(st, make_float2(8388608.0f, 8388608.0f));
-  const float2 lo = f2sub(f2add_rm(a, C), C);
-  const float2 d = f2sub(a, lo);
-  const float2 th = f2mul(rf, st);
-  const float2 q = f2add(lo, make_float2(d.x > th.x ? st.x : 0.0f, d.y > th.y ? st.y : 0.0f));
-  return make_float2(__uint_as_float(__float_as_uint(q.x) | (__float_as_uint(v.x) & 0x80000000u)),
-                     __uint_as_float(__float_as_uint(q.y) | (__float_as_uint(v.y) & 0x80000000u)));
-}
-
-// The draws of a word holding two 16-bit values, as r * 2^-16 (exact).
-__device__ __forceinline__ float2 draw_pair(uint32_t w) {
-  return f2mul(make_float2((float)(w & 0xFFFFu), (float)(w >> 16)),
-               make_float2(1.0f / 65536.0f, 1.0f / 65536.0f));
+// Stochastic rounding of two scaled values v whose draws are the 16-bit
+// halves r of w (element 0 low). With a = |v| in [lo, lo + st) on the E2M1
+// grid, the value goes up iff r < 2^16 (a - lo) / st, i.e. iff a - lo > th
+// with th = r * st * 2^-16; equivalently the result is the smallest multiple
+// of st that is >= a - th (lo is a multiple of st, and a - th > lo - st).
+// Every step is exact in fp32 (nothing depends on an FMA contraction):
+//   st = max(1, 2^E(a)) / 2 (E = unbiased exponent; 1/2 below 1); the grid
+//     points of [lo, lo + st] are multiples of st, and values in (6, 8) that
+//     reach 8 saturate to 6 in the E2M1 conversion as they round down to 6;
+//   th = (2^23 + r) * K - 2^23 * K with K = st * 2^-16 (an exact r * K from
+//     one rounding; 2^23 + r is built from r's bits);
+//   x = a - th is exact for a >= 1/2 (both are multiples of ulp(a) within
+//     one binade of x) and otherwise has the sign and the ceiling of the
+//     exact difference;
+//   the ceiling is (x + C, rounded up) - C with C = 3 * 2^22 * st, whose
+//     binade (ulp st) holds x + C for every |x| < 8.
+// The sign is carried as a factor +-1 (exact). Returns the chosen grid
+// values, whose E2M1 conversion is then exact.
+__device__ __forceinline__ float2 sr_pair(float2 v, uint32_t w) {
+  const uint32_t b0 = __float_as_uint(v.x), b1 = __float_as_uint(v.y);
+  const float2 sg = make_float2(__uint_as_float((b0 & 0x80000000u) | 0x3F800000u),
+                                __uint_as_float((b1 & 0x80000000u) | 0x3F800000u));
+  const float2 a = f2mul(v, sg);
+  const float2 st2 = make_float2(fmaxf(__uint_as_float(b0 & 0x7F800000u), 1.0f),
+                                 fmaxf(__uint_as_float(b1 & 0x7F800000u), 1.0f));
+  const float2 C = f2mul(st2, make_float2(6291456.0f, 6291456.0f));        // 3 * 2^21
+  const float2 K = f2mul(st2, make_float2(7.62939453125e-6f, 7.62939453125e-6f));  // 2^-17
+  const float2 Kn = f2mul(st2, make_float2(-64.0f, -64.0f));               // -2^23 * K
+  const float2 f = make_float2(__uint_as_float(0x4B000000u | (w & 0xFFFFu)),
+                               __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7432)));
+  const float2 th = f2fma(f, K, Kn);
+  const float2 x = f2sub(a, th);
+  const float2 q = f2sub(f2add_rp(x, C), C);
+  return f2mul(q, sg);
 }
 
 // SR of 16 scaled values; word k of w holds the draws of pair R[k].
 __device__ __forceinline__ void sr16(float2 (&V)[8], const uint32_t (&w)[8]) {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) V[k] = sr_pair(V[k], draw_pair(w[k]));
+  for (int k = 0; k < 8; ++k) V[k] = sr_pair(V[k], w[k]);
 }
 
 // ------------------------------------------------------- fast division ---

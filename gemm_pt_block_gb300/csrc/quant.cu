@@ -287,7 +287,7 @@ __device__ __forceinline__ uint4 finish32(float2 (&R)[16], const OrientArgs& o, 
   for (int k = 0; k < 16; ++k) R[k] = f2mul(R[k], is);
   if (o.sr) {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) R[k] = sr_pair(R[k], draw_pair(w[k]));
+    for (int k = 0; k < 16; ++k) R[k] = sr_pair(R[k], w[k]);
   }
   *e_out = e;
   return encode32(R);
