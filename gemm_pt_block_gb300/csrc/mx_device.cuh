@@ -206,13 +206,18 @@ __device__ __forceinline__ void stage32(float2 (&R)[16], int h) {
 // order h = 1, 2, 4, 8, 16, c applied last.
 __device__ __forceinline__ void hadamard32_lane(float2 (&R)[16], uint32_t sign_mask) {
   if (sign_mask) {
+    // Stage h = 1 with the signs folded in: (s0 x0 + s1 x1, s0 x0 - s1 x1),
+    // each an exact product and one rounded sum (s = +-1).
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      R[k].x = __uint_as_float(__float_as_uint(R[k].x) ^ ((sign_mask >> (2 * k)) << 31));
-      R[k].y = __uint_as_float(__float_as_uint(R[k].y) ^ ((sign_mask >> (2 * k + 1)) << 31));
+      const float s0 = __uint_as_float(0x3F800000u | (((sign_mask >> (2 * k)) & 1u) << 31));
+      const float s1 = __uint_as_float(0x3F800000u | (((sign_mask >> (2 * k + 1)) & 1u) << 31));
+      const float t = __fmul_rn(R[k].y, s1);
+      R[k] = make_float2(__fmaf_rn(R[k].x, s0, t), __fmaf_rn(R[k].x, s0, -t));
     }
+  } else {
+    stage32(R, 1);
   }
-  stage32(R, 1);
   stage32(R, 2);
   stage32(R, 4);
   stage32(R, 8);
@@ -299,11 +304,11 @@ __device__ __forceinline__ uint2 encode16(const float2 (&V)[8]) {
 //   st = max(1, 2^E(a)) / 2 (E = unbiased exponent; 1/2 below 1); the grid
 //     points of [lo, lo + st] are multiples of st, and values in (6, 8) that
 //     reach 8 saturate to 6 in the E2M1 conversion as they round down to 6;
-//   th = (2^23 + r) * K - 2^23 * K with K = st * 2^-16 (an exact r * K from
-//     one rounding; 2^23 + r is built from r's bits);
-//   x = a - th is exact for a >= 1/2 (both are multiples of ulp(a) within
-//     one binade of x) and otherwise has the sign and the ceiling of the
-//     exact difference;
+//   th = r * st * 2^-16 is exact (r has 16 bits; r is recovered exactly as
+//     (2^23 + r) - 2^23 from a float assembled from r's bits);
+//   x = a - th, taken with one rounding as fma(r, -st * 2^-16, a), is exact
+//     for a >= 1/2 (both are multiples of ulp(a) within one binade of x) and
+//     otherwise has the sign and the ceiling of the exact difference;
 //   the ceiling is (x + C, rounded up) - C with C = 3 * 2^22 * st, whose
 //     binade (ulp st) holds x + C for every |x| < 8.
 // The sign is carried as a factor +-1 (exact). Returns the chosen grid
@@ -316,12 +321,11 @@ __device__ __forceinline__ float2 sr_pair(float2 v, uint32_t w) {
   const float2 st2 = make_float2(fmaxf(__uint_as_float(b0 & 0x7F800000u), 1.0f),
                                  fmaxf(__uint_as_float(b1 & 0x7F800000u), 1.0f));
   const float2 C = f2mul(st2, make_float2(6291456.0f, 6291456.0f));        // 3 * 2^21
-  const float2 K = f2mul(st2, make_float2(7.62939453125e-6f, 7.62939453125e-6f));  // 2^-17
-  const float2 Kn = f2mul(st2, make_float2(-64.0f, -64.0f));               // -2^23 * K
+  const float2 nK = f2mul(st2, make_float2(-7.62939453125e-6f, -7.62939453125e-6f));  // -2^-17
   const float2 f = make_float2(__uint_as_float(0x4B000000u | (w & 0xFFFFu)),
                                __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7432)));
-  const float2 th = f2fma(f, K, Kn);
-  const float2 x = f2sub(a, th);
+  const float2 r = f2sub(f, make_float2(8388608.0f, 8388608.0f));
+  const float2 x = f2fma(r, nK, a);
   const float2 q = f2sub(f2add_rp(x, C), C);
   return f2mul(q, sg);
 }
