@@ -317,7 +317,7 @@ def _traffic_record():
 
 # ------------------------------------------------------------ CPU oracle ---
 
-def cpu_oracle_sample(spec: Spec, r: int = 128):
+def cpu_oracle_sample(spec: Spec, r: int = 2048):
     """Times the oracle on a bounded sample of the same step: for every quantize
     op an r-row band (row-wise output) and an r-column band (column-wise output),
     and for every GEMM r output rows (dequantize + fp64 product). Inputs are
@@ -429,6 +429,54 @@ def measure_e2e(st: Step, steps: int, ws: int):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
 
 
+def run_op(args):
+    """Time one operation of the step alone (its own tensors only, so a profiler
+    can capture a full-size launch with a small device footprint)."""
+    import torch
+    import gemm_pt_block_gb300 as mx
+
+    spec = make_spec(args.workload)
+    qs = {q.name: q for q in spec.quants}
+    gs = {g.label: g for g in spec.gemms}
+    if args.op in qs:
+        sub = Spec(spec.name, spec.desc, [qs[args.op]], [])
+    elif args.op in gs:
+        g = gs[args.op]
+        sub = Spec(spec.name, spec.desc, [qs[n] for n in dict.fromkeys((g.a[0], g.b[0]))], [g])
+    else:
+        raise SystemExit(f"--op must be one of {sorted(qs) + sorted(gs)}")
+    device = torch.device("cuda", 0)
+    st = Step(sub, device)
+    if sub.gemms:
+        st.run()   # quantize the operands once
+        g = sub.gemms[0]
+        qa, sa = st.operand(g.a)
+        qb, sb = st.operand(g.b)
+        fn = lambda: mx.mxfp4_gemm(qa, sa, qb, sb, g.M, g.N, g.K, c=st.outs[g.label])
+        work, unit = sub.gemm_flops()[0] / 1e12, "TFLOP/s"
+    else:
+        q = sub.quants[0]
+        qr, sr, qc, sc = st.bufs[q.name]
+        x = st.inputs[q.name]
+        fn = lambda: mx.mxfp4_quantize(x, q.prow, q.pcol, q_row=qr, s_row=sr, q_col=qc, s_col=sc)
+        work, unit = sub.quant_bytes()[0] / 1e9, "GB/s"
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if mx.device_status() != 0:
+        raise RuntimeError("a bounded device-side wait ran out")
+    print(json.dumps({"op": args.op, "workload": args.workload, "ms": ms,
+                      "rate": work / (ms / 1e3), "unit": unit, "launches": args.steps}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,9 +486,15 @@ def main():
     ap.add_argument("--workload", default="70b-layer", choices=WORKLOADS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", default=None,
+                    help="profiling aid: allocate and time only this operation of the workload's "
+                         "step (a quantizer name such as dY, or a GEMM label such as Fprop); prints "
+                         "a short JSON line instead of the benchmark line")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.op:
+        return run_op(args)
 
     import torch
 

@@ -316,7 +316,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t par, uint32
 }
 
 template <typename InT>
-__global__ void __launch_bounds__(kTileThreads, 4)
+__global__ void __launch_bounds__(kTileThreads, 3)
 quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols,
                   uint32_t ntiles, FastDiv tiles_x, const __grid_constant__ OrientArgs orow,
                   const __grid_constant__ OrientArgs ocol, int do_row, int do_col) {
