@@ -27,6 +27,7 @@ from .binding import (  # noqa: F401
     Mxfp4Error,
     QuantParams,
     device_status,
+    selftest_wait_timeout,
     hadamard32,
     lib,
     lib_path,

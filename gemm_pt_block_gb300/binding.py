@@ -97,6 +97,8 @@ def lib() -> ctypes.CDLL:
         L.mxfp4_last_error.argtypes = []
         L.mxfp4_device_status.restype = i32
         L.mxfp4_device_status.argtypes = [P]
+        L.mxfp4_selftest_wait_timeout.restype = i32
+        L.mxfp4_selftest_wait_timeout.argtypes = [P]
         _lib = L
     return _lib
 
@@ -210,3 +212,10 @@ def device_status(stream=None) -> int:
     """Synchronizes the stream and returns (and clears) the GEMM's device error word."""
     s = torch.cuda.current_stream() if stream is None else stream
     return int(lib().mxfp4_device_status(ctypes.c_void_p(s.cuda_stream)))
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Enqueue the bounded-wait self-test (a wait that can only run out); its
+    outcome, MXFP4_ERR_TIMEOUT, is then read with device_status()."""
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(lib().mxfp4_selftest_wait_timeout(ctypes.c_void_p(s.cuda_stream)))

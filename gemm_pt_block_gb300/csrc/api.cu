@@ -170,4 +170,10 @@ mxfp4_status mxfp4_device_status(void* stream) {
   return err ? fail(static_cast<mxfp4_status>(err), "device error word %u", err) : MXFP4_OK;
 }
 
+mxfp4_status mxfp4_selftest_wait_timeout(void* stream) {
+  cudaError_t e = mx::launch_wait_probe(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return from_cuda(e, "mxfp4_selftest_wait_timeout");
+  return MXFP4_OK;
+}
+
 }  // extern "C"

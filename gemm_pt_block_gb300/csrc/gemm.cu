@@ -607,6 +607,26 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   return cudaGetLastError();
 }
 
+namespace {
+// Self-test of the bounded waits: the one waiting thread waits on an mbarrier
+// that nothing ever completes; after the wait limit it raises the error word
+// (MXFP4_ERR_TIMEOUT) and returns, as a GEMM wait that ran out would.
+__global__ void wait_timeout_probe_kernel() {
+  __shared__ CtlT<1> ctl;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&ctl.full[0]), 1);
+    ctl.abort = 0;
+    ptx::fence_mbar_init();
+    (void)wait_bar(ptx::smem_u32(&ctl.full[0]), 0u, &ctl);
+  }
+}
+}  // namespace
+
+cudaError_t launch_wait_probe(cudaStream_t st) {
+  wait_timeout_probe_kernel<<<1, 32, 0, st>>>();
+  return cudaGetLastError();
+}
+
 cudaError_t read_device_error(cudaStream_t st, uint32_t* err) {
   cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return e;

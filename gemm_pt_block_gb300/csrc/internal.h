@@ -43,5 +43,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
 cudaError_t read_quant_error(uint32_t* err);
 // Reads and clears the device error words (synchronizes st).
 cudaError_t read_device_error(cudaStream_t st, uint32_t* err);
+// One-thread kernel whose bounded wait never completes (sets the error word).
+cudaError_t launch_wait_probe(cudaStream_t st);
 
 }  // namespace mx

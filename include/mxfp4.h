@@ -166,6 +166,15 @@ const char* mxfp4_last_error(void);
  * first. */
 mxfp4_status mxfp4_device_status(void* stream);
 
+/* Diagnostic for the library's own failure reporting (the pages have no
+ * counterpart). Enqueues on `stream` a one-thread kernel that waits on a
+ * device barrier nothing ever signals; the wait gives up after its limit
+ * (about 2 s), records MXFP4_ERR_TIMEOUT in the device error word exactly as
+ * a GEMM wait that ran out would, and the kernel returns, leaving the context
+ * usable. Returns the launch status; read the outcome with
+ * mxfp4_device_status (which also clears it). */
+mxfp4_status mxfp4_selftest_wait_timeout(void* stream);
+
 #ifdef __cplusplus
 }
 #endif
