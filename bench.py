@@ -46,6 +46,9 @@ LAYERS = {
                   "70B-dense-shaped layer training step: tokens 16384, d 8192, ffn 28672"),
     "8b-mlp-up": (8192, 4096, 14336, 1002,
                   "Llama-3.1-8B-shaped MLP up-proj training step: tokens 8192, d 4096, ffn 14336"),
+    "70b-layer-det": (16384, 8192, 28672, 1003,
+                      "70B-dense-shaped layer training step, deterministic rotation: tokens 16384, "
+                      "d 8192, ffn 28672"),
 }
 # Square sweep points: quantize A and B (1x32 floor nearest-even) + one n^3 GEMM.
 SQUARES = {f"sq{n}": n for n in (1024, 2048, 4096, 8192, 16384)}
@@ -102,8 +105,8 @@ def make_spec(name: str) -> Spec:
     P, mma = mx.QuantParams, mx.LAYOUT_MMA
     if name in LAYERS:
         T, D, F, seed, desc = LAYERS[name]
-        big = name == "70b-layer"
-        mask = synth.sign_mask(seed)
+        big = name.startswith("70b-layer")
+        mask = 0 if name.endswith("-det") else synth.sign_mask(seed)
         # 70B step: W, dY in 32x32 blocks, round-up scales, random-sign rotation
         # for Wgrad, SR on Dgrad's dY. 8B step: 1x32 floor, deterministic
         # rotation + SR for the Wgrad operands only. Each tensor has its own
@@ -317,7 +320,7 @@ def _traffic_record():
 
 # ------------------------------------------------------------ CPU oracle ---
 
-def cpu_oracle_sample(spec: Spec, r: int = 2048):
+def cpu_oracle_sample(spec: Spec, r: int = 4096):
     """Times the oracle on a bounded sample of the same step: for every quantize
     op an r-row band (row-wise output) and an r-column band (column-wise output),
     and for every GEMM r output rows (dequantize + fp64 product). Inputs are
@@ -429,6 +432,41 @@ def measure_e2e(st: Step, steps: int, ws: int):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
 
 
+def measure_linear(spec: Spec, st: "Step", steps: int):
+    """The same layer step through the autograd op (mxfp4_linear forward +
+    backward on the step's X, W and dY, recipe taken from the workload), timed
+    with CUDA events; includes autograd's bookkeeping and its fp32 -> bf16
+    gradient casts."""
+    import torch
+    import gemm_pt_block_gb300 as mx
+
+    q = {o.name: o for o in spec.quants}
+    recipe = mx.LinearRecipe(q["X"].prow, q["X"].pcol, q["W"].prow, q["W"].pcol,
+                             q["dY"].prow, q["dY"].pcol)
+    x = st.inputs["X"].detach().requires_grad_()
+    w = st.inputs["W"].detach().requires_grad_()
+    g = st.inputs["dY"].float()
+
+    def one():
+        y = mx.mxfp4_linear(x, w, recipe)
+        return torch.autograd.grad(y, (x, w), g)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del g
+    return {"value": sum(spec.gemm_flops()) / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": ms, "steps": steps,
+            "what": "mxfp4_linear forward + backward (autograd) on the step's tensors"}
+
+
 def run_op(args):
     """Time one operation of the step alone (its own tensors only, so a profiler
     can capture a full-size launch with a small device footprint)."""
@@ -477,6 +515,60 @@ def run_op(args):
     return 0
 
 
+def run_sweep(args):
+    """Quantizer throughput over the square sweep (algorithmic bytes / time,
+    against the measured HBM copy peak). Between timed launches a 512 MB
+    buffer is rewritten so every launch starts with a cold L2."""
+    import torch
+    import gemm_pt_block_gb300 as mx
+    import synth
+
+    P = mx.QuantParams
+    peaks, src = _peaks()
+    hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    steps = max(args.steps, 3)
+    for n in sorted(SQUARES.values()):
+        x = synth.dev_student_t(n, n, 3.0, 1005, "cuda")
+        mask = synth.sign_mask(1005)
+        variants = []
+        for rnd, rname in ((mx.ROUND_RTN, "rtn"), (mx.ROUND_SR, "sr")):
+            for blk, sm, bname in ((mx.BLOCK_1X32, mx.SCALE_FLOOR, "1x32-floor"),
+                                   (mx.BLOCK_32X32, mx.SCALE_ROUNDUP, "32x32-roundup")):
+                for wht, wname in ((False, "norot"), (True, "rot")):
+                    p = P(blk, sm, rnd, mx.LAYOUT_MMA, wht, mask if wht else 0, 1005, 0)
+                    variants.append((f"row {rname} {bname} {wname}", p, None))
+        for blk, sm, bname in ((mx.BLOCK_1X32, mx.SCALE_FLOOR, "1x32-floor"),
+                               (mx.BLOCK_32X32, mx.SCALE_ROUNDUP, "32x32-roundup")):
+            p = P(blk, sm, mx.ROUND_RTN, mx.LAYOUT_MMA)
+            variants.append((f"dual rtn {bname} norot", p, p))
+        for name, prow, pcol in variants:
+            out = mx.mxfp4_quantize(x, prow, pcol)
+            kw = dict(q_row=out[0], s_row=out[1], q_col=out[2], s_col=out[3])
+            for _ in range(2):
+                mx.mxfp4_quantize(x, prow, pcol, **kw)
+            times = []
+            for _ in range(steps):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                mx.mxfp4_quantize(x, prow, pcol, **kw)
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.median(times)
+            byts = n * n * (2 + ((prow is not None) + (pcol is not None)) * (0.5 + 1 / 32))
+            gbs = byts / (ms / 1e3) / 1e9
+            print(json.dumps({"sweep": name, "n": n, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm,
+                              "hbm_peak_source": src, "l2": "flushed (512 MB rewrite) before each launch"}),
+                  flush=True)
+            del out, kw
+        del x
+    if mx.device_status() != 0:
+        raise RuntimeError("a bounded device-side wait ran out")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -486,6 +578,11 @@ def main():
     ap.add_argument("--workload", default="70b-layer", choices=WORKLOADS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="quantizer sweep on square bf16 inputs n = 1024..16384: eight row-wise "
+                         "variants ({RTN, SR} x {1x32 floor, 32x32 round-up} x {no rotation, "
+                         "random-sign rotation}) and both dual-orientation block types; one JSON "
+                         "line per point (L2 flushed between launches)")
     ap.add_argument("--op", default=None,
                     help="profiling aid: allocate and time only this operation of the workload's "
                          "step (a quantizer name such as dY, or a GEMM label such as Fprop); prints "
@@ -495,6 +592,8 @@ def main():
         return run_reference(args)
     if args.op:
         return run_op(args)
+    if args.sweep:
+        return run_sweep(args)
 
     import torch
 
@@ -594,6 +693,8 @@ def main():
     }
     if not args.no_e2e:
         line["e2e"] = measure_e2e(st, max(1, min(args.steps, 5)), ws)
+    if len(spec.gemms) == 3 and not args.no_e2e:
+        line["autograd_linear"] = measure_linear(spec, st, max(1, min(args.steps, 5)))
     if not args.no_cpu_baseline and rank == 0 and ws == 1:
         dt, flops, qb, threads, sdesc = cpu_oracle_sample(spec)
         line["cpu_baseline"] = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads,

@@ -36,3 +36,4 @@ from .binding import (  # noqa: F401
     mxfp4_quantize,
     scale_numel,
 )
+from .linear import LinearRecipe, Mxfp4Linear, mxfp4_linear, recipe_1d, recipe_2d_sr  # noqa: F401

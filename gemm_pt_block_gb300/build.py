@@ -26,7 +26,7 @@ UNITS = {
     "quant.cu": ["--fmad=false"],
     "gemm.cu": [],
 }
-HEADERS = ["internal.h", "mx_device.cuh", "ptx.cuh"]
+HEADERS = ["internal.h", "mx_device.cuh", "ptx.cuh", "tma_host.h"]
 
 
 def nvcc() -> str:

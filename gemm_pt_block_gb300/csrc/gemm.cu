@@ -32,6 +32,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "tma_host.h"
 
 namespace mx {
 namespace {
@@ -494,19 +495,7 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
 }  // namespace pair
 
 // ---------------------------------------------------------------- host ---
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return tma_encode_fn(); }
 
 bool make_code_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t kbytes,
                    uint32_t box_rows) {
@@ -576,6 +565,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
     *why = "driver entry point cuTensorMapEncodeTiled not available";
     return cudaErrorNotSupported;
   }
+  ensure_context();
   CUtensorMap ta, tb;
   if (M % 256 == 0) {
     // CTA pairs: 256 x 256 tiles.
@@ -590,6 +580,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
     const int grid = 2 * (num_tiles < pairs ? num_tiles : pairs);
     int64_t gm = kGroupBytes / (256 * (K / 2));
     gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
+    (void)cudaGetLastError();  // drop a stale error left by an earlier call
     pair::mxf4_gemm_pair_kernel<<<grid, THREADS, pair::SMEM_BYTES, st>>>(
         ta, tb, tsa, tsb, c, ldc, (int)M, (int)N, (int)K, (int)gm);
     return cudaGetLastError();
@@ -602,6 +593,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   const int grid = num_tiles < d.sms ? num_tiles : d.sms;
   int64_t gm = kGroupBytes / (BM * (K / 2));
   gm = gm < 8 ? 8 : (gm > 64 ? 64 : gm);
+  (void)cudaGetLastError();  // drop a stale error left by an earlier call
   mxf4_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sa, sb, c, ldc, (int)M, (int)N,
                                                       (int)K, (int)gm);
   return cudaGetLastError();
@@ -623,6 +615,7 @@ __global__ void wait_timeout_probe_kernel() {
 }  // namespace
 
 cudaError_t launch_wait_probe(cudaStream_t st) {
+  (void)cudaGetLastError();  // drop a stale error left by an earlier call
   wait_timeout_probe_kernel<<<1, 32, 0, st>>>();
   return cudaGetLastError();
 }

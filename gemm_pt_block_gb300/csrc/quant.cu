@@ -544,6 +544,7 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
     const int64_t total = rows * (cols >> 4);
     const unsigned grid =
         resident_ctas(quant_rows_1x32_kernel<InT>, (total + kThreads - 1) / kThreads, 0, kThreads);
+    (void)cudaGetLastError();  // drop a stale error left by an earlier call
     quant_rows_1x32_kernel<InT><<<grid, kThreads, 0, st>>>(
         x, (uint32_t)total, make_fastdiv((uint32_t)(cols >> 4)), cols, ld, *row);
     return cudaGetLastError();
@@ -564,6 +565,7 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
   OrientArgs dummy{};
   const int64_t tx = (cols + kTile - 1) / kTile, ty = (rows + kTile - 1) / kTile;
   const unsigned grid = resident_ctas(quant_tile_kernel<InT>, tx * ty, smem, kTileThreads);
+  (void)cudaGetLastError();  // drop a stale error left by an earlier call
   quant_tile_kernel<InT><<<grid, kTileThreads, smem, st>>>(
       tm, rows, cols, (uint32_t)(tx * ty), make_fastdiv((uint32_t)tx), row ? *row : dummy,
       col ? *col : dummy, row != nullptr, col != nullptr);
@@ -582,6 +584,7 @@ cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t 
                               uint32_t sign_mask, bool inverse, float* y, cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   const unsigned nb = blocks_for(rows * (cols >> 4));
+  (void)cudaGetLastError();  // drop a stale error left by an earlier call
   if (f32_in)
     hadamard32_kernel<float><<<nb, kThreads, 0, st>>>(static_cast<const float*>(x), rows, cols,
                                                       ld, sign_mask, inverse, y);
@@ -603,6 +606,7 @@ cudaError_t read_quant_error(uint32_t* err) {
 cudaError_t launch_dequantize(const uint8_t* q, const uint8_t* s, bool mma_layout, int64_t rows,
                               int64_t cols, float* out, cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
+  (void)cudaGetLastError();  // drop a stale error left by an earlier call
   dequant_kernel<<<blocks_for(rows * (cols >> 4)), kThreads, 0, st>>>(q, s, mma_layout, rows,
                                                                       cols, out);
   return cudaGetLastError();

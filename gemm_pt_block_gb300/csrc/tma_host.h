@@ -24,6 +24,19 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tma_encode_fn() {
   return fn;
 }
 
+// The tensor-map encoder is a driver-API call: it needs the device's context to
+// be current in the calling thread, which a thread that has not yet made a
+// runtime call that binds it (for example a framework's worker thread) may
+// lack. Binds the current device's primary context once per thread.
+inline void ensure_context() {
+  thread_local bool bound = false;
+  if (!bound) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaSetDevice(dev);
+    bound = true;
+  }
+}
+
 // 2-D row-major tensor [rows, cols] with leading dimension ld (elements), box
 // [box_rows, box_cols], 128-byte swizzle (box_cols * elem_bytes must be <= 128),
 // out-of-bounds elements read as zero.
@@ -32,6 +45,7 @@ inline bool make_tma_2d(CUtensorMap* m, CUtensorMapDataType dt, uint32_t elem_by
                         uint32_t box_cols) {
   auto fn = tma_encode_fn();
   if (!fn) return false;
+  ensure_context();
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)(ld * elem_bytes)};
   const cuuint32_t box[2] = {box_cols, box_rows};
