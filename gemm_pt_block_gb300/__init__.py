@@ -33,6 +33,7 @@ from .binding import (  # noqa: F401
     lib_path,
     mxfp4_dequantize,
     mxfp4_gemm,
+    mxfp4_gemm_quantize,
     mxfp4_quantize,
     scale_numel,
 )

@@ -89,6 +89,9 @@ def lib() -> ctypes.CDLL:
         L.mxfp4_dequantize.argtypes = [P, P, i32, i64, i64, P, P]
         L.mxfp4_gemm.restype = i32
         L.mxfp4_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
+        L.mxfp4_gemm_quantize.restype = i32
+        L.mxfp4_gemm_quantize.argtypes = [P, P, P, P, i64, i64, i64, P, i64,
+                                          ctypes.POINTER(_CParams), P, P, P]
         L.hadamard32.restype = i32
         L.hadamard32.argtypes = [P, i32, i64, i64, i64, ctypes.c_uint32, i32, P, P]
         L.mxfp4_status_string.restype = ctypes.c_char_p
@@ -193,6 +196,26 @@ def mxfp4_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.T
     _check(lib().mxfp4_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), ldc,
                             _stream(qa, stream)))
     return c
+
+
+def mxfp4_gemm_quantize(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
+                        M: int, N: int, K: int, out: QuantParams, *, with_c: bool = False, c=None,
+                        q_out=None, s_out=None, stream=None):
+    """GEMM whose epilogue quantizes C row-wise with `out`: returns (q_out, s_out, c),
+    c None unless with_c (or c given); codes/scales as mxfp4_quantize(C, out)."""
+    for t, n in ((qa, "qa"), (sa, "sa"), (qb, "qb"), (sb, "sb")):
+        if not t.is_cuda or t.dtype != torch.uint8:
+            raise ValueError(f"{n} must be a CUDA uint8 tensor")
+    if c is None and with_c:
+        c = torch.empty((M, N), dtype=torch.float32, device=qa.device)
+    q_out = torch.empty((M, N // 2), dtype=torch.uint8, device=qa.device) if q_out is None else q_out
+    s_out = _scales_out(M, N, out, qa.device) if s_out is None else s_out
+    ldc = c.stride(0) if c is not None else N
+    op = out._c()
+    _check(lib().mxfp4_gemm_quantize(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K,
+                                     _ptr(c) if c is not None else None, ldc, ctypes.byref(op),
+                                     _ptr(q_out), _ptr(s_out), _stream(qa, stream)))
+    return q_out, s_out, c
 
 
 def hadamard32(x: torch.Tensor, sign_mask: int = 0, inverse: bool = False, *, y=None, stream=None):

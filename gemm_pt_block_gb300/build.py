@@ -24,9 +24,9 @@ COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-ftz=false",
 UNITS = {
     "api.cu": [],
     "quant.cu": ["--fmad=false"],
-    "gemm.cu": [],
+    "gemm.cu": ["--fmad=false"],
 }
-HEADERS = ["internal.h", "mx_device.cuh", "ptx.cuh", "tma_host.h"]
+HEADERS = ["internal.h", "mx_device.cuh", "ptx.cuh", "quant_device.cuh", "tma_host.h"]
 
 
 def nvcc() -> str:

@@ -129,23 +129,47 @@ mxfp4_status mxfp4_dequantize(const uint8_t* q, const uint8_t* s, int32_t scale_
                    "mxfp4_dequantize launch");
 }
 
+namespace {
+mxfp4_status gemm_common(const char* name, const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
+                         int64_t ldc, const mx::OrientArgs* qout, void* stream) {
+  if (!qa || !sa || !qb || !sb || (!c && !qout)) return fail(MXFP4_ERR_INVALID_ARG, "%s: NULL pointer", name);
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0)
+    return fail(MXFP4_ERR_SHAPE, "%s needs M %% 128 == 0, N %% 256 == 0, K %% 256 == 0 (got %lld, %lld, %lld)",
+                name, (long long)M, (long long)N, (long long)K);
+  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30) || (M / 128) * (N / 256) > (1ll << 30))
+    return fail(MXFP4_ERR_SHAPE, "%s dimensions too large", name);
+  if (c && ldc < N) return fail(MXFP4_ERR_SHAPE, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
+  if (!aligned16(qa) || !aligned16(qb) || !aligned16(sa) || !aligned16(sb) || !aligned16(c) ||
+      (c && ldc % 8 != 0))
+    return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");
+  const char* why = "";
+  cudaError_t e = mx::launch_gemm(qa, sa, qb, sb, M, N, K, c, ldc, qout,
+                                  static_cast<cudaStream_t>(stream), &why);
+  if (e == cudaErrorNotSupported) return fail(MXFP4_ERR_UNSUPPORTED, "%s", why);
+  if (e == cudaErrorInvalidValue && why[0]) return fail(MXFP4_ERR_ALIGN, "%s", why);
+  return from_cuda(e, name);
+}
+}  // namespace
+
 mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
                         int64_t ldc, void* stream) {
-  if (!qa || !sa || !qb || !sb || !c) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
-  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0)
-    return fail(MXFP4_ERR_SHAPE, "mxfp4_gemm needs M %% 128 == 0, N %% 256 == 0, K %% 256 == 0 (got %lld, %lld, %lld)",
-                (long long)M, (long long)N, (long long)K);
-  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30) || (M / 128) * (N / 256) > (1ll << 30))
-    return fail(MXFP4_ERR_SHAPE, "mxfp4_gemm dimensions too large");
-  if (ldc < N) return fail(MXFP4_ERR_SHAPE, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
-  if (!aligned16(qa) || !aligned16(qb) || !aligned16(sa) || !aligned16(sb) || !aligned16(c) || ldc % 8 != 0)
-    return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");
-  const char* why = "";
-  cudaError_t e = mx::launch_gemm(qa, sa, qb, sb, M, N, K, c, ldc, static_cast<cudaStream_t>(stream), &why);
-  if (e == cudaErrorNotSupported) return fail(MXFP4_ERR_UNSUPPORTED, "%s", why);
-  if (e == cudaErrorInvalidValue && why[0]) return fail(MXFP4_ERR_ALIGN, "%s", why);
-  return from_cuda(e, "mxfp4_gemm launch");
+  if (!c) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
+  return gemm_common("mxfp4_gemm", qa, sa, qb, sb, M, N, K, c, ldc, nullptr, stream);
+}
+
+mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                                 const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
+                                 int64_t ldc, const mxfp4_quant_params* out, uint8_t* q_out,
+                                 uint8_t* s_out, void* stream) {
+  if (!out) return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_gemm_quantize: out params are required");
+  mx::OrientArgs qo{};
+  if (M > 0 && N > 0) {
+    mxfp4_status st = check_params(out, q_out, s_out, M, N, "out", &qo);
+    if (st) return st;
+  }
+  return gemm_common("mxfp4_gemm_quantize", qa, sa, qb, sb, M, N, K, c, ldc, &qo, stream);
 }
 
 mxfp4_status hadamard32(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,

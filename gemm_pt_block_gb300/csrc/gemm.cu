@@ -32,6 +32,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant_device.cuh"
 #include "tma_host.h"
 
 namespace mx {
@@ -128,10 +129,46 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
   nb = w / gm;
 }
 
+// One epilogue thread's results: 128 consecutive fp32 values of row `row`
+// (columns c0 .. c0 + 127). They are stored to C when C is given, and with
+// kQ they are also quantized row-wise (four 32-runs) exactly as the quantizer
+// would quantize that row of C.
+template <bool kQ>
+__device__ __forceinline__ void epilogue_out(const uint32_t (&r0)[64], const uint32_t (&r1)[64],
+                                             float* C, int64_t ldc, int64_t row, int64_t c0,
+                                             int64_t N, const OrientArgs& qo) {
+  if (!kQ || C != nullptr) {
+    float4* dst = reinterpret_cast<float4*>(C + row * ldc + c0);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      dst[j] = make_float4(__uint_as_float(r0[4 * j]), __uint_as_float(r0[4 * j + 1]),
+                           __uint_as_float(r0[4 * j + 2]), __uint_as_float(r0[4 * j + 3]));
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      dst[16 + j] = make_float4(__uint_as_float(r1[4 * j]), __uint_as_float(r1[4 * j + 1]),
+                                __uint_as_float(r1[4 * j + 2]), __uint_as_float(r1[4 * j + 3]));
+  }
+  if constexpr (kQ) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      float2 R[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int i = (b & 1) * 32 + 2 * k;
+        R[k] = b < 2 ? make_float2(__uint_as_float(r0[i]), __uint_as_float(r0[i + 1]))
+                     : make_float2(__uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
+      }
+      quantize_run32(R, row, c0 + 32 * b, N, qo);
+    }
+  }
+}
+
+template <bool kQ>
 __global__ void __launch_bounds__(THREADS, 1)
 mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const uint8_t* __restrict__ sa, const uint8_t* __restrict__ sb,
-                 float* __restrict__ C, int64_t ldc, int M, int N, int K, int group_m) {
+                 float* __restrict__ C, int64_t ldc, int M, int N, int K, int group_m,
+                 const __grid_constant__ OrientArgs qo) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -274,15 +311,7 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctl->acc_empty));
       acc_phase ^= 1u;
       const int64_t row = (int64_t)mb * BM + q * 32 + lane;
-      float4* dst = reinterpret_cast<float4*>(C + row * ldc + (int64_t)nb * BN + h * 128);
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        dst[j] = make_float4(__uint_as_float(r0[4 * j]), __uint_as_float(r0[4 * j + 1]),
-                             __uint_as_float(r0[4 * j + 2]), __uint_as_float(r0[4 * j + 3]));
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        dst[16 + j] = make_float4(__uint_as_float(r1[4 * j]), __uint_as_float(r1[4 * j + 1]),
-                                  __uint_as_float(r1[4 * j + 2]), __uint_as_float(r1[4 * j + 3]));
+      epilogue_out<kQ>(r0, r1, C, ldc, row, (int64_t)nb * BN + h * 128, N, qo);
     }
   }
 
@@ -328,10 +357,12 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
          ((uint32_t)(256 >> 4) << 24) | (sf_id << 29);
 }
 
+template <bool kQ>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                      float* __restrict__ C, int64_t ldc, int M, int N, int K, int group_m) {
+                      float* __restrict__ C, int64_t ldc, int M, int N, int K, int group_m,
+                      const __grid_constant__ OrientArgs qo) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -472,15 +503,7 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       if (lane == 0) ptx::mbar_arrive_cluster(acc_empty_leader);
       acc_phase ^= 1u;
       const int64_t row = (int64_t)mb * 2 * BM + rank * BM + q * 32 + lane;
-      float4* dst = reinterpret_cast<float4*>(C + row * ldc + (int64_t)nb * BNP + h * 128);
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        dst[j] = make_float4(__uint_as_float(r0[4 * j]), __uint_as_float(r0[4 * j + 1]),
-                             __uint_as_float(r0[4 * j + 2]), __uint_as_float(r0[4 * j + 3]));
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        dst[16 + j] = make_float4(__uint_as_float(r1[4 * j]), __uint_as_float(r1[4 * j + 1]),
-                                  __uint_as_float(r1[4 * j + 2]), __uint_as_float(r1[4 * j + 3]));
+      epilogue_out<kQ>(r0, r1, C, ldc, row, (int64_t)nb * BNP + h * 128, N, qo);
     }
   }
 
@@ -538,10 +561,14 @@ DevInfo& dev_info(int dev) {
     cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
     if (d.major == 10) {
-      cudaFuncSetAttribute(mxf4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(mxf4_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_BYTES);
-      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           pair::SMEM_BYTES);
+      cudaFuncSetAttribute(mxf4_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SMEM_BYTES);
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
     }
     d.attr_set = true;
   }
@@ -552,7 +579,9 @@ DevInfo& dev_info(int dev) {
 
 cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
-                        int64_t ldc, cudaStream_t st, const char** why) {
+                        int64_t ldc, const OrientArgs* qout, cudaStream_t st, const char** why) {
+  const OrientArgs none{};
+  const OrientArgs& qo = qout ? *qout : none;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -581,8 +610,12 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
     int64_t gm = kGroupBytes / (256 * (K / 2));
     gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
     (void)cudaGetLastError();  // drop a stale error left by an earlier call
-    pair::mxf4_gemm_pair_kernel<<<grid, THREADS, pair::SMEM_BYTES, st>>>(
-        ta, tb, tsa, tsb, c, ldc, (int)M, (int)N, (int)K, (int)gm);
+    if (qout)
+      pair::mxf4_gemm_pair_kernel<true><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
+          ta, tb, tsa, tsb, c, ldc, (int)M, (int)N, (int)K, (int)gm, qo);
+    else
+      pair::mxf4_gemm_pair_kernel<false><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
+          ta, tb, tsa, tsb, c, ldc, (int)M, (int)N, (int)K, (int)gm, qo);
     return cudaGetLastError();
   }
   if (!make_code_map(&ta, qa, M, K / 2, BM) || !make_code_map(&tb, qb, N, K / 2, BN)) {
@@ -594,8 +627,12 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   int64_t gm = kGroupBytes / (BM * (K / 2));
   gm = gm < 8 ? 8 : (gm > 64 ? 64 : gm);
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
-  mxf4_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sa, sb, c, ldc, (int)M, (int)N,
-                                                      (int)K, (int)gm);
+  if (qout)
+    mxf4_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sa, sb, c, ldc, (int)M,
+                                                             (int)N, (int)K, (int)gm, qo);
+  else
+    mxf4_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sa, sb, c, ldc, (int)M,
+                                                              (int)N, (int)K, (int)gm, qo);
   return cudaGetLastError();
 }
 

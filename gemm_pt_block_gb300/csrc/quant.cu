@@ -17,6 +17,7 @@
 
 #include "internal.h"
 #include "mx_device.cuh"
+#include "quant_device.cuh"
 #include "ptx.cuh"
 #include "tma_host.h"
 
@@ -133,12 +134,6 @@ __device__ __forceinline__ uint2 quantize_halves(float2 (&R)[8], int upper, cons
   }
   *e_out = e;
   return encode16(R);
-}
-
-__device__ __forceinline__ void store_scale(const OrientArgs& o, int64_t orow, int64_t kb,
-                                            int64_t nkb, int e) {
-  const int64_t off = o.mma_layout ? mma_scale_offset(orow, kb, nkb) : orow * nkb + kb;
-  o.s[off] = (uint8_t)(e + 127);
 }
 
 // ------------------------------------------------- row-wise, 1x32 blocks ---
@@ -265,32 +260,6 @@ __device__ __forceinline__ void read_col(const uint8_t* st, const uint32_t (&o)[
 
 __device__ __forceinline__ bool same_draws(const OrientArgs& a, const OrientArgs& b) {
   return a.sr && b.sr && a.seed == b.seed && a.stream == b.stream;
-}
-
-// Draw words for 32 consecutive source elements i0 .. i0 + 31 (i0 % 32 == 0).
-__device__ __forceinline__ void draws32(const PhiloxKeys& k, uint32_t stream, uint64_t i0,
-                                        uint32_t (&w)[16]) {
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    const uint64_t g = (i0 >> 3) + h;
-    const U4 a = philox4x32_10(U4{(uint32_t)g, (uint32_t)(g >> 32), stream, 0u}, k);
-    w[4 * h] = a.x; w[4 * h + 1] = a.y; w[4 * h + 2] = a.z; w[4 * h + 3] = a.w;
-  }
-}
-
-// Scale, round and encode one 32-run whose max-abs is M.
-__device__ __forceinline__ uint4 finish32(float2 (&R)[16], const OrientArgs& o, float M,
-                                          const uint32_t (&w)[16], int* e_out) {
-  const int e = scale_exponent(M, o.roundup);
-  const float2 is = make_float2(inv_scale(e), inv_scale(e));
-#pragma unroll
-  for (int k = 0; k < 16; ++k) R[k] = f2mul(R[k], is);
-  if (o.sr) {
-#pragma unroll
-    for (int k = 0; k < 16; ++k) R[k] = sr_pair(R[k], w[k]);
-  }
-  *e_out = e;
-  return encode32(R);
 }
 
 __device__ __forceinline__ void named_sync_consumers() {

@@ -1,0 +1,60 @@
+// quant_device.cuh -- per-run quantization steps shared by the quantizer
+// kernels and the GEMM epilogue that quantizes its output (sm_103a).
+#pragma once
+#include <cstdint>
+
+#include "internal.h"
+#include "mx_device.cuh"
+
+namespace mx {
+
+__device__ __forceinline__ void store_scale(const OrientArgs& o, int64_t orow, int64_t kb,
+                                            int64_t nkb, int e) {
+  const int64_t off = o.mma_layout ? mma_scale_offset(orow, kb, nkb) : orow * nkb + kb;
+  o.s[off] = (uint8_t)(e + 127);
+}
+
+// Draw words for 32 consecutive source elements i0 .. i0 + 31 (i0 % 32 == 0).
+__device__ __forceinline__ void draws32(const PhiloxKeys& k, uint32_t stream, uint64_t i0,
+                                        uint32_t (&w)[16]) {
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const uint64_t g = (i0 >> 3) + h;
+    const U4 a = philox4x32_10(U4{(uint32_t)g, (uint32_t)(g >> 32), stream, 0u}, k);
+    w[4 * h] = a.x; w[4 * h + 1] = a.y; w[4 * h + 2] = a.z; w[4 * h + 3] = a.w;
+  }
+}
+
+// Scale, round and encode one 32-run whose max-abs is M.
+__device__ __forceinline__ uint4 finish32(float2 (&R)[16], const OrientArgs& o, float M,
+                                          const uint32_t (&w)[16], int* e_out) {
+  const int e = scale_exponent(M, o.roundup);
+  const float2 is = make_float2(inv_scale(e), inv_scale(e));
+#pragma unroll
+  for (int k = 0; k < 16; ++k) R[k] = f2mul(R[k], is);
+  if (o.sr) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) R[k] = sr_pair(R[k], w[k]);
+  }
+  *e_out = e;
+  return encode32(R);
+}
+
+// Row-wise quantization of 32 consecutive values of output row `row` (columns
+// c0 .. c0 + 31 of a [rows, cols] tensor) held by one lane as 16 pairs, as the
+// quantizer treats a 32-run: rotate (optional), block max (over the warp's 32
+// rows, one per lane, for 32x32 blocks), scale, round, pack, store.
+__device__ __forceinline__ void quantize_run32(float2 (&R)[16], int64_t row, int64_t c0, int64_t cols,
+                                               const OrientArgs& o) {
+  if (o.wht) hadamard32_lane(R, o.sign_mask);
+  float M = absmax32(R);
+  if (o.block) M = warp_max(M);
+  uint32_t w[16];
+  if (o.sr) draws32(o.keys, o.stream, (uint64_t)(row * cols + c0), w);
+  int e;
+  const uint4 packed = finish32(R, o, M, w, &e);
+  *reinterpret_cast<uint4*>(o.q + row * (cols >> 1) + (c0 >> 1)) = packed;
+  store_scale(o, row, c0 >> 5, cols >> 5, e);
+}
+
+}  // namespace mx

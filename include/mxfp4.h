@@ -146,6 +146,22 @@ mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
                         int64_t ldc, void* stream);
 
+/* The same GEMM with the quantizer fused into its epilogue ([News], para. 2:
+ * the rotation and rounding run where the producing GEMM writes its output):
+ * C is quantized row-wise (along N) straight from the accumulator, with the
+ * parameters `out` (any block, scale mode, rounding, rotation and scale layout
+ * mxfp4_quantize accepts). The codes q_out [M, N/2] and scales s_out
+ * ([M, N/32] or MXFP4_LAYOUT_MMA) are bit-identical to mxfp4_quantize of the
+ * fp32 C this call computes, with cols = N (stochastic draws keyed by the
+ * element index m * N + n). c may be NULL: then no fp32 output is written
+ * (ldc is ignored), which saves its HBM traffic.
+ *  Shapes as mxfp4_gemm; MMA scale layout needs nothing more (M % 128,
+ *  N % 128 hold). q_out must be 16-byte aligned. */
+mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                                 const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
+                                 int64_t ldc, const mxfp4_quant_params* out, uint8_t* q_out,
+                                 uint8_t* s_out, void* stream);
+
 /* Stand-alone 32-point block rotation along cols ([News], para. 2):
  *  forward (inverse == 0): y = c * H * diag(s) * x per 32-block;
  *  inverse (inverse == 1): y = diag(s) * c * H * x.
