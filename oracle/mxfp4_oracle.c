@@ -220,40 +220,45 @@ static float load_elem(const void* x, int dtype, int64_t ld, int64_t r, int64_t 
 /* Quantize output rows [i0, i1) of one orientation. In the row orientation
  * output row i is source row i and position k is source column k; in the
  * column orientation output row i is source column i and k is source row k.
- * Blocks [News, para. 1; TIBQ, "The fix: 2D blocks"]: 1x32 = 32 consecutive
- * k of one output row; 32x32 = the aligned 32 x 32 tile of output rows and k,
- * whose one scale is stored on each of its 32 rows. With the rotation on, each
+ * Blocks [News, para. 1; TIBQ, "The fix: 2D blocks", "The evidence" Table 4]:
+ * 1x32 = 32 consecutive k of one output row; b x b (b = 32 or 64) = the
+ * aligned b x b tile of output rows and k, whose one scale is stored on each
+ * of its rows for each of its b/32 runs of 32 k. With the rotation on, each
  * 1x32 run along k is rotated first and the block max is taken afterwards. */
 static int quantize_orient(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
                            const orc_params* p, int col_orient, int64_t i0, int64_t i1,
                            uint8_t* q, uint8_t* s) {
   const int64_t nout = col_orient ? cols : rows;  /* output rows */
   const int64_t K = col_orient ? rows : cols;     /* quantization axis */
-  const int g = (p->block == ORC_BLOCK_32X32) ? 32 : 1;
-  if (K % 32 != 0 || i0 < 0 || i1 > nout || i0 > i1) return -1;
-  if (g == 32 && (nout % 32 != 0 || i0 % 32 != 0 || i1 % 32 != 0)) return -1;
+  /* g output rows by bw values of k share one scale */
+  const int g = p->block == ORC_BLOCK_64X64 ? 64 : (p->block == ORC_BLOCK_32X32 ? 32 : 1);
+  const int bw = p->block == ORC_BLOCK_64X64 ? 64 : 32;
+  if (K % bw != 0 || i0 < 0 || i1 > nout || i0 > i1) return -1;
+  if (g > 1 && (nout % g != 0 || i0 % g != 0 || i1 % g != 0)) return -1;
   const int64_t nkb = K / 32;
   const int64_t ngroups = (i1 - i0) / g;
   int bad = 0;
 #pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
   for (int64_t gi = 0; gi < ngroups; ++gi) {
     const int64_t ib = i0 + gi * g;
-    float y[32][32];
-    for (int64_t kb = 0; kb < nkb && !bad; ++kb) {
+    float y[64][64];
+    for (int64_t kb0 = 0; kb0 < K / bw && !bad; ++kb0) {
       float M = 0.0f;
       for (int t = 0; t < g; ++t) {
         const int64_t i = ib + t;
-        float blk[32];
-        for (int j = 0; j < 32; ++j) {
-          const int64_t k = kb * 32 + j;
-          blk[j] = col_orient ? load_elem(x, dtype, ld, k, i) : load_elem(x, dtype, ld, i, k);
-          if (!isfinite(blk[j])) bad = 1; /* inputs must be finite */
+        for (int r = 0; r < bw / 32; ++r) {
+          float blk[32];
+          for (int j = 0; j < 32; ++j) {
+            const int64_t k = kb0 * bw + r * 32 + j;
+            blk[j] = col_orient ? load_elem(x, dtype, ld, k, i) : load_elem(x, dtype, ld, i, k);
+            if (!isfinite(blk[j])) bad = 1; /* inputs must be finite */
+          }
+          if (p->wht)
+            orc_wht32(blk, p->wht_sign_mask, 0, &y[t][r * 32]);
+          else
+            memcpy(&y[t][r * 32], blk, sizeof(blk));
         }
-        if (p->wht)
-          orc_wht32(blk, p->wht_sign_mask, 0, y[t]);
-        else
-          memcpy(y[t], blk, sizeof(blk));
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < bw; ++j) {
           float a = fabsf(y[t][j]);
           if (a > M) M = a;
         }
@@ -263,9 +268,9 @@ static int quantize_orient(const void* x, int dtype, int64_t rows, int64_t cols,
       for (int t = 0; t < g; ++t) {
         const int64_t i = ib + t;
         const int64_t orow = i - i0;
-        s[orow * nkb + kb] = (uint8_t)(e + 127);
-        for (int j = 0; j < 32; ++j) {
-          const int64_t k = kb * 32 + j;
+        for (int r = 0; r < bw / 32; ++r) s[orow * nkb + kb0 * (bw / 32) + r] = (uint8_t)(e + 127);
+        for (int j = 0; j < bw; ++j) {
+          const int64_t k = kb0 * bw + j;
           const float v = y[t][j] * inv_scale;
           int code;
           if (p->rounding == ORC_ROUND_SR) {

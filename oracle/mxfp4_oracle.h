@@ -21,7 +21,7 @@
 extern "C" {
 #endif
 
-enum { ORC_BLOCK_1X32 = 0, ORC_BLOCK_32X32 = 1 };
+enum { ORC_BLOCK_1X32 = 0, ORC_BLOCK_32X32 = 1, ORC_BLOCK_64X64 = 2 };
 enum { ORC_SCALE_FLOOR = 0, ORC_SCALE_ROUNDUP = 1 };
 enum { ORC_ROUND_RTN = 0, ORC_ROUND_SR = 1 };
 enum { ORC_LAYOUT_ROWMAJOR = 0, ORC_LAYOUT_MMA = 1 };

@@ -309,6 +309,58 @@ def test_32x32_blocks_are_transposition_invariant():
         assert np.all(sr.reshape(4, 32, 3) == sr.reshape(4, 32, 3)[:, :1, :])
 
 
+@pytest.mark.parametrize("mode", [oracle.SCALE_FLOOR, oracle.SCALE_ROUNDUP])
+def test_64x64_blocks_by_elementwise_definition(mode):
+    """64x64 blocks (TIBQ "The evidence", Table 4): one scale per aligned 64x64
+    tile from the tile's max-abs, stored on each row for both of its 32-runs;
+    each code is nearest-even of x / 2^e. Checked element by element against
+    numpy tile maxima and the pinned scalar exponent and rounding; the tile
+    exponent is also the largest of its four 32x32 exponents."""
+    rows, cols = 128, 192
+    xb = _bf16(synth.student_t(rows, cols, 3.0, seed=61))
+    xf = xb.view(np.uint16).astype(np.uint32) << 16
+    xv = xf.view(np.float32).reshape(rows, cols)
+    p = oracle.Params(block=oracle.BLOCK_64X64, scale_mode=mode)
+    q, s = oracle.quantize_rows(xb, p)
+    s32 = oracle.quantize_rows(xb, oracle.Params(block=oracle.BLOCK_32X32, scale_mode=mode))[1]
+    for ti in range(rows // 64):
+        for tj in range(cols // 64):
+            tile = xv[64 * ti:64 * ti + 64, 64 * tj:64 * tj + 64]
+            e = oracle.scale_exponent(float(np.max(np.abs(tile))), mode)
+            sb = s[64 * ti:64 * ti + 64, 2 * tj:2 * tj + 2]
+            assert np.all(sb == e + 127)
+            assert e + 127 == int(s32[64 * ti:64 * ti + 64, 2 * tj:2 * tj + 2].max())
+            for r in range(64):
+                for c in range(64):
+                    rr, cc = 64 * ti + r, 64 * tj + c
+                    code = (int(q[rr, cc // 2]) >> (4 * (cc & 1))) & 0xF
+                    assert code == oracle.round_rtn(float(tile[r, c]) * 2.0 ** -e)
+
+
+def test_64x64_blocks_are_transposition_invariant_and_rotate_per_run():
+    x = _bf16(synth.normal(128, 192, 0.02, seed=62))
+    p = oracle.Params(block=oracle.BLOCK_64X64, scale_mode=oracle.SCALE_ROUNDUP)
+    qr, sr = oracle.quantize_rows(x, p)
+    qc, sc = oracle.quantize_cols(x, p)
+    dr = oracle.dequantize(qr, sr, 128, 192)
+    dc = oracle.dequantize(qc, sc, 192, 128)
+    assert np.array_equal(dr, dc.T)
+    # with the rotation: the tile scale comes from the rotated 32-runs
+    mask = synth.sign_mask(62)
+    pw = oracle.Params(block=oracle.BLOCK_64X64, scale_mode=oracle.SCALE_ROUNDUP, wht=True,
+                       wht_sign_mask=mask)
+    _, sw = oracle.quantize_rows(x, pw)
+    xv = (x.view(np.uint16).astype(np.uint32) << 16).view(np.float32).reshape(128, 192)
+    for ti in range(2):
+        for tj in range(3):
+            m = 0.0
+            for r in range(64 * ti, 64 * ti + 64):
+                for h in range(2):
+                    run = xv[r, 64 * tj + 32 * h:64 * tj + 32 * h + 32]
+                    m = max(m, float(np.max(np.abs(oracle.wht32(run, mask)))))
+            assert int(sw[64 * ti, 2 * tj]) == oracle.scale_exponent(m, oracle.SCALE_ROUNDUP) + 127
+
+
 def test_1x32_blocks_disagree_under_transposition():
     """1D blocks: the same element gets different scales in the two orientations."""
     x = _bf16(synth.student_t(128, 128, 4.0, seed=41))
