@@ -16,6 +16,7 @@ Calls (same names as the C ABI):
 from .binding import (  # noqa: F401
     BLOCK_1X32,
     BLOCK_32X32,
+    BLOCK_64X64,
     DTYPE_BF16,
     DTYPE_F32,
     LAYOUT_MMA,

@@ -15,7 +15,7 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libmxfp4.so"
 
-BLOCK_1X32, BLOCK_32X32 = 0, 1
+BLOCK_1X32, BLOCK_32X32, BLOCK_64X64 = 0, 1, 2
 SCALE_FLOOR, SCALE_ROUNDUP = 0, 1
 ROUND_RTN, ROUND_SR = 0, 1
 LAYOUT_ROWMAJOR, LAYOUT_MMA = 0, 1

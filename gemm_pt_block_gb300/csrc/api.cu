@@ -33,8 +33,12 @@ mxfp4_status check_params(const mxfp4_quant_params* p, uint8_t* q, uint8_t* s, i
   if ((!q || !s) && out_rows * k > 0)
     return fail(MXFP4_ERR_INVALID_ARG, "%s: output pointers must be non-NULL", name);
   if (!aligned16(q)) return fail(MXFP4_ERR_ALIGN, "%s: codes pointer not 16-byte aligned", name);
-  if (p->block != MXFP4_BLOCK_1X32 && p->block != MXFP4_BLOCK_32X32)
+  if (p->block != MXFP4_BLOCK_1X32 && p->block != MXFP4_BLOCK_32X32 &&
+      p->block != MXFP4_BLOCK_64X64)
     return fail(MXFP4_ERR_INVALID_ARG, "%s: bad block %d", name, p->block);
+  if (p->block == MXFP4_BLOCK_64X64 && (out_rows % 64 != 0 || k % 64 != 0))
+    return fail(MXFP4_ERR_SHAPE, "%s: 64x64 blocks need rows %% 64 == 0 and K %% 64 == 0 (got %lld x %lld)",
+                name, (long long)out_rows, (long long)k);
   if (p->scale_mode != MXFP4_SCALE_FLOOR && p->scale_mode != MXFP4_SCALE_ROUNDUP)
     return fail(MXFP4_ERR_INVALID_ARG, "%s: bad scale_mode %d", name, p->scale_mode);
   if (p->rounding != MXFP4_ROUND_RTN && p->rounding != MXFP4_ROUND_SR)
@@ -101,7 +105,7 @@ mxfp4_status mxfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int64_
   if (st) return st;
   if (rows > 0 && cols / 16 > (int64_t)0xFFFFFFFF / rows)
     return fail(MXFP4_ERR_SHAPE, "tensor too large: rows * cols / 16 must be below 2^32");
-  const bool need_rows32 = col || (row && row->block == MXFP4_BLOCK_32X32);
+  const bool need_rows32 = col || (row && row->block != MXFP4_BLOCK_1X32);
   if (need_rows32 && rows % 32 != 0)
     return fail(MXFP4_ERR_SHAPE, "rows (%lld) must be a multiple of 32 for column-wise or 32x32 output",
                 (long long)rows);
@@ -164,6 +168,9 @@ mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uin
                                  int64_t ldc, const mxfp4_quant_params* out, uint8_t* q_out,
                                  uint8_t* s_out, void* stream) {
   if (!out) return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_gemm_quantize: out params are required");
+  if (out->block == MXFP4_BLOCK_64X64)
+    return fail(MXFP4_ERR_UNSUPPORTED,
+                "mxfp4_gemm_quantize: 64x64 blocks span two epilogue warps; quantize C separately");
   mx::OrientArgs qo{};
   if (M > 0 && N > 0) {
     mxfp4_status st = check_params(out, q_out, s_out, M, N, "out", &qo);

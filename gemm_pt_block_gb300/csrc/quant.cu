@@ -266,6 +266,15 @@ __device__ __forceinline__ void named_sync_consumers() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 }
 
+// 64x64 blocks: each of the four consumer warps holds the max of one 32x32
+// quarter of the tile; combine them through shared memory. Every consumer
+// warp calls this (it contains a barrier of the four).
+__device__ __forceinline__ float tile_max4(float m, float* slots, int warp, int lane) {
+  if (lane == 0) slots[warp] = m;
+  named_sync_consumers();
+  return fmaxf(fmaxf(slots[0], slots[1]), fmaxf(slots[2], slots[3]));
+}
+
 // Bounded wait; false on timeout (which also raises the CTA's abort flag and
 // the library error word) or when the CTA has already aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t par, uint32_t* abort_flag) {
@@ -284,7 +293,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t par, uint32
   }
 }
 
-template <typename InT>
+template <typename InT, bool kSq64>
 __global__ void __launch_bounds__(kTileThreads, 3)
 quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols,
                   uint32_t ntiles, FastDiv tiles_x, const __grid_constant__ OrientArgs orow,
@@ -348,6 +357,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
   }
 
   // --------------------------------------------------------------- consumers
+  __shared__ float bmax[2][2][4];   // [tile parity][orientation][warp]: 64x64 maxima
   const bool share = do_row && do_col && same_draws(orow, ocol);
   uint32_t j = 0;
   for (uint32_t tl = blockIdx.x; tl < ntiles; tl += gridDim.x, ++j) {
@@ -360,65 +370,142 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
     int64_t R0, C0;
     origin(tl, R0, C0);
 
-    // ---- phase 1: rows ----
-    if (ok) {
-      const int rl = 32 * (warp & 1) + lane, cl = 32 * (warp >> 1);
-      const int64_t r = R0 + rl, c = C0 + cl;
-      const bool valid = r < rows && c < cols;
-      float2 R[16];
-      read_run(st, rl, cl, R, InT());
-      uint32_t w[16];
-      if (do_col && ocol.sr) {
-        draws32(ocol.keys, ocol.stream, (uint64_t)(r * cols + c), w);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<uint4*>(tb + tile_off(rl, cl + 8 * i, uint16_t())) =
-              make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-      }
-      if (do_row) {
-        if (orow.wht) hadamard32_lane(R, orow.sign_mask);
-        float M = absmax32(R);
-        if (orow.block) M = warp_max(M);
-        if (orow.sr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
-        int e;
-        const uint4 packed = finish32(R, orow, M, w, &e);
-        if (valid) {
-          *reinterpret_cast<uint4*>(orow.q + r * (cols >> 1) + (c >> 1)) = packed;
-          store_scale(orow, r, c >> 5, cols >> 5, e);
+    if constexpr (!kSq64) {
+      // ---- phase 1: rows ----
+      if (ok) {
+        const int rl = 32 * (warp & 1) + lane, cl = 32 * (warp >> 1);
+        const int64_t r = R0 + rl, c = C0 + cl;
+        const bool valid = r < rows && c < cols;
+        float2 R[16];
+        read_run(st, rl, cl, R, InT());
+        uint32_t w[16];
+        if (do_col && ocol.sr) {
+          draws32(ocol.keys, ocol.stream, (uint64_t)(r * cols + c), w);
+  #pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(tb + tile_off(rl, cl + 8 * i, uint16_t())) =
+                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+        if (do_row) {
+          if (orow.wht) hadamard32_lane(R, orow.sign_mask);
+          float M = absmax32(R);
+          if (orow.block) M = warp_max(M);
+          if (orow.sr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
+          int e;
+          const uint4 packed = finish32(R, orow, M, w, &e);
+          if (valid) {
+            *reinterpret_cast<uint4*>(orow.q + r * (cols >> 1) + (c >> 1)) = packed;
+            store_scale(orow, r, c >> 5, cols >> 5, e);
+          }
         }
       }
-    }
 
-    // ---- phase 2: columns (quantization of x^T along rows) ----
-    if (do_col) {
-      if (ocol.sr) named_sync_consumers();   // the draws were written by other warps
-      if (ok) {
+      // ---- phase 2: columns (quantization of x^T along rows) ----
+      if (do_col) {
+        if (ocol.sr) named_sync_consumers();   // the draws were written by other warps
+        if (ok) {
+          const int cl = 32 * (warp & 1) + lane, rl = 32 * (warp >> 1);
+          const int64_t oc = C0 + cl, k0 = R0 + rl;
+          const bool valid = oc < cols && k0 < rows;
+          float2 R[16];
+          uint32_t o[8];
+          col_offsets(rl, cl, o, InT());
+          read_col(st, o, R, InT());
+          if (ocol.wht) hadamard32_lane(R, ocol.sign_mask);
+          float M = absmax32(R);
+          if (ocol.block) M = warp_max(M);
+          uint32_t w[16];
+          if (ocol.sr) {
+            uint32_t ob[8];   // the draw buffer is laid out like a bf16 tile
+            col_offsets(rl, cl, ob, uint16_t());
+  #pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const uint32_t a = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k) & 7] + 1024 * (k >> 2));
+              const uint32_t b = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k + 1) & 7] + 1024 * (k >> 2));
+              w[k] = a | (b << 16);
+            }
+          }
+          int e;
+          const uint4 packed = finish32(R, ocol, M, w, &e);
+          if (valid) {
+            *reinterpret_cast<uint4*>(ocol.q + oc * (rows >> 1) + (k0 >> 1)) = packed;
+            store_scale(ocol, oc, k0 >> 5, rows >> 5, e);
+          }
+        }
+      }
+    } else {
+      // 64x64 blocks: the block max needs all four consumer warps, so the
+      // barriers sit outside the per-warp "ok" branches.
+      // ---- phase 1: rows ----
+      {
+        const int rl = 32 * (warp & 1) + lane, cl = 32 * (warp >> 1);
+        const int64_t r = R0 + rl, c = C0 + cl;
+        const bool valid = r < rows && c < cols;
+        float2 R[16];
+        uint32_t w[16];
+        float M = 0.0f;
+        if (ok) {
+          read_run(st, rl, cl, R, InT());
+          if (do_col && ocol.sr) {
+            draws32(ocol.keys, ocol.stream, (uint64_t)(r * cols + c), w);
+  #pragma unroll
+            for (int i = 0; i < 4; ++i)
+              *reinterpret_cast<uint4*>(tb + tile_off(rl, cl + 8 * i, uint16_t())) =
+                  make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+          if (do_row) {
+            if (orow.wht) hadamard32_lane(R, orow.sign_mask);
+            M = absmax32(R);
+            if (orow.block) M = warp_max(M);
+          }
+        }
+        if (do_row && orow.block == 2) M = tile_max4(M, bmax[j & 1][0], warp, lane);
+        if (ok && do_row) {
+          if (orow.sr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
+          int e;
+          const uint4 packed = finish32(R, orow, M, w, &e);
+          if (valid) {
+            *reinterpret_cast<uint4*>(orow.q + r * (cols >> 1) + (c >> 1)) = packed;
+            store_scale(orow, r, c >> 5, cols >> 5, e);
+          }
+        }
+      }
+
+      // ---- phase 2: columns (quantization of x^T along rows) ----
+      if (do_col) {
+        if (ocol.sr) named_sync_consumers();   // the draws were written by other warps
         const int cl = 32 * (warp & 1) + lane, rl = 32 * (warp >> 1);
         const int64_t oc = C0 + cl, k0 = R0 + rl;
         const bool valid = oc < cols && k0 < rows;
         float2 R[16];
-        uint32_t o[8];
-        col_offsets(rl, cl, o, InT());
-        read_col(st, o, R, InT());
-        if (ocol.wht) hadamard32_lane(R, ocol.sign_mask);
-        float M = absmax32(R);
-        if (ocol.block) M = warp_max(M);
-        uint32_t w[16];
-        if (ocol.sr) {
-          uint32_t ob[8];   // the draw buffer is laid out like a bf16 tile
-          col_offsets(rl, cl, ob, uint16_t());
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const uint32_t a = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k) & 7] + 1024 * (k >> 2));
-            const uint32_t b = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k + 1) & 7] + 1024 * (k >> 2));
-            w[k] = a | (b << 16);
-          }
+        float M = 0.0f;
+        if (ok) {
+          uint32_t o[8];
+          col_offsets(rl, cl, o, InT());
+          read_col(st, o, R, InT());
+          if (ocol.wht) hadamard32_lane(R, ocol.sign_mask);
+          M = absmax32(R);
+          if (ocol.block) M = warp_max(M);
         }
-        int e;
-        const uint4 packed = finish32(R, ocol, M, w, &e);
-        if (valid) {
-          *reinterpret_cast<uint4*>(ocol.q + oc * (rows >> 1) + (k0 >> 1)) = packed;
-          store_scale(ocol, oc, k0 >> 5, rows >> 5, e);
+        if (ocol.block == 2) M = tile_max4(M, bmax[j & 1][1], warp, lane);
+        if (ok) {
+          uint32_t w[16];
+          if (ocol.sr) {
+            uint32_t ob[8];   // the draw buffer is laid out like a bf16 tile
+            col_offsets(rl, cl, ob, uint16_t());
+  #pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const uint32_t a = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k) & 7] + 1024 * (k >> 2));
+              const uint32_t b = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k + 1) & 7] + 1024 * (k >> 2));
+              w[k] = a | (b << 16);
+            }
+          }
+          int e;
+          const uint4 packed = finish32(R, ocol, M, w, &e);
+          if (valid) {
+            *reinterpret_cast<uint4*>(ocol.q + oc * (rows >> 1) + (k0 >> 1)) = packed;
+            store_scale(ocol, oc, k0 >> 5, rows >> 5, e);
+          }
         }
       }
     }
@@ -528,14 +615,19 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
   int dev = 0;
   cudaGetDevice(&dev);
   if (!attr_set[dev & 63]) {
-    cudaFuncSetAttribute(quant_tile_kernel<InT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(quant_tile_kernel<InT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         smem);
+    cudaFuncSetAttribute(quant_tile_kernel<InT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         smem);
     attr_set[dev & 63] = true;
   }
   OrientArgs dummy{};
   const int64_t tx = (cols + kTile - 1) / kTile, ty = (rows + kTile - 1) / kTile;
-  const unsigned grid = resident_ctas(quant_tile_kernel<InT>, tx * ty, smem, kTileThreads);
+  const bool sq64 = (row && row->block == 2) || (col && col->block == 2);
+  auto kern = sq64 ? quant_tile_kernel<InT, true> : quant_tile_kernel<InT, false>;
+  const unsigned grid = resident_ctas(quant_tile_kernel<InT, false>, tx * ty, smem, kTileThreads);
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
-  quant_tile_kernel<InT><<<grid, kTileThreads, smem, st>>>(
+  kern<<<grid, kTileThreads, smem, st>>>(
       tm, rows, cols, (uint32_t)(tx * ty), make_fastdiv((uint32_t)tx), row ? *row : dummy,
       col ? *col : dummy, row != nullptr, col != nullptr);
   return cudaGetLastError();

@@ -54,7 +54,7 @@ typedef enum {
   MXFP4_ERR_TIMEOUT = 6      /* a bounded device-side wait ran out */
 } mxfp4_status;
 
-enum { MXFP4_BLOCK_1X32 = 0, MXFP4_BLOCK_32X32 = 1 };
+enum { MXFP4_BLOCK_1X32 = 0, MXFP4_BLOCK_32X32 = 1, MXFP4_BLOCK_64X64 = 2 };
 enum { MXFP4_SCALE_FLOOR = 0, MXFP4_SCALE_ROUNDUP = 1 };
 enum { MXFP4_ROUND_RTN = 0, MXFP4_ROUND_SR = 1 };
 enum { MXFP4_LAYOUT_ROWMAJOR = 0, MXFP4_LAYOUT_MMA = 1 };
@@ -66,6 +66,10 @@ enum { MXFP4_DTYPE_BF16 = 0, MXFP4_DTYPE_F32 = 1 };
  *               MXFP4_BLOCK_32X32: the aligned 32 x 32 tile shares one scale,
  *               written on each of its 32 rows of the scale array [TIBQ,
  *               "The fix, and its supporting cast", 2D blocks].
+ *               MXFP4_BLOCK_64X64: the aligned 64 x 64 tile shares one scale,
+ *               written on each of its 64 rows for both of its 32-runs [TIBQ,
+ *               "The evidence", Table 4 block sizes]; needs rows and K
+ *               multiples of 64 (not available in mxfp4_gemm_quantize).
  *  scale_mode   MXFP4_SCALE_FLOOR: e = floor(log2 M) - 2 (OCP Microscaling
  *               v1.0; the block max may saturate at 6).
  *               MXFP4_SCALE_ROUNDUP: e = ceil(log2(M / 6)), nothing clips

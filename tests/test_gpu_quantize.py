@@ -59,6 +59,52 @@ def test_quantize_matrix_mma_layout(orient, block, rnd, wht):
     assert_same(got, want, f"{orient} mma")
 
 
+@pytest.mark.parametrize("orient", ["row", "col", "both"])
+@pytest.mark.parametrize("scale,rnd", list(itertools.product(SCALES, ROUNDS)))
+@pytest.mark.parametrize("wht", WHTS, ids=["nowht", "detwht", "rndwht"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_quantize_64x64_blocks(orient, scale, rnd, wht, dtype):
+    """64x64 square blocks: the four consumer warps' 32x32 maxima are combined
+    per tile; 192 x 320 (3 x 5 tiles)."""
+    rows, cols = 192, 320
+    x = _input(rows, cols, dtype, seed=91 + scale)
+    p = oracle.Params(block=oracle.BLOCK_64X64, scale_mode=scale, rounding=rnd, wht=wht[0],
+                      wht_sign_mask=wht[1], seed=0x5EED, sr_stream=4)
+    prow = p if orient in ("row", "both") else None
+    pcol = p if orient in ("col", "both") else None
+    got = gpu_quantize(x.to(DEV), prow, pcol)
+    want = oracle_quantize(oracle_input(x), prow, pcol)
+    assert_same(got, want, f"64x64 {orient}")
+
+
+@pytest.mark.parametrize("pair", ["64row_32col", "1row_64col", "64both_mma"])
+def test_quantize_64x64_mixed_and_mma(pair):
+    rows, cols = 256, 384
+    x = _input(rows, cols, "bf16", seed=93)
+    b64 = oracle.Params(block=oracle.BLOCK_64X64, scale_mode=oracle.SCALE_ROUNDUP,
+                        rounding=oracle.ROUND_SR, seed=3, sr_stream=1)
+    if pair == "64row_32col":
+        prow, pcol, lay = b64, oracle.Params(block=oracle.BLOCK_32X32, rounding=oracle.ROUND_SR,
+                                            wht=True, wht_sign_mask=0x1357, seed=3, sr_stream=1), 0
+    elif pair == "1row_64col":
+        prow, pcol, lay = oracle.Params(), b64, 0
+    else:
+        prow, pcol, lay = b64, b64, 1
+    got = gpu_quantize(x.to(DEV), prow, pcol, lay, lay)
+    want = oracle_quantize(oracle_input(x), prow, pcol, lay, lay)
+    assert_same(got, want, pair)
+
+
+def test_quantize_64x64_rejects_unaligned_shapes():
+    import gemm_pt_block_gb300 as mx
+
+    p = mx.QuantParams(block=mx.BLOCK_64X64)
+    with pytest.raises(mx.Mxfp4Error):
+        mx.mxfp4_quantize(torch.zeros(96, 128, device=DEV, dtype=torch.bfloat16), p)
+    with pytest.raises(mx.Mxfp4Error):
+        mx.mxfp4_quantize(torch.zeros(128, 96, device=DEV, dtype=torch.bfloat16), p)
+
+
 def test_quantize_mixed_orientation_params():
     """Row-wise RTN/floor next to column-wise rotated SR/round-up in one pass."""
     x = synth.laplace(256, 512, 1e-3, seed=41, outlier_frac=0.001)
