@@ -243,6 +243,26 @@ def _dist():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(value: float, ws: int, device="cpu") -> float:
+    """The largest `value` over all ranks (the job is as slow as its slowest
+    replica); a no-op for one rank. `device` must suit the process group's
+    backend (a CUDA device for NCCL, the CPU for gloo)."""
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(work_per_rank: float, ws: int, ms: float) -> float:
+    """Whole-job throughput: the work of all replicas over the (max) step time,
+    per second (weak scaling: every rank does the same work)."""
+    return ws * work_per_rank / (ms / 1e3)
+
+
 class ClockSampler:
     """Samples nvidia-smi SM clocks and throttle reasons while the block runs."""
 
@@ -423,12 +443,9 @@ def measure_e2e(st: Step, steps: int, ws: int):
     e.record()
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
-    if ws > 1:
-        t = torch.tensor([ms], device=next(iter(st.outs.values())).device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, ws, next(iter(st.outs.values())).device)
     flops = sum(st.spec.gemm_flops())
-    return {"value": ws * flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+    return {"value": job_rate(flops, ws, ms) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
 
 
@@ -638,11 +655,7 @@ def main():
             st.run(events=evs[i])
         t1.record()
         barrier()
-    total_ms = t0.elapsed_time(t1)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), ws, device)
     ms_step = total_ms / args.steps
     per_launch = [statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
                   for j in range(st.launches)]
@@ -656,7 +669,7 @@ def main():
     labels = spec.labels()
     gemm_tflops = sum(gwork) / (sum(g_ms) / 1e3) / 1e12
     quant_gbs = sum(qwork) / (sum(q_ms) / 1e3) / 1e9
-    value = ws * sum(gwork) / (ms_step / 1e3) / 1e12
+    value = job_rate(sum(gwork), ws, ms_step) / 1e12
 
     # Dominant kernel by share of the step: the GEMM (per-launch average).
     achieved = statistics.mean(f / (m / 1e3) / 1e12 for f, m in zip(gwork, g_ms))
