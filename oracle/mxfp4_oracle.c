@@ -143,7 +143,9 @@ void orc_wht32(const float in[32], uint32_t sign_mask, int inverse, float out[32
  * M == 0 gives e = -127. e is clamped to the E8M0 range [-127, 127]; the
  * stored byte is e + 127 (0xFF, the E8M0 NaN, is never produced).
  * Computed with exact fp64 frexp/ldexp. */
-int orc_scale_exponent(float M, int scale_mode) {
+int orc_scale_exponent_fmt(float M, int scale_mode, int elem_format) {
+  const int emax = elem_format == ORC_FORMAT_E4M3 ? 8 : 2;         /* exponent of the largest element */
+  const double vmax = elem_format == ORC_FORMAT_E4M3 ? 448.0 : 6.0; /* largest element value */
   int e;
   if (!(M > 0.0f)) {
     e = -127;
@@ -151,15 +153,48 @@ int orc_scale_exponent(float M, int scale_mode) {
     int E2;
     (void)frexp((double)M, &E2);      /* M = m * 2^E2, m in [0.5, 1) */
     int fl = E2 - 1;                  /* floor(log2 M) */
-    e = fl - 2;
+    e = fl - emax;
     if (scale_mode == ORC_SCALE_ROUNDUP) {
-      while (ldexp(6.0, e) < (double)M) ++e;      /* smallest e: 6*2^e >= M */
-      while (ldexp(6.0, e - 1) >= (double)M) --e;
+      while (ldexp(vmax, e) < (double)M) ++e;      /* smallest e: vmax*2^e >= M */
+      while (ldexp(vmax, e - 1) >= (double)M) --e;
     }
   }
   if (e < -127) e = -127;
   if (e > 127) e = 127;
   return e;
+}
+
+int orc_scale_exponent(float M, int scale_mode) {
+  return orc_scale_exponent_fmt(M, scale_mode, ORC_FORMAT_E2M1);
+}
+
+/* -------------------------------------------------------------- E4M3 ---- */
+/* MXFP8 element format [TIBQ, "The fix, and its supporting cast": MXFP8 for
+ * queries and keys; the OCP Microscaling v1.0 family the News page names]. */
+float orc_e4m3_value(int code) {
+  const int sgn = (code >> 7) & 1, E = (code >> 3) & 15, m = code & 7;
+  double v;
+  if (E == 15 && m == 7) return NAN;
+  if (E == 0)
+    v = ldexp((double)m, -9);                       /* subnormal: m/8 * 2^-6 */
+  else
+    v = ldexp(1.0 + m / 8.0, E - 7);
+  return (float)(sgn ? -v : v);
+}
+
+int orc_round_e4m3_rtn(float v) {
+  double a = fabs((double)v);
+  if (a > 448.0) a = 448.0;                         /* saturate */
+  int best = 0;
+  double bestd = a;
+  for (int k = 1; k < 127; ++k) {                   /* the finite non-negative codes */
+    const double d = fabs(a - (double)orc_e4m3_value(k));
+    if (d < bestd || (d == bestd && (k % 2) == 0 && (best % 2) != 0)) {
+      best = k;
+      bestd = d;
+    }
+  }
+  return (signbit(v) ? 0x80 : 0) | best;
 }
 
 /* ------------------------------------------------------------ rounding ---- */
@@ -233,7 +268,10 @@ static int quantize_orient(const void* x, int dtype, int64_t rows, int64_t cols,
   /* g output rows by bw values of k share one scale */
   const int g = p->block == ORC_BLOCK_64X64 ? 64 : (p->block == ORC_BLOCK_32X32 ? 32 : 1);
   const int bw = p->block == ORC_BLOCK_64X64 ? 64 : 32;
+  const int e4m3 = p->elem_format == ORC_FORMAT_E4M3;
   if (K % bw != 0 || i0 < 0 || i1 > nout || i0 > i1) return -1;
+  if (p->elem_format != ORC_FORMAT_E2M1 && !e4m3) return -1;
+  if (e4m3 && p->rounding != ORC_ROUND_RTN) return -1;   /* nearest only for MXFP8 */
   if (g > 1 && (nout % g != 0 || i0 % g != 0 || i1 % g != 0)) return -1;
   const int64_t nkb = K / 32;
   const int64_t ngroups = (i1 - i0) / g;
@@ -263,7 +301,7 @@ static int quantize_orient(const void* x, int dtype, int64_t rows, int64_t cols,
           if (a > M) M = a;
         }
       }
-      const int e = orc_scale_exponent(M, p->scale_mode);
+      const int e = orc_scale_exponent_fmt(M, p->scale_mode, p->elem_format);
       const float inv_scale = ldexpf(1.0f, -e); /* 2^-e, exact (2^-127 is subnormal) */
       for (int t = 0; t < g; ++t) {
         const int64_t i = ib + t;
@@ -273,6 +311,10 @@ static int quantize_orient(const void* x, int dtype, int64_t rows, int64_t cols,
           const int64_t k = kb0 * bw + j;
           const float v = y[t][j] * inv_scale;
           int code;
+          if (e4m3) {
+            q[orow * K + k] = (uint8_t)orc_round_e4m3_rtn(v);
+            continue;
+          }
           if (p->rounding == ORC_ROUND_SR) {
             const int64_t src = col_orient ? (k * cols + i) : (i * cols + k);
             code = orc_round_sr(v, orc_sr_bits(p->seed, p->sr_stream, (uint64_t)src));
@@ -361,6 +403,19 @@ int orc_dequantize_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t r
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t c = 0; c < cols; ++c)
       out[r * cols + c] = deq_one(q, s, layout, rows, cols, r, c);
+  return 0;
+}
+
+int orc_dequantize_e4m3_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
+                            int64_t cols, double* out) {
+  if (deq_check(layout, rows, cols)) return -1;
+  const int64_t nkb = cols / 32;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      const uint8_t sb = (layout == ORC_LAYOUT_MMA) ? s[orc_mma_scale_offset(r, c / 32, rows, nkb)]
+                                                    : s[r * nkb + c / 32];
+      out[r * cols + c] = sb == 0xFF ? NAN : ldexp((double)orc_e4m3_value(q[r * cols + c]), (int)sb - 127);
+    }
   return 0;
 }
 

@@ -26,6 +26,7 @@ enum { ORC_SCALE_FLOOR = 0, ORC_SCALE_ROUNDUP = 1 };
 enum { ORC_ROUND_RTN = 0, ORC_ROUND_SR = 1 };
 enum { ORC_LAYOUT_ROWMAJOR = 0, ORC_LAYOUT_MMA = 1 };
 enum { ORC_DTYPE_BF16 = 0, ORC_DTYPE_F32 = 1 };
+enum { ORC_FORMAT_E2M1 = 0, ORC_FORMAT_E4M3 = 1 };
 
 typedef struct {
   int block;              /* ORC_BLOCK_* */
@@ -36,6 +37,7 @@ typedef struct {
   uint32_t wht_sign_mask; /* bit i set => sign -1 on element i of a block */
   uint64_t seed;          /* Philox key */
   uint32_t sr_stream;     /* Philox counter word 2 */
+  int elem_format;        /* ORC_FORMAT_*: E2M1 (MXFP4) or E4M3 (MXFP8, nearest only) */
 } orc_params;
 
 /* E2M1 code (4 bits, bit 3 = sign) -> value. */
@@ -57,9 +59,21 @@ int orc_scale_exponent(float M, int scale_mode);
 int orc_round_rtn(float v);
 int orc_round_sr(float v, uint32_t r16);
 
+/* OCP FP8 E4M3 (8 bits: sign, 4 exponent bits with bias 7, 3 mantissa bits;
+ * no infinities, S.1111.111 is NaN, largest finite 448): code -> value, and
+ * the nearest code to v (ties to the even code, saturating at 448, sign kept). */
+float orc_e4m3_value(int code);
+int orc_round_e4m3_rtn(float v);
+
+/* Scale exponent for an element format: floor: floor(log2 M) - emax (emax 2
+ * for E2M1, 8 for E4M3); round-up: the smallest e with max * 2^e >= M (max 6
+ * or 448). orc_scale_exponent is the E2M1 case. */
+int orc_scale_exponent_fmt(float M, int scale_mode, int elem_format);
+
 /* Row-wise quantization of rows [r0, r1) of x [rows, cols] (leading dim ld,
- * elements), along cols. q: [(r1-r0), cols/2] bytes, s: [(r1-r0), cols/32]
- * bytes, both row-major. Returns 0 on success, nonzero on bad arguments. */
+ * elements), along cols. q: [(r1-r0), cols/2] bytes (E4M3: [(r1-r0), cols]),
+ * s: [(r1-r0), cols/32] bytes, both row-major. Returns 0 on success, nonzero
+ * on bad arguments. */
 int orc_quantize_rows(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
                       const orc_params* p, int64_t r0, int64_t r1, uint8_t* q, uint8_t* s);
 
@@ -81,6 +95,9 @@ int orc_dequantize_f32(const uint8_t* q, const uint8_t* s, int layout, int64_t r
                        int64_t cols, float* out);
 int orc_dequantize_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
                        int64_t cols, double* out);
+/* The same for E4M3 codes q [rows, cols] (one byte per element). */
+int orc_dequantize_e4m3_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
+                            int64_t cols, double* out);
 
 /* Stand-alone rotation along cols of x; y [rows, cols] fp32 row-major. */
 int orc_hadamard32(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,

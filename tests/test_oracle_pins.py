@@ -471,3 +471,84 @@ def test_gemm_ref_agrees_with_pairs():
     c, a = oracle.gemm_pairs(qa, sa, qb, sb, M, N, K, ms, ns)
     assert np.allclose(C[ms, ns], c, rtol=0, atol=1e-12 * a.max())
     assert np.allclose(A[ms, ns], a, rtol=1e-14)
+
+
+# ------------------------------------------------------------ MXFP8 (E4M3) --
+
+def test_e4m3_decode_matches_torch_float8_e4m3fn():
+    """All 256 E4M3 codes decode like PyTorch's float8_e4m3fn (OCP FP8 E4M3:
+    bias 7, no infinities, S.1111.111 = NaN, largest finite 448)."""
+    import torch
+
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).float().numpy()
+    for c in range(256):
+        got = oracle.e4m3_value(c)
+        if np.isnan(ref[c]):
+            assert math.isnan(got)
+        else:
+            assert got == ref[c], c
+
+
+def test_e4m3_nearest_even_matches_torch_and_saturates():
+    import torch
+
+    vals = [oracle.e4m3_value(c) for c in range(127)]          # 0 .. 448
+    pts = []
+    for a, b in zip(vals[:-1], vals[1:]):
+        mid = (a + b) / 2
+        pts += [a, mid, np.nextafter(np.float32(mid), np.float32(0)),
+                np.nextafter(np.float32(mid), np.float32(1e9)), b]
+    rng = np.random.default_rng(71)
+    pts += list(rng.uniform(0, 448, 4000).astype(np.float32))
+    pts += list((2.0 ** rng.uniform(-14, -6, 1000)).astype(np.float32))   # subnormal range
+    x = np.array(pts, dtype=np.float32)
+    x = np.concatenate([x, -x])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for v, r in zip(x, ref):
+        assert oracle.round_e4m3_rtn(float(v)) == int(r), float(v)
+    for v in (448.0, 460.0, 464.0, 1000.0, 3.0e38):
+        assert oracle.round_e4m3_rtn(v) == 0x7E
+        assert oracle.round_e4m3_rtn(-v) == 0xFE
+
+
+def test_e4m3_scale_exponent_definitions():
+    rng = np.random.default_rng(72)
+    for M in list(2.0 ** rng.uniform(-100, 100, 300)) + [448.0, 449.0, 896.0, 1.0, 0.75]:
+        M = float(np.float32(M))
+        fl = math.floor(math.log2(Fraction(M))) if M > 0 else None
+        ef = oracle.scale_exponent_fmt(M, oracle.SCALE_FLOOR, oracle.FORMAT_E4M3)
+        eu = oracle.scale_exponent_fmt(M, oracle.SCALE_ROUNDUP, oracle.FORMAT_E4M3)
+        # floor(log2 M) from exact rational comparison
+        while Fraction(2) ** (fl + 1) <= Fraction(M):
+            fl += 1
+        while Fraction(2) ** fl > Fraction(M):
+            fl -= 1
+        assert ef == max(-127, min(127, fl - 8))
+        assert 448 * Fraction(2) ** eu >= Fraction(M) > 448 * Fraction(2) ** (eu - 1)
+
+
+def test_mxfp8_quantize_by_elementwise_definition():
+    """1x32 and 32x32 MXFP8 blocks: e from the block max (pinned exponent), each
+    byte the nearest E4M3 code of x / 2^e (pinned rounding)."""
+    rows, cols = 64, 96
+    xb = _bf16(synth.student_t(rows, cols, 3.0, seed=73))
+    xv = (xb.view(np.uint16).astype(np.uint32) << 16).view(np.float32).reshape(rows, cols)
+    for block, g in ((oracle.BLOCK_1X32, 1), (oracle.BLOCK_32X32, 32)):
+        for mode in (oracle.SCALE_FLOOR, oracle.SCALE_ROUNDUP):
+            p = oracle.Params(block=block, scale_mode=mode, elem_format=oracle.FORMAT_E4M3)
+            q, s = oracle.quantize_rows(xb, p)
+            assert q.shape == (rows, cols)
+            for r0 in range(0, rows, g):
+                for kb in range(cols // 32):
+                    blk = xv[r0:r0 + g, 32 * kb:32 * kb + 32]
+                    e = oracle.scale_exponent_fmt(float(np.max(np.abs(blk))), mode, oracle.FORMAT_E4M3)
+                    assert np.all(s[r0:r0 + g, kb] == e + 127)
+                    for i in range(g):
+                        for j in range(32):
+                            want = oracle.round_e4m3_rtn(float(blk[i, j]) * 2.0 ** -e)
+                            assert q[r0 + i, 32 * kb + j] == want
+            d = oracle.dequantize(q, s, rows, cols, fmt=oracle.FORMAT_E4M3)
+            assert np.all(np.isfinite(d))
+    with pytest.raises(ValueError):    # stochastic rounding is MXFP4-only
+        oracle.quantize_rows(xb, oracle.Params(rounding=oracle.ROUND_SR, elem_format=oracle.FORMAT_E4M3))
