@@ -19,6 +19,8 @@ from .binding import (  # noqa: F401
     BLOCK_64X64,
     DTYPE_BF16,
     DTYPE_F32,
+    FORMAT_E2M1,
+    FORMAT_E4M3,
     LAYOUT_MMA,
     LAYOUT_ROWMAJOR,
     ROUND_RTN,

@@ -16,6 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libmxfp4.so"
 
 BLOCK_1X32, BLOCK_32X32, BLOCK_64X64 = 0, 1, 2
+FORMAT_E2M1, FORMAT_E4M3 = 0, 1
 SCALE_FLOOR, SCALE_ROUNDUP = 0, 1
 ROUND_RTN, ROUND_SR = 0, 1
 LAYOUT_ROWMAJOR, LAYOUT_MMA = 0, 1
@@ -43,7 +44,7 @@ class _CParams(ctypes.Structure):
         ("wht_sign_mask", ctypes.c_uint32),
         ("seed", ctypes.c_uint64),
         ("sr_stream", ctypes.c_uint32),
-        ("reserved", ctypes.c_uint32),
+        ("elem_format", ctypes.c_uint32),
     ]
 
 
@@ -58,11 +59,17 @@ class QuantParams:
     wht_sign_mask: int = 0
     seed: int = 0
     sr_stream: int = 0
+    elem_format: int = 0          # FORMAT_E2M1 (MXFP4) or FORMAT_E4M3 (MXFP8)
 
     def _c(self) -> _CParams:
         return _CParams(self.block, self.scale_mode, self.rounding, self.scale_layout,
                         int(bool(self.wht)), self.wht_sign_mask & 0xFFFFFFFF,
-                        self.seed & 0xFFFFFFFFFFFFFFFF, self.sr_stream & 0xFFFFFFFF, 0)
+                        self.seed & 0xFFFFFFFFFFFFFFFF, self.sr_stream & 0xFFFFFFFF,
+                        self.elem_format)
+
+    def code_cols(self, k: int) -> int:
+        """Bytes of codes per output row for K elements."""
+        return k if self.elem_format == FORMAT_E4M3 else k // 2
 
 
 _lib = None
@@ -157,10 +164,10 @@ def mxfp4_quantize(x: torch.Tensor, row: QuantParams | None = None, col: QuantPa
     ld = x.stride(0) if rows > 1 else cols
     dev = x.device
     if row is not None:
-        q_row = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev) if q_row is None else q_row
+        q_row = torch.empty((rows, row.code_cols(cols)), dtype=torch.uint8, device=dev) if q_row is None else q_row
         s_row = _scales_out(rows, cols, row, dev) if s_row is None else s_row
     if col is not None:
-        q_col = torch.empty((cols, rows // 2), dtype=torch.uint8, device=dev) if q_col is None else q_col
+        q_col = torch.empty((cols, col.code_cols(rows)), dtype=torch.uint8, device=dev) if q_col is None else q_col
         s_col = _scales_out(cols, rows, col, dev) if s_col is None else s_col
     rp = row._c() if row is not None else None
     cp = col._c() if col is not None else None
@@ -208,7 +215,7 @@ def mxfp4_gemm_quantize(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb
             raise ValueError(f"{n} must be a CUDA uint8 tensor")
     if c is None and with_c:
         c = torch.empty((M, N), dtype=torch.float32, device=qa.device)
-    q_out = torch.empty((M, N // 2), dtype=torch.uint8, device=qa.device) if q_out is None else q_out
+    q_out = torch.empty((M, out.code_cols(N)), dtype=torch.uint8, device=qa.device) if q_out is None else q_out
     s_out = _scales_out(M, N, out, qa.device) if s_out is None else s_out
     ldc = c.stride(0) if c is not None else N
     op = out._c()

@@ -46,7 +46,10 @@ mxfp4_status check_params(const mxfp4_quant_params* p, uint8_t* q, uint8_t* s, i
   if (p->scale_layout != MXFP4_LAYOUT_ROWMAJOR && p->scale_layout != MXFP4_LAYOUT_MMA)
     return fail(MXFP4_ERR_INVALID_ARG, "%s: bad scale_layout %d", name, p->scale_layout);
   if (p->wht != 0 && p->wht != 1) return fail(MXFP4_ERR_INVALID_ARG, "%s: wht must be 0/1", name);
-  if (p->reserved != 0) return fail(MXFP4_ERR_INVALID_ARG, "%s: reserved field must be 0", name);
+  if (p->elem_format != MXFP4_FORMAT_E2M1 && p->elem_format != MXFP4_FORMAT_E4M3)
+    return fail(MXFP4_ERR_INVALID_ARG, "%s: bad elem_format %u", name, p->elem_format);
+  if (p->elem_format == MXFP4_FORMAT_E4M3 && p->rounding == MXFP4_ROUND_SR)
+    return fail(MXFP4_ERR_UNSUPPORTED, "%s: stochastic rounding is available for E2M1 only", name);
   if (p->scale_layout == MXFP4_LAYOUT_MMA && (out_rows % 128 != 0 || k % 128 != 0))
     return fail(MXFP4_ERR_SHAPE,
                 "%s: tensor-core scale layout needs rows %% 128 == 0 and K %% 128 == 0 (got %lld x %lld)",
@@ -56,6 +59,7 @@ mxfp4_status check_params(const mxfp4_quant_params* p, uint8_t* q, uint8_t* s, i
   o->sr = p->rounding == MXFP4_ROUND_SR;
   o->mma_layout = p->scale_layout == MXFP4_LAYOUT_MMA;
   o->wht = p->wht;
+  o->e4m3 = p->elem_format == MXFP4_FORMAT_E4M3;
   o->sign_mask = p->wht_sign_mask;
   o->seed = p->seed;
   o->stream = p->sr_stream;

@@ -15,6 +15,7 @@ struct OrientArgs {
   int32_t sr;           // 0: nearest-even, 1: stochastic
   int32_t mma_layout;   // scale array layout: 0 row-major, 1 tensor-core tiles
   int32_t wht;          // rotate 32-runs along the quantization axis first
+  int32_t e4m3;         // element format: 0 E2M1 (MXFP4), 1 E4M3 (MXFP8)
   uint32_t sign_mask;
   uint64_t seed;
   uint32_t stream;

@@ -125,7 +125,7 @@ __device__ __forceinline__ uint2 quantize_halves(float2 (&R)[8], int upper, cons
     hadamard_halves(R, upper);
   }
   const float M = reduce(pair_absmax(R));
-  const int e = scale_exponent(M, o.roundup);
+  const int e = scale_exponent(M, o.roundup, o.e4m3);
   scale_all(R, inv_scale(e));
   if (o.sr) {
     uint32_t w[8];
@@ -133,7 +133,7 @@ __device__ __forceinline__ uint2 quantize_halves(float2 (&R)[8], int upper, cons
     sr16(R, w);
   }
   *e_out = e;
-  return encode16(R);
+  return o.e4m3 ? uint2{0u, 0u} : encode16(R);
 }
 
 // ------------------------------------------------- row-wise, 1x32 blocks ---
@@ -169,7 +169,10 @@ quant_rows_1x32_kernel(const InT* __restrict__ x, uint32_t total, FastDiv halves
     const uint2 packed = quantize_halves<InT>(R, upper, o, (uint64_t)((int64_t)r * cols + c0),
                                               [](float m) { return m; }, &e);
     if (valid) {
-      *reinterpret_cast<uint2*>(o.q + (int64_t)r * (cols >> 1) + (c0 >> 1)) = packed;
+      if (o.e4m3)
+        *reinterpret_cast<uint4*>(o.q + (int64_t)r * cols + c0) = encode16_e4m3(R);
+      else
+        *reinterpret_cast<uint2*>(o.q + (int64_t)r * (cols >> 1) + (c0 >> 1)) = packed;
       if (!upper) store_scale(o, r, c0 >> 5, cols >> 5, e);
     }
   }
@@ -391,10 +394,9 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           float M = absmax32(R);
           if (orow.block) M = warp_max(M);
           if (orow.sr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
-          int e;
-          const uint4 packed = finish32(R, orow, M, w, &e);
+          const int e = scale_run32<false>(R, orow, M, w);
           if (valid) {
-            *reinterpret_cast<uint4*>(orow.q + r * (cols >> 1) + (c >> 1)) = packed;
+            store_run32<false>(orow, r, c, cols, R);
             store_scale(orow, r, c >> 5, cols >> 5, e);
           }
         }
@@ -425,10 +427,9 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
               w[k] = a | (b << 16);
             }
           }
-          int e;
-          const uint4 packed = finish32(R, ocol, M, w, &e);
+          const int e = scale_run32<false>(R, ocol, M, w);
           if (valid) {
-            *reinterpret_cast<uint4*>(ocol.q + oc * (rows >> 1) + (k0 >> 1)) = packed;
+            store_run32<false>(ocol, oc, k0, rows, R);
             store_scale(ocol, oc, k0 >> 5, rows >> 5, e);
           }
         }
@@ -462,10 +463,9 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
         if (do_row && orow.block == 2) M = tile_max4(M, bmax[j & 1][0], warp, lane);
         if (ok && do_row) {
           if (orow.sr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
-          int e;
-          const uint4 packed = finish32(R, orow, M, w, &e);
+          const int e = scale_run32(R, orow, M, w);
           if (valid) {
-            *reinterpret_cast<uint4*>(orow.q + r * (cols >> 1) + (c >> 1)) = packed;
+            store_run32(orow, r, c, cols, R);
             store_scale(orow, r, c >> 5, cols >> 5, e);
           }
         }
@@ -500,10 +500,9 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
               w[k] = a | (b << 16);
             }
           }
-          int e;
-          const uint4 packed = finish32(R, ocol, M, w, &e);
+          const int e = scale_run32(R, ocol, M, w);
           if (valid) {
-            *reinterpret_cast<uint4*>(ocol.q + oc * (rows >> 1) + (k0 >> 1)) = packed;
+            store_run32(ocol, oc, k0, rows, R);
             store_scale(ocol, oc, k0 >> 5, rows >> 5, e);
           }
         }
@@ -623,7 +622,9 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
   }
   OrientArgs dummy{};
   const int64_t tx = (cols + kTile - 1) / kTile, ty = (rows + kTile - 1) / kTile;
-  const bool sq64 = (row && row->block == 2) || (col && col->block == 2);
+  // The general variant handles 64x64 blocks and E4M3 codes; the other one is
+  // the leaner E2M1 path for 1x32 / 32x32 blocks.
+  const bool sq64 = (row && (row->block == 2 || row->e4m3)) || (col && (col->block == 2 || col->e4m3));
   auto kern = sq64 ? quant_tile_kernel<InT, true> : quant_tile_kernel<InT, false>;
   const unsigned grid = resident_ctas(quant_tile_kernel<InT, false>, tx * ty, smem, kTileThreads);
   (void)cudaGetLastError();  // drop a stale error left by an earlier call

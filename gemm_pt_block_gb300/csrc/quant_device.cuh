@@ -25,10 +25,13 @@ __device__ __forceinline__ void draws32(const PhiloxKeys& k, uint32_t stream, ui
   }
 }
 
-// Scale, round and encode one 32-run whose max-abs is M.
-__device__ __forceinline__ uint4 finish32(float2 (&R)[16], const OrientArgs& o, float M,
-                                          const uint32_t (&w)[16], int* e_out) {
-  const int e = scale_exponent(M, o.roundup);
+// Scale one 32-run whose max-abs is M, in place (and round it stochastically
+// when asked; nearest rounding happens in the conversion). Returns e.
+// kAnyFormat = false compiles the E2M1 case only.
+template <bool kAnyFormat = true>
+__device__ __forceinline__ int scale_run32(float2 (&R)[16], const OrientArgs& o, float M,
+                                           const uint32_t (&w)[16]) {
+  const int e = scale_exponent(M, o.roundup, kAnyFormat && o.e4m3);
   const float2 is = make_float2(inv_scale(e), inv_scale(e));
 #pragma unroll
   for (int k = 0; k < 16; ++k) R[k] = f2mul(R[k], is);
@@ -36,8 +39,21 @@ __device__ __forceinline__ uint4 finish32(float2 (&R)[16], const OrientArgs& o, 
 #pragma unroll
     for (int k = 0; k < 16; ++k) R[k] = sr_pair(R[k], w[k]);
   }
-  *e_out = e;
-  return encode32(R);
+  return e;
+}
+
+// Encode a scaled 32-run of output row `orow`, K positions k0 .. k0 + 31, and
+// store it: E2M1 two per byte ([rows, K/2]) or E4M3 one per byte ([rows, K]).
+template <bool kAnyFormat = true>
+__device__ __forceinline__ void store_run32(const OrientArgs& o, int64_t orow, int64_t k0,
+                                            int64_t K, const float2 (&R)[16]) {
+  if (kAnyFormat && o.e4m3) {
+    uint4* d = reinterpret_cast<uint4*>(o.q + orow * K + k0);
+    d[0] = encode16_e4m3(&R[0]);
+    d[1] = encode16_e4m3(&R[8]);
+  } else {
+    *reinterpret_cast<uint4*>(o.q + orow * (K >> 1) + (k0 >> 1)) = encode32(R);
+  }
 }
 
 // Row-wise quantization of 32 consecutive values of output row `row` (columns
@@ -51,9 +67,8 @@ __device__ __forceinline__ void quantize_run32(float2 (&R)[16], int64_t row, int
   if (o.block) M = warp_max(M);
   uint32_t w[16];
   if (o.sr) draws32(o.keys, o.stream, (uint64_t)(row * cols + c0), w);
-  int e;
-  const uint4 packed = finish32(R, o, M, w, &e);
-  *reinterpret_cast<uint4*>(o.q + row * (cols >> 1) + (c0 >> 1)) = packed;
+  const int e = scale_run32(R, o, M, w);
+  store_run32(o, row, c0, cols, R);
   store_scale(o, row, c0 >> 5, cols >> 5, e);
 }
 

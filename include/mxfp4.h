@@ -59,6 +59,11 @@ enum { MXFP4_SCALE_FLOOR = 0, MXFP4_SCALE_ROUNDUP = 1 };
 enum { MXFP4_ROUND_RTN = 0, MXFP4_ROUND_SR = 1 };
 enum { MXFP4_LAYOUT_ROWMAJOR = 0, MXFP4_LAYOUT_MMA = 1 };
 enum { MXFP4_DTYPE_BF16 = 0, MXFP4_DTYPE_F32 = 1 };
+/* Element format of the codes: E2M1 (MXFP4, two codes per byte) or E4M3
+ * (MXFP8, OCP FP8 E4M3, one code per byte) [TIBQ, "The fix, and its
+ * supporting cast": MXFP8 for queries and keys]. Both share the E8M0 block
+ * scale and its layouts. */
+enum { MXFP4_FORMAT_E2M1 = 0, MXFP4_FORMAT_E4M3 = 1 };
 
 /* Quantization parameters of one output orientation.
  *  block        MXFP4_BLOCK_1X32: 32 consecutive elements along the
@@ -104,7 +109,7 @@ typedef struct {
   uint32_t wht_sign_mask;
   uint64_t seed;
   uint32_t sr_stream;
-  uint32_t reserved; /* must be 0 */
+  uint32_t elem_format; /* MXFP4_FORMAT_E2M1 (0) or MXFP4_FORMAT_E4M3 (1) */
 } mxfp4_quant_params;
 
 /* Fused MXFP4 quantizer ([News], paras. 1-2; [TIBQ] P_i = round(X_i / S)).
@@ -120,6 +125,11 @@ typedef struct {
  *  Shapes: cols % 32 == 0; rows % 32 == 0 when col != NULL or either
  *  orientation uses 32x32 blocks; MMA scale layout needs the output's row
  *  count % 128 == 0 and its K % 128 == 0. Else MXFP4_ERR_SHAPE.
+ *  With elem_format MXFP4_FORMAT_E4M3 the codes take one byte per element
+ *  (q_row [rows, cols], q_col [cols, rows]), the scale is chosen for the
+ *  largest E4M3 value 448 (floor: floor(log2 M) - 8; round-up: the smallest
+ *  e with 448 * 2^e >= M) and the rounding is nearest-even with saturation
+ *  (stochastic rounding: MXFP4_ERR_UNSUPPORTED).
  *  Inputs must be finite, and with the rotation on every rotated value must
  *  be finite too (|x| < 2^122 suffices); otherwise the codes are unspecified. */
 mxfp4_status mxfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,

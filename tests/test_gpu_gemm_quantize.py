@@ -74,3 +74,19 @@ def test_fused_rejects_bad_arguments():
     bad = mx.QuantParams(5, mx.SCALE_FLOOR, mx.ROUND_RTN, mx.LAYOUT_MMA)
     with pytest.raises(mx.Mxfp4Error):
         mx.mxfp4_gemm_quantize(*t, 256, 256, 256, bad)        # bad block
+
+
+@pytest.mark.parametrize("block", [0, 1])
+def test_fused_mxfp8_output(block):
+    import gemm_pt_block_gb300 as mx
+
+    M, N, K = 256, 512, 512
+    p = mx.QuantParams(block, mx.SCALE_ROUNDUP, mx.ROUND_RTN, mx.LAYOUT_MMA,
+                       elem_format=mx.FORMAT_E4M3)
+    *_, t = _operands(M, N, K, 17)
+    c = mx.mxfp4_gemm(*t, M, N, K)
+    ref = mx.mxfp4_quantize(c, p)
+    q, s, _ = mx.mxfp4_gemm_quantize(*t, M, N, K, p)
+    torch.cuda.synchronize()
+    assert q.shape == (M, N)
+    assert torch.equal(q, ref[0]) and torch.equal(s, ref[1])

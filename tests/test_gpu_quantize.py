@@ -305,3 +305,48 @@ def test_nearest_even_dense_fp32_sweep():
         want = oracle_quantize(x, p, None)
         assert np.all(want[1] == 127)
         assert_same(got, want, "dense fp32 sweep")
+
+
+# ------------------------------------------------------------------ MXFP8 --
+
+@pytest.mark.parametrize("orient", ["row", "col", "both"])
+@pytest.mark.parametrize("block", [oracle.BLOCK_1X32, oracle.BLOCK_32X32, oracle.BLOCK_64X64])
+@pytest.mark.parametrize("scale", SCALES)
+@pytest.mark.parametrize("wht", WHTS[:2], ids=["nowht", "detwht"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_mxfp8_matches_oracle(orient, block, scale, wht, dtype):
+    """E4M3 elements with E8M0 block scales, one byte per element."""
+    rows, cols = (192, 320) if block == oracle.BLOCK_64X64 else (160, 352)
+    if orient == "row" and block == oracle.BLOCK_1X32:
+        rows = 150                         # row kernel, ragged row count
+    x = _input(rows, cols, dtype, seed=101 + block)
+    p = oracle.Params(block=block, scale_mode=scale, wht=wht[0], wht_sign_mask=wht[1],
+                      elem_format=oracle.FORMAT_E4M3)
+    prow = p if orient in ("row", "both") else None
+    pcol = p if orient in ("col", "both") else None
+    got = gpu_quantize(x.to(DEV), prow, pcol)
+    want = oracle_quantize(oracle_input(x), prow, pcol)
+    assert_same(got, want, f"mxfp8 {orient}")
+
+
+def test_mxfp8_every_bf16_value_and_mma_layout():
+    """Every finite bf16 pattern as input (all block maxima, subnormals,
+    saturation), row-wise; then the tensor-core scale layout."""
+    import gemm_pt_block_gb300 as mx
+
+    bits = np.arange(65536, dtype=np.uint32)
+    keep = (bits & 0x7F80) != 0x7F80
+    vals = bits[keep].astype(np.uint16)
+    n = (vals.size // 64) * 64
+    x = vals[:n].reshape(-1, 64)
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+    p = oracle.Params(elem_format=oracle.FORMAT_E4M3, scale_mode=oracle.SCALE_ROUNDUP)
+    got = gpu_quantize(xt.to(DEV), p, None)
+    want = oracle_quantize(x, p, None)
+    assert_same(got, want, "mxfp8 bf16 sweep")
+    xm = _input(256, 384, "bf16", seed=103)
+    pm = oracle.Params(block=oracle.BLOCK_32X32, elem_format=oracle.FORMAT_E4M3)
+    assert_same(gpu_quantize(xm.to(DEV), pm, pm, 1, 1), oracle_quantize(oracle_input(xm), pm, pm, 1, 1),
+                "mxfp8 mma")
+    with pytest.raises(mx.Mxfp4Error):
+        mx.mxfp4_quantize(xm.to(DEV), mx.QuantParams(rounding=mx.ROUND_SR, elem_format=mx.FORMAT_E4M3))
