@@ -37,6 +37,7 @@ from .binding import (  # noqa: F401
     mxfp4_dequantize,
     mxfp4_gemm,
     mxfp4_gemm_quantize,
+    mxfp8_gemm,
     mxfp4_quantize,
     scale_numel,
 )

@@ -96,6 +96,8 @@ def lib() -> ctypes.CDLL:
         L.mxfp4_dequantize.argtypes = [P, P, i32, i64, i64, P, P]
         L.mxfp4_gemm.restype = i32
         L.mxfp4_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
+        L.mxfp8_gemm.restype = i32
+        L.mxfp8_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
         L.mxfp4_gemm_quantize.restype = i32
         L.mxfp4_gemm_quantize.argtypes = [P, P, P, P, i64, i64, i64, P, i64,
                                           ctypes.POINTER(_CParams), P, P, P]
@@ -201,6 +203,21 @@ def mxfp4_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.T
         c = torch.empty((M, N), dtype=torch.float32, device=qa.device)
     ldc = c.stride(0) if ldc is None else ldc
     _check(lib().mxfp4_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), ldc,
+                            _stream(qa, stream)))
+    return c
+
+
+def mxfp8_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
+               M: int, N: int, K: int, *, c=None, ldc: int | None = None, stream=None):
+    """C[M, N] fp32 = deq(A) deq(B)^T for MXFP8 operands: E4M3 codes [M, K] / [N, K],
+    E8M0 scales in tensor-core layout."""
+    for t, n in ((qa, "qa"), (sa, "sa"), (qb, "qb"), (sb, "sb")):
+        if not t.is_cuda or t.dtype != torch.uint8:
+            raise ValueError(f"{n} must be a CUDA uint8 tensor")
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=qa.device)
+    ldc = c.stride(0) if ldc is None else ldc
+    _check(lib().mxfp8_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), ldc,
                             _stream(qa, stream)))
     return c
 

@@ -167,6 +167,25 @@ mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   return gemm_common("mxfp4_gemm", qa, sa, qb, sb, M, N, K, c, ldc, nullptr, stream);
 }
 
+mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
+                        int64_t ldc, void* stream) {
+  if (!qa || !sa || !qb || !sb || !c) return fail(MXFP4_ERR_INVALID_ARG, "mxfp8_gemm: NULL pointer");
+  if (M <= 0 || N <= 0 || K <= 0 || M % 256 != 0 || N % 256 != 0 || K % 128 != 0)
+    return fail(MXFP4_ERR_SHAPE, "mxfp8_gemm needs M %% 256 == 0, N %% 256 == 0, K %% 128 == 0 (got %lld, %lld, %lld)",
+                (long long)M, (long long)N, (long long)K);
+  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30))
+    return fail(MXFP4_ERR_SHAPE, "mxfp8_gemm dimensions too large");
+  if (ldc < N) return fail(MXFP4_ERR_SHAPE, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
+  if (!aligned16(qa) || !aligned16(qb) || !aligned16(sa) || !aligned16(sb) || !aligned16(c) || ldc % 8 != 0)
+    return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");
+  const char* why = "";
+  cudaError_t e = mx::launch_gemm_f8(qa, sa, qb, sb, M, N, K, c, ldc, static_cast<cudaStream_t>(stream), &why);
+  if (e == cudaErrorNotSupported) return fail(MXFP4_ERR_UNSUPPORTED, "%s", why);
+  if (e == cudaErrorInvalidValue && why[0]) return fail(MXFP4_ERR_ALIGN, "%s", why);
+  return from_cuda(e, "mxfp8_gemm");
+}
+
 mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                                  const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
                                  int64_t ldc, const mxfp4_quant_params* out, uint8_t* q_out,

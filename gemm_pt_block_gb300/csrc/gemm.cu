@@ -352,12 +352,19 @@ static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle align
 using Ctl = CtlT<STAGES>;
 static_assert(sizeof(Ctl) <= CTL_BYTES, "control block");
 
+// kF8: kind::mxf8f6f4 with E4M3 operands (type code 0) instead of kind::mxf4's
+// E2M1 (type code 1).
+template <bool kF8 = false>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
-  return (sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) | (1u << 23) |
+  const uint32_t t = kF8 ? 0u : 1u;
+  return (sf_id << 4) | (t << 7) | (t << 10) | ((uint32_t)(BNP >> 3) << 17) | (1u << 23) |
          ((uint32_t)(256 >> 4) << 24) | (sf_id << 29);
 }
 
-template <bool kQ>
+// kF8: MXFP8 operands: codes one byte per element, so a 128-byte stage row is
+// 128 elements of K (4 MMAs of K = 32), with one 512-byte scale tile of A and
+// one per 128-row band of B per stage.
+template <bool kQ, bool kF8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -370,9 +377,10 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
   const bool leader = rank == 0;
-  const int num_m = M / (2 * BM), num_n = N / BNP, num_k = K / BK;
+  const int num_m = M / (2 * BM), num_n = N / BNP, num_k = K / (kF8 ? BK / 2 : BK);
   const int num_tiles = num_m * num_n;
   const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+  constexpr uint32_t kTx = kF8 ? 2u * (A_BYTES + B_BYTES + 512 + 1024) : TX_BYTES;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -415,12 +423,13 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
           if (!(ok = wait_bar(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl))) break;
           const uint32_t full_local = ptx::smem_u32(&ctl->full[stage]);
           const uint32_t full_leader = ptx::mapa(full_local, 0);
-          if (leader) ptx::mbar_arrive_expect_tx(full_local, TX_BYTES);
+          if (leader) ptx::mbar_arrive_expect_tx(full_local, kTx);
           const uint32_t st = ptx::smem_u32(smem + stage * STAGE_BYTES);
+          const int kt = kF8 ? kb : 2 * kb;   // first 128-wide scale tile of the stage
           ptx::tma_load_2d_pair(st, &tmA, kb * BKB, a_row, full_leader);
           ptx::tma_load_2d_pair(st + A_BYTES, &tmB, kb * BKB, b_row, full_leader);
-          ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES, &tmSA, 0, 2 * kb, a_row / 128, full_leader);
-          ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES + SFA_BYTES, &tmSB, 0, 2 * kb, nb * 2,
+          ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES, &tmSA, 0, kt, a_row / 128, full_leader);
+          ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES + SFA_BYTES, &tmSB, 0, kt, nb * 2,
                                 full_leader);
           ++issued_rounds;
           if (++stage == STAGES) {
@@ -450,22 +459,39 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
           const uint32_t st = ptx::smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sfa_s = st + A_BYTES + B_BYTES;
           const uint32_t sfb_s = sfa_s + SFA_BYTES;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            ptx::tc_cp_pair_32x128b_warpx4(tmem + SFA_COL + 4 * c,
-                                           ptx::smem_desc(sfa_s + c * 512, 0, 128, 0));
+          if constexpr (kF8) {
+            // One K tile: A's tile to SFA_COL, B's bands to SFB_COL + 4 t; MMA k
+            // reads byte k of each row's word.
+            ptx::tc_cp_pair_32x128b_warpx4(tmem + SFA_COL, ptx::smem_desc(sfa_s, 0, 128, 0));
 #pragma unroll
             for (int t = 0; t < 2; ++t)
-              ptx::tc_cp_pair_32x128b_warpx4(tmem + SFB_COL + 8 * c + 4 * t,
-                                             ptx::smem_desc(sfb_s + t * 1024 + c * 512, 0, 128, 0));
-          }
+              ptx::tc_cp_pair_32x128b_warpx4(tmem + SFB_COL + 4 * t,
+                                             ptx::smem_desc(sfb_s + t * 512, 0, 128, 0));
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
-            const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
-            ptx::mma_mxf4_pair(tmem + ACC_COL, ad, bd, make_idesc((k & 1) * 2),
-                               tmem + SFA_COL + 4 * (k >> 1), tmem + SFB_COL + 8 * (k >> 1),
-                               (kb | k) != 0);
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
+              const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
+              ptx::mma_mxf8_pair(tmem + ACC_COL, ad, bd, make_idesc<true>(k), tmem + SFA_COL,
+                                 tmem + SFB_COL, (kb | k) != 0);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              ptx::tc_cp_pair_32x128b_warpx4(tmem + SFA_COL + 4 * c,
+                                             ptx::smem_desc(sfa_s + c * 512, 0, 128, 0));
+#pragma unroll
+              for (int t = 0; t < 2; ++t)
+                ptx::tc_cp_pair_32x128b_warpx4(tmem + SFB_COL + 8 * c + 4 * t,
+                                               ptx::smem_desc(sfb_s + t * 1024 + c * 512, 0, 128, 0));
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
+              const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
+              ptx::mma_mxf4_pair(tmem + ACC_COL, ad, bd, make_idesc((k & 1) * 2),
+                                 tmem + SFA_COL + 4 * (k >> 1), tmem + SFB_COL + 8 * (k >> 1),
+                                 (kb | k) != 0);
+            }
           }
           ptx::tc_commit_pair_multicast(ptx::smem_u32(&ctl->empty[stage]), 0x3);
           if (++stage == STAGES) {
@@ -535,10 +561,11 @@ bool make_code_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t kb
 // Scale array in the tensor-core layout as a 3-D tensor of 32-bit words:
 // [rows/128 bands][K/128 tiles][128 words (512 bytes)]; a box covers 2 tiles
 // (one 256-deep K stage) of `bands` consecutive bands.
-bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t K, uint32_t bands) {
+bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t K, uint32_t bands,
+                    uint32_t ktiles = 2) {
   const cuuint64_t dims[3] = {128, (cuuint64_t)(K / 128), (cuuint64_t)(rows / 128)};
   const cuuint64_t strides[2] = {512, (cuuint64_t)(K / 128) * 512};
-  const cuuint32_t box[3] = {128, 2, bands};
+  const cuuint32_t box[3] = {128, ktiles, bands};
   const cuuint32_t es[3] = {1, 1, 1};
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(base), dims, strides,
                      box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -568,6 +595,8 @@ DevInfo& dev_info(int dev) {
       cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<false>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
       cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<false, true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
     }
     d.attr_set = true;
@@ -654,6 +683,40 @@ __global__ void wait_timeout_probe_kernel() {
 cudaError_t launch_wait_probe(cudaStream_t st) {
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
   wait_timeout_probe_kernel<<<1, 32, 0, st>>>();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
+                           int64_t ldc, cudaStream_t st, const char** why) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  DevInfo& d = dev_info(dev);
+  if (d.major != 10) {
+    *why = "tcgen05 block-scaled MMA needs an sm_100-family (GB300 sm_103) device";
+    return cudaErrorNotSupported;
+  }
+  if (!encode_fn()) {
+    *why = "driver entry point cuTensorMapEncodeTiled not available";
+    return cudaErrorNotSupported;
+  }
+  ensure_context();
+  CUtensorMap ta, tb, tsa, tsb;
+  if (!make_code_map(&ta, qa, M, K, pair::BM) || !make_code_map(&tb, qb, N, K, pair::BNH) ||
+      !make_scale_map(&tsa, sa, M, K, 1, 1) || !make_scale_map(&tsb, sb, N, K, 2, 1)) {
+    *why = "cuTensorMapEncodeTiled rejected the operand layout";
+    return cudaErrorInvalidValue;
+  }
+  const int num_tiles = (int)((M / 256) * (N / pair::BNP));
+  const int pairs = d.sms / 2;
+  const int grid = 2 * (num_tiles < pairs ? num_tiles : pairs);
+  int64_t gm = kGroupBytes / (256 * K);
+  gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
+  const OrientArgs none{};
+  (void)cudaGetLastError();  // drop a stale error left by an earlier call
+  pair::mxf4_gemm_pair_kernel<false, true><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
+      ta, tb, tsa, tsb, c, ldc, (int)M, (int)N, (int)K, (int)gm, none);
   return cudaGetLastError();
 }
 

@@ -160,6 +160,15 @@ mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
                         int64_t ldc, void* stream);
 
+/* The MXFP8 counterpart of mxfp4_gemm ([TIBQ], "The fix, and its supporting
+ * cast": MXFP8 for queries and keys): qa [M, K] and qb [N, K] E4M3 codes
+ * (MXFP4_FORMAT_E4M3, one byte per element), sa / sb E8M0 scales per 32
+ * elements in MXFP4_LAYOUT_MMA, C fp32 [M, N] = sum_k deqA[m, k] deqB[n, k].
+ *  Shapes: M % 256 == 0, N % 256 == 0, K % 128 == 0. */
+mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
+                        int64_t ldc, void* stream);
+
 /* The same GEMM with the quantizer fused into its epilogue ([News], para. 2:
  * the rotation and rounding run where the producing GEMM writes its output):
  * C is quantized row-wise (along N) straight from the accumulator, with the
