@@ -96,10 +96,12 @@ def lib() -> ctypes.CDLL:
         L.mxfp4_dequantize.argtypes = [P, P, i32, i64, i64, P, P]
         L.mxfp4_gemm.restype = i32
         L.mxfp4_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
+        L.mxfp4_gemm_ex.restype = i32
+        L.mxfp4_gemm_ex.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P]
         L.mxfp8_gemm.restype = i32
-        L.mxfp8_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
+        L.mxfp8_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P]
         L.mxfp4_gemm_quantize.restype = i32
-        L.mxfp4_gemm_quantize.argtypes = [P, P, P, P, i64, i64, i64, P, i64,
+        L.mxfp4_gemm_quantize.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64,
                                           ctypes.POINTER(_CParams), P, P, P]
         L.hadamard32.restype = i32
         L.hadamard32.argtypes = [P, i32, i64, i64, i64, ctypes.c_uint32, i32, P, P]
@@ -193,52 +195,74 @@ def mxfp4_dequantize(q: torch.Tensor, s: torch.Tensor, rows: int, cols: int,
     return out
 
 
-def mxfp4_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
-               M: int, N: int, K: int, *, c=None, ldc: int | None = None, stream=None):
-    """C[M, N] fp32 = deq(A) deq(B)^T; A, B K-major packed codes, scales in tensor-core layout."""
+def _check_operands(qa, sa, qb, sb) -> None:
     for t, n in ((qa, "qa"), (sa, "sa"), (qb, "qb"), (sb, "sb")):
         if not t.is_cuda or t.dtype != torch.uint8:
             raise ValueError(f"{n} must be a CUDA uint8 tensor")
+
+
+def _c_dtype(c, out_dtype) -> int:
+    dt = c.dtype if c is not None else out_dtype
+    if dt == torch.float32:
+        return DTYPE_F32
+    if dt == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError("C must be float32 or bfloat16")
+
+
+def mxfp4_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
+               M: int, N: int, K: int, *, c=None, ldc: int | None = None,
+               out_dtype: torch.dtype = torch.float32, stream=None):
+    """C[M, N] = deq(A) deq(B)^T (fp32 sums, stored as fp32 or bf16: out_dtype, or
+    c's dtype); A, B K-major packed codes, scales in tensor-core layout."""
+    _check_operands(qa, sa, qb, sb)
+    cdt = _c_dtype(c, out_dtype)
     if c is None:
-        c = torch.empty((M, N), dtype=torch.float32, device=qa.device)
+        c = torch.empty((M, N), dtype=out_dtype, device=qa.device)
     ldc = c.stride(0) if ldc is None else ldc
-    _check(lib().mxfp4_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), ldc,
-                            _stream(qa, stream)))
+    if cdt == DTYPE_F32:
+        _check(lib().mxfp4_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), ldc,
+                                _stream(qa, stream)))
+    else:
+        _check(lib().mxfp4_gemm_ex(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), cdt,
+                                   ldc, _stream(qa, stream)))
     return c
 
 
 def mxfp8_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
-               M: int, N: int, K: int, *, c=None, ldc: int | None = None, stream=None):
-    """C[M, N] fp32 = deq(A) deq(B)^T for MXFP8 operands: E4M3 codes [M, K] / [N, K],
-    E8M0 scales in tensor-core layout."""
-    for t, n in ((qa, "qa"), (sa, "sa"), (qb, "qb"), (sb, "sb")):
-        if not t.is_cuda or t.dtype != torch.uint8:
-            raise ValueError(f"{n} must be a CUDA uint8 tensor")
+               M: int, N: int, K: int, *, c=None, ldc: int | None = None,
+               out_dtype: torch.dtype = torch.float32, stream=None):
+    """C[M, N] = deq(A) deq(B)^T for MXFP8 operands: E4M3 codes [M, K] / [N, K],
+    E8M0 scales in tensor-core layout; C fp32 or bf16 as in mxfp4_gemm."""
+    _check_operands(qa, sa, qb, sb)
+    cdt = _c_dtype(c, out_dtype)
     if c is None:
-        c = torch.empty((M, N), dtype=torch.float32, device=qa.device)
+        c = torch.empty((M, N), dtype=out_dtype, device=qa.device)
     ldc = c.stride(0) if ldc is None else ldc
-    _check(lib().mxfp8_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), ldc,
+    _check(lib().mxfp8_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), cdt, ldc,
                             _stream(qa, stream)))
     return c
 
 
 def mxfp4_gemm_quantize(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
                         M: int, N: int, K: int, out: QuantParams, *, with_c: bool = False, c=None,
-                        q_out=None, s_out=None, stream=None):
+                        out_dtype: torch.dtype = torch.float32, q_out=None, s_out=None,
+                        stream=None):
     """GEMM whose epilogue quantizes C row-wise with `out`: returns (q_out, s_out, c),
-    c None unless with_c (or c given); codes/scales as mxfp4_quantize(C, out)."""
-    for t, n in ((qa, "qa"), (sa, "sa"), (qb, "qb"), (sb, "sb")):
-        if not t.is_cuda or t.dtype != torch.uint8:
-            raise ValueError(f"{n} must be a CUDA uint8 tensor")
+    c None unless with_c (or c given; fp32 or bf16); codes/scales as
+    mxfp4_quantize(C, out) of the fp32 C."""
+    _check_operands(qa, sa, qb, sb)
+    cdt = _c_dtype(c, out_dtype)
     if c is None and with_c:
-        c = torch.empty((M, N), dtype=torch.float32, device=qa.device)
+        c = torch.empty((M, N), dtype=out_dtype, device=qa.device)
     q_out = torch.empty((M, out.code_cols(N)), dtype=torch.uint8, device=qa.device) if q_out is None else q_out
     s_out = _scales_out(M, N, out, qa.device) if s_out is None else s_out
     ldc = c.stride(0) if c is not None else N
     op = out._c()
     _check(lib().mxfp4_gemm_quantize(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K,
-                                     _ptr(c) if c is not None else None, ldc, ctypes.byref(op),
-                                     _ptr(q_out), _ptr(s_out), _stream(qa, stream)))
+                                     _ptr(c) if c is not None else None, cdt, ldc,
+                                     ctypes.byref(op), _ptr(q_out), _ptr(s_out),
+                                     _stream(qa, stream)))
     return q_out, s_out, c
 
 

@@ -139,9 +139,11 @@ mxfp4_status mxfp4_dequantize(const uint8_t* q, const uint8_t* s, int32_t scale_
 
 namespace {
 mxfp4_status gemm_common(const char* name, const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
-                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
-                         int64_t ldc, const mx::OrientArgs* qout, void* stream) {
+                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                         int32_t c_dtype, int64_t ldc, const mx::OrientArgs* qout, void* stream) {
   if (!qa || !sa || !qb || !sb || (!c && !qout)) return fail(MXFP4_ERR_INVALID_ARG, "%s: NULL pointer", name);
+  if (c_dtype != MXFP4_DTYPE_BF16 && c_dtype != MXFP4_DTYPE_F32)
+    return fail(MXFP4_ERR_INVALID_ARG, "%s: bad c_dtype %d", name, c_dtype);
   if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0)
     return fail(MXFP4_ERR_SHAPE, "%s needs M %% 128 == 0, N %% 256 == 0, K %% 256 == 0 (got %lld, %lld, %lld)",
                 name, (long long)M, (long long)N, (long long)K);
@@ -152,8 +154,8 @@ mxfp4_status gemm_common(const char* name, const uint8_t* qa, const uint8_t* sa,
       (c && ldc % 8 != 0))
     return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");
   const char* why = "";
-  cudaError_t e = mx::launch_gemm(qa, sa, qb, sb, M, N, K, c, ldc, qout,
-                                  static_cast<cudaStream_t>(stream), &why);
+  cudaError_t e = mx::launch_gemm(qa, sa, qb, sb, M, N, K, c, c_dtype == MXFP4_DTYPE_BF16, ldc,
+                                  qout, static_cast<cudaStream_t>(stream), &why);
   if (e == cudaErrorNotSupported) return fail(MXFP4_ERR_UNSUPPORTED, "%s", why);
   if (e == cudaErrorInvalidValue && why[0]) return fail(MXFP4_ERR_ALIGN, "%s", why);
   return from_cuda(e, name);
@@ -164,13 +166,23 @@ mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
                         int64_t ldc, void* stream) {
   if (!c) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
-  return gemm_common("mxfp4_gemm", qa, sa, qb, sb, M, N, K, c, ldc, nullptr, stream);
+  return gemm_common("mxfp4_gemm", qa, sa, qb, sb, M, N, K, c, MXFP4_DTYPE_F32, ldc, nullptr,
+                     stream);
+}
+
+mxfp4_status mxfp4_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                           int32_t c_dtype, int64_t ldc, void* stream) {
+  if (!c) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
+  return gemm_common("mxfp4_gemm_ex", qa, sa, qb, sb, M, N, K, c, c_dtype, ldc, nullptr, stream);
 }
 
 mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
-                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
-                        int64_t ldc, void* stream) {
+                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                        int32_t c_dtype, int64_t ldc, void* stream) {
   if (!qa || !sa || !qb || !sb || !c) return fail(MXFP4_ERR_INVALID_ARG, "mxfp8_gemm: NULL pointer");
+  if (c_dtype != MXFP4_DTYPE_BF16 && c_dtype != MXFP4_DTYPE_F32)
+    return fail(MXFP4_ERR_INVALID_ARG, "mxfp8_gemm: bad c_dtype %d", c_dtype);
   if (M <= 0 || N <= 0 || K <= 0 || M % 256 != 0 || N % 256 != 0 || K % 128 != 0)
     return fail(MXFP4_ERR_SHAPE, "mxfp8_gemm needs M %% 256 == 0, N %% 256 == 0, K %% 128 == 0 (got %lld, %lld, %lld)",
                 (long long)M, (long long)N, (long long)K);
@@ -180,16 +192,17 @@ mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   if (!aligned16(qa) || !aligned16(qb) || !aligned16(sa) || !aligned16(sb) || !aligned16(c) || ldc % 8 != 0)
     return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");
   const char* why = "";
-  cudaError_t e = mx::launch_gemm_f8(qa, sa, qb, sb, M, N, K, c, ldc, static_cast<cudaStream_t>(stream), &why);
+  cudaError_t e = mx::launch_gemm_f8(qa, sa, qb, sb, M, N, K, c, c_dtype == MXFP4_DTYPE_BF16, ldc,
+                                     static_cast<cudaStream_t>(stream), &why);
   if (e == cudaErrorNotSupported) return fail(MXFP4_ERR_UNSUPPORTED, "%s", why);
   if (e == cudaErrorInvalidValue && why[0]) return fail(MXFP4_ERR_ALIGN, "%s", why);
   return from_cuda(e, "mxfp8_gemm");
 }
 
 mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
-                                 const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
-                                 int64_t ldc, const mxfp4_quant_params* out, uint8_t* q_out,
-                                 uint8_t* s_out, void* stream) {
+                                 const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                                 int32_t c_dtype, int64_t ldc, const mxfp4_quant_params* out,
+                                 uint8_t* q_out, uint8_t* s_out, void* stream) {
   if (!out) return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_gemm_quantize: out params are required");
   if (out->block == MXFP4_BLOCK_64X64)
     return fail(MXFP4_ERR_UNSUPPORTED,
@@ -199,7 +212,7 @@ mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uin
     mxfp4_status st = check_params(out, q_out, s_out, M, N, "out", &qo);
     if (st) return st;
   }
-  return gemm_common("mxfp4_gemm_quantize", qa, sa, qb, sb, M, N, K, c, ldc, &qo, stream);
+  return gemm_common("mxfp4_gemm_quantize", qa, sa, qb, sb, M, N, K, c, c_dtype, ldc, &qo, stream);
 }
 
 mxfp4_status hadamard32(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,

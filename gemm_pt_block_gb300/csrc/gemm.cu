@@ -25,6 +25,7 @@
 // library's device error word, stops issuing work, and still frees its tensor
 // memory before exiting.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include <cstdint>
@@ -129,24 +130,43 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
   nb = w / gm;
 }
 
+// Two fp32 bit patterns to a bf16 pair (nearest-even), lo in the low half.
+__device__ __forceinline__ uint32_t bf16x2(uint32_t lo, uint32_t hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 // One epilogue thread's results: 128 consecutive fp32 values of row `row`
-// (columns c0 .. c0 + 127). They are stored to C when C is given, and with
-// kQ they are also quantized row-wise (four 32-runs) exactly as the quantizer
-// would quantize that row of C.
+// (columns c0 .. c0 + 127). They are stored to C when C is given (fp32, or
+// bf16 rounded to nearest-even when c_bf16), and with kQ they are also
+// quantized row-wise (four 32-runs) from the fp32 values, exactly as the
+// quantizer would quantize that row of an fp32 C.
 template <bool kQ>
 __device__ __forceinline__ void epilogue_out(const uint32_t (&r0)[64], const uint32_t (&r1)[64],
-                                             float* C, int64_t ldc, int64_t row, int64_t c0,
-                                             int64_t N, const OrientArgs& qo) {
+                                             void* C, int c_bf16, int64_t ldc, int64_t row,
+                                             int64_t c0, int64_t N, const OrientArgs& qo) {
   if (!kQ || C != nullptr) {
-    float4* dst = reinterpret_cast<float4*>(C + row * ldc + c0);
+    if (c_bf16) {
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(C) + row * ldc + c0);
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      dst[j] = make_float4(__uint_as_float(r0[4 * j]), __uint_as_float(r0[4 * j + 1]),
-                           __uint_as_float(r0[4 * j + 2]), __uint_as_float(r0[4 * j + 3]));
+      for (int j = 0; j < 8; ++j)
+        dst[j] = make_uint4(bf16x2(r0[8 * j], r0[8 * j + 1]), bf16x2(r0[8 * j + 2], r0[8 * j + 3]),
+                            bf16x2(r0[8 * j + 4], r0[8 * j + 5]), bf16x2(r0[8 * j + 6], r0[8 * j + 7]));
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      dst[16 + j] = make_float4(__uint_as_float(r1[4 * j]), __uint_as_float(r1[4 * j + 1]),
-                                __uint_as_float(r1[4 * j + 2]), __uint_as_float(r1[4 * j + 3]));
+      for (int j = 0; j < 8; ++j)
+        dst[8 + j] = make_uint4(bf16x2(r1[8 * j], r1[8 * j + 1]), bf16x2(r1[8 * j + 2], r1[8 * j + 3]),
+                                bf16x2(r1[8 * j + 4], r1[8 * j + 5]), bf16x2(r1[8 * j + 6], r1[8 * j + 7]));
+    } else {
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(C) + row * ldc + c0);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        dst[j] = make_float4(__uint_as_float(r0[4 * j]), __uint_as_float(r0[4 * j + 1]),
+                             __uint_as_float(r0[4 * j + 2]), __uint_as_float(r0[4 * j + 3]));
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        dst[16 + j] = make_float4(__uint_as_float(r1[4 * j]), __uint_as_float(r1[4 * j + 1]),
+                                  __uint_as_float(r1[4 * j + 2]), __uint_as_float(r1[4 * j + 3]));
+    }
   }
   if constexpr (kQ) {
 #pragma unroll
@@ -167,7 +187,7 @@ template <bool kQ>
 __global__ void __launch_bounds__(THREADS, 1)
 mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const uint8_t* __restrict__ sa, const uint8_t* __restrict__ sb,
-                 float* __restrict__ C, int64_t ldc, int M, int N, int K, int group_m,
+                 void* __restrict__ C, int c_bf16, int64_t ldc, int M, int N, int K, int group_m,
                  const __grid_constant__ OrientArgs qo) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -311,7 +331,7 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctl->acc_empty));
       acc_phase ^= 1u;
       const int64_t row = (int64_t)mb * BM + q * 32 + lane;
-      epilogue_out<kQ>(r0, r1, C, ldc, row, (int64_t)nb * BN + h * 128, N, qo);
+      epilogue_out<kQ>(r0, r1, C, c_bf16, ldc, row, (int64_t)nb * BN + h * 128, N, qo);
     }
   }
 
@@ -368,7 +388,7 @@ template <bool kQ, bool kF8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                      float* __restrict__ C, int64_t ldc, int M, int N, int K, int group_m,
+                      void* __restrict__ C, int c_bf16, int64_t ldc, int M, int N, int K, int group_m,
                       const __grid_constant__ OrientArgs qo) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -529,7 +549,7 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       if (lane == 0) ptx::mbar_arrive_cluster(acc_empty_leader);
       acc_phase ^= 1u;
       const int64_t row = (int64_t)mb * 2 * BM + rank * BM + q * 32 + lane;
-      epilogue_out<kQ>(r0, r1, C, ldc, row, (int64_t)nb * BNP + h * 128, N, qo);
+      epilogue_out<kQ>(r0, r1, C, c_bf16, ldc, row, (int64_t)nb * BNP + h * 128, N, qo);
     }
   }
 
@@ -607,8 +627,9 @@ DevInfo& dev_info(int dev) {
 }  // namespace
 
 cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
-                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
-                        int64_t ldc, const OrientArgs* qout, cudaStream_t st, const char** why) {
+                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                        bool c_bf16, int64_t ldc, const OrientArgs* qout, cudaStream_t st,
+                        const char** why) {
   const OrientArgs none{};
   const OrientArgs& qo = qout ? *qout : none;
   int dev = 0;
@@ -641,10 +662,10 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
     (void)cudaGetLastError();  // drop a stale error left by an earlier call
     if (qout)
       pair::mxf4_gemm_pair_kernel<true><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
-          ta, tb, tsa, tsb, c, ldc, (int)M, (int)N, (int)K, (int)gm, qo);
+          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, qo);
     else
       pair::mxf4_gemm_pair_kernel<false><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
-          ta, tb, tsa, tsb, c, ldc, (int)M, (int)N, (int)K, (int)gm, qo);
+          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, qo);
     return cudaGetLastError();
   }
   if (!make_code_map(&ta, qa, M, K / 2, BM) || !make_code_map(&tb, qb, N, K / 2, BN)) {
@@ -657,10 +678,10 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   gm = gm < 8 ? 8 : (gm > 64 ? 64 : gm);
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
   if (qout)
-    mxf4_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sa, sb, c, ldc, (int)M,
+    mxf4_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sa, sb, c, (int)c_bf16, ldc, (int)M,
                                                              (int)N, (int)K, (int)gm, qo);
   else
-    mxf4_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sa, sb, c, ldc, (int)M,
+    mxf4_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sa, sb, c, (int)c_bf16, ldc, (int)M,
                                                               (int)N, (int)K, (int)gm, qo);
   return cudaGetLastError();
 }
@@ -687,8 +708,8 @@ cudaError_t launch_wait_probe(cudaStream_t st) {
 }
 
 cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
-                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
-                           int64_t ldc, cudaStream_t st, const char** why) {
+                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                           bool c_bf16, int64_t ldc, cudaStream_t st, const char** why) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -716,7 +737,7 @@ cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
   const OrientArgs none{};
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
   pair::mxf4_gemm_pair_kernel<false, true><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
-      ta, tb, tsa, tsb, c, ldc, (int)M, (int)N, (int)K, (int)gm, none);
+      ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, none);
   return cudaGetLastError();
 }
 

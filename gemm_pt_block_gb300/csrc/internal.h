@@ -40,8 +40,9 @@ cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t 
 // qout: also quantize C row-wise in the epilogue (nullptr: plain GEMM); c may
 // then be nullptr (no fp32 output).
 cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
-                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
-                        int64_t ldc, const OrientArgs* qout, cudaStream_t st, const char** why);
+                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                        bool c_bf16, int64_t ldc, const OrientArgs* qout, cudaStream_t st,
+                        const char** why);
 // Reads and clears the quantizer's device error word.
 cudaError_t read_quant_error(uint32_t* err);
 // Reads and clears the device error words (synchronizes st).
@@ -49,8 +50,8 @@ cudaError_t read_device_error(cudaStream_t st, uint32_t* err);
 // MXFP8 GEMM (E4M3 codes [M, K], [N, K] bytes; E8M0 scales in the tensor-core
 // layout): CTA pairs, M % 256 == 0, N % 256 == 0, K % 128 == 0.
 cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
-                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
-                           int64_t ldc, cudaStream_t st, const char** why);
+                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                           bool c_bf16, int64_t ldc, cudaStream_t st, const char** why);
 // One-thread kernel whose bounded wait never completes (sets the error word).
 cudaError_t launch_wait_probe(cudaStream_t st);
 

@@ -18,9 +18,10 @@ since c H diag(s) is orthogonal (Tseng, "Training LLMs with MXFP4",
 Abstract: stochastic rounding with the random Hadamard transform).
 
 Everything runs in the library's CUDA kernels; this module only chains the
-calls and keeps the codes between the passes. Outputs and gradients are fp32
-(the GEMM accumulates in fp32); autograd casts gradients to the parameters'
-dtype.
+calls and keeps the codes between the passes. The GEMMs accumulate in fp32
+and store their result in the type it is wanted in: Y in `out_dtype` (fp32 by
+default, or bf16), dX in X's dtype and dW in W's dtype (bf16 is the fp32 sum
+rounded to nearest-even inside the GEMM's epilogue, so no separate cast runs).
 """
 from __future__ import annotations
 
@@ -79,7 +80,8 @@ def _check_shapes(T: int, D: int, F: int) -> None:
 
 class _Mxfp4LinearFn(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, x: torch.Tensor, w: torch.Tensor, recipe: LinearRecipe, step: int):
+    def forward(ctx, x: torch.Tensor, w: torch.Tensor, recipe: LinearRecipe, step: int,
+                out_dtype: torch.dtype):
         T, D = x.shape
         F = w.shape[0]
         _check_shapes(T, D, F)
@@ -90,9 +92,9 @@ class _Mxfp4LinearFn(torch.autograd.Function):
                         dy_col=replace(r.dy_col, seed=r.dy_col.seed + step))
         xq, xs, xqc, xsc = mxfp4_quantize(x, r.x_row, r.x_col)
         wq, ws, wqc, wsc = mxfp4_quantize(w, r.w_row, r.w_col)
-        y = mxfp4_gemm(xq, xs, wq, ws, T, F, D)
+        y = mxfp4_gemm(xq, xs, wq, ws, T, F, D, out_dtype=out_dtype)
         ctx.save_for_backward(xqc, xsc, wqc, wsc)
-        ctx.recipe, ctx.dims = r, (T, D, F)
+        ctx.recipe, ctx.dims, ctx.dtypes = r, (T, D, F), (x.dtype, w.dtype)
         return y
 
     @staticmethod
@@ -102,27 +104,37 @@ class _Mxfp4LinearFn(torch.autograd.Function):
         r = ctx.recipe
         dy = dy.contiguous()
         gq, gs, gqc, gsc = mxfp4_quantize(dy, r.dy_row, r.dy_col)
-        dx = mxfp4_gemm(gq, gs, wqc, wsc, T, D, F) if ctx.needs_input_grad[0] else None
-        dw = mxfp4_gemm(gqc, gsc, xqc, xsc, F, D, T) if ctx.needs_input_grad[1] else None
-        return dx, dw, None, None
+        xdt, wdt = ctx.dtypes
+        dx = (mxfp4_gemm(gq, gs, wqc, wsc, T, D, F, out_dtype=xdt)
+              if ctx.needs_input_grad[0] else None)
+        dw = (mxfp4_gemm(gqc, gsc, xqc, xsc, F, D, T, out_dtype=wdt)
+              if ctx.needs_input_grad[1] else None)
+        return dx, dw, None, None, None
 
 
 def mxfp4_linear(x: torch.Tensor, w: torch.Tensor, recipe: LinearRecipe | None = None,
-                 step: int = 0) -> torch.Tensor:
-    """Y = X W^T with MXFP4 forward and backward GEMMs (fp32 result).
+                 step: int = 0, out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
+    """Y = X W^T with MXFP4 forward and backward GEMMs; Y in out_dtype (fp32 or
+    bf16), gradients in their inputs' dtypes.
 
     x [T, D] and w [F, D] are bf16 or fp32 CUDA tensors; T, D, F must be
     multiples of 256. `step` offsets the stochastic-rounding seeds so each
     training step draws fresh bits."""
-    return _Mxfp4LinearFn.apply(x, w, recipe or recipe_2d_sr(), step)
+    for t, n in ((x, "x"), (w, "w")):
+        if t.dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError(f"{n} must be bfloat16 or float32")
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out_dtype must be bfloat16 or float32")
+    return _Mxfp4LinearFn.apply(x, w, recipe or recipe_2d_sr(), step, out_dtype)
 
 
 class Mxfp4Linear(torch.nn.Module):
     """Bias-free linear layer whose three GEMMs run in MXFP4."""
 
     def __init__(self, in_features: int, out_features: int, recipe: LinearRecipe | None = None,
-                 device=None, dtype=torch.bfloat16):
+                 device=None, dtype=torch.bfloat16, out_dtype: torch.dtype = torch.float32):
         super().__init__()
+        self.out_dtype = out_dtype
         self.weight = torch.nn.Parameter(torch.empty(out_features, in_features, device=device,
                                                      dtype=dtype))
         torch.nn.init.normal_(self.weight, std=in_features ** -0.5)
@@ -131,7 +143,8 @@ class Mxfp4Linear(torch.nn.Module):
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
         lead = x.shape[:-1]
-        y = mxfp4_linear(x.reshape(-1, x.shape[-1]), self.weight, self.recipe, self.step)
+        y = mxfp4_linear(x.reshape(-1, x.shape[-1]), self.weight, self.recipe, self.step,
+                         self.out_dtype)
         if self.training:
             self.step += 1
         return y.reshape(*lead, y.shape[-1])

@@ -160,14 +160,24 @@ mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
                         int64_t ldc, void* stream);
 
+/* mxfp4_gemm with a choice of output type ([News], para. 2: a bf16 C is what
+ * the next layer reads): c_dtype MXFP4_DTYPE_F32 writes C as mxfp4_gemm does;
+ * MXFP4_DTYPE_BF16 writes each fp32 sum rounded to bf16 (nearest-even), c a
+ * bf16 [M, N] array with leading dimension ldc (ldc % 8 == 0, c 16-byte
+ * aligned). Other c_dtype values return MXFP4_ERR_INVALID_ARG. */
+mxfp4_status mxfp4_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                           int32_t c_dtype, int64_t ldc, void* stream);
+
 /* The MXFP8 counterpart of mxfp4_gemm ([TIBQ], "The fix, and its supporting
  * cast": MXFP8 for queries and keys): qa [M, K] and qb [N, K] E4M3 codes
  * (MXFP4_FORMAT_E4M3, one byte per element), sa / sb E8M0 scales per 32
- * elements in MXFP4_LAYOUT_MMA, C fp32 [M, N] = sum_k deqA[m, k] deqB[n, k].
+ * elements in MXFP4_LAYOUT_MMA, C [M, N] = sum_k deqA[m, k] deqB[n, k] in fp32,
+ * stored as c_dtype (fp32, or bf16 nearest-even) as in mxfp4_gemm_ex.
  *  Shapes: M % 256 == 0, N % 256 == 0, K % 128 == 0. */
 mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
-                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
-                        int64_t ldc, void* stream);
+                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                        int32_t c_dtype, int64_t ldc, void* stream);
 
 /* The same GEMM with the quantizer fused into its epilogue ([News], para. 2:
  * the rotation and rounding run where the producing GEMM writes its output):
@@ -176,14 +186,15 @@ mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
  * mxfp4_quantize accepts). The codes q_out [M, N/2] and scales s_out
  * ([M, N/32] or MXFP4_LAYOUT_MMA) are bit-identical to mxfp4_quantize of the
  * fp32 C this call computes, with cols = N (stochastic draws keyed by the
- * element index m * N + n). c may be NULL: then no fp32 output is written
- * (ldc is ignored), which saves its HBM traffic.
+ * element index m * N + n); they come from the fp32 sums even when C itself
+ * is stored as bf16 (c_dtype as in mxfp4_gemm_ex). c may be NULL: then no C
+ * is written (c_dtype and ldc are ignored), which saves its HBM traffic.
  *  Shapes as mxfp4_gemm; MMA scale layout needs nothing more (M % 128,
  *  N % 128 hold). q_out must be 16-byte aligned. */
 mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
-                                 const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
-                                 int64_t ldc, const mxfp4_quant_params* out, uint8_t* q_out,
-                                 uint8_t* s_out, void* stream);
+                                 const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                                 int32_t c_dtype, int64_t ldc, const mxfp4_quant_params* out,
+                                 uint8_t* q_out, uint8_t* s_out, void* stream);
 
 /* Stand-alone 32-point block rotation along cols ([News], para. 2):
  *  forward (inverse == 0): y = c * H * diag(s) * x per 32-block;

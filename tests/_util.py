@@ -65,3 +65,22 @@ def gemm_tolerance_check(c: np.ndarray, ref: np.ndarray, absref: np.ndarray, rel
         raise AssertionError(f"{len(bad)} GEMM outputs outside |err| <= {rel} sum|ab|; first {i}: "
                              f"got {c[i]!r} ref {ref[i]!r} sum|ab| {absref[i]!r}")
     return float((err / np.maximum(absref, 1e-300)).max())
+
+
+def bf16_to_f64(c: torch.Tensor) -> np.ndarray:
+    return c.float().cpu().numpy().astype(np.float64)
+
+
+def gemm_tolerance_check_bf16(c: np.ndarray, ref: np.ndarray, absref: np.ndarray,
+                              rel: float = 1e-5):
+    """C stored as bf16: the fp32 sum's bound plus bf16's rounding, at most 2^-8
+    of the fp32 value (half a unit in the 8th significant bit)."""
+    err = np.abs(c - ref)
+    t = rel * absref
+    lim = t + 2.0 ** -8 * (np.abs(ref) + t)
+    ok = err <= lim
+    if not ok.all():
+        bad = np.argwhere(~ok)
+        i = tuple(bad[0])
+        raise AssertionError(f"{len(bad)} bf16 GEMM outputs outside the bound; first {i}: "
+                             f"got {c[i]!r} ref {ref[i]!r} sum|ab| {absref[i]!r}")

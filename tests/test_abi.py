@@ -92,6 +92,15 @@ def test_host_side_validation(L):
     assert L.mxfp4_gemm(good, good, good, good, 128, 256, 256, good, 100, None) == 2
     assert L.mxfp4_gemm(None, good, good, good, 128, 256, 256, good, 256, None) == 1
     assert L.mxfp4_gemm(good, good, good, good, 128, 256, 256, P((1 << 20) + 4), 256, None) == 3
+    # bf16 / fp32 C selection
+    assert L.mxfp4_gemm_ex(good, good, good, good, 128, 256, 256, good, 2, 256, None) == 1
+    assert L.mxfp4_gemm_ex(good, good, good, good, 100, 256, 256, good, 0, 256, None) == 2
+    assert L.mxfp4_gemm_ex(good, good, good, good, 128, 256, 256, good, 0, 260, None) == 3
+    assert L.mxfp8_gemm(good, good, good, good, 256, 256, 256, good, 3, 256, None) == 1
+    assert L.mxfp8_gemm(good, good, good, good, 128, 256, 128, good, 0, 256, None) == 2
+    pq = mx.QuantParams()._c()
+    assert L.mxfp4_gemm_quantize(good, good, good, good, 128, 256, 256, good, 5, 256,
+                                 ctypes.byref(pq), good, good, None) == 1
     # dequantize / hadamard32
     assert L.mxfp4_dequantize(good, good, 1, 64, 128, good, None) == 2
     assert L.mxfp4_dequantize(good, good, 2, 64, 128, good, None) == 1

@@ -112,3 +112,29 @@ def test_first_call_from_a_fresh_thread():
     t.join()
     assert "err" not in box, box.get("err")
     assert all(torch.equal(a, b) for a, b in zip(box["out"], ref))
+
+
+def test_linear_bf16_output_and_direct_bf16_gradients():
+    """out_dtype=bf16: Y is the fp32 layer's Y rounded to nearest-even; with the
+    same dY values the gradients are bit-identical to the fp32-output layer's
+    (each written by the GEMM in its input's dtype)."""
+    import gemm_pt_block_gb300 as mx
+
+    T, D, F = 256, 512, 768
+    r = mx.recipe_2d_sr(synth.sign_mask(77), seed=5)
+    x = synth.student_t(T, D, 4.0, 4400).to(DEV)
+    w = synth.normal(F, D, 0.02, 4401).to(DEV)
+    g = synth.laplace(T, F, 1e-3, 4402).to(DEV)          # bf16
+    outs = {}
+    for dt in (torch.float32, torch.bfloat16):
+        xd, wd = x.clone().requires_grad_(), w.clone().requires_grad_()
+        y = mx.mxfp4_linear(xd, wd, r, out_dtype=dt)
+        y.backward(g.to(dt))
+        torch.cuda.synchronize()
+        outs[dt] = (y.detach(), xd.grad, wd.grad)
+    y32, dx32, dw32 = outs[torch.float32]
+    y16, dx16, dw16 = outs[torch.bfloat16]
+    assert y16.dtype == torch.bfloat16 and dx16.dtype == torch.bfloat16 and dw16.dtype == torch.bfloat16
+    assert torch.equal(y16.view(torch.int16), y32.to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(dx16.view(torch.int16), dx32.view(torch.int16))
+    assert torch.equal(dw16.view(torch.int16), dw32.view(torch.int16))
