@@ -23,7 +23,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mxfp4_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle_mxfp4.so")
 
-BLOCK_1X32, BLOCK_32X32, BLOCK_64X64 = 0, 1, 2
+BLOCK_1X32, BLOCK_32X32, BLOCK_64X64, BLOCK_1X16 = 0, 1, 2, 3
 FORMAT_E2M1, FORMAT_E4M3 = 0, 1
 SCALE_FLOOR, SCALE_ROUNDUP = 0, 1
 ROUND_RTN, ROUND_SR = 0, 1
@@ -59,6 +59,7 @@ class _Params(ctypes.Structure):
         ("seed", ctypes.c_uint64),
         ("sr_stream", ctypes.c_uint32),
         ("elem_format", ctypes.c_int),
+        ("tensor_exp", ctypes.c_int),
     ]
 
 
@@ -72,12 +73,17 @@ class Params:
     seed: int = 0
     sr_stream: int = 0
     elem_format: int = 0        # FORMAT_E2M1 (MXFP4) or FORMAT_E4M3 (MXFP8)
+    tensor_exp: int = 0         # BLOCK_1X16 (NVFP4): per-tensor factor 2^tensor_exp
 
     def _c(self) -> _Params:
         return _Params(self.block, self.scale_mode, self.rounding, LAYOUT_ROWMAJOR,
                        int(bool(self.wht)), self.wht_sign_mask & 0xFFFFFFFF,
                        self.seed & 0xFFFFFFFFFFFFFFFF, self.sr_stream & 0xFFFFFFFF,
-                       self.elem_format)
+                       self.elem_format, self.tensor_exp)
+
+    def scale_cols(self, k: int) -> int:
+        """Scale bytes per output row for quantization axis length k."""
+        return k // 16 if self.block == BLOCK_1X16 else k // 32
 
 
 _lib = None
@@ -124,6 +130,13 @@ def lib() -> ctypes.CDLL:
         L.orc_hadamard32.argtypes = [P, ctypes.c_int, i64, i64, i64, ctypes.c_uint32, ctypes.c_int, P]
         L.orc_gemm_pairs.restype = ctypes.c_int
         L.orc_gemm_pairs.argtypes = [P, P, P, P, ctypes.c_int, i64, i64, i64, i64, P, P, P, P]
+        L.orc_nv_scale_code.restype = ctypes.c_int
+        L.orc_nv_scale_code.argtypes = [ctypes.c_float, ctypes.c_int, ctypes.c_int]
+        L.orc_dequantize_nv_f64.restype = ctypes.c_int
+        L.orc_dequantize_nv_f64.argtypes = [P, P, ctypes.c_int, i64, i64, ctypes.c_int, P]
+        L.orc_gemm_pairs_nv.restype = ctypes.c_int
+        L.orc_gemm_pairs_nv.argtypes = [P, P, ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int,
+                                        i64, i64, i64, i64, P, P, P, P]
         _lib = L
     return _lib
 
@@ -195,6 +208,11 @@ def round_sr(v: float, r16: int) -> int:
     return int(lib().orc_round_sr(ctypes.c_float(v), r16))
 
 
+def nv_scale_code(M: float, k: int, mode: int) -> int:
+    """E4M3 code of the NVFP4 block scale for block max-abs M under factor 2^k."""
+    return int(lib().orc_nv_scale_code(ctypes.c_float(M), k, mode))
+
+
 # ------------------------------------------------------------------ tensors --
 
 def quantize_rows(x: np.ndarray, p: Params, r0: int = 0, r1: int | None = None):
@@ -203,7 +221,7 @@ def quantize_rows(x: np.ndarray, p: Params, r0: int = 0, r1: int | None = None):
     rows, cols = x.shape
     r1 = rows if r1 is None else r1
     q = np.zeros((r1 - r0, cols if p.elem_format == FORMAT_E4M3 else cols // 2), dtype=np.uint8)
-    s = np.zeros((r1 - r0, cols // 32), dtype=np.uint8)
+    s = np.zeros((r1 - r0, p.scale_cols(cols)), dtype=np.uint8)
     cp = p._c()
     rc = lib().orc_quantize_rows(_ptr(x), dt, rows, cols, ld, ctypes.byref(cp), r0, r1, _ptr(q), _ptr(s))
     if rc:
@@ -217,7 +235,7 @@ def quantize_cols(x: np.ndarray, p: Params, c0: int = 0, c1: int | None = None):
     rows, cols = x.shape
     c1 = cols if c1 is None else c1
     q = np.zeros((c1 - c0, rows if p.elem_format == FORMAT_E4M3 else rows // 2), dtype=np.uint8)
-    s = np.zeros((c1 - c0, rows // 32), dtype=np.uint8)
+    s = np.zeros((c1 - c0, p.scale_cols(rows)), dtype=np.uint8)
     cp = p._c()
     rc = lib().orc_quantize_cols(_ptr(x), dt, rows, cols, ld, ctypes.byref(cp), c0, c1, _ptr(q), _ptr(s))
     if rc:
@@ -254,6 +272,17 @@ def dequantize(q: np.ndarray, s: np.ndarray, rows: int, cols: int,
     return out
 
 
+def dequantize_nv(q: np.ndarray, s: np.ndarray, rows: int, cols: int, tensor_exp: int = 0,
+                  layout: int = LAYOUT_ROWMAJOR) -> np.ndarray:
+    """NVFP4 reconstruction (fp64): E2M1 code x E4M3 scale x 2^tensor_exp."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    out = np.zeros((rows, cols), dtype=np.float64)
+    if lib().orc_dequantize_nv_f64(_ptr(q), _ptr(s), layout, rows, cols, tensor_exp, _ptr(out)):
+        raise ValueError("oracle dequantize_nv: bad shape")
+    return out
+
+
 def hadamard32(x: np.ndarray, sign_mask: int = 0, inverse: bool = False) -> np.ndarray:
     x, dt, ld = _as_input(x)
     rows, cols = x.shape
@@ -287,3 +316,25 @@ def gemm_ref(qa, sa, qb, sb, M, N, K, layout=LAYOUT_MMA, rows=None):
     if rows is not None:
         A = A[np.asarray(rows)]
     return A @ B.T, np.abs(A) @ np.abs(B).T
+
+
+def gemm_ref_nv(qa, sa, ka, qb, sb, kb, M, N, K, layout=LAYOUT_MMA):
+    """fp64 reference C = deq(A) deq(B)^T for NVFP4 operands (per-tensor
+    factors 2^ka, 2^kb) and the tolerance base sum_k |a*b|."""
+    A = dequantize_nv(qa, sa, M, K, ka, layout)
+    B = dequantize_nv(qb, sb, N, K, kb, layout)
+    return A @ B.T, np.abs(A) @ np.abs(B).T
+
+
+def gemm_pairs_nv(qa, sa, ka, qb, sb, kb, M, N, K, ms, ns, layout=LAYOUT_MMA):
+    """Brute-force fp64 C[m, n] and sum_k |a*b| of NVFP4 operands for listed (m, n)."""
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    c = np.zeros(len(ms), dtype=np.float64)
+    a = np.zeros(len(ms), dtype=np.float64)
+    qa, sa, qb, sb = [np.ascontiguousarray(t, dtype=np.uint8) for t in (qa, sa, qb, sb)]
+    rc = lib().orc_gemm_pairs_nv(_ptr(qa), _ptr(sa), ka, _ptr(qb), _ptr(sb), kb, layout, M, N, K,
+                                 len(ms), _ptr(ms), _ptr(ns), _ptr(c), _ptr(a))
+    if rc:
+        raise ValueError(f"oracle gemm_pairs_nv failed ({rc})")
+    return c, a

@@ -197,6 +197,39 @@ int orc_round_e4m3_rtn(float v) {
   return (signbit(v) ? 0x80 : 0) | best;
 }
 
+/* NVFP4 block scale [TIBQ, "Why FP4 training is the current frontier": 1x16
+ * blocks (NVFP4) whose shared scale S is chosen from the block's max-abs].
+ * Readings (the page gives only the block size and that S follows the block
+ * max): S is an E4M3 value (the NVFP4 scale format) applied under a
+ * per-tensor power-of-two factor 2^k, so the block scale is S * 2^k. The two
+ * scale modes carry over from the E8M0 case: round-up ("truncation-free") is
+ * the smallest S with 6 * S * 2^k >= M; floor mode, which has no power-of-two
+ * meaning for E4M3, is read as the nearest S to M / (6 * 2^k) (ties to the
+ * even code; a block max may then exceed 6 S 2^k by up to half an E4M3 step
+ * and those elements saturate). Both saturate at 448. Direct search over the
+ * 127 finite non-negative codes with exact fp64 arithmetic: M * 2^-k and
+ * 6 * S are exact, and below the saturation point so is the distance to the
+ * nearest candidates. */
+int orc_nv_scale_code(float M, int k, int scale_mode) {
+  const double y = ldexp((double)M, -k);
+  if (scale_mode == ORC_SCALE_ROUNDUP) {
+    for (int c = 0; c < 127; ++c)
+      if (6.0 * (double)orc_e4m3_value(c) >= y) return c;
+    return 126;
+  }
+  if (y >= 6.0 * 448.0) return 126;   /* saturate (keeps every distance below exact) */
+  int best = 0;
+  double bestd = fabs(y);
+  for (int c = 1; c < 127; ++c) {
+    const double d = fabs(6.0 * (double)orc_e4m3_value(c) - y);
+    if (d < bestd || (d == bestd && (c % 2) == 0 && (best % 2) != 0)) {
+      best = c;
+      bestd = d;
+    }
+  }
+  return best;
+}
+
 /* ------------------------------------------------------------ rounding ---- */
 
 /* Round-to-nearest onto the E2M1 grid [TIBQ, "Stochastic rounding in the
@@ -260,9 +293,16 @@ static float load_elem(const void* x, int dtype, int64_t ld, int64_t r, int64_t 
  * aligned b x b tile of output rows and k, whose one scale is stored on each
  * of its rows for each of its b/32 runs of 32 k. With the rotation on, each
  * 1x32 run along k is rotated first and the block max is taken afterwards. */
+static int quantize_orient_nv(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                              const orc_params* p, int col_orient, int64_t i0, int64_t i1,
+                              uint8_t* q, uint8_t* s);
+
 static int quantize_orient(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
                            const orc_params* p, int col_orient, int64_t i0, int64_t i1,
                            uint8_t* q, uint8_t* s) {
+  if (p->block == ORC_BLOCK_1X16)
+    return quantize_orient_nv(x, dtype, rows, cols, ld, p, col_orient, i0, i1, q, s);
+  if (p->tensor_exp != 0) return -1;   /* the per-tensor factor belongs to NVFP4 */
   const int64_t nout = col_orient ? cols : rows;  /* output rows */
   const int64_t K = col_orient ? rows : cols;     /* quantization axis */
   /* g output rows by bw values of k share one scale */
@@ -324,6 +364,68 @@ static int quantize_orient(const void* x, int dtype, int64_t rows, int64_t cols,
           uint8_t* byte = &q[orow * (K / 2) + k / 2];
           if ((k & 1) == 0)
             *byte = (uint8_t)((*byte & 0xF0u) | (uint8_t)code);   /* even k: low nibble */
+          else
+            *byte = (uint8_t)((*byte & 0x0Fu) | (uint8_t)(code << 4));
+        }
+      }
+    }
+  }
+  return bad ? -3 : 0;
+}
+
+/* NVFP4: blocks of 16 consecutive k of one output row, each with its E4M3
+ * scale S (orc_nv_scale_code) under the factor 2^k. With the rotation on,
+ * each 32-run along k is rotated first (the rotation does not depend on the
+ * block size), then both of its 16-blocks are scaled. Scaling reading: one
+ * fp32 reciprocal of the block scale, r = 1 / (S * 2^k) rounded to nearest,
+ * and one rounded fp32 product per element, v = y * r (r = 0 when S = 0, so
+ * such a block encodes as signed zeros). Rounding as for MXFP4; the random
+ * bits are keyed by the source index as there. */
+static int quantize_orient_nv(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                              const orc_params* p, int col_orient, int64_t i0, int64_t i1,
+                              uint8_t* q, uint8_t* s) {
+  const int64_t nout = col_orient ? cols : rows;
+  const int64_t K = col_orient ? rows : cols;
+  if (K % 32 != 0 || i0 < 0 || i1 > nout || i0 > i1) return -1;
+  if (p->elem_format != ORC_FORMAT_E2M1) return -1;
+  if (p->tensor_exp < -100 || p->tensor_exp > 100) return -1;
+  const int64_t nkb = K / 16;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+  for (int64_t i = i0; i < i1; ++i) {
+    const int64_t orow = i - i0;
+    for (int64_t kr = 0; kr < K / 32 && !bad; ++kr) {
+      float blk[32], y[32];
+      for (int j = 0; j < 32; ++j) {
+        const int64_t k = kr * 32 + j;
+        blk[j] = col_orient ? load_elem(x, dtype, ld, k, i) : load_elem(x, dtype, ld, i, k);
+        if (!isfinite(blk[j])) bad = 1;
+      }
+      if (p->wht)
+        orc_wht32(blk, p->wht_sign_mask, 0, y);
+      else
+        memcpy(y, blk, sizeof(blk));
+      for (int h = 0; h < 2; ++h) {
+        float M = 0.0f;
+        for (int j = 16 * h; j < 16 * h + 16; ++j)
+          if (fabsf(y[j]) > M) M = fabsf(y[j]);
+        const int sc = orc_nv_scale_code(M, p->tensor_exp, p->scale_mode);
+        s[orow * nkb + 2 * kr + h] = (uint8_t)sc;
+        const float S = ldexpf(orc_e4m3_value(sc), p->tensor_exp);   /* exact */
+        const float r = S == 0.0f ? 0.0f : 1.0f / S;
+        for (int j = 16 * h; j < 16 * h + 16; ++j) {
+          const int64_t k = kr * 32 + j;
+          const float v = y[j] * r;
+          int code;
+          if (p->rounding == ORC_ROUND_SR) {
+            const int64_t src = col_orient ? (k * cols + i) : (i * cols + k);
+            code = orc_round_sr(v, orc_sr_bits(p->seed, p->sr_stream, (uint64_t)src));
+          } else {
+            code = orc_round_rtn(v);
+          }
+          uint8_t* byte = &q[orow * (K / 2) + k / 2];
+          if ((k & 1) == 0)
+            *byte = (uint8_t)((*byte & 0xF0u) | (uint8_t)code);
           else
             *byte = (uint8_t)((*byte & 0x0Fu) | (uint8_t)(code << 4));
         }
@@ -419,6 +521,33 @@ int orc_dequantize_e4m3_f64(const uint8_t* q, const uint8_t* s, int layout, int6
   return 0;
 }
 
+/* NVFP4 reconstruction: E2M1(code) * E4M3(scale) * 2^tensor_exp. */
+static double deq_one_nv(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
+                         int64_t cols, int tensor_exp, int64_t r, int64_t c) {
+  const int64_t nkb = cols / 16;
+  const uint8_t byte = q[r * (cols / 2) + c / 2];
+  const int code = (c & 1) ? (byte >> 4) : (byte & 0x0F);
+  const uint8_t sb = (layout == ORC_LAYOUT_MMA) ? s[orc_mma_scale_offset(r, c / 16, rows, nkb)]
+                                                : s[r * nkb + c / 16];
+  return ldexp((double)orc_e2m1_value(code) * (double)orc_e4m3_value(sb), tensor_exp);
+}
+
+static int deq_check_nv(int layout, int64_t rows, int64_t cols) {
+  if (cols % 32 != 0 || rows < 0) return -1;
+  if (layout == ORC_LAYOUT_MMA && (rows % 128 != 0 || (cols / 16) % 4 != 0)) return -1;
+  return 0;
+}
+
+int orc_dequantize_nv_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
+                          int64_t cols, int tensor_exp, double* out) {
+  if (deq_check_nv(layout, rows, cols)) return -1;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c)
+      out[r * cols + c] = deq_one_nv(q, s, layout, rows, cols, tensor_exp, r, c);
+  return 0;
+}
+
 /* ------------------------------------------------------------ hadamard ---- */
 
 int orc_hadamard32(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
@@ -450,6 +579,27 @@ int orc_gemm_pairs(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb, cons
     double acc = 0.0, acc_abs = 0.0;
     for (int64_t k = 0; k < K; ++k) {
       const double prod = deq_one(qa, sa, layout, M, K, m, k) * deq_one(qb, sb, layout, N, K, n, k);
+      acc += prod;
+      acc_abs += fabs(prod);
+    }
+    c[t] = acc;
+    abs_sum[t] = acc_abs;
+  }
+  return 0;
+}
+
+int orc_gemm_pairs_nv(const uint8_t* qa, const uint8_t* sa, int ka, const uint8_t* qb,
+                      const uint8_t* sb, int kb, int layout, int64_t M, int64_t N, int64_t K,
+                      int64_t npairs, const int64_t* ms, const int64_t* ns, double* c,
+                      double* abs_sum) {
+  if (deq_check_nv(layout, M, K) || deq_check_nv(layout, N, K)) return -1;
+  for (int64_t t = 0; t < npairs; ++t) {
+    const int64_t m = ms[t], n = ns[t];
+    if (m < 0 || m >= M || n < 0 || n >= N) return -2;
+    double acc = 0.0, acc_abs = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double prod = deq_one_nv(qa, sa, layout, M, K, ka, m, k) *
+                          deq_one_nv(qb, sb, layout, N, K, kb, n, k);
       acc += prod;
       acc_abs += fabs(prod);
     }

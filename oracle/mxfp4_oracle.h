@@ -21,7 +21,7 @@
 extern "C" {
 #endif
 
-enum { ORC_BLOCK_1X32 = 0, ORC_BLOCK_32X32 = 1, ORC_BLOCK_64X64 = 2 };
+enum { ORC_BLOCK_1X32 = 0, ORC_BLOCK_32X32 = 1, ORC_BLOCK_64X64 = 2, ORC_BLOCK_1X16 = 3 };
 enum { ORC_SCALE_FLOOR = 0, ORC_SCALE_ROUNDUP = 1 };
 enum { ORC_ROUND_RTN = 0, ORC_ROUND_SR = 1 };
 enum { ORC_LAYOUT_ROWMAJOR = 0, ORC_LAYOUT_MMA = 1 };
@@ -38,6 +38,7 @@ typedef struct {
   uint64_t seed;          /* Philox key */
   uint32_t sr_stream;     /* Philox counter word 2 */
   int elem_format;        /* ORC_FORMAT_*: E2M1 (MXFP4) or E4M3 (MXFP8, nearest only) */
+  int tensor_exp;         /* 1x16 (NVFP4) only: per-tensor factor 2^tensor_exp; else 0 */
 } orc_params;
 
 /* E2M1 code (4 bits, bit 3 = sign) -> value. */
@@ -70,9 +71,17 @@ int orc_round_e4m3_rtn(float v);
  * or 448). orc_scale_exponent is the E2M1 case. */
 int orc_scale_exponent_fmt(float M, int scale_mode, int elem_format);
 
+/* NVFP4 block scale: the E4M3 code (0 .. 126) of the scale S of a 1x16 block
+ * with max-abs M under the per-tensor factor 2^k. Round-up mode: the smallest
+ * E4M3 value S with 6 * S * 2^k >= M (nothing clips; 448 if none is large
+ * enough). Floor mode reads as "nearest": the E4M3 value nearest to
+ * M / (6 * 2^k), ties to the even code, saturating at 448. */
+int orc_nv_scale_code(float M, int k, int scale_mode);
+
 /* Row-wise quantization of rows [r0, r1) of x [rows, cols] (leading dim ld,
  * elements), along cols. q: [(r1-r0), cols/2] bytes (E4M3: [(r1-r0), cols]),
- * s: [(r1-r0), cols/32] bytes, both row-major. Returns 0 on success, nonzero
+ * s: [(r1-r0), cols/32] bytes (1x16 blocks: cols/16 E4M3 codes), both
+ * row-major. Returns 0 on success, nonzero
  * on bad arguments. */
 int orc_quantize_rows(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
                       const orc_params* p, int64_t r0, int64_t r1, uint8_t* q, uint8_t* s);
@@ -99,6 +108,12 @@ int orc_dequantize_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t r
 int orc_dequantize_e4m3_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
                             int64_t cols, double* out);
 
+/* The same for NVFP4: q [rows, cols/2] E2M1 codes, s [rows, cols/16] E4M3
+ * scale codes (layout as given; the tensor-core layout with cols/16 scale
+ * columns), value = E2M1(code) * E4M3(s) * 2^tensor_exp. */
+int orc_dequantize_nv_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
+                          int64_t cols, int tensor_exp, double* out);
+
 /* Stand-alone rotation along cols of x; y [rows, cols] fp32 row-major. */
 int orc_hadamard32(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
                    uint32_t sign_mask, int inverse, float* y);
@@ -108,6 +123,12 @@ int orc_hadamard32(const void* x, int dtype, int64_t rows, int64_t cols, int64_t
 int orc_gemm_pairs(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb, const uint8_t* sb,
                    int layout, int64_t M, int64_t N, int64_t K, int64_t npairs,
                    const int64_t* ms, const int64_t* ns, double* c, double* abs_sum);
+
+/* orc_gemm_pairs for NVFP4 operands (scales as in orc_dequantize_nv_f64). */
+int orc_gemm_pairs_nv(const uint8_t* qa, const uint8_t* sa, int ka, const uint8_t* qb,
+                      const uint8_t* sb, int kb, int layout, int64_t M, int64_t N, int64_t K,
+                      int64_t npairs, const int64_t* ms, const int64_t* ns, double* c,
+                      double* abs_sum);
 
 #ifdef __cplusplus
 }

@@ -552,3 +552,204 @@ def test_mxfp8_quantize_by_elementwise_definition():
             assert np.all(np.isfinite(d))
     with pytest.raises(ValueError):    # stochastic rounding is MXFP4-only
         oracle.quantize_rows(xb, oracle.Params(rounding=oracle.ROUND_SR, elem_format=oracle.FORMAT_E4M3))
+
+
+# ------------------------------------------------------- NVFP4 (1x16, E4M3) --
+
+def _e4m3_grid_round(t: Fraction, up: bool) -> Fraction:
+    """Closed form of E4M3 rounding of a non-negative rational t: the grid
+    spacing is 2^-9 below 2^-6 and 2^(E-3) in binade [2^E, 2^(E+1)); round up
+    (ceiling) or to nearest with ties to an even multiple of the spacing (the
+    even code); values above 448 saturate to 448."""
+    if t == 0:
+        return Fraction(0)
+    if t < Fraction(1, 64):
+        ulp = Fraction(1, 512)
+    else:
+        E = math.floor(math.log2(t))
+        while Fraction(2) ** (E + 1) <= t:
+            E += 1
+        while Fraction(2) ** E > t:
+            E -= 1
+        ulp = Fraction(2) ** (E - 3)
+    n = t / ulp
+    if up:
+        m = math.ceil(n)
+    else:
+        m = math.floor(n)
+        if n - m > Fraction(1, 2) or (n - m == Fraction(1, 2) and m % 2 == 1):
+            m += 1
+    return min(m * ulp, Fraction(448))
+
+
+def test_nv_scale_code_closed_forms_all_bf16():
+    """Every positive finite bf16 block max, three per-tensor factors, both
+    modes: the scale equals the closed-form E4M3 rounding of M / (6 * 2^k)
+    (ceiling for round-up, nearest-even for floor mode)."""
+    Ms = list(_all_positive_bf16_f32()[::3]) + [np.float32(6.0), np.float32(7.0),
+                                               np.float32(6 * 448), np.float32(6 * 480)]
+    for k in (0, 9, -12):
+        for M in Ms:
+            M = float(M)
+            t = Fraction(M) / (6 * Fraction(2) ** k)
+            for mode, up in ((oracle.SCALE_ROUNDUP, True), (oracle.SCALE_FLOOR, False)):
+                c = oracle.nv_scale_code(M, k, mode)
+                assert 0 <= c <= 126
+                assert Fraction(oracle.e4m3_value(c)) == _e4m3_grid_round(t, up), (M, k, mode)
+    assert oracle.nv_scale_code(0.0, 0, oracle.SCALE_ROUNDUP) == 0
+    assert oracle.nv_scale_code(0.0, 0, oracle.SCALE_FLOOR) == 0
+
+
+def test_nv_scale_code_nearest_matches_torch_e4m3_where_no_tie():
+    """Nearest mode against PyTorch's float8_e4m3fn rounding of the fp32 value
+    M / 6 (for these M the fp32 quotient is exact, so there is no double
+    rounding: M = 6 * (value on a fine grid))."""
+    import torch
+
+    rng = np.random.default_rng(91)
+    fine = (rng.integers(1, 1 << 11, 3000) * 2.0 ** rng.integers(-20, 0, 3000)).astype(np.float32)
+    fine = fine[fine <= 448]
+    M = (fine.astype(np.float64) * 6).astype(np.float32)
+    assert np.all(M.astype(np.float64) / 6 == fine.astype(np.float64))
+    ref = torch.from_numpy(fine).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for m, r in zip(M, ref):
+        assert oracle.nv_scale_code(float(m), 0, oracle.SCALE_FLOOR) == int(r), float(m)
+
+
+def test_nvfp4_worked_block():
+    """A hand-worked 1x16 block. Max 7: round-up scale 1.25 (the smallest E4M3
+    S with 6 S >= 7), nearest scale 1.125 (7/6 = 1.1667 is nearer 1.125 than
+    1.25). Elements times the fp32 reciprocal, then E2M1 nearest-even."""
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, :4] = [7.0, 3.5, -1.0, 0.2]
+    x[0, 16:] = 0.0
+    up = oracle.Params(block=oracle.BLOCK_1X16, scale_mode=oracle.SCALE_ROUNDUP)
+    q, s = oracle.quantize_rows(x, up)
+    assert s.shape == (1, 2)
+    assert oracle.e4m3_value(int(s[0, 0])) == 1.25 and s[0, 1] == 0
+    # 7*0.8 = 5.6 -> 6 (code 7); 3.5*0.8 = 2.8 -> 3 (code 5); -0.8 -> -1 (0xA); 0.16 -> 0
+    assert q[0, 0] == (5 << 4 | 7) and q[0, 1] == (0 << 4 | 0xA)
+    nearest = oracle.Params(block=oracle.BLOCK_1X16, scale_mode=oracle.SCALE_FLOOR)
+    q, s = oracle.quantize_rows(x, nearest)
+    assert oracle.e4m3_value(int(s[0, 0])) == 1.125
+    # 7/1.125 = 6.22 -> saturates at 6; 3.11 -> 3; -0.89 -> -1; 0.18 -> 0
+    assert q[0, 0] == (5 << 4 | 7) and q[0, 1] == (0 << 4 | 0xA)
+    d = oracle.dequantize_nv(q, s, 1, 32)
+    assert list(d[0, :4]) == [6.75, 3.375, -1.125, 0.0]
+
+
+@pytest.mark.parametrize("mode", [oracle.SCALE_FLOOR, oracle.SCALE_ROUNDUP])
+def test_nvfp4_quantize_by_elementwise_definition(mode):
+    """Block indexing, scale placement and packing: each 16-block's scale code
+    from its max (pinned above), each element the nearest E2M1 code of
+    x * fp32(1 / (S 2^k)); row-major [rows, cols/16] scales."""
+    rows, cols, k = 32, 96, -3
+    xb = _bf16(synth.student_t(rows, cols, 3.0, seed=92))
+    xv = (xb.astype(np.uint32) << 16).view(np.float32).reshape(rows, cols)
+    p = oracle.Params(block=oracle.BLOCK_1X16, scale_mode=mode, tensor_exp=k)
+    q, s = oracle.quantize_rows(xb, p)
+    assert q.shape == (rows, cols // 2) and s.shape == (rows, cols // 16)
+    for r in range(rows):
+        for b in range(cols // 16):
+            blk = xv[r, 16 * b:16 * b + 16]
+            c = oracle.nv_scale_code(float(np.abs(blk).max()), k, mode)
+            assert s[r, b] == c
+            S = np.float32(oracle.e4m3_value(c) * 2.0 ** k)
+            rcp = np.float32(1) / S
+            for j in range(16):
+                col = 16 * b + j
+                code = (q[r, col // 2] >> (4 * (col & 1))) & 0xF
+                assert code == _nearest_even(float(np.float32(blk[j] * rcp))), (r, col)
+
+
+def test_nvfp4_roundup_never_clips_and_error_bound():
+    x = _bf16(synth.laplace(64, 256, 1e-3, seed=93, outlier_frac=0.01, outlier_mult=100.0))
+    xf = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    k = math.ceil(math.log2(np.abs(xf).max() / (6 * 448)))    # largest block scale <= 448
+    q, s = oracle.quantize_rows(x, oracle.Params(block=oracle.BLOCK_1X16,
+                                                 scale_mode=oracle.SCALE_ROUNDUP, tensor_exp=k))
+    d = oracle.dequantize_nv(q, s, 64, 256, k)
+    S = np.array([[oracle.e4m3_value(int(c)) for c in row] for row in s]).repeat(16, axis=1) * 2.0 ** k
+    assert np.all(np.abs(xf) <= 6 * S)                        # nothing clips
+    a = np.abs(xf) / S
+    half_step = np.where(a < 2, 0.25, np.where(a < 4, 0.5, 1.0)) * S
+    assert np.all(np.abs(d - xf) <= half_step * (1 + 2.0 ** -20))
+
+
+def test_nvfp4_tensor_factor_is_an_exact_rescaling():
+    """Quantizing x * 2^j with factor 2^j gives the codes and scales of x with
+    factor 1 (power-of-two scaling commutes with every rounding step)."""
+    x = synth.student_t(32, 128, 4.0, seed=94).float().numpy()
+    for mode in (oracle.SCALE_FLOOR, oracle.SCALE_ROUNDUP):
+        for rnd in (oracle.ROUND_RTN, oracle.ROUND_SR):
+            base = oracle.Params(block=oracle.BLOCK_1X16, scale_mode=mode, rounding=rnd, seed=5)
+            q0, s0 = oracle.quantize_rows(x, base)
+            for j in (-20, 13):
+                xs = (x.astype(np.float64) * 2.0 ** j).astype(np.float32)
+                p = oracle.Params(block=oracle.BLOCK_1X16, scale_mode=mode, rounding=rnd, seed=5,
+                                  tensor_exp=j)
+                q1, s1 = oracle.quantize_rows(xs, p)
+                assert np.array_equal(q0, q1) and np.array_equal(s0, s1)
+
+
+def test_nvfp4_columns_rotation_and_rejects():
+    x = _bf16(synth.student_t(64, 96, 4.0, seed=95))
+    xf = (x.astype(np.uint32) << 16).view(np.float32).reshape(64, 96)
+    p = oracle.Params(block=oracle.BLOCK_1X16, scale_mode=oracle.SCALE_ROUNDUP, tensor_exp=2)
+    qc, sc = oracle.quantize_cols(x, p)
+    qt, st = oracle.quantize_rows(np.ascontiguousarray(xf.T), p)
+    assert np.array_equal(qc, qt) and np.array_equal(sc, st)
+    mask = 0x13579BDF
+    pw = oracle.Params(block=oracle.BLOCK_1X16, wht=True, wht_sign_mask=mask)
+    qw, sw = oracle.quantize_rows(x, pw)
+    qh, sh = oracle.quantize_rows(oracle.hadamard32(x, mask), oracle.Params(block=oracle.BLOCK_1X16))
+    assert np.array_equal(qw, qh) and np.array_equal(sw, sh)
+    with pytest.raises(ValueError):       # the per-tensor factor is NVFP4's
+        oracle.quantize_rows(x, oracle.Params(tensor_exp=1))
+    with pytest.raises(ValueError):       # E2M1 elements only
+        oracle.quantize_rows(x, oracle.Params(block=oracle.BLOCK_1X16, elem_format=oracle.FORMAT_E4M3))
+
+
+def test_nvfp4_sr_unbiased():
+    """Stochastic rounding under round-up scales: the mean reconstruction over
+    independent seeds approaches x."""
+    rows, cols = 16, 64
+    x = synth.normal(rows, cols, 1.0, seed=96).float().numpy()
+    acc = np.zeros((rows, cols))
+    n = 400
+    for seed in range(n):
+        p = oracle.Params(block=oracle.BLOCK_1X16, scale_mode=oracle.SCALE_ROUNDUP,
+                          rounding=oracle.ROUND_SR, seed=seed)
+        q, s = oracle.quantize_rows(x, p)
+        acc += oracle.dequantize_nv(q, s, rows, cols)
+    mean = acc / n
+    S = np.array([[oracle.e4m3_value(int(c)) for c in row] for row in s]).repeat(16, axis=1)
+    # the per-element spread is at most one grid step (<= 2 S): 5 sigma of the mean
+    assert np.all(np.abs(mean - x) <= 5 * 2 * S / np.sqrt(n) / 2 + 2 * S * 2.0 ** -16)
+
+
+def test_nvfp4_dequantize_and_gemm_pairs_exact():
+    rows, cols = 128, 64
+    rng = np.random.default_rng(97)
+    q = rng.integers(0, 256, (rows, cols // 2), dtype=np.uint8)
+    s = rng.integers(0, 127, (rows, cols // 16), dtype=np.uint8)   # finite E4M3 codes
+    d = oracle.dequantize_nv(q, s, rows, cols, tensor_exp=-4)
+    for r in range(0, rows, 17):
+        for c in range(cols):
+            code = int(q[r, c // 2] >> (4 * (c & 1))) & 0xF
+            want = (-1) ** (code >> 3) * GRID[code & 7] * Fraction(oracle.e4m3_value(int(s[r, c // 16]))) / 16
+            assert Fraction(d[r, c]) == want
+    sm = oracle.scales_to_mma(s)
+    assert np.array_equal(oracle.dequantize_nv(q, sm, rows, cols, -4, oracle.LAYOUT_MMA), d)
+    # GEMM pairs: exact rational sum of the dequantized products
+    qb = rng.integers(0, 256, (rows, cols // 2), dtype=np.uint8)
+    sb = rng.integers(40, 70, (rows, cols // 16), dtype=np.uint8)
+    db = oracle.dequantize_nv(qb, sb, rows, cols, tensor_exp=3)
+    ms = np.array([0, 5, 127, 64]); ns = np.array([3, 127, 0, 64])
+    c, a = oracle.gemm_pairs_nv(q, sm, -4, qb, oracle.scales_to_mma(sb), 3, rows, rows, cols, ms, ns)
+    for t, (m, n) in enumerate(zip(ms, ns)):
+        exact = sum(Fraction(d[m, k]) * Fraction(db[n, k]) for k in range(cols))
+        assert Fraction(c[t]) == exact
+        assert a[t] == sum(abs(Fraction(d[m, k]) * Fraction(db[n, k])) for k in range(cols))
+    C, A = oracle.gemm_ref_nv(q, sm, -4, qb, oracle.scales_to_mma(sb), 3, rows, rows, cols)
+    assert np.allclose(C[ms, ns], c, rtol=0, atol=1e-12 * a.max())
