@@ -25,13 +25,14 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
 import sys
 import threading
 import time
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -49,6 +50,9 @@ LAYERS = {
     "70b-layer-det": (16384, 8192, 28672, 1003,
                       "70B-dense-shaped layer training step, deterministic rotation: tokens 16384, "
                       "d 8192, ffn 28672"),
+    "70b-layer-nvfp4": (16384, 8192, 28672, 1003,
+                        "70B-dense-shaped layer training step in NVFP4 (1x16 blocks, E4M3 scales "
+                        "under per-tensor power-of-two factors): tokens 16384, d 8192, ffn 28672"),
 }
 # Square sweep points: quantize A and B (1x32 floor nearest-even) + one n^3 GEMM.
 SQUARES = {f"sq{n}": n for n in (1024, 2048, 4096, 8192, 16384)}
@@ -84,11 +88,17 @@ class Spec:
     desc: str
     quants: list = field(default_factory=list)
     gemms: list = field(default_factory=list)
+    nvfp4: bool = False   # 1x16 blocks with E4M3 scales; GEMMs through nvfp4_gemm
+
+    def scale_bytes_per_elem(self) -> float:
+        return 1 / 16 if self.nvfp4 else 1 / 32
 
     def quant_bytes(self):
         """Algorithmic bytes per quantize launch: read the bf16 input once, write
-        each requested orientation's codes (0.5 B/elem) and scales (1/32 B/elem)."""
-        return [q.rows * q.cols * (2 + ((q.prow is not None) + (q.pcol is not None)) * (0.5 + 1 / 32))
+        each requested orientation's codes (0.5 B/elem) and scales (1/32 B/elem;
+        1/16 for NVFP4)."""
+        sb = self.scale_bytes_per_elem()
+        return [q.rows * q.cols * (2 + ((q.prow is not None) + (q.pcol is not None)) * (0.5 + sb))
                 for q in self.quants]
 
     def gemm_flops(self):
@@ -130,6 +140,13 @@ def make_spec(name: str) -> Spec:
         s.gemms = [GemmOp("Fprop", ("X", "row"), ("W", "row"), T, F, D),
                    GemmOp("Dgrad", ("dY", "row"), ("W", "col"), T, D, F),
                    GemmOp("Wgrad", ("dY", "col"), ("X", "col"), F, D, T)]
+        if name.endswith("-nvfp4"):
+            # The same recipe with every block 1x16 (E4M3 scales, round-up);
+            # each tensor's factor 2^k comes from its max-abs (set in Step).
+            s.nvfp4 = True
+            for q in s.quants:
+                q.prow = replace(q.prow, block=mx.BLOCK_1X16, scale_mode=mx.SCALE_ROUNDUP)
+                q.pcol = replace(q.pcol, block=mx.BLOCK_1X16, scale_mode=mx.SCALE_ROUNDUP)
         return s
     if name == "tiny":
         mask = synth.sign_mask(1000)
@@ -182,17 +199,26 @@ class Step:
     def __init__(self, spec: Spec, device):
         import torch
 
+        import gemm_pt_block_gb300 as mx
+
         self.spec = spec
         u8 = torch.uint8
-        self.inputs, self.bufs, self.outs = {}, {}, {}
+        self.inputs, self.bufs, self.outs, self.params = {}, {}, {}, {}
         for q in spec.quants:
             self.inputs[q.name] = gen_input(q, device)
+            prow, pcol = q.prow, q.pcol
+            if spec.nvfp4:   # per-tensor factor from the tensor's max-abs (set up once)
+                k = mx.nvfp4_tensor_exp(float(self.inputs[q.name].float().abs().max()))
+                prow = prow and replace(prow, tensor_exp=k)
+                pcol = pcol and replace(pcol, tensor_exp=k)
+            self.params[q.name] = (prow, pcol)
             r, c = q.rows, q.cols
+            ns = int(r * c * spec.scale_bytes_per_elem())
             self.bufs[q.name] = (
                 torch.empty(r, c // 2, dtype=u8, device=device) if q.prow else None,
-                torch.empty(r * c // 32, dtype=u8, device=device) if q.prow else None,
+                torch.empty(ns, dtype=u8, device=device) if q.prow else None,
                 torch.empty(c, r // 2, dtype=u8, device=device) if q.pcol else None,
-                torch.empty(r * c // 32, dtype=u8, device=device) if q.pcol else None)
+                torch.empty(ns, dtype=u8, device=device) if q.pcol else None)
         for g in spec.gemms:
             self.outs[g.label] = torch.empty(g.M, g.N, device=device)
         torch.cuda.empty_cache()
@@ -205,6 +231,10 @@ class Step:
         q, s, qc, sc = self.bufs[ref[0]]
         return (q, s) if ref[1] == "row" else (qc, sc)
 
+    def tensor_exp(self, ref) -> int:
+        prow, pcol = self.params[ref[0]]
+        return (prow if ref[1] == "row" else pcol).tensor_exp
+
     def run(self, inputs=None, events=None):
         """Enqueue the step on the current stream; events[i], events[i+1] bracket launch i."""
         import gemm_pt_block_gb300 as mx
@@ -215,14 +245,19 @@ class Step:
             events[0].record()
         for q in self.spec.quants:
             qr, sr, qc, sc = self.bufs[q.name]
-            mx.mxfp4_quantize(inp[q.name], q.prow, q.pcol, q_row=qr, s_row=sr, q_col=qc, s_col=sc)
+            prow, pcol = self.params[q.name]
+            mx.mxfp4_quantize(inp[q.name], prow, pcol, q_row=qr, s_row=sr, q_col=qc, s_col=sc)
             k += 1
             if events is not None:
                 events[k].record()
         for g in self.spec.gemms:
             qa, sa = self.operand(g.a)
             qb, sb = self.operand(g.b)
-            mx.mxfp4_gemm(qa, sa, qb, sb, g.M, g.N, g.K, c=self.outs[g.label])
+            if self.spec.nvfp4:
+                mx.nvfp4_gemm(qa, sa, self.tensor_exp(g.a), qb, sb, self.tensor_exp(g.b),
+                              g.M, g.N, g.K, c=self.outs[g.label])
+            else:
+                mx.mxfp4_gemm(qa, sa, qb, sb, g.M, g.N, g.K, c=self.outs[g.label])
             k += 1
             if events is not None:
                 events[k].record()
@@ -349,34 +384,52 @@ def cpu_oracle_sample(spec: Spec, r: int = 4096):
     import oracle
     import synth
 
-    def op(p):
-        return None if p is None else oracle.Params(p.block, p.scale_mode, p.rounding, p.wht,
-                                                     p.wht_sign_mask, p.seed, p.sr_stream)
+    import numpy as np
 
+    def op(p, band):
+        if p is None:
+            return None
+        k = 0
+        if p.block == oracle.BLOCK_1X16:   # the band's own per-tensor factor
+            amax = float(np.abs((band.astype(np.uint32) << 16).view(np.float32)).max())
+            k = math.ceil(math.log2(amax / 2688.0)) if amax > 0 else 0
+        return oracle.Params(p.block, p.scale_mode, p.rounding, p.wht, p.wht_sign_mask, p.seed,
+                             p.sr_stream, p.elem_format, k)
+
+    sb = spec.scale_bytes_per_elem()
     jobs, qbytes, flops = [], 0.0, 0.0
     for q in spec.quants:
         rr = min(r, q.rows)
         if q.prow is not None:
             band = synth.bf16_bits(gen_input(q, "cpu", rows=rr))
-            jobs.append(("rows", band, op(q.prow)))
-            qbytes += band.size * (2 + 0.5 + 1 / 32)
+            jobs.append(("rows", band, op(q.prow, band)))
+            qbytes += band.size * (2 + 0.5 + sb)
         if q.pcol is not None:
             cc = min(r, q.cols)
             band = synth.bf16_bits(gen_input(q, "cpu", cols=cc, seed_offset=1))
-            jobs.append(("cols", band, op(q.pcol)))
-            qbytes += band.size * (2 + 0.5 + 1 / 32)
+            jobs.append(("cols", band, op(q.pcol, band)))
+            qbytes += band.size * (2 + 0.5 + sb)
     gem = []
     for g in spec.gemms:
         m = min(r, g.M)
-        gem.append((synth.random_codes(m, g.K, 1), synth.random_scales(m, g.K, 2),
-                    synth.random_codes(g.N, g.K, 3), synth.random_scales(g.N, g.K, 4), m, g.N, g.K))
+        if spec.nvfp4:   # random E4M3 scale codes near 1
+            sa = np.random.default_rng(2).integers(40, 70, m * g.K // 16, dtype=np.uint8)
+            sbb = np.random.default_rng(4).integers(40, 70, g.N * g.K // 16, dtype=np.uint8)
+        else:
+            sa, sbb = synth.random_scales(m, g.K, 2), synth.random_scales(g.N, g.K, 4)
+        gem.append((synth.random_codes(m, g.K, 1), sa, synth.random_codes(g.N, g.K, 3), sbb,
+                    m, g.N, g.K))
         flops += 2.0 * m * g.N * g.K
     t0 = time.perf_counter()
     for kind, band, p in jobs:
         (oracle.quantize_rows if kind == "rows" else oracle.quantize_cols)(band, p)
-    for qa, sa, qb, sb, m, N, K in gem:
-        A = oracle.dequantize(qa, sa.reshape(m, K // 32), m, K, f64=True)
-        B = oracle.dequantize(qb, sb.reshape(N, K // 32), N, K, f64=True)
+    for qa, sa, qb, sbb, m, N, K in gem:
+        if spec.nvfp4:
+            A = oracle.dequantize_nv(qa, sa.reshape(m, K // 16), m, K)
+            B = oracle.dequantize_nv(qb, sbb.reshape(N, K // 16), N, K)
+        else:
+            A = oracle.dequantize(qa, sa.reshape(m, K // 32), m, K, f64=True)
+            B = oracle.dequantize(qb, sbb.reshape(N, K // 32), N, K, f64=True)
         _ = A @ B.T
     dt = time.perf_counter() - t0
     threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
@@ -494,10 +547,11 @@ def run_op(args):
     qs = {q.name: q for q in spec.quants}
     gs = {g.label: g for g in spec.gemms}
     if args.op in qs:
-        sub = Spec(spec.name, spec.desc, [qs[args.op]], [])
+        sub = Spec(spec.name, spec.desc, [qs[args.op]], [], spec.nvfp4)
     elif args.op in gs:
         g = gs[args.op]
-        sub = Spec(spec.name, spec.desc, [qs[n] for n in dict.fromkeys((g.a[0], g.b[0]))], [g])
+        sub = Spec(spec.name, spec.desc, [qs[n] for n in dict.fromkeys((g.a[0], g.b[0]))], [g],
+                   spec.nvfp4)
     else:
         raise SystemExit(f"--op must be one of {sorted(qs) + sorted(gs)}")
     device = torch.device("cuda", 0)
@@ -507,13 +561,18 @@ def run_op(args):
         g = sub.gemms[0]
         qa, sa = st.operand(g.a)
         qb, sb = st.operand(g.b)
-        fn = lambda: mx.mxfp4_gemm(qa, sa, qb, sb, g.M, g.N, g.K, c=st.outs[g.label])
+        if sub.nvfp4:
+            ka, kb = st.tensor_exp(g.a), st.tensor_exp(g.b)
+            fn = lambda: mx.nvfp4_gemm(qa, sa, ka, qb, sb, kb, g.M, g.N, g.K, c=st.outs[g.label])
+        else:
+            fn = lambda: mx.mxfp4_gemm(qa, sa, qb, sb, g.M, g.N, g.K, c=st.outs[g.label])
         work, unit = sub.gemm_flops()[0] / 1e12, "TFLOP/s"
     else:
         q = sub.quants[0]
         qr, sr, qc, sc = st.bufs[q.name]
         x = st.inputs[q.name]
-        fn = lambda: mx.mxfp4_quantize(x, q.prow, q.pcol, q_row=qr, s_row=sr, q_col=qc, s_col=sc)
+        prow, pcol = st.params[q.name]
+        fn = lambda: mx.mxfp4_quantize(x, prow, pcol, q_row=qr, s_row=sr, q_col=qc, s_col=sc)
         work, unit = sub.quant_bytes()[0] / 1e9, "GB/s"
     for _ in range(args.warmup):
         fn()
@@ -677,7 +736,8 @@ def main():
     traffic = None
     if tr is not None and tr.get("workload") == args.workload:
         traffic = float(tr["dram_bytes_per_launch"])
-    roofline = {"bound": "tensor", "kernel": "mxf4_gemm_kernel", "achieved": achieved,
+    roofline = {"bound": "tensor", "kernel": "mxf4_gemm_pair_kernel" + ("<NVFP4>" if spec.nvfp4 else ""),
+                "achieved": achieved,
                 "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak, "traffic": traffic,
                 "peak_source": f"{peak_src}: bf16_tflops_sustained x {FP4_OVER_BF16:g} (nominal dense FP4:BF16)"}
     share = {lab: m / ms_step for lab, m in zip(labels, per_launch)}
@@ -696,7 +756,8 @@ def main():
             "quantize": {"gbs": quant_gbs, "frac_of_hbm": quant_gbs / hbm_peak,
                          "ms": dict(zip(labels[:nq], q_ms)),
                          "gbs_each": {lab: b / (m / 1e3) / 1e9 for lab, b, m in zip(labels[:nq], qwork, q_ms)},
-                         "bytes_model": "bf16 read + per orientation 0.5 B codes + 1/32 B scales per element"},
+                         "bytes_model": "bf16 read + per orientation 0.5 B codes + "
+                                        + ("1/16" if spec.nvfp4 else "1/32") + " B scales per element"},
             "share_of_step": share,
             "peaks": {"fp4_tflops": fp4_peak, "hbm_gbs": hbm_peak, "source": peak_src},
         },
@@ -706,7 +767,7 @@ def main():
     }
     if not args.no_e2e:
         line["e2e"] = measure_e2e(st, max(1, min(args.steps, 5)), ws)
-    if len(spec.gemms) == 3 and not args.no_e2e:
+    if len(spec.gemms) == 3 and not spec.nvfp4 and not args.no_e2e:
         line["autograd_linear"] = measure_linear(spec, st, max(1, min(args.steps, 5)))
     if not args.no_cpu_baseline and rank == 0 and ws == 1:
         dt, flops, qb, threads, sdesc = cpu_oracle_sample(spec)

@@ -10,13 +10,17 @@ Calls (same names as the C ABI):
   mxfp4_quantize    fused rotation + E8M0 scale + E2M1 rounding + packing,
                     row-wise and/or column-wise in one pass
   mxfp4_dequantize  codes * 2^(scale - 127) -> fp32
-  mxfp4_gemm        block-scaled MXFP4 GEMM on tcgen05 tensor cores
+  mxfp4_gemm        block-scaled MXFP4 GEMM on tcgen05 tensor cores (fp32 or
+                    bf16 C); mxfp4_gemm_quantize with the quantizer in its
+                    epilogue; mxfp8_gemm (E4M3) and nvfp4_gemm (1x16 blocks,
+                    E4M3 scales)
   hadamard32        stand-alone 32-point block rotation
 """
 from .binding import (  # noqa: F401
     BLOCK_1X32,
     BLOCK_32X32,
     BLOCK_64X64,
+    BLOCK_1X16,
     DTYPE_BF16,
     DTYPE_F32,
     FORMAT_E2M1,
@@ -38,6 +42,8 @@ from .binding import (  # noqa: F401
     mxfp4_gemm,
     mxfp4_gemm_quantize,
     mxfp8_gemm,
+    nvfp4_gemm,
+    nvfp4_tensor_exp,
     mxfp4_quantize,
     scale_numel,
 )

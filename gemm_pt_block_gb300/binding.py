@@ -15,7 +15,7 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libmxfp4.so"
 
-BLOCK_1X32, BLOCK_32X32, BLOCK_64X64 = 0, 1, 2
+BLOCK_1X32, BLOCK_32X32, BLOCK_64X64, BLOCK_1X16 = 0, 1, 2, 3
 FORMAT_E2M1, FORMAT_E4M3 = 0, 1
 SCALE_FLOOR, SCALE_ROUNDUP = 0, 1
 ROUND_RTN, ROUND_SR = 0, 1
@@ -45,6 +45,7 @@ class _CParams(ctypes.Structure):
         ("seed", ctypes.c_uint64),
         ("sr_stream", ctypes.c_uint32),
         ("elem_format", ctypes.c_uint32),
+        ("tensor_exp", ctypes.c_int32),
     ]
 
 
@@ -60,16 +61,38 @@ class QuantParams:
     seed: int = 0
     sr_stream: int = 0
     elem_format: int = 0          # FORMAT_E2M1 (MXFP4) or FORMAT_E4M3 (MXFP8)
+    tensor_exp: int = 0           # BLOCK_1X16 (NVFP4): per-tensor factor 2^tensor_exp
 
     def _c(self) -> _CParams:
         return _CParams(self.block, self.scale_mode, self.rounding, self.scale_layout,
                         int(bool(self.wht)), self.wht_sign_mask & 0xFFFFFFFF,
                         self.seed & 0xFFFFFFFFFFFFFFFF, self.sr_stream & 0xFFFFFFFF,
-                        self.elem_format)
+                        self.elem_format, self.tensor_exp)
 
     def code_cols(self, k: int) -> int:
         """Bytes of codes per output row for K elements."""
         return k if self.elem_format == FORMAT_E4M3 else k // 2
+
+    def scale_cols(self, k: int) -> int:
+        """Scale bytes per output row for K elements (one per block along K)."""
+        return k // 16 if self.block == BLOCK_1X16 else k // 32
+
+
+def nvfp4_tensor_exp(amax: float) -> int:
+    """Per-tensor exponent k = ceil(log2(amax / 2688)) for NVFP4: the smallest k
+    whose largest block scale, amax / (6 * 2^k), fits E4M3's 448."""
+    import math
+
+    if not math.isfinite(amax):
+        raise ValueError("nvfp4_tensor_exp: the tensor's max-abs must be finite")
+    if not amax > 0:
+        return 0
+    k = math.ceil(math.log2(amax / 2688.0))
+    while amax > 2688.0 * 2.0 ** k:
+        k += 1
+    while k > -100 and amax <= 2688.0 * 2.0 ** (k - 1):
+        k -= 1
+    return max(-100, min(100, k))
 
 
 _lib = None
@@ -98,6 +121,8 @@ def lib() -> ctypes.CDLL:
         L.mxfp4_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
         L.mxfp4_gemm_ex.restype = i32
         L.mxfp4_gemm_ex.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P]
+        L.nvfp4_gemm.restype = i32
+        L.nvfp4_gemm.argtypes = [P, P, i32, P, P, i32, i64, i64, i64, P, i32, i64, P]
         L.mxfp8_gemm.restype = i32
         L.mxfp8_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P]
         L.mxfp4_gemm_quantize.restype = i32
@@ -138,14 +163,14 @@ def _cuda2d(x: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must be 2-D with unit column stride")
 
 
-def scale_numel(rows: int, k: int) -> int:
-    return rows * (k // 32)
+def scale_numel(rows: int, k: int, block: int = BLOCK_1X32) -> int:
+    return rows * (k // 16 if block == BLOCK_1X16 else k // 32)
 
 
 def _scales_out(rows: int, k: int, p: QuantParams, dev) -> torch.Tensor:
     if p.scale_layout == LAYOUT_MMA:
-        return torch.empty(scale_numel(rows, k), dtype=torch.uint8, device=dev)
-    return torch.empty((rows, k // 32), dtype=torch.uint8, device=dev)
+        return torch.empty(scale_numel(rows, k, p.block), dtype=torch.uint8, device=dev)
+    return torch.empty((rows, p.scale_cols(k)), dtype=torch.uint8, device=dev)
 
 
 def mxfp4_quantize(x: torch.Tensor, row: QuantParams | None = None, col: QuantParams | None = None,
@@ -154,8 +179,8 @@ def mxfp4_quantize(x: torch.Tensor, row: QuantParams | None = None, col: QuantPa
 
     Returns (q_row, s_row, q_col, s_col); entries for an orientation not asked
     for are None. Codes are [rows, cols/2] (row-wise) / [cols, rows/2]
-    (column-wise) uint8; scales are [out_rows, K/32] (row-major layout) or flat
-    (tensor-core layout).
+    (column-wise) uint8; scales are [out_rows, K/32] (K/16 for NVFP4's 1x16
+    blocks; row-major layout) or flat (tensor-core layout).
     """
     _cuda2d(x, "x")
     if x.dtype == torch.bfloat16:
@@ -241,6 +266,21 @@ def mxfp8_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.T
     ldc = c.stride(0) if ldc is None else ldc
     _check(lib().mxfp8_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), cdt, ldc,
                             _stream(qa, stream)))
+    return c
+
+
+def nvfp4_gemm(qa: torch.Tensor, sa: torch.Tensor, ka: int, qb: torch.Tensor, sb: torch.Tensor,
+               kb: int, M: int, N: int, K: int, *, c=None, ldc: int | None = None,
+               out_dtype: torch.dtype = torch.float32, stream=None):
+    """C[M, N] = 2^(ka + kb) deq(A) deq(B)^T for NVFP4 operands: E2M1 codes [M, K/2] /
+    [N, K/2], E4M3 scales per 16 in tensor-core layout, ka / kb their tensor_exp."""
+    _check_operands(qa, sa, qb, sb)
+    cdt = _c_dtype(c, out_dtype)
+    if c is None:
+        c = torch.empty((M, N), dtype=out_dtype, device=qa.device)
+    ldc = c.stride(0) if ldc is None else ldc
+    _check(lib().nvfp4_gemm(_ptr(qa), _ptr(sa), ka, _ptr(qb), _ptr(sb), kb, M, N, K, _ptr(c), cdt,
+                            ldc, _stream(qa, stream)))
     return c
 
 

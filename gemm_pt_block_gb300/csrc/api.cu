@@ -3,6 +3,7 @@
 // work itself is enqueued by the launchers in quant.cu and gemm.cu.
 #include <cstdarg>
 #include <cstdint>
+#include <cmath>
 #include <cstdio>
 
 #include "../../include/mxfp4.h"
@@ -34,8 +35,15 @@ mxfp4_status check_params(const mxfp4_quant_params* p, uint8_t* q, uint8_t* s, i
     return fail(MXFP4_ERR_INVALID_ARG, "%s: output pointers must be non-NULL", name);
   if (!aligned16(q)) return fail(MXFP4_ERR_ALIGN, "%s: codes pointer not 16-byte aligned", name);
   if (p->block != MXFP4_BLOCK_1X32 && p->block != MXFP4_BLOCK_32X32 &&
-      p->block != MXFP4_BLOCK_64X64)
+      p->block != MXFP4_BLOCK_64X64 && p->block != MXFP4_BLOCK_1X16)
     return fail(MXFP4_ERR_INVALID_ARG, "%s: bad block %d", name, p->block);
+  const bool nv = p->block == MXFP4_BLOCK_1X16;
+  if (nv && (p->tensor_exp < -100 || p->tensor_exp > 100))
+    return fail(MXFP4_ERR_INVALID_ARG, "%s: tensor_exp %d outside [-100, 100]", name, p->tensor_exp);
+  if (!nv && p->tensor_exp != 0)
+    return fail(MXFP4_ERR_INVALID_ARG, "%s: tensor_exp is for 1x16 (NVFP4) blocks only", name);
+  if (nv && p->elem_format != MXFP4_FORMAT_E2M1)
+    return fail(MXFP4_ERR_UNSUPPORTED, "%s: 1x16 blocks take E2M1 elements", name);
   if (p->block == MXFP4_BLOCK_64X64 && (out_rows % 64 != 0 || k % 64 != 0))
     return fail(MXFP4_ERR_SHAPE, "%s: 64x64 blocks need rows %% 64 == 0 and K %% 64 == 0 (got %lld x %lld)",
                 name, (long long)out_rows, (long long)k);
@@ -54,7 +62,10 @@ mxfp4_status check_params(const mxfp4_quant_params* p, uint8_t* q, uint8_t* s, i
     return fail(MXFP4_ERR_SHAPE,
                 "%s: tensor-core scale layout needs rows %% 128 == 0 and K %% 128 == 0 (got %lld x %lld)",
                 name, (long long)out_rows, (long long)k);
-  o->block = p->block;
+  o->block = nv ? 0 : p->block;
+  o->nv = nv;
+  o->nv_p2k = nv ? ldexpf(1.0f, p->tensor_exp) : 1.0f;
+  o->nv_zmul = nv ? (float)(ldexp(1.0, -p->tensor_exp) / 6.0) : 1.0f;
   o->roundup = p->scale_mode == MXFP4_SCALE_ROUNDUP;
   o->sr = p->rounding == MXFP4_ROUND_SR;
   o->mma_layout = p->scale_layout == MXFP4_LAYOUT_MMA;
@@ -109,7 +120,8 @@ mxfp4_status mxfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int64_
   if (st) return st;
   if (rows > 0 && cols / 16 > (int64_t)0xFFFFFFFF / rows)
     return fail(MXFP4_ERR_SHAPE, "tensor too large: rows * cols / 16 must be below 2^32");
-  const bool need_rows32 = col || (row && row->block != MXFP4_BLOCK_1X32);
+  const bool need_rows32 =
+      col || (row && row->block != MXFP4_BLOCK_1X32 && row->block != MXFP4_BLOCK_1X16);
   if (need_rows32 && rows % 32 != 0)
     return fail(MXFP4_ERR_SHAPE, "rows (%lld) must be a multiple of 32 for column-wise or 32x32 output",
                 (long long)rows);
@@ -199,6 +211,31 @@ mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   return from_cuda(e, "mxfp8_gemm");
 }
 
+mxfp4_status nvfp4_gemm(const uint8_t* qa, const uint8_t* sa, int32_t ka, const uint8_t* qb,
+                        const uint8_t* sb, int32_t kb, int64_t M, int64_t N, int64_t K, void* c,
+                        int32_t c_dtype, int64_t ldc, void* stream) {
+  if (!qa || !sa || !qb || !sb || !c) return fail(MXFP4_ERR_INVALID_ARG, "nvfp4_gemm: NULL pointer");
+  if (c_dtype != MXFP4_DTYPE_BF16 && c_dtype != MXFP4_DTYPE_F32)
+    return fail(MXFP4_ERR_INVALID_ARG, "nvfp4_gemm: bad c_dtype %d", c_dtype);
+  if (ka < -100 || ka > 100 || kb < -100 || kb > 100 || ka + kb < -126 || ka + kb > 126)
+    return fail(MXFP4_ERR_INVALID_ARG, "nvfp4_gemm: tensor exponents %d, %d out of range", ka, kb);
+  if (M <= 0 || N <= 0 || K <= 0 || M % 256 != 0 || N % 256 != 0 || K % 256 != 0)
+    return fail(MXFP4_ERR_SHAPE, "nvfp4_gemm needs M %% 256 == 0, N %% 256 == 0, K %% 256 == 0 (got %lld, %lld, %lld)",
+                (long long)M, (long long)N, (long long)K);
+  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30))
+    return fail(MXFP4_ERR_SHAPE, "nvfp4_gemm dimensions too large");
+  if (ldc < N) return fail(MXFP4_ERR_SHAPE, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
+  if (!aligned16(qa) || !aligned16(qb) || !aligned16(sa) || !aligned16(sb) || !aligned16(c) || ldc % 8 != 0)
+    return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");
+  const char* why = "";
+  cudaError_t e = mx::launch_gemm_nv(qa, sa, qb, sb, M, N, K, ldexpf(1.0f, ka + kb), c,
+                                     c_dtype == MXFP4_DTYPE_BF16, ldc,
+                                     static_cast<cudaStream_t>(stream), &why);
+  if (e == cudaErrorNotSupported) return fail(MXFP4_ERR_UNSUPPORTED, "%s", why);
+  if (e == cudaErrorInvalidValue && why[0]) return fail(MXFP4_ERR_ALIGN, "%s", why);
+  return from_cuda(e, "nvfp4_gemm");
+}
+
 mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                                  const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                                  int32_t c_dtype, int64_t ldc, const mxfp4_quant_params* out,
@@ -207,6 +244,9 @@ mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uin
   if (out->block == MXFP4_BLOCK_64X64)
     return fail(MXFP4_ERR_UNSUPPORTED,
                 "mxfp4_gemm_quantize: 64x64 blocks span two epilogue warps; quantize C separately");
+  if (out->block == MXFP4_BLOCK_1X16)
+    return fail(MXFP4_ERR_UNSUPPORTED,
+                "mxfp4_gemm_quantize: 1x16 (NVFP4) output is not fused; quantize C separately");
   mx::OrientArgs qo{};
   if (M > 0 && N > 0) {
     mxfp4_status st = check_params(out, q_out, s_out, M, N, "out", &qo);

@@ -371,6 +371,20 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + CTL_BYTES + 1024;
 static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
 using Ctl = CtlT<STAGES>;
 static_assert(sizeof(Ctl) <= CTL_BYTES, "control block");
+// NVFP4 stages: the same codes plus four scale tiles of A and eight of B.
+constexpr int NV_STAGES = 5;
+constexpr int NV_STAGE_BYTES = A_BYTES + B_BYTES + 4 * 512 + 8 * 512;   // 38 KB
+constexpr int NV_SMEM_BYTES = NV_STAGES * NV_STAGE_BYTES + CTL_BYTES + 1024;
+constexpr uint32_t SFB_COL_NV = SFA_COL + 16;   // A: 4 tiles x 4 columns, B: 4 x 8
+static_assert(NV_STAGE_BYTES % 1024 == 0 && NV_STAGES <= STAGES, "NVFP4 ring");
+static_assert(SFB_COL_NV + 32 <= TMEM_COLS, "NVFP4 scale columns");
+enum : int { kMxf4 = 0, kMxf8 = 1, kNvf4 = 2 };
+
+// kind::mxf4nvf4 with E2M1 A and B (type code 1), K-major, UE4M3 scales (bit
+// 23 clear), scale_vec::4X (both scale-factor selectors 0).
+__device__ __forceinline__ uint32_t make_idesc_nv() {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
 
 // kF8: kind::mxf8f6f4 with E4M3 operands (type code 0) instead of kind::mxf4's
 // E2M1 (type code 1).
@@ -381,29 +395,44 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
          ((uint32_t)(256 >> 4) << 24) | (sf_id << 29);
 }
 
-// kF8: MXFP8 operands: codes one byte per element, so a 128-byte stage row is
-// 128 elements of K (4 MMAs of K = 32), with one 512-byte scale tile of A and
-// one per 128-row band of B per stage.
-template <bool kQ, bool kF8 = false>
+// kKind selects the operand format:
+//  kMxf4: E2M1 codes with E8M0 scales per 32 (kind::mxf4, scale_vec::2X): a
+//    stage row is 256 elements of K, two 512-byte scale tiles of A and two per
+//    128-row band of B; MMA k reads bytes 2 (k % 2) .. of each row's word;
+//  kMxf8: E4M3 codes, one byte per element, so a 128-byte stage row is 128
+//    elements of K (4 MMAs of K = 32), with one 512-byte scale tile of A and
+//    one per 128-row band of B per stage; MMA k reads byte k of the word;
+//  kNvf4: E2M1 codes with E4M3 scales per 16 (kind::mxf4nvf4, scale_vec::4X):
+//    each 512-byte scale tile covers one MMA's K = 64, so a stage brings four
+//    tiles of A and four per band of B (twelve scale copies), and each MMA
+//    reads a whole word; the fp32 sums are multiplied by alpha (the operands'
+//    power-of-two tensor factors) in the epilogue. Five stages of 38 KB.
+template <bool kQ, int kKind = kMxf4>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                       void* __restrict__ C, int c_bf16, int64_t ldc, int M, int N, int K, int group_m,
-                      const __grid_constant__ OrientArgs qo) {
+                      float alpha, const __grid_constant__ OrientArgs qo) {
+  constexpr bool kF8 = kKind == kMxf8, kNv = kKind == kNvf4;
+  constexpr int kStages = kNv ? NV_STAGES : STAGES;
+  constexpr int kStageBytes = kNv ? NV_STAGE_BYTES : STAGE_BYTES;
+  constexpr int kSfaBytes = kNv ? 4 * 512 : SFA_BYTES;
+  constexpr uint32_t kSfbCol = kNv ? SFB_COL_NV : SFB_COL;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
   const bool leader = rank == 0;
   const int num_m = M / (2 * BM), num_n = N / BNP, num_k = K / (kF8 ? BK / 2 : BK);
   const int num_tiles = num_m * num_n;
   const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
-  constexpr uint32_t kTx = kF8 ? 2u * (A_BYTES + B_BYTES + 512 + 1024) : TX_BYTES;
+  constexpr uint32_t kTx = kF8 ? 2u * (A_BYTES + B_BYTES + 512 + 1024)
+                               : (kNv ? 2u * kStageBytes : TX_BYTES);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(ptx::smem_u32(&ctl->full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&ctl->empty[s]), 1);
     }
@@ -444,15 +473,15 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
           const uint32_t full_local = ptx::smem_u32(&ctl->full[stage]);
           const uint32_t full_leader = ptx::mapa(full_local, 0);
           if (leader) ptx::mbar_arrive_expect_tx(full_local, kTx);
-          const uint32_t st = ptx::smem_u32(smem + stage * STAGE_BYTES);
-          const int kt = kF8 ? kb : 2 * kb;   // first 128-wide scale tile of the stage
+          const uint32_t st = ptx::smem_u32(smem + stage * kStageBytes);
+          const int kt = kF8 ? kb : (kNv ? 4 * kb : 2 * kb);   // first scale tile of the stage
           ptx::tma_load_2d_pair(st, &tmA, kb * BKB, a_row, full_leader);
           ptx::tma_load_2d_pair(st + A_BYTES, &tmB, kb * BKB, b_row, full_leader);
           ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES, &tmSA, 0, kt, a_row / 128, full_leader);
-          ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES + SFA_BYTES, &tmSB, 0, kt, nb * 2,
+          ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES + kSfaBytes, &tmSB, 0, kt, nb * 2,
                                 full_leader);
           ++issued_rounds;
-          if (++stage == STAGES) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -460,8 +489,8 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       }
       // Wait until the leader's commits have released every stage this CTA
       // filled, so no remote arrive targets this CTA after it exits.
-      for (int s = 0; s < STAGES; ++s) {
-        const uint32_t n = issued_rounds / STAGES + ((uint32_t)s < issued_rounds % STAGES ? 1u : 0u);
+      for (int s = 0; s < kStages; ++s) {
+        const uint32_t n = issued_rounds / kStages + ((uint32_t)s < issued_rounds % kStages ? 1u : 0u);
         if (n) drain_wait(ptx::smem_u32(&ctl->empty[s]), (n - 1) & 1u);
       }
     }
@@ -476,10 +505,29 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         for (int kb = 0; kb < num_k; ++kb) {
           if (!(ok = wait_bar(ptx::smem_u32(&ctl->full[stage]), phase, ctl))) break;
           ptx::tc_fence_after();
-          const uint32_t st = ptx::smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t st = ptx::smem_u32(smem + stage * kStageBytes);
           const uint32_t sfa_s = st + A_BYTES + B_BYTES;
-          const uint32_t sfb_s = sfa_s + SFA_BYTES;
-          if constexpr (kF8) {
+          const uint32_t sfb_s = sfa_s + kSfaBytes;
+          if constexpr (kNv) {
+            // Four K tiles, one per MMA: A's tile k to SFA_COL + 4 k, B's band t
+            // of tile k to kSfbCol + 8 k + 4 t; each MMA reads whole words.
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              ptx::tc_cp_pair_32x128b_warpx4(tmem + SFA_COL + 4 * k,
+                                             ptx::smem_desc(sfa_s + k * 512, 0, 128, 0));
+#pragma unroll
+              for (int t = 0; t < 2; ++t)
+                ptx::tc_cp_pair_32x128b_warpx4(tmem + kSfbCol + 8 * k + 4 * t,
+                                               ptx::smem_desc(sfb_s + t * 2048 + k * 512, 0, 128, 0));
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
+              const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
+              ptx::mma_nvf4_pair(tmem + ACC_COL, ad, bd, make_idesc_nv(), tmem + SFA_COL + 4 * k,
+                                 tmem + kSfbCol + 8 * k, (kb | k) != 0);
+            }
+          } else if constexpr (kF8) {
             // One K tile: A's tile to SFA_COL, B's bands to SFB_COL + 4 t; MMA k
             // reads byte k of each row's word.
             ptx::tc_cp_pair_32x128b_warpx4(tmem + SFA_COL, ptx::smem_desc(sfa_s, 0, 128, 0));
@@ -514,7 +562,7 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             }
           }
           ptx::tc_commit_pair_multicast(ptx::smem_u32(&ctl->empty[stage]), 0x3);
-          if (++stage == STAGES) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -549,6 +597,13 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       if (lane == 0) ptx::mbar_arrive_cluster(acc_empty_leader);
       acc_phase ^= 1u;
       const int64_t row = (int64_t)mb * 2 * BM + rank * BM + q * 32 + lane;
+      if constexpr (kNv) {   // exact: alpha is a power of two
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          r0[i] = __float_as_uint(__fmul_rn(__uint_as_float(r0[i]), alpha));
+          r1[i] = __float_as_uint(__fmul_rn(__uint_as_float(r1[i]), alpha));
+        }
+      }
       epilogue_out<kQ>(r0, r1, C, c_bf16, ldc, row, (int64_t)nb * BNP + h * 128, N, qo);
     }
   }
@@ -579,12 +634,13 @@ bool make_code_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t kb
 }
 
 // Scale array in the tensor-core layout as a 3-D tensor of 32-bit words:
-// [rows/128 bands][K/128 tiles][128 words (512 bytes)]; a box covers 2 tiles
-// (one 256-deep K stage) of `bands` consecutive bands.
+// [rows/128 bands][K/tile_k tiles][128 words (512 bytes)] (a tile covers 128
+// elements of K with a scale per 32, 64 with a scale per 16); a box covers
+// `ktiles` tiles (one K stage) of `bands` consecutive bands.
 bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t K, uint32_t bands,
-                    uint32_t ktiles = 2) {
-  const cuuint64_t dims[3] = {128, (cuuint64_t)(K / 128), (cuuint64_t)(rows / 128)};
-  const cuuint64_t strides[2] = {512, (cuuint64_t)(K / 128) * 512};
+                    uint32_t ktiles = 2, int64_t tile_k = 128) {
+  const cuuint64_t dims[3] = {128, (cuuint64_t)(K / tile_k), (cuuint64_t)(rows / 128)};
+  const cuuint64_t strides[2] = {512, (cuuint64_t)(K / tile_k) * 512};
   const cuuint32_t box[3] = {128, ktiles, bands};
   const cuuint32_t es[3] = {1, 1, 1};
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(base), dims, strides,
@@ -616,8 +672,10 @@ DevInfo& dev_info(int dev) {
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
       cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
-      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<false, true>,
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<false, pair::kMxf8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<false, pair::kNvf4>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, pair::NV_SMEM_BYTES);
     }
     d.attr_set = true;
   }
@@ -662,10 +720,10 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
     (void)cudaGetLastError();  // drop a stale error left by an earlier call
     if (qout)
       pair::mxf4_gemm_pair_kernel<true><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
-          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, qo);
+          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, qo);
     else
       pair::mxf4_gemm_pair_kernel<false><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
-          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, qo);
+          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, qo);
     return cudaGetLastError();
   }
   if (!make_code_map(&ta, qa, M, K / 2, BM) || !make_code_map(&tb, qb, N, K / 2, BN)) {
@@ -736,8 +794,42 @@ cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
   gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
   const OrientArgs none{};
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
-  pair::mxf4_gemm_pair_kernel<false, true><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
-      ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, none);
+  pair::mxf4_gemm_pair_kernel<false, pair::kMxf8><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
+      ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, none);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_nv(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, float alpha,
+                           void* c, bool c_bf16, int64_t ldc, cudaStream_t st, const char** why) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  DevInfo& d = dev_info(dev);
+  if (d.major != 10) {
+    *why = "tcgen05 block-scaled MMA needs an sm_100-family (GB300 sm_103) device";
+    return cudaErrorNotSupported;
+  }
+  if (!encode_fn()) {
+    *why = "driver entry point cuTensorMapEncodeTiled not available";
+    return cudaErrorNotSupported;
+  }
+  ensure_context();
+  CUtensorMap ta, tb, tsa, tsb;
+  if (!make_code_map(&ta, qa, M, K / 2, pair::BM) || !make_code_map(&tb, qb, N, K / 2, pair::BNH) ||
+      !make_scale_map(&tsa, sa, M, K, 1, 4, 64) || !make_scale_map(&tsb, sb, N, K, 2, 4, 64)) {
+    *why = "cuTensorMapEncodeTiled rejected the operand layout";
+    return cudaErrorInvalidValue;
+  }
+  const int num_tiles = (int)((M / 256) * (N / pair::BNP));
+  const int pairs = d.sms / 2;
+  const int grid = 2 * (num_tiles < pairs ? num_tiles : pairs);
+  int64_t gm = kGroupBytes / (256 * (K / 2));
+  gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
+  const OrientArgs none{};
+  (void)cudaGetLastError();  // drop a stale error left by an earlier call
+  pair::mxf4_gemm_pair_kernel<false, pair::kNvf4><<<grid, THREADS, pair::NV_SMEM_BYTES, st>>>(
+      ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, alpha, none);
   return cudaGetLastError();
 }
 

@@ -10,12 +10,15 @@ namespace mx {
 // One output orientation of the quantizer, already validated. The Philox round
 // keys and per-lane sign words are precomputed on the host (see api.cu).
 struct OrientArgs {
-  int32_t block;        // 0: 1x32, 1: 32x32
+  int32_t block;        // 0: 1-D (1x32, or 1x16 with nv), 1: 32x32, 2: 64x64
   int32_t roundup;      // scale mode: 0 floor, 1 round-up
   int32_t sr;           // 0: nearest-even, 1: stochastic
   int32_t mma_layout;   // scale array layout: 0 row-major, 1 tensor-core tiles
   int32_t wht;          // rotate 32-runs along the quantization axis first
   int32_t e4m3;         // element format: 0 E2M1 (MXFP4), 1 E4M3 (MXFP8)
+  int32_t nv;           // 1x16 blocks with E4M3 scales (NVFP4); block is then 0
+  float nv_p2k;         // NVFP4: 2^tensor_exp
+  float nv_zmul;        // NVFP4: 2^-tensor_exp / 6 rounded to fp32 (first guess only)
   uint32_t sign_mask;
   uint64_t seed;
   uint32_t stream;
@@ -52,6 +55,12 @@ cudaError_t read_device_error(cudaStream_t st, uint32_t* err);
 cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                            const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                            bool c_bf16, int64_t ldc, cudaStream_t st, const char** why);
+// NVFP4 GEMM (E2M1 codes [M, K/2], [N, K/2]; E4M3 scales per 16 in the
+// tensor-core layout with K/16 scale columns): C = alpha * sum, alpha a power
+// of two; CTA pairs, M % 256 == 0, N % 256 == 0, K % 256 == 0.
+cudaError_t launch_gemm_nv(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, float alpha,
+                           void* c, bool c_bf16, int64_t ldc, cudaStream_t st, const char** why);
 // One-thread kernel whose bounded wait never completes (sets the error word).
 cudaError_t launch_wait_probe(cudaStream_t st);
 

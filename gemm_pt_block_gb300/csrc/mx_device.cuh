@@ -307,6 +307,61 @@ __device__ __forceinline__ uint4 encode16_e4m3(const float2* V) {
                     e4m3x4(V[4].x, V[4].y, V[5].x, V[5].y), e4m3x4(V[6].x, V[6].y, V[7].x, V[7].y));
 }
 
+// ------------------------------------------------------ NVFP4 scales ---
+// Non-negative E4M3 code c (0 .. 126) -> value, exact: (8 + m) 2^(E - 10) for
+// exponent field E > 0, m 2^-9 for E = 0.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t E = c >> 3, m = c & 7u;
+  return E ? __uint_as_float(((E + 120u) << 23) | (m << 20)) : __fmul_rn((float)m, 0.001953125f);
+}
+
+struct NvScale {
+  uint32_t code;  // E4M3 code of S
+  float rcp;      // fp32 nearest 1 / (S 2^k), 0 when S = 0
+};
+
+// Scale of one 1x16 block with max-abs M under the per-tensor factor 2^k
+// (p2k = 2^k; zmul = 2^-k / 6 rounded to fp32). A first guess, the nearest
+// E4M3 value to M * zmul (hardware conversion), is within one code of the
+// answer; it is then fixed by exact comparisons of M with thresholds that are
+// exact in fp32: 6 S 2^k (round-up: the smallest S with 6 S 2^k >= M) or the
+// midpoints 3 (S_c + S_c+1) 2^k (nearest, ties to the even code; M >= 2688
+// 2^k saturates at 448).
+__device__ __forceinline__ NvScale nv_scale(float M, bool roundup, float p2k, float zmul) {
+  const float z = __fmul_rn(M, zmul);
+  uint32_t c;
+  asm("{.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %1;\n\tcvt.u32.u16 %0, t;}"
+      : "=r"(c) : "f"(z));
+  c &= 0x7Fu;
+  if (roundup) {
+    if (c < 126u && __fmul_rn(__fmul_rn(6.0f, e4m3_value(c)), p2k) < M)
+      ++c;
+    else if (c > 0u && __fmul_rn(__fmul_rn(6.0f, e4m3_value(c - 1u)), p2k) >= M)
+      --c;
+  } else if (M >= __fmul_rn(2688.0f, p2k)) {
+    c = 126u;
+  } else {
+    if (c < 126u) {
+      const float t = __fmul_rn(__fmul_rn(3.0f, __fadd_rn(e4m3_value(c), e4m3_value(c + 1u))), p2k);
+      if (M > t || (M == t && (c & 1u))) ++c;          // a tie goes to the even code c + 1
+    }
+    if (c > 0u) {
+      const float t = __fmul_rn(__fmul_rn(3.0f, __fadd_rn(e4m3_value(c - 1u), e4m3_value(c))), p2k);
+      if (M < t || (M == t && (c & 1u))) --c;          // a tie goes to the even code c - 1
+    }
+  }
+  const float S = __fmul_rn(e4m3_value(c), p2k);
+  return NvScale{c, c ? __frcp_rn(S) : 0.0f};
+}
+
+// Max-abs of the 16 values one lane holds.
+__device__ __forceinline__ float absmax16(const float2* R) {
+  float m = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m = max3(m, fabsf(R[k].x), fabsf(R[k].y));
+  return m;
+}
+
 __device__ __forceinline__ uint4 encode32(const float2 (&V)[16]) {
   return make_uint4(e2m1x8(V[0].x, V[0].y, V[1].x, V[1].y, V[2].x, V[2].y, V[3].x, V[3].y),
                     e2m1x8(V[4].x, V[4].y, V[5].x, V[5].y, V[6].x, V[6].y, V[7].x, V[7].y),

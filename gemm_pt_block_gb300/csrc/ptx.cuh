@@ -183,6 +183,20 @@ __device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t adesc, u
       : "memory");
 }
 
+// NVFP4 operands (E2M1 x E2M1, one UE4M3 scale per 16 elements of K; K = 64 per
+// instruction, four scales per row in one tensor-memory word), for a CTA pair.
+__device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 // Arrive on the mbarrier at the same offset in every CTA of `mask` once all
 // prior tcgen05 async operations of this thread finish.
 __device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar, uint16_t mask) {

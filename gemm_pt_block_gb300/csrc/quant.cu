@@ -124,6 +124,17 @@ __device__ __forceinline__ uint2 quantize_halves(float2 (&R)[8], int upper, cons
     if (!is_bf16<InT>() && o.sm_half[upper]) apply_signs(R, o.sm_half[upper]);
     hadamard_halves(R, upper);
   }
+  if (o.nv) {   // NVFP4: the lane's 16 elements are one block with an E4M3 scale
+    const NvScale sc = nv_scale(absmax16(R), o.roundup, o.nv_p2k, o.nv_zmul);
+    scale_all(R, sc.rcp);
+    if (o.sr) {
+      uint32_t w[8];
+      draws16(o.keys, o.stream, i0, w);
+      sr16(R, w);
+    }
+    *e_out = (int)sc.code;
+    return encode16(R);
+  }
   const float M = reduce(pair_absmax(R));
   const int e = scale_exponent(M, o.roundup, o.e4m3);
   scale_all(R, inv_scale(e));
@@ -173,7 +184,10 @@ quant_rows_1x32_kernel(const InT* __restrict__ x, uint32_t total, FastDiv halves
         *reinterpret_cast<uint4*>(o.q + (int64_t)r * cols + c0) = encode16_e4m3(R);
       else
         *reinterpret_cast<uint2*>(o.q + (int64_t)r * (cols >> 1) + (c0 >> 1)) = packed;
-      if (!upper) store_scale(o, r, c0 >> 5, cols >> 5, e);
+      if (o.nv)
+        o.s[scale_offset(o, r, c0 >> 4, cols >> 4)] = (uint8_t)e;
+      else if (!upper)
+        store_scale(o, r, c0 >> 5, cols >> 5, e);
     }
   }
 }
@@ -466,7 +480,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           const int e = scale_run32(R, orow, M, w);
           if (valid) {
             store_run32(orow, r, c, cols, R);
-            store_scale(orow, r, c >> 5, cols >> 5, e);
+            store_run_scales(orow, r, c, cols, e);
           }
         }
       }
@@ -503,7 +517,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           const int e = scale_run32(R, ocol, M, w);
           if (valid) {
             store_run32(ocol, oc, k0, rows, R);
-            store_scale(ocol, oc, k0 >> 5, rows >> 5, e);
+            store_run_scales(ocol, oc, k0, rows, e);
           }
         }
       }
@@ -622,9 +636,10 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
   }
   OrientArgs dummy{};
   const int64_t tx = (cols + kTile - 1) / kTile, ty = (rows + kTile - 1) / kTile;
-  // The general variant handles 64x64 blocks and E4M3 codes; the other one is
-  // the leaner E2M1 path for 1x32 / 32x32 blocks.
-  const bool sq64 = (row && (row->block == 2 || row->e4m3)) || (col && (col->block == 2 || col->e4m3));
+  // The general variant handles 64x64 blocks, E4M3 codes and NVFP4's 1x16
+  // blocks; the other one is the leaner E2M1 path for 1x32 / 32x32 blocks.
+  const bool sq64 = (row && (row->block == 2 || row->e4m3 || row->nv)) ||
+                    (col && (col->block == 2 || col->e4m3 || col->nv));
   auto kern = sq64 ? quant_tile_kernel<InT, true> : quant_tile_kernel<InT, false>;
   const unsigned grid = resident_ctas(quant_tile_kernel<InT, false>, tx * ty, smem, kTileThreads);
   (void)cudaGetLastError();  // drop a stale error left by an earlier call

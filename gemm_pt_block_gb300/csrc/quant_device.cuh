@@ -8,10 +8,27 @@
 
 namespace mx {
 
+__device__ __forceinline__ int64_t scale_offset(const OrientArgs& o, int64_t orow, int64_t kb,
+                                                int64_t nkb) {
+  return o.mma_layout ? mma_scale_offset(orow, kb, nkb) : orow * nkb + kb;
+}
+
+// E8M0 scale 2^e of block kb of output row orow (nkb blocks per row).
 __device__ __forceinline__ void store_scale(const OrientArgs& o, int64_t orow, int64_t kb,
                                             int64_t nkb, int e) {
-  const int64_t off = o.mma_layout ? mma_scale_offset(orow, kb, nkb) : orow * nkb + kb;
-  o.s[off] = (uint8_t)(e + 127);
+  o.s[scale_offset(o, orow, kb, nkb)] = (uint8_t)(e + 127);
+}
+
+// The scales of the 32-run at K positions k0 .. k0 + 31 of output row orow as
+// scale_run32 returns them: one E8M0 byte, or (NVFP4) the E4M3 codes of its
+// two 16-blocks, which are adjacent in both layouts (k0 / 16 is even).
+template <bool kNvfp4 = true>
+__device__ __forceinline__ void store_run_scales(const OrientArgs& o, int64_t orow, int64_t k0,
+                                                 int64_t K, int e) {
+  if (kNvfp4 && o.nv)
+    *reinterpret_cast<uint16_t*>(o.s + scale_offset(o, orow, k0 >> 4, K >> 4)) = (uint16_t)e;
+  else
+    store_scale(o, orow, k0 >> 5, K >> 5, e);
 }
 
 // Draw words for 32 consecutive source elements i0 .. i0 + 31 (i0 % 32 == 0).
@@ -26,11 +43,28 @@ __device__ __forceinline__ void draws32(const PhiloxKeys& k, uint32_t stream, ui
 }
 
 // Scale one 32-run whose max-abs is M, in place (and round it stochastically
-// when asked; nearest rounding happens in the conversion). Returns e.
-// kAnyFormat = false compiles the E2M1 case only.
-template <bool kAnyFormat = true>
+// when asked; nearest rounding happens in the conversion). Returns e, or for
+// NVFP4 (whose two 16-blocks take their own maxima and E4M3 scales) the two
+// scale codes, first block in the low byte. kAnyFormat = false compiles the
+// E2M1 / E8M0 case only; kNvfp4 = false leaves NVFP4 out.
+template <bool kAnyFormat = true, bool kNvfp4 = kAnyFormat>
 __device__ __forceinline__ int scale_run32(float2 (&R)[16], const OrientArgs& o, float M,
                                            const uint32_t (&w)[16]) {
+  if (kNvfp4 && o.nv) {
+    const NvScale a = nv_scale(absmax16(&R[0]), o.roundup, o.nv_p2k, o.nv_zmul);
+    const NvScale b = nv_scale(absmax16(&R[8]), o.roundup, o.nv_p2k, o.nv_zmul);
+    const float2 ra = make_float2(a.rcp, a.rcp), rb = make_float2(b.rcp, b.rcp);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      R[k] = f2mul(R[k], ra);
+      R[8 + k] = f2mul(R[8 + k], rb);
+    }
+    if (o.sr) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) R[k] = sr_pair(R[k], w[k]);
+    }
+    return (int)(a.code | (b.code << 8));
+  }
   const int e = scale_exponent(M, o.roundup, kAnyFormat && o.e4m3);
   const float2 is = make_float2(inv_scale(e), inv_scale(e));
 #pragma unroll
@@ -67,9 +101,9 @@ __device__ __forceinline__ void quantize_run32(float2 (&R)[16], int64_t row, int
   if (o.block) M = warp_max(M);
   uint32_t w[16];
   if (o.sr) draws32(o.keys, o.stream, (uint64_t)(row * cols + c0), w);
-  const int e = scale_run32(R, o, M, w);
+  const int e = scale_run32<true, false>(R, o, M, w);   // no NVFP4 output here
   store_run32(o, row, c0, cols, R);
-  store_scale(o, row, c0 >> 5, cols >> 5, e);
+  store_run_scales<false>(o, row, c0, cols, e);
 }
 
 }  // namespace mx

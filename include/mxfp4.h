@@ -54,7 +54,7 @@ typedef enum {
   MXFP4_ERR_TIMEOUT = 6      /* a bounded device-side wait ran out */
 } mxfp4_status;
 
-enum { MXFP4_BLOCK_1X32 = 0, MXFP4_BLOCK_32X32 = 1, MXFP4_BLOCK_64X64 = 2 };
+enum { MXFP4_BLOCK_1X32 = 0, MXFP4_BLOCK_32X32 = 1, MXFP4_BLOCK_64X64 = 2, MXFP4_BLOCK_1X16 = 3 };
 enum { MXFP4_SCALE_FLOOR = 0, MXFP4_SCALE_ROUNDUP = 1 };
 enum { MXFP4_ROUND_RTN = 0, MXFP4_ROUND_SR = 1 };
 enum { MXFP4_LAYOUT_ROWMAJOR = 0, MXFP4_LAYOUT_MMA = 1 };
@@ -75,12 +75,26 @@ enum { MXFP4_FORMAT_E2M1 = 0, MXFP4_FORMAT_E4M3 = 1 };
  *               written on each of its 64 rows for both of its 32-runs [TIBQ,
  *               "The evidence", Table 4 block sizes]; needs rows and K
  *               multiples of 64 (not available in mxfp4_gemm_quantize).
+ *               MXFP4_BLOCK_1X16: NVFP4 [TIBQ, "Why FP4 training is the
+ *               current frontier of precision reduction": 1 x 16 blocks]: 16
+ *               consecutive E2M1 elements share an E4M3 scale S (one byte,
+ *               OCP FP8 E4M3, codes 0..126) under the per-tensor factor
+ *               2^tensor_exp; the element value is code * S * 2^tensor_exp.
+ *               Scale arrays hold K/16 bytes per output row (both layouts;
+ *               the tensor-core layout with K/16 scale columns). Elements are
+ *               scaled by one fp32 reciprocal per block, r = RN(1 / (S *
+ *               2^tensor_exp)) (0 when S = 0), v = RN(y * r). E2M1 elements
+ *               only.
  *  scale_mode   MXFP4_SCALE_FLOOR: e = floor(log2 M) - 2 (OCP Microscaling
  *               v1.0; the block max may saturate at 6).
  *               MXFP4_SCALE_ROUNDUP: e = ceil(log2(M / 6)), nothing clips
  *               [TIBQ, "Truncation-free scaling"]. M is the block max-abs
  *               after the optional rotation; M == 0 gives e = -127; e is
  *               clamped to [-127, 127].
+ *               With MXFP4_BLOCK_1X16 (E4M3 scale): round-up is the smallest
+ *               S with 6 * S * 2^tensor_exp >= M (nothing clips); floor mode
+ *               reads as nearest: the S nearest to M / (6 * 2^tensor_exp),
+ *               ties to the even code; both saturate at S = 448.
  *  rounding     MXFP4_ROUND_RTN: nearest grid point, ties to the even code,
  *               saturating at 6. MXFP4_ROUND_SR: stochastic rounding [TIBQ,
  *               "Stochastic rounding in the backward pass"; Tseng, Abstract]:
@@ -98,6 +112,11 @@ enum { MXFP4_FORMAT_E2M1 = 0, MXFP4_FORMAT_E4M3 = 1 };
  *               c = fp32(1/sqrt(32)) applied last as one rounded multiply.
  *  wht_sign_mask bit i set => s_i = -1 (0 = the deterministic rotation).
  *  seed, sr_stream  Philox key and counter word 2 (used by MXFP4_ROUND_SR).
+ *  elem_format  MXFP4_FORMAT_E2M1 or MXFP4_FORMAT_E4M3.
+ *  tensor_exp   MXFP4_BLOCK_1X16 only (else it must be 0): the exponent k of
+ *               the per-tensor factor 2^k, in [-100, 100]. Choosing
+ *               k = ceil(log2(amax / 2688)) for the tensor's max-abs amax keeps
+ *               every block scale within E4M3's range.
  * All arithmetic is IEEE fp32 without fused multiply-add or flush-to-zero, so
  * results are bit-reproducible across calls and streams. */
 typedef struct {
@@ -110,6 +129,7 @@ typedef struct {
   uint64_t seed;
   uint32_t sr_stream;
   uint32_t elem_format; /* MXFP4_FORMAT_E2M1 (0) or MXFP4_FORMAT_E4M3 (1) */
+  int32_t tensor_exp;   /* MXFP4_BLOCK_1X16: per-tensor factor 2^tensor_exp */
 } mxfp4_quant_params;
 
 /* Fused MXFP4 quantizer ([News], paras. 1-2; [TIBQ] P_i = round(X_i / S)).
@@ -123,8 +143,10 @@ typedef struct {
  *         invariant under stochastic rounding too.
  *  At least one of row / col must be non-NULL.
  *  Shapes: cols % 32 == 0; rows % 32 == 0 when col != NULL or either
- *  orientation uses 32x32 blocks; MMA scale layout needs the output's row
- *  count % 128 == 0 and its K % 128 == 0. Else MXFP4_ERR_SHAPE.
+ *  orientation uses 32x32 or 64x64 blocks; MMA scale layout needs the
+ *  output's row count % 128 == 0 and its K % 128 == 0. Else MXFP4_ERR_SHAPE.
+ *  With MXFP4_BLOCK_1X16 the scale arrays are s_row [rows, cols/16] and
+ *  s_col [cols, rows/16].
  *  With elem_format MXFP4_FORMAT_E4M3 the codes take one byte per element
  *  (q_row [rows, cols], q_col [cols, rows]), the scale is chosen for the
  *  largest E4M3 value 448 (floor: floor(log2 M) - 8; round-up: the smallest
@@ -177,6 +199,19 @@ mxfp4_status mxfp4_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
  *  Shapes: M % 256 == 0, N % 256 == 0, K % 128 == 0. */
 mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                        int32_t c_dtype, int64_t ldc, void* stream);
+
+/* Block-scaled NVFP4 GEMM (the 1 x 16 block format of [TIBQ], "Why FP4
+ * training is the current frontier of precision reduction"):
+ *   C[m, n] = 2^(ka + kb) * sum_k qa[m, k] SA[m, k/16] * qb[n, k] SB[n, k/16]
+ * with E2M1 codes qa [M, K/2], qb [N, K/2], E4M3 scales sa / sb in
+ * MXFP4_LAYOUT_MMA with K/16 scale columns (as mxfp4_quantize writes them for
+ * MXFP4_BLOCK_1X16), ka / kb the operands' tensor_exp. fp32 accumulation; the
+ * factor 2^(ka + kb) is applied exactly to the fp32 sums; C stored as c_dtype
+ * (fp32, or bf16 nearest-even) with leading dimension ldc.
+ *  Shapes: M % 256 == 0, N % 256 == 0, K % 256 == 0; |ka + kb| <= 126. */
+mxfp4_status nvfp4_gemm(const uint8_t* qa, const uint8_t* sa, int32_t ka, const uint8_t* qb,
+                        const uint8_t* sb, int32_t kb, int64_t M, int64_t N, int64_t K, void* c,
                         int32_t c_dtype, int64_t ldc, void* stream);
 
 /* The same GEMM with the quantizer fused into its epilogue ([News], para. 2:

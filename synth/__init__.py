@@ -115,7 +115,8 @@ def dev_laplace(rows: int, cols: int, b: float, seed: int, device, outlier_frac:
                 outlier_mult: float = 100.0) -> torch.Tensor:
     """Laplace(0, b) by inverse CDF; round(outlier_frac * n) distinct entries x outlier_mult."""
     g = _gen(device, seed)
-    u = torch.rand(rows, cols, generator=g, device=device) - 0.5
+    # u in (-1/2, 1/2): a draw of exactly 0 would give -1/2 and an infinite value
+    u = (torch.rand(rows, cols, generator=g, device=device) - 0.5).clamp_(min=-0.5 + 2.0 ** -25)
     a = -b * torch.sign(u) * torch.log1p(-2.0 * u.abs())
     n = int(round(outlier_frac * rows * cols))
     if n:

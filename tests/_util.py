@@ -14,7 +14,8 @@ def cuda_params(p: oracle.Params, layout: int):
 
     return mx.QuantParams(block=p.block, scale_mode=p.scale_mode, rounding=p.rounding,
                           scale_layout=layout, wht=p.wht, wht_sign_mask=p.wht_sign_mask,
-                          seed=p.seed, sr_stream=p.sr_stream, elem_format=p.elem_format)
+                          seed=p.seed, sr_stream=p.sr_stream, elem_format=p.elem_format,
+                          tensor_exp=p.tensor_exp)
 
 
 def oracle_input(x: torch.Tensor) -> np.ndarray:
