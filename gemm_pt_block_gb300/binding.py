@@ -117,6 +117,8 @@ def lib() -> ctypes.CDLL:
                                      ctypes.POINTER(_CParams), P, P, P]
         L.mxfp4_dequantize.restype = i32
         L.mxfp4_dequantize.argtypes = [P, P, i32, i64, i64, P, P]
+        L.mxfp4_dequantize_ex.restype = i32
+        L.mxfp4_dequantize_ex.argtypes = [P, P, i32, i32, ctypes.c_uint32, i32, i64, i64, P, P]
         L.mxfp4_gemm.restype = i32
         L.mxfp4_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
         L.mxfp4_gemm_ex.restype = i32
@@ -211,12 +213,22 @@ def mxfp4_quantize(x: torch.Tensor, row: QuantParams | None = None, col: QuantPa
 
 
 def mxfp4_dequantize(q: torch.Tensor, s: torch.Tensor, rows: int, cols: int,
-                     scale_layout: int = LAYOUT_ROWMAJOR, *, out=None, stream=None):
+                     scale_layout: int = LAYOUT_ROWMAJOR, *, params: QuantParams | None = None,
+                     out=None, stream=None):
+    """fp32 [rows, cols] reconstruction of codes q with scales s. `params` (the
+    parameters the tensor was quantized with) selects the format: MXFP4 by
+    default, MXFP8 (elem_format E4M3) or NVFP4 (block 1x16, its tensor_exp);
+    its scale_layout is used when given."""
     if not q.is_cuda or not s.is_cuda:
         raise ValueError("q and s must be CUDA tensors")
     out = torch.empty((rows, cols), dtype=torch.float32, device=q.device) if out is None else out
-    _check(lib().mxfp4_dequantize(_ptr(q), _ptr(s), scale_layout, rows, cols, _ptr(out),
-                                  _stream(q, stream)))
+    if params is None:
+        _check(lib().mxfp4_dequantize(_ptr(q), _ptr(s), scale_layout, rows, cols, _ptr(out),
+                                      _stream(q, stream)))
+    else:
+        _check(lib().mxfp4_dequantize_ex(_ptr(q), _ptr(s), params.scale_layout, params.block,
+                                         params.elem_format, params.tensor_exp, rows, cols,
+                                         _ptr(out), _stream(q, stream)))
     return out
 
 

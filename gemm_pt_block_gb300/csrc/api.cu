@@ -134,19 +134,48 @@ mxfp4_status mxfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int64_
                    "mxfp4_quantize launch");
 }
 
+namespace {
+mxfp4_status dequantize_common(const char* name, const uint8_t* q, const uint8_t* s,
+                               int32_t scale_layout, int fmt, int32_t tensor_exp, int64_t rows,
+                               int64_t cols, float* out, void* stream) {
+  if ((!q || !s || !out) && rows * cols > 0) return fail(MXFP4_ERR_INVALID_ARG, "%s: NULL pointer", name);
+  if (scale_layout != MXFP4_LAYOUT_ROWMAJOR && scale_layout != MXFP4_LAYOUT_MMA)
+    return fail(MXFP4_ERR_INVALID_ARG, "%s: bad scale_layout %d", name, scale_layout);
+  if (rows < 0 || cols < 0 || cols % 32 != 0)
+    return fail(MXFP4_ERR_SHAPE, "%s: cols (%lld) must be a non-negative multiple of 32", name,
+                (long long)cols);
+  if (scale_layout == MXFP4_LAYOUT_MMA && (rows % 128 != 0 || cols % 128 != 0))
+    return fail(MXFP4_ERR_SHAPE, "%s: tensor-core scale layout needs rows and cols %% 128 == 0", name);
+  if (!aligned16(q) || !aligned16(out))
+    return fail(MXFP4_ERR_ALIGN, "%s: q / out must be 16-byte aligned", name);
+  return from_cuda(mx::launch_dequantize(q, s, scale_layout == MXFP4_LAYOUT_MMA, rows, cols, fmt,
+                                         ldexpf(1.0f, tensor_exp), out,
+                                         static_cast<cudaStream_t>(stream)),
+                   name);
+}
+}  // namespace
+
 mxfp4_status mxfp4_dequantize(const uint8_t* q, const uint8_t* s, int32_t scale_layout,
                               int64_t rows, int64_t cols, float* out, void* stream) {
-  if ((!q || !s || !out) && rows * cols > 0) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
-  if (scale_layout != MXFP4_LAYOUT_ROWMAJOR && scale_layout != MXFP4_LAYOUT_MMA)
-    return fail(MXFP4_ERR_INVALID_ARG, "bad scale_layout %d", scale_layout);
-  if (rows < 0 || cols < 0 || cols % 32 != 0)
-    return fail(MXFP4_ERR_SHAPE, "cols (%lld) must be a non-negative multiple of 32", (long long)cols);
-  if (scale_layout == MXFP4_LAYOUT_MMA && (rows % 128 != 0 || cols % 128 != 0))
-    return fail(MXFP4_ERR_SHAPE, "tensor-core scale layout needs rows and cols %% 128 == 0");
-  if (!aligned16(q) || !aligned16(out)) return fail(MXFP4_ERR_ALIGN, "q / out must be 16-byte aligned");
-  return from_cuda(mx::launch_dequantize(q, s, scale_layout == MXFP4_LAYOUT_MMA, rows, cols, out,
-                                         static_cast<cudaStream_t>(stream)),
-                   "mxfp4_dequantize launch");
+  return dequantize_common("mxfp4_dequantize", q, s, scale_layout, 0, 0, rows, cols, out, stream);
+}
+
+mxfp4_status mxfp4_dequantize_ex(const uint8_t* q, const uint8_t* s, int32_t scale_layout,
+                                 int32_t block, uint32_t elem_format, int32_t tensor_exp,
+                                 int64_t rows, int64_t cols, float* out, void* stream) {
+  if (block != MXFP4_BLOCK_1X32 && block != MXFP4_BLOCK_32X32 && block != MXFP4_BLOCK_64X64 &&
+      block != MXFP4_BLOCK_1X16)
+    return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_dequantize_ex: bad block %d", block);
+  if (elem_format != MXFP4_FORMAT_E2M1 && elem_format != MXFP4_FORMAT_E4M3)
+    return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_dequantize_ex: bad elem_format %u", elem_format);
+  const bool nv = block == MXFP4_BLOCK_1X16;
+  if (nv && elem_format != MXFP4_FORMAT_E2M1)
+    return fail(MXFP4_ERR_UNSUPPORTED, "mxfp4_dequantize_ex: 1x16 blocks take E2M1 elements");
+  if (nv ? (tensor_exp < -100 || tensor_exp > 100) : tensor_exp != 0)
+    return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_dequantize_ex: bad tensor_exp %d", tensor_exp);
+  const int fmt = nv ? 2 : (elem_format == MXFP4_FORMAT_E4M3 ? 1 : 0);
+  return dequantize_common("mxfp4_dequantize_ex", q, s, scale_layout, fmt, tensor_exp, rows, cols,
+                           out, stream);
 }
 
 namespace {

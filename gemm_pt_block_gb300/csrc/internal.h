@@ -36,8 +36,9 @@ void prepare_orient(OrientArgs* o);
 // All launchers return the cudaError_t of the launch.
 cudaError_t launch_quantize(const void* x, bool f32_in, int64_t rows, int64_t cols, int64_t ld,
                             const OrientArgs* row, const OrientArgs* col, cudaStream_t st);
+// fmt: 0 MXFP4, 1 MXFP8 (E4M3 codes), 2 NVFP4 (E4M3 scales per 16, times p2k).
 cudaError_t launch_dequantize(const uint8_t* q, const uint8_t* s, bool mma_layout, int64_t rows,
-                              int64_t cols, float* out, cudaStream_t st);
+                              int64_t cols, int fmt, float p2k, float* out, cudaStream_t st);
 cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t cols, int64_t ld,
                               uint32_t sign_mask, bool inverse, float* y, cudaStream_t st);
 // qout: also quantize C row-wise in the epilogue (nullptr: plain GEMM); c may

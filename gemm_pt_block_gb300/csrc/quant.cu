@@ -310,7 +310,12 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t par, uint32
   }
 }
 
-template <typename InT, bool kSq64>
+// kVar: kLean (1x32 / 32x32 blocks, E2M1 codes), kGeneral (also 64x64 blocks
+// and E4M3 codes, any mix of orientations), kNv (both requested orientations
+// NVFP4: the lean structure with the 1x16 E4M3-scale step).
+enum : int { kLean = 0, kGeneral = 1, kNv = 2 };
+
+template <typename InT, int kVar>
 __global__ void __launch_bounds__(kTileThreads, 3)
 quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols,
                   uint32_t ntiles, FastDiv tiles_x, const __grid_constant__ OrientArgs orow,
@@ -387,7 +392,8 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
     int64_t R0, C0;
     origin(tl, R0, C0);
 
-    if constexpr (!kSq64) {
+    if constexpr (kVar != kGeneral) {
+      constexpr bool nv = kVar == kNv;
       // ---- phase 1: rows ----
       if (ok) {
         const int rl = 32 * (warp & 1) + lane, cl = 32 * (warp >> 1);
@@ -405,13 +411,13 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
         }
         if (do_row) {
           if (orow.wht) hadamard32_lane(R, orow.sign_mask);
-          float M = absmax32(R);
-          if (orow.block) M = warp_max(M);
+          float M = nv ? 0.0f : absmax32(R);    // NVFP4 takes its two 16-block maxima itself
+          if (!nv && orow.block) M = warp_max(M);
           if (orow.sr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
-          const int e = scale_run32<false>(R, orow, M, w);
+          const int e = scale_run32<false, nv>(R, orow, M, w);
           if (valid) {
             store_run32<false>(orow, r, c, cols, R);
-            store_scale(orow, r, c >> 5, cols >> 5, e);
+            store_run_scales<nv>(orow, r, c, cols, e);
           }
         }
       }
@@ -428,8 +434,8 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           col_offsets(rl, cl, o, InT());
           read_col(st, o, R, InT());
           if (ocol.wht) hadamard32_lane(R, ocol.sign_mask);
-          float M = absmax32(R);
-          if (ocol.block) M = warp_max(M);
+          float M = nv ? 0.0f : absmax32(R);
+          if (!nv && ocol.block) M = warp_max(M);
           uint32_t w[16];
           if (ocol.sr) {
             uint32_t ob[8];   // the draw buffer is laid out like a bf16 tile
@@ -441,10 +447,10 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
               w[k] = a | (b << 16);
             }
           }
-          const int e = scale_run32<false>(R, ocol, M, w);
+          const int e = scale_run32<false, nv>(R, ocol, M, w);
           if (valid) {
             store_run32<false>(ocol, oc, k0, rows, R);
-            store_scale(ocol, oc, k0 >> 5, rows >> 5, e);
+            store_run_scales<nv>(ocol, oc, k0, rows, e);
           }
         }
       }
@@ -557,26 +563,52 @@ hadamard32_kernel(const InT* __restrict__ x, int64_t rows, int64_t cols, int64_t
 }
 
 // ---------------------------------------------------------- dequantize ---
+// Full E4M3 byte -> value (sign, NaN for S.1111.111), exact.
+__device__ __forceinline__ float e4m3_decode(uint32_t b) {
+  const uint32_t mag = b & 0x7Fu;
+  const float v = mag == 0x7Fu ? __uint_as_float(0x7FC00000u) : e4m3_value(mag);
+  return (b & 0x80u) ? -v : v;
+}
+
+// E8M0 byte -> 2^(byte - 127); 0xFF is NaN.
+__device__ __forceinline__ float e8m0_decode(uint32_t sb) {
+  return sb == 255u ? __uint_as_float(0x7FC00000u)
+         : sb == 0u ? __uint_as_float(0x00400000u)   // 2^-127 (subnormal)
+                    : __uint_as_float(sb << 23);
+}
+
+// One thread per 16 consecutive elements of a row. Every product is exact
+// (an E2M1 or E4M3 value times a power of two or an E4M3 scale).
+//  kFmt 0: MXFP4 (E2M1 codes, E8M0 scale per 32);
+//  kFmt 1: MXFP8 (E4M3 codes, one byte each, E8M0 scale per 32);
+//  kFmt 2: NVFP4 (E2M1 codes, E4M3 scale per 16, times p2k = 2^tensor_exp).
+template <int kFmt>
 __global__ void __launch_bounds__(kThreads)
 dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int mma_layout,
-               int64_t rows, int64_t cols, float* __restrict__ out) {
+               int64_t rows, int64_t cols, float p2k, float* __restrict__ out) {
   const int64_t halves = cols >> 4;
   const int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   if (t >= rows * halves) return;
   const int64_t r = t / halves, c0 = (t - r * halves) << 4;
-  const int64_t nkb = cols >> 5;
-  const uint2 w = __ldg(reinterpret_cast<const uint2*>(q + r * (cols >> 1) + (c0 >> 1)));
-  const int64_t so = mma_layout ? mma_scale_offset(r, c0 >> 5, nkb) : r * nkb + (c0 >> 5);
+  const int64_t nkb = kFmt == 2 ? cols >> 4 : cols >> 5;
+  const int64_t kb = kFmt == 2 ? c0 >> 4 : c0 >> 5;
+  const int64_t so = mma_layout ? mma_scale_offset(r, kb, nkb) : r * nkb + kb;
   const uint32_t sb = __ldg(s + so);
-  const float scale = sb == 255u ? __uint_as_float(0x7FC00000u)
-                      : sb == 0u ? __uint_as_float(0x00400000u)   // 2^-127 (subnormal)
-                                 : __uint_as_float(sb << 23);
+  const float scale = kFmt == 2 ? __fmul_rn(e4m3_decode(sb), p2k) : e8m0_decode(sb);
   float v[16];
+  if constexpr (kFmt == 1) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(q + r * cols + c0));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const uint32_t code = ((j < 8 ? w.x : w.y) >> (4 * (j & 7))) & 0xFu;
-    const float m = e2m1_magnitude(code & 7u);
-    v[j] = __fmul_rn((code & 8u) ? -m : m, scale);
+    for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(e4m3_decode((ws[j >> 2] >> (8 * (j & 3))) & 0xFFu), scale);
+  } else {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(q + r * (cols >> 1) + (c0 >> 1)));
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t code = ((j < 8 ? w.x : w.y) >> (4 * (j & 7))) & 0xFu;
+      const float m = e2m1_magnitude(code & 7u);
+      v[j] = __fmul_rn((code & 8u) ? -m : m, scale);
+    }
   }
   float4* o = reinterpret_cast<float4*>(out + r * cols + c0);
 #pragma unroll
@@ -628,20 +660,25 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
   int dev = 0;
   cudaGetDevice(&dev);
   if (!attr_set[dev & 63]) {
-    cudaFuncSetAttribute(quant_tile_kernel<InT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(quant_tile_kernel<InT, kLean>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          smem);
-    cudaFuncSetAttribute(quant_tile_kernel<InT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(quant_tile_kernel<InT, kGeneral>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(quant_tile_kernel<InT, kNv>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          smem);
     attr_set[dev & 63] = true;
   }
   OrientArgs dummy{};
   const int64_t tx = (cols + kTile - 1) / kTile, ty = (rows + kTile - 1) / kTile;
-  // The general variant handles 64x64 blocks, E4M3 codes and NVFP4's 1x16
-  // blocks; the other one is the leaner E2M1 path for 1x32 / 32x32 blocks.
-  const bool sq64 = (row && (row->block == 2 || row->e4m3 || row->nv)) ||
-                    (col && (col->block == 2 || col->e4m3 || col->nv));
-  auto kern = sq64 ? quant_tile_kernel<InT, true> : quant_tile_kernel<InT, false>;
-  const unsigned grid = resident_ctas(quant_tile_kernel<InT, false>, tx * ty, smem, kTileThreads);
+  // The lean variant covers 1x32 / 32x32 E2M1 outputs, the NVFP4 one outputs
+  // that are all 1x16; anything else (64x64 blocks, E4M3 codes, NVFP4 mixed
+  // with another block type) takes the general one.
+  auto is_lean = [](const OrientArgs* o) { return !o || (o->block != 2 && !o->e4m3 && !o->nv); };
+  auto is_nv = [](const OrientArgs* o) { return !o || o->nv; };
+  auto kern = (is_lean(row) && is_lean(col)) ? quant_tile_kernel<InT, kLean>
+              : (is_nv(row) && is_nv(col))   ? quant_tile_kernel<InT, kNv>
+                                             : quant_tile_kernel<InT, kGeneral>;
+  const unsigned grid = resident_ctas(quant_tile_kernel<InT, kLean>, tx * ty, smem, kTileThreads);
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
   kern<<<grid, kTileThreads, smem, st>>>(
       tm, rows, cols, (uint32_t)(tx * ty), make_fastdiv((uint32_t)tx), row ? *row : dummy,
@@ -681,11 +718,16 @@ cudaError_t read_quant_error(uint32_t* err) {
 }
 
 cudaError_t launch_dequantize(const uint8_t* q, const uint8_t* s, bool mma_layout, int64_t rows,
-                              int64_t cols, float* out, cudaStream_t st) {
+                              int64_t cols, int fmt, float p2k, float* out, cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
-  dequant_kernel<<<blocks_for(rows * (cols >> 4)), kThreads, 0, st>>>(q, s, mma_layout, rows,
-                                                                      cols, out);
+  const unsigned nb = blocks_for(rows * (cols >> 4));
+  if (fmt == 1)
+    dequant_kernel<1><<<nb, kThreads, 0, st>>>(q, s, mma_layout, rows, cols, p2k, out);
+  else if (fmt == 2)
+    dequant_kernel<2><<<nb, kThreads, 0, st>>>(q, s, mma_layout, rows, cols, p2k, out);
+  else
+    dequant_kernel<0><<<nb, kThreads, 0, st>>>(q, s, mma_layout, rows, cols, p2k, out);
   return cudaGetLastError();
 }
 

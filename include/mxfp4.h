@@ -167,6 +167,21 @@ mxfp4_status mxfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int64_
 mxfp4_status mxfp4_dequantize(const uint8_t* q, const uint8_t* s, int32_t scale_layout,
                               int64_t rows, int64_t cols, float* out, void* stream);
 
+/* Reconstruction for every format mxfp4_quantize writes, described by the
+ * block, elem_format and tensor_exp it was quantized with:
+ *  E2M1 with 1x32 / 32x32 / 64x64 blocks: as mxfp4_dequantize;
+ *  MXFP4_FORMAT_E4M3 (MXFP8): q [rows, cols] one E4M3 byte per element,
+ *    out = E4M3(byte) * 2^(scale - 127);
+ *  MXFP4_BLOCK_1X16 (NVFP4): q [rows, cols/2], s one E4M3 byte per 16
+ *    elements ([rows, cols/16] or the tensor-core layout with cols/16 scale
+ *    columns), out = E2M1(code) * E4M3(scale) * 2^tensor_exp.
+ * Every product is exact in fp32; NaN scale or code bytes give NaN.
+ *  Shapes and layouts as mxfp4_dequantize; tensor_exp in [-100, 100] for
+ *  1x16 blocks, 0 otherwise (else MXFP4_ERR_INVALID_ARG). */
+mxfp4_status mxfp4_dequantize_ex(const uint8_t* q, const uint8_t* s, int32_t scale_layout,
+                                 int32_t block, uint32_t elem_format, int32_t tensor_exp,
+                                 int64_t rows, int64_t cols, float* out, void* stream);
+
 /* Block-scaled MXFP4 GEMM ([Tseng], Abstract: "MXFP4 GEMMs"; [Cim], Abstract:
  * Fprop, Dgrad and Wgrad all take this form):
  *   C[m, n] = sum_k deqA[m, k] * deqB[n, k]   (fp32 accumulation)

@@ -117,6 +117,10 @@ def test_host_side_validation(L):
     # dequantize / hadamard32
     assert L.mxfp4_dequantize(good, good, 1, 64, 128, good, None) == 2
     assert L.mxfp4_dequantize(good, good, 2, 64, 128, good, None) == 1
+    assert L.mxfp4_dequantize_ex(good, good, 0, 3, 1, 0, 64, 128, good, None) == 4   # 1x16 + E4M3
+    assert L.mxfp4_dequantize_ex(good, good, 0, 0, 0, 2, 64, 128, good, None) == 1   # tensor_exp
+    assert L.mxfp4_dequantize_ex(good, good, 0, 7, 0, 0, 64, 128, good, None) == 1   # block
+    assert L.mxfp4_dequantize_ex(good, good, 1, 3, 0, 0, 64, 128, good, None) == 2   # MMA rows
     assert L.hadamard32(good, 0, 4, 40, 40, 0, 0, good, None) == 2
     assert L.hadamard32(good, 0, 4, 32, 32, 0, 2, good, None) == 1
     assert b"multiple of 32" in L.mxfp4_last_error() or len(L.mxfp4_last_error()) > 0

@@ -248,3 +248,52 @@ def test_nvfp4_gemm_full_size_sampled(M, N, K):
     ref, absref = oracle.gemm_pairs_nv(qa.cpu().numpy(), sa.cpu().numpy(), -2, qb.cpu().numpy(),
                                        sb.cpu().numpy(), 1, M, N, K, ms, ns)
     gemm_tolerance_check(c[torch.from_numpy(ms), torch.from_numpy(ns)].cpu().numpy(), ref, absref)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_nvfp4_mixed_with_other_block_types(dtype):
+    """One orientation NVFP4, the other 1x32 / 32x32 / 64x64 MXFP4 (the general
+    tile variant), both against the oracle."""
+    rows, cols = 192, 320
+    x = _input(rows, cols, dtype, seed=55)
+    nv = oracle.Params(block=oracle.BLOCK_1X16, scale_mode=oracle.SCALE_FLOOR,
+                       rounding=oracle.ROUND_SR, wht=True, wht_sign_mask=0x0F0F00FF, seed=3,
+                       sr_stream=7, tensor_exp=_k(x))
+    for blk in (oracle.BLOCK_1X32, oracle.BLOCK_32X32, oracle.BLOCK_64X64):
+        mxp = oracle.Params(block=blk, scale_mode=oracle.SCALE_ROUNDUP, rounding=oracle.ROUND_SR,
+                            seed=3, sr_stream=7)
+        for prow, pcol in ((nv, mxp), (mxp, nv)):
+            got = gpu_quantize(x.to(DEV), prow, pcol)
+            want = oracle_quantize(oracle_input(x), prow, pcol)
+            assert_same(got, want, f"mixed {blk}")
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8", "nvfp4"])
+def test_dequantize_ex_every_format(fmt, layout):
+    """GPU reconstruction of each format against the oracle's, bit for bit
+    (every product is exact), over all code values and a spread of scales."""
+    import gemm_pt_block_gb300 as mx
+
+    rows, cols = 256, 384
+    rng = np.random.default_rng(300 + layout)
+    if fmt == "mxfp8":
+        q = rng.integers(0, 256, (rows, cols), dtype=np.uint8)
+        q[(q & 0x7F) == 0x7F] = 0x3F                      # no NaN codes
+        s = rng.integers(100, 150, (rows, cols // 32), dtype=np.uint8)
+        want = oracle.dequantize(q, s, rows, cols, f64=True, fmt=oracle.FORMAT_E4M3)
+        p = mx.QuantParams(elem_format=mx.FORMAT_E4M3, scale_layout=layout)
+    elif fmt == "nvfp4":
+        q = rng.integers(0, 256, (rows, cols // 2), dtype=np.uint8)
+        s = rng.integers(0, 127, (rows, cols // 16), dtype=np.uint8)
+        want = oracle.dequantize_nv(q, s, rows, cols, tensor_exp=-9)
+        p = mx.QuantParams(block=mx.BLOCK_1X16, tensor_exp=-9, scale_layout=layout)
+    else:
+        q = rng.integers(0, 256, (rows, cols // 2), dtype=np.uint8)
+        s = rng.integers(90, 160, (rows, cols // 32), dtype=np.uint8)
+        want = oracle.dequantize(q, s, rows, cols, f64=True)
+        p = mx.QuantParams(scale_layout=layout)
+    sd = oracle.scales_to_mma(s) if layout else s
+    got = mx.mxfp4_dequantize(*_dev(q, sd), rows, cols, params=p)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy().astype(np.float64), want)
