@@ -356,6 +356,19 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+def source_digest(path: str) -> str:
+    """Hash of a C++/CUDA source with comments and whitespace removed, so that
+    a record taken on a kernel stays valid across comment edits only."""
+    import re
+
+    with open(path) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    text = re.sub(r"\s+", "", text)
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
 def _traffic_record():
     """DRAM traffic per GEMM launch from the committed ncu summary, if it was
     taken on the current GEMM source (else None)."""
@@ -368,9 +381,7 @@ def _traffic_record():
                 if ":" in ln and not ln.startswith("#"):
                     k, v = ln.split(":", 1)
                     rec[k.strip()] = v.strip()
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()[:16]
-        return rec if rec.get("gemm_cu_sha256_16") == digest else None
+        return rec if rec.get("gemm_cu_code_sha256_16") == source_digest(src) else None
     except OSError:
         return None
 

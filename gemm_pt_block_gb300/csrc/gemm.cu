@@ -21,6 +21,10 @@
 //  * warps 2..9: epilogue -- drain the 128 x 256 fp32 accumulator from tensor
 //    memory into registers, release it so the next tile's MMAs can start, then
 //    store to global memory.
+// The CTA-pair kernel below (cta_group::2, 256 x 256 tiles) is the one used
+// whenever M % 256 == 0; it also serves the MXFP8 (kind::mxf8f6f4, E4M3
+// operands) and NVFP4 (kind::mxf4nvf4, E4M3 scales per 16) GEMMs. Epilogues
+// store C as fp32 or bf16 and can quantize it row-wise on the way out.
 // Every mbarrier wait is bounded (about 2 s): on expiry the CTA sets the
 // library's device error word, stops issuing work, and still frees its tensor
 // memory before exiting.
