@@ -129,6 +129,7 @@ def lib() -> ctypes.CDLL:
         L.mxfp8_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P]
         L.mxfp4_gemm_quantize.restype = i32
         L.mxfp4_gemm_quantize.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64,
+                                          ctypes.POINTER(_CParams), P, P,
                                           ctypes.POINTER(_CParams), P, P, P]
         L.hadamard32.restype = i32
         L.hadamard32.argtypes = [P, i32, i64, i64, i64, ctypes.c_uint32, i32, P, P]
@@ -297,25 +298,43 @@ def nvfp4_gemm(qa: torch.Tensor, sa: torch.Tensor, ka: int, qb: torch.Tensor, sb
 
 
 def mxfp4_gemm_quantize(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
-                        M: int, N: int, K: int, out: QuantParams, *, with_c: bool = False, c=None,
+                        M: int, N: int, K: int, out: QuantParams | None = None, *,
+                        col: QuantParams | None = None, with_c: bool = False, c=None,
                         out_dtype: torch.dtype = torch.float32, q_out=None, s_out=None,
-                        stream=None):
-    """GEMM whose epilogue quantizes C row-wise with `out`: returns (q_out, s_out, c),
-    c None unless with_c (or c given; fp32 or bf16); codes/scales as
-    mxfp4_quantize(C, out) of the fp32 C."""
+                        q_col=None, s_col=None, stream=None):
+    """GEMM whose epilogue quantizes C: row-wise with `out` and/or column-wise
+    (C^T along M) with `col`. Returns (q_out, s_out, c) when only `out` is
+    given, else (q_out, s_out, q_col, s_col, c) (None for an orientation not
+    asked for); c is None unless with_c (or c given; fp32 or bf16). The codes
+    and scales equal mxfp4_quantize(C, out, col) of the fp32 C."""
     _check_operands(qa, sa, qb, sb)
+    if out is None and col is None:
+        raise ValueError("out (row-wise) or col params are required")
     cdt = _c_dtype(c, out_dtype)
     if c is None and with_c:
         c = torch.empty((M, N), dtype=out_dtype, device=qa.device)
-    q_out = torch.empty((M, out.code_cols(N)), dtype=torch.uint8, device=qa.device) if q_out is None else q_out
-    s_out = _scales_out(M, N, out, qa.device) if s_out is None else s_out
+    if out is not None:
+        q_out = torch.empty((M, out.code_cols(N)), dtype=torch.uint8, device=qa.device) if q_out is None else q_out
+        s_out = _scales_out(M, N, out, qa.device) if s_out is None else s_out
+    if col is not None:
+        q_col = torch.empty((N, col.code_cols(M)), dtype=torch.uint8, device=qa.device) if q_col is None else q_col
+        s_col = _scales_out(N, M, col, qa.device) if s_col is None else s_col
     ldc = c.stride(0) if c is not None else N
-    op = out._c()
+    op = out._c() if out is not None else None
+    cp = col._c() if col is not None else None
     _check(lib().mxfp4_gemm_quantize(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K,
                                      _ptr(c) if c is not None else None, cdt, ldc,
-                                     ctypes.byref(op), _ptr(q_out), _ptr(s_out),
+                                     ctypes.byref(op) if op is not None else None,
+                                     _ptr(q_out if out is not None else None),
+                                     _ptr(s_out if out is not None else None),
+                                     ctypes.byref(cp) if cp is not None else None,
+                                     _ptr(q_col if col is not None else None),
+                                     _ptr(s_col if col is not None else None),
                                      _stream(qa, stream)))
-    return q_out, s_out, c
+    if col is None:
+        return q_out, s_out, c
+    return (q_out if out is not None else None, s_out if out is not None else None,
+            q_col, s_col, c)
 
 
 def hadamard32(x: torch.Tensor, sign_mask: int = 0, inverse: bool = False, *, y=None, stream=None):

@@ -181,8 +181,10 @@ mxfp4_status mxfp4_dequantize_ex(const uint8_t* q, const uint8_t* s, int32_t sca
 namespace {
 mxfp4_status gemm_common(const char* name, const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                          const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
-                         int32_t c_dtype, int64_t ldc, const mx::OrientArgs* qout, void* stream) {
-  if (!qa || !sa || !qb || !sb || (!c && !qout)) return fail(MXFP4_ERR_INVALID_ARG, "%s: NULL pointer", name);
+                         int32_t c_dtype, int64_t ldc, const mx::OrientArgs* qout,
+                         const mx::OrientArgs* qcol, void* stream) {
+  if (!qa || !sa || !qb || !sb || (!c && !qout && !qcol))
+    return fail(MXFP4_ERR_INVALID_ARG, "%s: NULL pointer", name);
   if (c_dtype != MXFP4_DTYPE_BF16 && c_dtype != MXFP4_DTYPE_F32)
     return fail(MXFP4_ERR_INVALID_ARG, "%s: bad c_dtype %d", name, c_dtype);
   if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0)
@@ -196,7 +198,7 @@ mxfp4_status gemm_common(const char* name, const uint8_t* qa, const uint8_t* sa,
     return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");
   const char* why = "";
   cudaError_t e = mx::launch_gemm(qa, sa, qb, sb, M, N, K, c, c_dtype == MXFP4_DTYPE_BF16, ldc,
-                                  qout, static_cast<cudaStream_t>(stream), &why);
+                                  qout, qcol, static_cast<cudaStream_t>(stream), &why);
   if (e == cudaErrorNotSupported) return fail(MXFP4_ERR_UNSUPPORTED, "%s", why);
   if (e == cudaErrorInvalidValue && why[0]) return fail(MXFP4_ERR_ALIGN, "%s", why);
   return from_cuda(e, name);
@@ -208,14 +210,15 @@ mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         int64_t ldc, void* stream) {
   if (!c) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
   return gemm_common("mxfp4_gemm", qa, sa, qb, sb, M, N, K, c, MXFP4_DTYPE_F32, ldc, nullptr,
-                     stream);
+                     nullptr, stream);
 }
 
 mxfp4_status mxfp4_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                            const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                            int32_t c_dtype, int64_t ldc, void* stream) {
   if (!c) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
-  return gemm_common("mxfp4_gemm_ex", qa, sa, qb, sb, M, N, K, c, c_dtype, ldc, nullptr, stream);
+  return gemm_common("mxfp4_gemm_ex", qa, sa, qb, sb, M, N, K, c, c_dtype, ldc, nullptr, nullptr,
+                     stream);
 }
 
 mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
@@ -267,21 +270,30 @@ mxfp4_status nvfp4_gemm(const uint8_t* qa, const uint8_t* sa, int32_t ka, const 
 
 mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                                  const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
-                                 int32_t c_dtype, int64_t ldc, const mxfp4_quant_params* out,
-                                 uint8_t* q_out, uint8_t* s_out, void* stream) {
-  if (!out) return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_gemm_quantize: out params are required");
-  if (out->block == MXFP4_BLOCK_64X64)
-    return fail(MXFP4_ERR_UNSUPPORTED,
-                "mxfp4_gemm_quantize: 64x64 blocks span two epilogue warps; quantize C separately");
-  if (out->block == MXFP4_BLOCK_1X16)
-    return fail(MXFP4_ERR_UNSUPPORTED,
-                "mxfp4_gemm_quantize: 1x16 (NVFP4) output is not fused; quantize C separately");
-  mx::OrientArgs qo{};
-  if (M > 0 && N > 0) {
-    mxfp4_status st = check_params(out, q_out, s_out, M, N, "out", &qo);
-    if (st) return st;
+                                 int32_t c_dtype, int64_t ldc, const mxfp4_quant_params* row,
+                                 uint8_t* q_row, uint8_t* s_row, const mxfp4_quant_params* col,
+                                 uint8_t* q_col, uint8_t* s_col, void* stream) {
+  if (!row && !col)
+    return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_gemm_quantize: row or col params are required");
+  for (const mxfp4_quant_params* p : {row, col}) {
+    if (p && p->block == MXFP4_BLOCK_64X64)
+      return fail(MXFP4_ERR_UNSUPPORTED,
+                  "mxfp4_gemm_quantize: 64x64 blocks span two epilogue warps; quantize C separately");
+    if (p && p->block == MXFP4_BLOCK_1X16)
+      return fail(MXFP4_ERR_UNSUPPORTED,
+                  "mxfp4_gemm_quantize: 1x16 (NVFP4) output is not fused; quantize C separately");
   }
-  return gemm_common("mxfp4_gemm_quantize", qa, sa, qb, sb, M, N, K, c, c_dtype, ldc, &qo, stream);
+  if (col && M % 256 != 0)
+    return fail(MXFP4_ERR_UNSUPPORTED,
+                "mxfp4_gemm_quantize: column-wise output needs M %% 256 == 0 (CTA-pair kernel)");
+  mx::OrientArgs ro{}, co{};
+  if (M > 0 && N > 0) {
+    mxfp4_status st;
+    if (row && (st = check_params(row, q_row, s_row, M, N, "row", &ro))) return st;
+    if (col && (st = check_params(col, q_col, s_col, N, M, "col", &co))) return st;
+  }
+  return gemm_common("mxfp4_gemm_quantize", qa, sa, qb, sb, M, N, K, c, c_dtype, ldc,
+                     row ? &ro : nullptr, col ? &co : nullptr, stream);
 }
 
 mxfp4_status hadamard32(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,

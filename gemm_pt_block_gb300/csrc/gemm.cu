@@ -142,9 +142,9 @@ __device__ __forceinline__ uint32_t bf16x2(uint32_t lo, uint32_t hi) {
 
 // One epilogue thread's results: 128 consecutive fp32 values of row `row`
 // (columns c0 .. c0 + 127). They are stored to C when C is given (fp32, or
-// bf16 rounded to nearest-even when c_bf16), and with kQ they are also
-// quantized row-wise (four 32-runs) from the fp32 values, exactly as the
-// quantizer would quantize that row of an fp32 C.
+// bf16 rounded to nearest-even when c_bf16), and with kQ (and a row-wise
+// output requested) they are also quantized row-wise (four 32-runs) from the
+// fp32 values, exactly as the quantizer would quantize that row of an fp32 C.
 template <bool kQ>
 __device__ __forceinline__ void epilogue_out(const uint32_t (&r0)[64], const uint32_t (&r1)[64],
                                              void* C, int c_bf16, int64_t ldc, int64_t row,
@@ -172,7 +172,7 @@ __device__ __forceinline__ void epilogue_out(const uint32_t (&r0)[64], const uin
                                   __uint_as_float(r1[4 * j + 2]), __uint_as_float(r1[4 * j + 3]));
     }
   }
-  if constexpr (kQ) {
+  if (kQ && qo.q != nullptr) {
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       float2 R[16];
@@ -184,6 +184,86 @@ __device__ __forceinline__ void epilogue_out(const uint32_t (&r0)[64], const uin
       }
       quantize_run32(R, row, c0 + 32 * b, N, qo);
     }
+  }
+}
+
+// Column-wise quantization of one 32 x 32 chunk of an epilogue warp's block of
+// C (rows row0 .. row0 + 31, lane l holding row row0 + l and, in v, its
+// values at columns n0 .. n0 + 31): the quantization of C^T along M, whose
+// output row n is column n of C and whose 32-runs run along m. The chunk goes
+// through the warp's shared buffers -- the values (tb, 32 x 33 floats) and,
+// for stochastic rounding, the draws keyed by source index m * N + n (db,
+// 32 x 17 words, a row's 32 16-bit draws packed as the quantizer packs them)
+// -- so that lane l then holds column n0 + l; that run is quantized as the
+// quantizer's column pass does (rotation, block max over the 32 lanes for
+// 32x32 blocks, scale, rounding, packing) and stored at q[n0 + l, row0 / 2 ..].
+__device__ __forceinline__ void col_chunk(const float2 (&v)[16], float* tb, uint32_t* db, int lane,
+                                          int64_t row0, int64_t n0, int64_t M, int64_t N,
+                                          const OrientArgs& qc) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    tb[lane * 33 + 2 * k] = v[k].x;
+    tb[lane * 33 + 2 * k + 1] = v[k].y;
+  }
+  if (qc.sr) {
+    uint32_t w[16];
+    draws32(qc.keys, qc.stream, (uint64_t)((row0 + lane) * N + n0), w);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) db[lane * 17 + k] = w[k];
+  }
+  __syncwarp();
+  float2 R[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k)
+    R[k] = make_float2(tb[(2 * k) * 33 + lane], tb[(2 * k + 1) * 33 + lane]);
+  uint32_t w[16];
+  if (qc.sr) {
+    const int sh = 16 * (lane & 1);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t d0 = (db[(2 * k) * 17 + (lane >> 1)] >> sh) & 0xFFFFu;
+      const uint32_t d1 = (db[(2 * k + 1) * 17 + (lane >> 1)] >> sh) & 0xFFFFu;
+      w[k] = d0 | (d1 << 16);
+    }
+  }
+  __syncwarp();   // the buffers are rewritten by the next chunk
+  const int64_t n = n0 + lane;
+  if (qc.wht) hadamard32_lane(R, qc.sign_mask);
+  float Mx = absmax32(R);
+  if (qc.block) Mx = warp_max(Mx);
+  const int e = scale_run32<true, false>(R, qc, Mx, w);
+  store_run32(qc, n, row0, M, R);
+  store_run_scales<false>(qc, n, row0, M, e);
+}
+
+// The epilogue with both orientations: C stored as in epilogue_out, then per
+// 32-column chunk the row-wise run (if qo.q) and the column-wise chunk (if
+// qc.q), so each chunk's registers die as the loop moves on.
+__device__ __forceinline__ void epilogue_rowcol(const uint32_t (&r0)[64], const uint32_t (&r1)[64],
+                                                void* C, int c_bf16, int64_t ldc, int64_t row,
+                                                int64_t c0, int64_t M, int64_t N,
+                                                const OrientArgs& qo, const OrientArgs& qc,
+                                                float* tb, uint32_t* db, int lane) {
+  if (C != nullptr) {
+    const OrientArgs none{};
+    epilogue_out<false>(r0, r1, C, c_bf16, ldc, row, c0, N, none);
+  }
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    float2 v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int i = (b & 1) * 32 + 2 * k;
+      v[k] = b < 2 ? make_float2(__uint_as_float(r0[i]), __uint_as_float(r0[i + 1]))
+                   : make_float2(__uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
+    }
+    if (qo.q != nullptr) {
+      float2 R[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) R[k] = v[k];
+      quantize_run32(R, row, c0 + 32 * b, N, qo);
+    }
+    if (qc.q != nullptr) col_chunk(v, tb, db, lane, row - lane, c0 + 32 * b, M, N, qc);
   }
 }
 
@@ -383,6 +463,12 @@ constexpr uint32_t SFB_COL_NV = SFA_COL + 16;   // A: 4 tiles x 4 columns, B: 4 
 static_assert(NV_STAGE_BYTES % 1024 == 0 && NV_STAGES <= STAGES, "NVFP4 ring");
 static_assert(SFB_COL_NV + 32 <= TMEM_COLS, "NVFP4 scale columns");
 enum : int { kMxf4 = 0, kMxf8 = 1, kNvf4 = 2 };
+// Column-wise epilogue quantization: per epilogue warp a 32 x 33 fp32 value
+// buffer and a 32 x 17 word draw buffer, after five stages.
+constexpr int QC_STAGES = 5;
+constexpr int kXposeBytes = 32 * 33 * 4 + 32 * 17 * 4;     // 6400
+constexpr int QC_SMEM_BYTES = QC_STAGES * STAGE_BYTES + CTL_BYTES + NUM_EPI_WARPS * kXposeBytes + 1024;
+static_assert(QC_SMEM_BYTES <= 227 * 1024, "column-wise epilogue buffers");
 
 // kind::mxf4nvf4 with E2M1 A and B (type code 1), K-major, UE4M3 scales (bit
 // 23 clear), scale_vec::4X (both scale-factor selectors 0).
@@ -411,14 +497,19 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
 //    tiles of A and four per band of B (twelve scale copies), and each MMA
 //    reads a whole word; the fp32 sums are multiplied by alpha (the operands'
 //    power-of-two tensor factors) in the epilogue. Five stages of 38 KB.
-template <bool kQ, int kKind = kMxf4>
+//
+// kQ: 0 plain; 1 C also quantized row-wise (qo); 2 row-wise (qo, if qo.q) and
+// column-wise (qc) -- five stages, the rest of shared memory holding each
+// epilogue warp's transposition buffers (kXposeBytes).
+template <int kQ, int kKind = kMxf4>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                       void* __restrict__ C, int c_bf16, int64_t ldc, int M, int N, int K, int group_m,
-                      float alpha, const __grid_constant__ OrientArgs qo) {
+                      float alpha, const __grid_constant__ OrientArgs qo,
+                      const __grid_constant__ OrientArgs qc) {
   constexpr bool kF8 = kKind == kMxf8, kNv = kKind == kNvf4;
-  constexpr int kStages = kNv ? NV_STAGES : STAGES;
+  constexpr int kStages = kNv ? NV_STAGES : (kQ == 2 ? QC_STAGES : STAGES);
   constexpr int kStageBytes = kNv ? NV_STAGE_BYTES : STAGE_BYTES;
   constexpr int kSfaBytes = kNv ? 4 * 512 : SFA_BYTES;
   constexpr uint32_t kSfbCol = kNv ? SFB_COL_NV : SFB_COL;
@@ -608,7 +699,14 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
           r1[i] = __float_as_uint(__fmul_rn(__uint_as_float(r1[i]), alpha));
         }
       }
-      epilogue_out<kQ>(r0, r1, C, c_bf16, ldc, row, (int64_t)nb * BNP + h * 128, N, qo);
+      const int64_t col0 = (int64_t)nb * BNP + h * 128;
+      if constexpr (kQ == 2) {
+        uint8_t* xb = smem + kStages * kStageBytes + CTL_BYTES + (warp - 2) * kXposeBytes;
+        epilogue_rowcol(r0, r1, C, c_bf16, ldc, row, col0, M, N, qo, qc,
+                        reinterpret_cast<float*>(xb), reinterpret_cast<uint32_t*>(xb + 4224), lane);
+      } else {
+        epilogue_out<kQ != 0>(r0, r1, C, c_bf16, ldc, row, col0, N, qo);
+      }
     }
   }
 
@@ -672,13 +770,15 @@ DevInfo& dev_info(int dev) {
                            SMEM_BYTES);
       cudaFuncSetAttribute(mxf4_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_BYTES);
-      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<false>,
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<0>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
-      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<true>,
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<1>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
-      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<false, pair::kMxf8>,
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<2>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, pair::QC_SMEM_BYTES);
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<0, pair::kMxf8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
-      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<false, pair::kNvf4>,
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<0, pair::kNvf4>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::NV_SMEM_BYTES);
     }
     d.attr_set = true;
@@ -690,10 +790,15 @@ DevInfo& dev_info(int dev) {
 
 cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
-                        bool c_bf16, int64_t ldc, const OrientArgs* qout, cudaStream_t st,
-                        const char** why) {
+                        bool c_bf16, int64_t ldc, const OrientArgs* qout, const OrientArgs* qcol,
+                        cudaStream_t st, const char** why) {
   const OrientArgs none{};
   const OrientArgs& qo = qout ? *qout : none;
+  const OrientArgs& qc = qcol ? *qcol : none;
+  if (qcol && M % 256 != 0) {
+    *why = "column-wise quantization in the GEMM epilogue needs M % 256 == 0 (CTA pairs)";
+    return cudaErrorNotSupported;
+  }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -722,12 +827,15 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
     int64_t gm = kGroupBytes / (256 * (K / 2));
     gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
     (void)cudaGetLastError();  // drop a stale error left by an earlier call
-    if (qout)
-      pair::mxf4_gemm_pair_kernel<true><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
-          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, qo);
+    if (qcol)
+      pair::mxf4_gemm_pair_kernel<2><<<grid, THREADS, pair::QC_SMEM_BYTES, st>>>(
+          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, qo, qc);
+    else if (qout)
+      pair::mxf4_gemm_pair_kernel<1><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
+          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, qo, none);
     else
-      pair::mxf4_gemm_pair_kernel<false><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
-          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, qo);
+      pair::mxf4_gemm_pair_kernel<0><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
+          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, qo, none);
     return cudaGetLastError();
   }
   if (!make_code_map(&ta, qa, M, K / 2, BM) || !make_code_map(&tb, qb, N, K / 2, BN)) {
@@ -798,8 +906,8 @@ cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
   gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
   const OrientArgs none{};
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
-  pair::mxf4_gemm_pair_kernel<false, pair::kMxf8><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
-      ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, none);
+  pair::mxf4_gemm_pair_kernel<0, pair::kMxf8><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
+      ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, none, none);
   return cudaGetLastError();
 }
 
@@ -832,8 +940,8 @@ cudaError_t launch_gemm_nv(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
   gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
   const OrientArgs none{};
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
-  pair::mxf4_gemm_pair_kernel<false, pair::kNvf4><<<grid, THREADS, pair::NV_SMEM_BYTES, st>>>(
-      ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, alpha, none);
+  pair::mxf4_gemm_pair_kernel<0, pair::kNvf4><<<grid, THREADS, pair::NV_SMEM_BYTES, st>>>(
+      ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, alpha, none, none);
   return cudaGetLastError();
 }
 

@@ -41,12 +41,13 @@ cudaError_t launch_dequantize(const uint8_t* q, const uint8_t* s, bool mma_layou
                               int64_t cols, int fmt, float p2k, float* out, cudaStream_t st);
 cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t cols, int64_t ld,
                               uint32_t sign_mask, bool inverse, float* y, cudaStream_t st);
-// qout: also quantize C row-wise in the epilogue (nullptr: plain GEMM); c may
-// then be nullptr (no fp32 output).
+// qout / qcol: also quantize C row-wise / column-wise (C^T along M) in the
+// epilogue (nullptr: not produced; column-wise needs M % 256 == 0); with
+// either, c may be nullptr (no C output).
 cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
-                        bool c_bf16, int64_t ldc, const OrientArgs* qout, cudaStream_t st,
-                        const char** why);
+                        bool c_bf16, int64_t ldc, const OrientArgs* qout, const OrientArgs* qcol,
+                        cudaStream_t st, const char** why);
 // Reads and clears the quantizer's device error word.
 cudaError_t read_quant_error(uint32_t* err);
 // Reads and clears the device error words (synchronizes st).

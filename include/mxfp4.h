@@ -230,21 +230,28 @@ mxfp4_status nvfp4_gemm(const uint8_t* qa, const uint8_t* sa, int32_t ka, const 
                         int32_t c_dtype, int64_t ldc, void* stream);
 
 /* The same GEMM with the quantizer fused into its epilogue ([News], para. 2:
- * the rotation and rounding run where the producing GEMM writes its output):
- * C is quantized row-wise (along N) straight from the accumulator, with the
- * parameters `out` (any block, scale mode, rounding, rotation and scale layout
- * mxfp4_quantize accepts). The codes q_out [M, N/2] and scales s_out
- * ([M, N/32] or MXFP4_LAYOUT_MMA) are bit-identical to mxfp4_quantize of the
- * fp32 C this call computes, with cols = N (stochastic draws keyed by the
- * element index m * N + n); they come from the fp32 sums even when C itself
- * is stored as bf16 (c_dtype as in mxfp4_gemm_ex). c may be NULL: then no C
- * is written (c_dtype and ldc are ignored), which saves its HBM traffic.
- *  Shapes as mxfp4_gemm; MMA scale layout needs nothing more (M % 128,
- *  N % 128 hold). q_out must be 16-byte aligned. */
+ * the rotation and rounding run where the producing GEMM writes its output).
+ * C is quantized straight from the accumulator in one or both orientations,
+ * exactly as mxfp4_quantize would quantize the fp32 C this call computes
+ * (x = C, rows = M, cols = N):
+ *  row  if non-NULL, along N: q_row [M, N/2], s_row ([M, N/32] or
+ *       MXFP4_LAYOUT_MMA);
+ *  col  if non-NULL, C^T along M (the orientation the next layer's Wgrad
+ *       consumes): q_col [N, M/2], s_col ([N, M/32] or MXFP4_LAYOUT_MMA);
+ *       needs M % 256 == 0 (else MXFP4_ERR_UNSUPPORTED).
+ * At least one of row / col must be non-NULL. Any block (except 64x64 and
+ * 1x16: MXFP4_ERR_UNSUPPORTED), scale mode, rounding, rotation, element
+ * format and scale layout mxfp4_quantize accepts; stochastic draws are keyed
+ * by the element index m * N + n of C in both orientations. The codes come
+ * from the fp32 sums even when C itself is stored as bf16 (c_dtype as in
+ * mxfp4_gemm_ex). c may be NULL: then no C is written (c_dtype and ldc are
+ * ignored), which saves its HBM traffic.
+ *  Shapes as mxfp4_gemm. q_row / q_col must be 16-byte aligned. */
 mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                                  const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
-                                 int32_t c_dtype, int64_t ldc, const mxfp4_quant_params* out,
-                                 uint8_t* q_out, uint8_t* s_out, void* stream);
+                                 int32_t c_dtype, int64_t ldc, const mxfp4_quant_params* row,
+                                 uint8_t* q_row, uint8_t* s_row, const mxfp4_quant_params* col,
+                                 uint8_t* q_col, uint8_t* s_col, void* stream);
 
 /* Stand-alone 32-point block rotation along cols ([News], para. 2):
  *  forward (inverse == 0): y = c * H * diag(s) * x per 32-block;
