@@ -221,11 +221,22 @@ class Step:
                 torch.empty(ns, dtype=u8, device=device) if q.pcol else None)
         for g in spec.gemms:
             self.outs[g.label] = torch.empty(g.M, g.N, device=device)
+        # one workspace for the GEMMs' scale images (the largest the step needs)
+        blk = 16 if spec.nvfp4 else 32
+        self.ws = torch.empty(max([mx.gemm_workspace_size(g.M, g.N, g.K, blk) for g in spec.gemms],
+                                  default=0), dtype=u8, device=device)
         torch.cuda.empty_cache()
 
     @property
-    def launches(self):
+    def ops(self):
         return len(self.spec.quants) + len(self.spec.gemms)
+
+    @property
+    def launches(self):
+        """Kernel launches per step: one per quantize, two per GEMM (the scale
+        images for the tensor-memory copies, then the GEMM) when it uses the
+        workspace, which every CTA-pair shape (M % 256 == 0) does."""
+        return len(self.spec.quants) + sum(2 if g.M % 256 == 0 else 1 for g in self.spec.gemms)
 
     def operand(self, ref):
         q, s, qc, sc = self.bufs[ref[0]]
@@ -257,9 +268,9 @@ class Step:
             qb, sb = self.operand(g.b)
             if self.spec.nvfp4:
                 mx.nvfp4_gemm(qa, sa, self.tensor_exp(g.a), qb, sb, self.tensor_exp(g.b),
-                              g.M, g.N, g.K, c=out[g.label])
+                              g.M, g.N, g.K, c=out[g.label], workspace=self.ws)
             else:
-                mx.mxfp4_gemm(qa, sa, qb, sb, g.M, g.N, g.K, c=out[g.label])
+                mx.mxfp4_gemm(qa, sa, qb, sb, g.M, g.N, g.K, c=out[g.label], workspace=self.ws)
             k += 1
             if events is not None:
                 events[k].record()
@@ -606,9 +617,11 @@ def run_op(args):
         qb, sb = st.operand(g.b)
         if sub.nvfp4:
             ka, kb = st.tensor_exp(g.a), st.tensor_exp(g.b)
-            fn = lambda: mx.nvfp4_gemm(qa, sa, ka, qb, sb, kb, g.M, g.N, g.K, c=st.outs[g.label])
+            fn = lambda: mx.nvfp4_gemm(qa, sa, ka, qb, sb, kb, g.M, g.N, g.K, c=st.outs[g.label],
+                                       workspace=st.ws)
         else:
-            fn = lambda: mx.mxfp4_gemm(qa, sa, qb, sb, g.M, g.N, g.K, c=st.outs[g.label])
+            fn = lambda: mx.mxfp4_gemm(qa, sa, qb, sb, g.M, g.N, g.K, c=st.outs[g.label],
+                                       workspace=st.ws)
         work, unit = sub.gemm_flops()[0] / 1e12, "TFLOP/s"
     else:
         q = sub.quants[0]
@@ -747,7 +760,7 @@ def main():
         st.run()
     barrier()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(st.launches + 1)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(st.ops + 1)]
            for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         barrier()
@@ -760,7 +773,7 @@ def main():
     total_ms = max_over_ranks(t0.elapsed_time(t1), ws, device)
     ms_step = total_ms / args.steps
     per_launch = [statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
-                  for j in range(st.launches)]
+                  for j in range(st.ops)]
     if mx.device_status() != 0:
         raise RuntimeError("a bounded device-side wait ran out during the benchmark")
 

@@ -42,6 +42,7 @@ from .binding import (  # noqa: F401
     mxfp4_gemm,
     mxfp4_gemm_quantize,
     mxfp8_gemm,
+    gemm_workspace_size,
     nvfp4_gemm,
     nvfp4_tensor_exp,
     mxfp4_quantize,

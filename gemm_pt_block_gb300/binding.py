@@ -121,10 +121,13 @@ def lib() -> ctypes.CDLL:
         L.mxfp4_dequantize_ex.argtypes = [P, P, i32, i32, ctypes.c_uint32, i32, i64, i64, P, P]
         L.mxfp4_gemm.restype = i32
         L.mxfp4_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
+        sz = ctypes.c_size_t
         L.mxfp4_gemm_ex.restype = i32
-        L.mxfp4_gemm_ex.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P]
+        L.mxfp4_gemm_ex.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P, sz, P]
+        L.mxfp4_gemm_workspace_size.restype = sz
+        L.mxfp4_gemm_workspace_size.argtypes = [i64, i64, i64, i32]
         L.nvfp4_gemm.restype = i32
-        L.nvfp4_gemm.argtypes = [P, P, i32, P, P, i32, i64, i64, i64, P, i32, i64, P]
+        L.nvfp4_gemm.argtypes = [P, P, i32, P, P, i32, i64, i64, i64, P, i32, i64, P, sz, P]
         L.mxfp8_gemm.restype = i32
         L.mxfp8_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P]
         L.mxfp4_gemm_quantize.restype = i32
@@ -248,22 +251,45 @@ def _c_dtype(c, out_dtype) -> int:
     raise TypeError("C must be float32 or bfloat16")
 
 
+def gemm_workspace_size(M: int, N: int, K: int, scale_block: int = 32) -> int:
+    """Bytes of the optional GEMM workspace (scale images): 4 (M + N) K / scale_block."""
+    return int(lib().mxfp4_gemm_workspace_size(M, N, K, scale_block))
+
+
+def _workspace(workspace, M: int, N: int, K: int, scale_block: int, device):
+    """(pointer, bytes) for the C call: a caller tensor, none (False), or a fresh
+    caller-owned tensor from PyTorch's allocator when the CTA-pair GEMM can use it."""
+    if workspace is False or (workspace is None and M % 256 != 0):
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(gemm_workspace_size(M, N, K, scale_block), dtype=torch.uint8,
+                                device=device)
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
 def mxfp4_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
                M: int, N: int, K: int, *, c=None, ldc: int | None = None,
-               out_dtype: torch.dtype = torch.float32, stream=None):
+               out_dtype: torch.dtype = torch.float32, workspace=None, stream=None):
     """C[M, N] = deq(A) deq(B)^T (fp32 sums, stored as fp32 or bf16: out_dtype, or
-    c's dtype); A, B K-major packed codes, scales in tensor-core layout."""
+    c's dtype); A, B K-major packed codes, scales in tensor-core layout.
+
+    `workspace`: None (default) lets the call use a scratch tensor for its scale
+    images (mxfp4_gemm_ex; same result, faster), a CUDA tensor supplies it,
+    False calls the plain mxfp4_gemm entry point (fp32 C) without one."""
     _check_operands(qa, sa, qb, sb)
     cdt = _c_dtype(c, out_dtype)
     if c is None:
         c = torch.empty((M, N), dtype=out_dtype, device=qa.device)
     ldc = c.stride(0) if ldc is None else ldc
-    if cdt == DTYPE_F32:
+    if workspace is False and cdt == DTYPE_F32:
         _check(lib().mxfp4_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), ldc,
                                 _stream(qa, stream)))
-    else:
-        _check(lib().mxfp4_gemm_ex(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), cdt,
-                                   ldc, _stream(qa, stream)))
+        return c
+    ws, nbytes = _workspace(workspace, M, N, K, 32, qa.device)
+    _check(lib().mxfp4_gemm_ex(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), cdt,
+                               ldc, _ptr(ws), nbytes, _stream(qa, stream)))
     return c
 
 
@@ -284,16 +310,18 @@ def mxfp8_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.T
 
 def nvfp4_gemm(qa: torch.Tensor, sa: torch.Tensor, ka: int, qb: torch.Tensor, sb: torch.Tensor,
                kb: int, M: int, N: int, K: int, *, c=None, ldc: int | None = None,
-               out_dtype: torch.dtype = torch.float32, stream=None):
+               out_dtype: torch.dtype = torch.float32, workspace=None, stream=None):
     """C[M, N] = 2^(ka + kb) deq(A) deq(B)^T for NVFP4 operands: E2M1 codes [M, K/2] /
-    [N, K/2], E4M3 scales per 16 in tensor-core layout, ka / kb their tensor_exp."""
+    [N, K/2], E4M3 scales per 16 in tensor-core layout, ka / kb their tensor_exp.
+    `workspace` as in mxfp4_gemm (False: none)."""
     _check_operands(qa, sa, qb, sb)
     cdt = _c_dtype(c, out_dtype)
     if c is None:
         c = torch.empty((M, N), dtype=out_dtype, device=qa.device)
     ldc = c.stride(0) if ldc is None else ldc
+    ws, nbytes = _workspace(workspace, M, N, K, 16, qa.device)
     _check(lib().nvfp4_gemm(_ptr(qa), _ptr(sa), ka, _ptr(qb), _ptr(sb), kb, M, N, K, _ptr(c), cdt,
-                            ldc, _stream(qa, stream)))
+                            ldc, _ptr(ws), nbytes, _stream(qa, stream)))
     return c
 
 

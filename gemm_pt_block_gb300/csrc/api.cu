@@ -182,7 +182,7 @@ namespace {
 mxfp4_status gemm_common(const char* name, const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                          const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                          int32_t c_dtype, int64_t ldc, const mx::OrientArgs* qout,
-                         const mx::OrientArgs* qcol, void* stream) {
+                         const mx::OrientArgs* qcol, void* ws, size_t ws_bytes, void* stream) {
   if (!qa || !sa || !qb || !sb || (!c && !qout && !qcol))
     return fail(MXFP4_ERR_INVALID_ARG, "%s: NULL pointer", name);
   if (c_dtype != MXFP4_DTYPE_BF16 && c_dtype != MXFP4_DTYPE_F32)
@@ -196,9 +196,10 @@ mxfp4_status gemm_common(const char* name, const uint8_t* qa, const uint8_t* sa,
   if (!aligned16(qa) || !aligned16(qb) || !aligned16(sa) || !aligned16(sb) || !aligned16(c) ||
       (c && ldc % 8 != 0))
     return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");
+  if (ws && !aligned16(ws)) return fail(MXFP4_ERR_ALIGN, "%s: workspace must be 16-byte aligned", name);
   const char* why = "";
   cudaError_t e = mx::launch_gemm(qa, sa, qb, sb, M, N, K, c, c_dtype == MXFP4_DTYPE_BF16, ldc,
-                                  qout, qcol, static_cast<cudaStream_t>(stream), &why);
+                                  qout, qcol, ws, ws_bytes, static_cast<cudaStream_t>(stream), &why);
   if (e == cudaErrorNotSupported) return fail(MXFP4_ERR_UNSUPPORTED, "%s", why);
   if (e == cudaErrorInvalidValue && why[0]) return fail(MXFP4_ERR_ALIGN, "%s", why);
   return from_cuda(e, name);
@@ -210,15 +211,21 @@ mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         int64_t ldc, void* stream) {
   if (!c) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
   return gemm_common("mxfp4_gemm", qa, sa, qb, sb, M, N, K, c, MXFP4_DTYPE_F32, ldc, nullptr,
-                     nullptr, stream);
+                     nullptr, nullptr, 0, stream);
+}
+
+size_t mxfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t scale_block) {
+  if (M <= 0 || N <= 0 || K <= 0 || (scale_block != 32 && scale_block != 16)) return 0;
+  return (size_t)mx::workspace_bytes(M, N, K, scale_block == 16);
 }
 
 mxfp4_status mxfp4_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                            const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
-                           int32_t c_dtype, int64_t ldc, void* stream) {
+                           int32_t c_dtype, int64_t ldc, void* workspace, size_t workspace_bytes,
+                           void* stream) {
   if (!c) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
   return gemm_common("mxfp4_gemm_ex", qa, sa, qb, sb, M, N, K, c, c_dtype, ldc, nullptr, nullptr,
-                     stream);
+                     workspace, workspace_bytes, stream);
 }
 
 mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
@@ -245,7 +252,8 @@ mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
 
 mxfp4_status nvfp4_gemm(const uint8_t* qa, const uint8_t* sa, int32_t ka, const uint8_t* qb,
                         const uint8_t* sb, int32_t kb, int64_t M, int64_t N, int64_t K, void* c,
-                        int32_t c_dtype, int64_t ldc, void* stream) {
+                        int32_t c_dtype, int64_t ldc, void* workspace, size_t workspace_bytes,
+                        void* stream) {
   if (!qa || !sa || !qb || !sb || !c) return fail(MXFP4_ERR_INVALID_ARG, "nvfp4_gemm: NULL pointer");
   if (c_dtype != MXFP4_DTYPE_BF16 && c_dtype != MXFP4_DTYPE_F32)
     return fail(MXFP4_ERR_INVALID_ARG, "nvfp4_gemm: bad c_dtype %d", c_dtype);
@@ -259,9 +267,11 @@ mxfp4_status nvfp4_gemm(const uint8_t* qa, const uint8_t* sa, int32_t ka, const 
   if (ldc < N) return fail(MXFP4_ERR_SHAPE, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
   if (!aligned16(qa) || !aligned16(qb) || !aligned16(sa) || !aligned16(sb) || !aligned16(c) || ldc % 8 != 0)
     return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");
+  if (workspace && !aligned16(workspace))
+    return fail(MXFP4_ERR_ALIGN, "nvfp4_gemm: workspace must be 16-byte aligned");
   const char* why = "";
   cudaError_t e = mx::launch_gemm_nv(qa, sa, qb, sb, M, N, K, ldexpf(1.0f, ka + kb), c,
-                                     c_dtype == MXFP4_DTYPE_BF16, ldc,
+                                     c_dtype == MXFP4_DTYPE_BF16, ldc, workspace, workspace_bytes,
                                      static_cast<cudaStream_t>(stream), &why);
   if (e == cudaErrorNotSupported) return fail(MXFP4_ERR_UNSUPPORTED, "%s", why);
   if (e == cudaErrorInvalidValue && why[0]) return fail(MXFP4_ERR_ALIGN, "%s", why);
@@ -293,7 +303,7 @@ mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uin
     if (col && (st = check_params(col, q_col, s_col, N, M, "col", &co))) return st;
   }
   return gemm_common("mxfp4_gemm_quantize", qa, sa, qb, sb, M, N, K, c, c_dtype, ldc,
-                     row ? &ro : nullptr, col ? &co : nullptr, stream);
+                     row ? &ro : nullptr, col ? &co : nullptr, nullptr, 0, stream);
 }
 
 mxfp4_status hadamard32(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,

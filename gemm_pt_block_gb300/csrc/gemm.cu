@@ -469,6 +469,23 @@ constexpr int QC_STAGES = 5;
 constexpr int kXposeBytes = 32 * 33 * 4 + 32 * 17 * 4;     // 6400
 constexpr int QC_SMEM_BYTES = QC_STAGES * STAGE_BYTES + CTL_BYTES + NUM_EPI_WARPS * kXposeBytes + 1024;
 static_assert(QC_SMEM_BYTES <= 227 * 1024, "column-wise epilogue buffers");
+// Scale-image variants (kImg): the scales arrive as 4 KB images built by
+// scale_images_kernel -- two 512-byte tiles, interleaved by 8-row group and
+// replicated four times -- and each image goes to tensor memory with one
+// 128x256b copy (8 columns, the same layout the 32x128b.warpx4 copies of two
+// tiles give). MXFP4: one image of A and two of B per stage (three copies
+// instead of six), five 44 KB stages; NVFP4: two of A and four of B (six
+// instead of twelve), four 56 KB stages.
+constexpr int IMG_BYTES = 4096;
+constexpr int MXI_STAGES = 5;
+constexpr int MXI_STAGE_BYTES = A_BYTES + B_BYTES + 3 * IMG_BYTES;
+constexpr int MXI_SMEM_BYTES = MXI_STAGES * MXI_STAGE_BYTES + CTL_BYTES + 1024;
+constexpr int NVI_STAGES = 4;
+constexpr int NVI_STAGE_BYTES = A_BYTES + B_BYTES + 6 * IMG_BYTES;
+constexpr int NVI_SMEM_BYTES = NVI_STAGES * NVI_STAGE_BYTES + CTL_BYTES + 1024;
+static_assert(MXI_SMEM_BYTES <= 227 * 1024 && NVI_SMEM_BYTES <= 227 * 1024, "image stages");
+static_assert(MXI_STAGE_BYTES % 1024 == 0 && NVI_STAGE_BYTES % 1024 == 0, "image stage alignment");
+static_assert(NVI_STAGES <= STAGES && MXI_STAGES <= STAGES, "control block depth");
 
 // kind::mxf4nvf4 with E2M1 A and B (type code 1), K-major, UE4M3 scales (bit
 // 23 clear), scale_vec::4X (both scale-factor selectors 0).
@@ -501,7 +518,7 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
 // kQ: 0 plain; 1 C also quantized row-wise (qo); 2 row-wise (qo, if qo.q) and
 // column-wise (qc) -- five stages, the rest of shared memory holding each
 // epilogue warp's transposition buffers (kXposeBytes).
-template <int kQ, int kKind = kMxf4>
+template <int kQ, int kKind = kMxf4, bool kImg = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -509,9 +526,13 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                       float alpha, const __grid_constant__ OrientArgs qo,
                       const __grid_constant__ OrientArgs qc) {
   constexpr bool kF8 = kKind == kMxf8, kNv = kKind == kNvf4;
-  constexpr int kStages = kNv ? NV_STAGES : (kQ == 2 ? QC_STAGES : STAGES);
-  constexpr int kStageBytes = kNv ? NV_STAGE_BYTES : STAGE_BYTES;
-  constexpr int kSfaBytes = kNv ? 4 * 512 : SFA_BYTES;
+  static_assert(!kImg || (kQ == 0 && !kF8), "scale images serve the plain MXFP4 / NVFP4 GEMMs");
+  constexpr int kAImgs = kNv ? 2 : 1, kBImgs = kNv ? 4 : 2;   // images per stage
+  constexpr int kStages = kImg ? (kNv ? NVI_STAGES : MXI_STAGES)
+                               : (kNv ? NV_STAGES : (kQ == 2 ? QC_STAGES : STAGES));
+  constexpr int kStageBytes = kImg ? (kNv ? NVI_STAGE_BYTES : MXI_STAGE_BYTES)
+                                   : (kNv ? NV_STAGE_BYTES : STAGE_BYTES);
+  constexpr int kSfaBytes = kImg ? kAImgs * IMG_BYTES : (kNv ? 4 * 512 : SFA_BYTES);
   constexpr uint32_t kSfbCol = kNv ? SFB_COL_NV : SFB_COL;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -524,7 +545,9 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
   const int num_tiles = num_m * num_n;
   const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
   constexpr uint32_t kTx = kF8 ? 2u * (A_BYTES + B_BYTES + 512 + 1024)
-                               : (kNv ? 2u * kStageBytes : TX_BYTES);
+                               : ((kNv || kImg) ? 2u * kStageBytes : TX_BYTES);
+  // 512-byte scale tiles per 128-row band (image path): K/128, or K/64 for NVFP4
+  const int ntiles = kNv ? K / 64 : K / 128;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -572,9 +595,17 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
           const int kt = kF8 ? kb : (kNv ? 4 * kb : 2 * kb);   // first scale tile of the stage
           ptx::tma_load_2d_pair(st, &tmA, kb * BKB, a_row, full_leader);
           ptx::tma_load_2d_pair(st + A_BYTES, &tmB, kb * BKB, b_row, full_leader);
-          ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES, &tmSA, 0, kt, a_row / 128, full_leader);
-          ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES + kSfaBytes, &tmSB, 0, kt, nb * 2,
-                                full_leader);
+          if constexpr (kImg) {
+            // A images: band * ntiles/2 + tile pair; B images: band pair * ntiles + tile.
+            ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES, &tmSA, 0, 0,
+                                  (a_row / 128) * (ntiles / 2) + kAImgs * kb, full_leader);
+            ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES + kSfaBytes, &tmSB, 0, 0,
+                                  nb * ntiles + kBImgs * kb, full_leader);
+          } else {
+            ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES, &tmSA, 0, kt, a_row / 128, full_leader);
+            ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES + kSfaBytes, &tmSB, 0, kt, nb * 2,
+                                  full_leader);
+          }
           ++issued_rounds;
           if (++stage == kStages) {
             stage = 0;
@@ -603,11 +634,24 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
           const uint32_t st = ptx::smem_u32(smem + stage * kStageBytes);
           const uint32_t sfa_s = st + A_BYTES + B_BYTES;
           const uint32_t sfb_s = sfa_s + kSfaBytes;
+          if constexpr (kImg) {
+            // A image i (tiles 2i, 2i + 1) to SFA_COL + 8 i; B image i (both
+            // bands of tile i) to the B columns + 8 i: the columns the narrow
+            // copies below would fill.
+#pragma unroll
+            for (int i = 0; i < kAImgs; ++i)
+              ptx::tc_cp_pair_128x256b(tmem + SFA_COL + 8 * i,
+                                       ptx::smem_desc(sfa_s + i * IMG_BYTES, 128, 256, 0));
+#pragma unroll
+            for (int i = 0; i < kBImgs; ++i)
+              ptx::tc_cp_pair_128x256b(tmem + kSfbCol + 8 * i,
+                                       ptx::smem_desc(sfb_s + i * IMG_BYTES, 128, 256, 0));
+          }
           if constexpr (kNv) {
             // Four K tiles, one per MMA: A's tile k to SFA_COL + 4 k, B's band t
             // of tile k to kSfbCol + 8 k + 4 t; each MMA reads whole words.
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < 4 && !kImg; ++k) {
               ptx::tc_cp_pair_32x128b_warpx4(tmem + SFA_COL + 4 * k,
                                              ptx::smem_desc(sfa_s + k * 512, 0, 128, 0));
 #pragma unroll
@@ -639,7 +683,7 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < 2 && !kImg; ++c) {
               ptx::tc_cp_pair_32x128b_warpx4(tmem + SFA_COL + 4 * c,
                                              ptx::smem_desc(sfa_s + c * 512, 0, 128, 0));
 #pragma unroll
@@ -751,6 +795,68 @@ bool make_scale_map(CUtensorMap* m, const uint8_t* base, int64_t rows, int64_t K
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale images as a 3-D tensor of 32-bit words {256, 4, n images} (4 KB
+// each); a box covers `imgs` consecutive images.
+bool make_image_map(CUtensorMap* m, const uint8_t* base, int64_t nimg, uint32_t imgs) {
+  const cuuint64_t dims[3] = {256, 4, (cuuint64_t)nimg};
+  const cuuint64_t strides[2] = {1024, 4096};
+  const cuuint32_t box[3] = {256, 4, imgs};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Scale images for the kImg kernels, built from the standard tensor-core scale
+// layout (512-byte tile (band, tile) at (band * ntiles + tile) * 512). An image
+// is 4 KB: four identical 1 KB replicas, each [row group g (4)][chunk c (2)]
+// [row j (8)][16 bytes], chunk c's bytes for row 8 g + j being that row's 16
+// bytes in the chunk's tile -- the 128-row x 32-byte matrix a 128x256b copy
+// reads, row r of which carries tile row r % 32. A-role images pair two
+// consecutive tiles of one band (index band * ntiles / 2 + tile / 2); B-role
+// images pair two bands at one tile (index band pair * ntiles + tile). One
+// thread copies one 16-byte piece.
+__global__ void __launch_bounds__(256)
+scale_images_kernel(const uint8_t* __restrict__ sa, uint8_t* __restrict__ ia, int64_t na,
+                    const uint8_t* __restrict__ sb, uint8_t* __restrict__ ib, int64_t nb,
+                    int64_t ntiles) {
+  int64_t t = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  const bool bside = t >= na;
+  if (bside) t -= na;
+  if (bside && t >= nb) return;
+  const int64_t img = t >> 8;
+  const int w = (int)(t & 255), g = (w >> 4) & 3, c = (w >> 3) & 1, j = w & 7;
+  int64_t tile;
+  if (!bside) {
+    const int64_t per = ntiles / 2, band = img / per;
+    tile = band * ntiles + 2 * (img - band * per) + c;
+  } else {
+    const int64_t q = img / ntiles;
+    tile = (2 * q + c) * ntiles + (img - q * ntiles);
+  }
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>((bside ? sb : sa) + tile * 512 + (8 * g + j) * 16));
+  *reinterpret_cast<uint4*>((bside ? ib : ia) + t * 16) = v;
+}
+
+// Bytes of one operand's scale images (four times its scale bytes).
+int64_t image_bytes(int64_t rows, int64_t K, bool nv) { return 4 * rows * (nv ? K / 16 : K / 32); }
+
+// Builds A's and B's images in ws (A first) and encodes their tensor maps.
+bool prepare_images(const uint8_t* sa, int64_t M, const uint8_t* sb, int64_t N, int64_t K, bool nv,
+                    uint8_t* ws, CUtensorMap* tsa, CUtensorMap* tsb, cudaStream_t st) {
+  const int64_t ntiles = nv ? K / 64 : K / 128;
+  uint8_t* ia = ws;
+  uint8_t* ib = ws + image_bytes(M, K, nv);
+  if (!make_image_map(tsa, ia, (M / 128) * (ntiles / 2), nv ? 2 : 1) ||
+      !make_image_map(tsb, ib, (N / 256) * ntiles, nv ? 4 : 2))
+    return false;
+  const int64_t na = image_bytes(M, K, nv) / 16, nb = image_bytes(N, K, nv) / 16;
+  scale_images_kernel<<<(unsigned)((na + nb + 255) / 256), 256, 0, st>>>(sa, ia, na, sb, ib, nb,
+                                                                          ntiles);
+  return true;
+}
+
 struct DevInfo {
   int sms = 0;
   int major = 0;
@@ -780,6 +886,10 @@ DevInfo& dev_info(int dev) {
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
       cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<0, pair::kNvf4>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::NV_SMEM_BYTES);
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<0, pair::kMxf4, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, pair::MXI_SMEM_BYTES);
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<0, pair::kNvf4, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, pair::NVI_SMEM_BYTES);
     }
     d.attr_set = true;
   }
@@ -788,10 +898,14 @@ DevInfo& dev_info(int dev) {
 
 }  // namespace
 
+int64_t workspace_bytes(int64_t M, int64_t N, int64_t K, bool nv) {
+  return image_bytes(M, K, nv) + image_bytes(N, K, nv);
+}
+
 cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                         bool c_bf16, int64_t ldc, const OrientArgs* qout, const OrientArgs* qcol,
-                        cudaStream_t st, const char** why) {
+                        void* ws, size_t ws_bytes, cudaStream_t st, const char** why) {
   const OrientArgs none{};
   const OrientArgs& qo = qout ? *qout : none;
   const OrientArgs& qc = qcol ? *qcol : none;
@@ -816,8 +930,12 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   if (M % 256 == 0) {
     // CTA pairs: 256 x 256 tiles.
     CUtensorMap tsa, tsb;
+    const bool img = ws != nullptr && !qout && !qcol &&
+                     ws_bytes >= (size_t)(image_bytes(M, K, false) + image_bytes(N, K, false));
+    (void)cudaGetLastError();  // drop a stale error left by an earlier call
     if (!make_code_map(&ta, qa, M, K / 2, pair::BM) || !make_code_map(&tb, qb, N, K / 2, pair::BNH) ||
-        !make_scale_map(&tsa, sa, M, K, 1) || !make_scale_map(&tsb, sb, N, K, 2)) {
+        !(img ? prepare_images(sa, M, sb, N, K, false, static_cast<uint8_t*>(ws), &tsa, &tsb, st)
+              : (make_scale_map(&tsa, sa, M, K, 1) && make_scale_map(&tsb, sb, N, K, 2)))) {
       *why = "cuTensorMapEncodeTiled rejected the operand layout";
       return cudaErrorInvalidValue;
     }
@@ -826,8 +944,10 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
     const int grid = 2 * (num_tiles < pairs ? num_tiles : pairs);
     int64_t gm = kGroupBytes / (256 * (K / 2));
     gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
-    (void)cudaGetLastError();  // drop a stale error left by an earlier call
-    if (qcol)
+    if (img)
+      pair::mxf4_gemm_pair_kernel<0, pair::kMxf4, true><<<grid, THREADS, pair::MXI_SMEM_BYTES, st>>>(
+          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, qo, none);
+    else if (qcol)
       pair::mxf4_gemm_pair_kernel<2><<<grid, THREADS, pair::QC_SMEM_BYTES, st>>>(
           ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, qo, qc);
     else if (qout)
@@ -913,7 +1033,8 @@ cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
 
 cudaError_t launch_gemm_nv(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                            const uint8_t* sb, int64_t M, int64_t N, int64_t K, float alpha,
-                           void* c, bool c_bf16, int64_t ldc, cudaStream_t st, const char** why) {
+                           void* c, bool c_bf16, int64_t ldc, void* ws, size_t ws_bytes,
+                           cudaStream_t st, const char** why) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -928,8 +1049,12 @@ cudaError_t launch_gemm_nv(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
   }
   ensure_context();
   CUtensorMap ta, tb, tsa, tsb;
+  const bool img =
+      ws != nullptr && ws_bytes >= (size_t)(image_bytes(M, K, true) + image_bytes(N, K, true));
+  (void)cudaGetLastError();  // drop a stale error left by an earlier call
   if (!make_code_map(&ta, qa, M, K / 2, pair::BM) || !make_code_map(&tb, qb, N, K / 2, pair::BNH) ||
-      !make_scale_map(&tsa, sa, M, K, 1, 4, 64) || !make_scale_map(&tsb, sb, N, K, 2, 4, 64)) {
+      !(img ? prepare_images(sa, M, sb, N, K, true, static_cast<uint8_t*>(ws), &tsa, &tsb, st)
+            : (make_scale_map(&tsa, sa, M, K, 1, 4, 64) && make_scale_map(&tsb, sb, N, K, 2, 4, 64)))) {
     *why = "cuTensorMapEncodeTiled rejected the operand layout";
     return cudaErrorInvalidValue;
   }
@@ -939,9 +1064,12 @@ cudaError_t launch_gemm_nv(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
   int64_t gm = kGroupBytes / (256 * (K / 2));
   gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
   const OrientArgs none{};
-  (void)cudaGetLastError();  // drop a stale error left by an earlier call
-  pair::mxf4_gemm_pair_kernel<0, pair::kNvf4><<<grid, THREADS, pair::NV_SMEM_BYTES, st>>>(
-      ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, alpha, none, none);
+  if (img)
+    pair::mxf4_gemm_pair_kernel<0, pair::kNvf4, true><<<grid, THREADS, pair::NVI_SMEM_BYTES, st>>>(
+        ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, alpha, none, none);
+  else
+    pair::mxf4_gemm_pair_kernel<0, pair::kNvf4><<<grid, THREADS, pair::NV_SMEM_BYTES, st>>>(
+        ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, alpha, none, none);
   return cudaGetLastError();
 }
 

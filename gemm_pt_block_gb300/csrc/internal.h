@@ -43,11 +43,15 @@ cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t 
                               uint32_t sign_mask, bool inverse, float* y, cudaStream_t st);
 // qout / qcol: also quantize C row-wise / column-wise (C^T along M) in the
 // epilogue (nullptr: not produced; column-wise needs M % 256 == 0); with
-// either, c may be nullptr (no C output).
+// either, c may be nullptr (no C output). ws: optional workspace of ws_bytes;
+// when it holds workspace_bytes(M, N, K) and neither quantized output is
+// asked for, the CTA-pair GEMM reads its scales as replicated images built
+// there first (same results, fewer tensor-memory copies).
+int64_t workspace_bytes(int64_t M, int64_t N, int64_t K, bool nv);
 cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                         bool c_bf16, int64_t ldc, const OrientArgs* qout, const OrientArgs* qcol,
-                        cudaStream_t st, const char** why);
+                        void* ws, size_t ws_bytes, cudaStream_t st, const char** why);
 // Reads and clears the quantizer's device error word.
 cudaError_t read_quant_error(uint32_t* err);
 // Reads and clears the device error words (synchronizes st).
@@ -62,7 +66,8 @@ cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
 // of two; CTA pairs, M % 256 == 0, N % 256 == 0, K % 256 == 0.
 cudaError_t launch_gemm_nv(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                            const uint8_t* sb, int64_t M, int64_t N, int64_t K, float alpha,
-                           void* c, bool c_bf16, int64_t ldc, cudaStream_t st, const char** why);
+                           void* c, bool c_bf16, int64_t ldc, void* ws, size_t ws_bytes,
+                           cudaStream_t st, const char** why);
 // One-thread kernel whose bounded wait never completes (sets the error word).
 cudaError_t launch_wait_probe(cudaStream_t st);
 

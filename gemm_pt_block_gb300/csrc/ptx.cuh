@@ -211,6 +211,13 @@ __device__ __forceinline__ void tc_cp_pair_32x128b_warpx4(uint32_t taddr, uint64
                : "memory");
 }
 
+// 128 lanes x 256 bits (8 columns) from a 128-row x 32-byte shared-memory
+// matrix (no swizzle; descriptor strides give the layout), for a CTA pair.
+__device__ __forceinline__ void tc_cp_pair_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
 // ------------------------------------------------------------ tcgen05 ---
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),

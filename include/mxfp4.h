@@ -38,6 +38,7 @@
 #ifndef MXFP4_H
 #define MXFP4_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -198,13 +199,28 @@ mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         int64_t ldc, void* stream);
 
 /* mxfp4_gemm with a choice of output type ([News], para. 2: a bf16 C is what
- * the next layer reads): c_dtype MXFP4_DTYPE_F32 writes C as mxfp4_gemm does;
- * MXFP4_DTYPE_BF16 writes each fp32 sum rounded to bf16 (nearest-even), c a
- * bf16 [M, N] array with leading dimension ldc (ldc % 8 == 0, c 16-byte
- * aligned). Other c_dtype values return MXFP4_ERR_INVALID_ARG. */
+ * the next layer reads) and an optional workspace:
+ *  c_dtype  MXFP4_DTYPE_F32 writes C as mxfp4_gemm does; MXFP4_DTYPE_BF16
+ *           writes each fp32 sum rounded to bf16 (nearest-even), c a bf16
+ *           [M, N] array with leading dimension ldc (ldc % 8 == 0, c 16-byte
+ *           aligned). Other values return MXFP4_ERR_INVALID_ARG.
+ *  workspace, workspace_bytes  caller-owned device memory (16-byte aligned;
+ *           NULL or too small: not used). With at least
+ *           mxfp4_gemm_workspace_size(M, N, K, 32) bytes and M % 256 == 0,
+ *           the call first rewrites sa / sb there as replicated scale images
+ *           (four copies of each pair of 512-byte scale tiles) so that the
+ *           GEMM moves its scales into tensor memory with half as many
+ *           copies. The result is bit-identical either way; the workspace
+ *           contents are scratch (overwritten, not read back). */
 mxfp4_status mxfp4_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                            const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
-                           int32_t c_dtype, int64_t ldc, void* stream);
+                           int32_t c_dtype, int64_t ldc, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* Workspace bytes for mxfp4_gemm_ex (scale_block 32) or nvfp4_gemm
+ * (scale_block 16): four times the scale bytes of both operands,
+ * 4 * (M + N) * K / scale_block. 0 for non-positive sizes or another block. */
+size_t mxfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t scale_block);
 
 /* The MXFP8 counterpart of mxfp4_gemm ([TIBQ], "The fix, and its supporting
  * cast": MXFP8 for queries and keys): qa [M, K] and qb [N, K] E4M3 codes
@@ -223,11 +239,15 @@ mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
  * MXFP4_LAYOUT_MMA with K/16 scale columns (as mxfp4_quantize writes them for
  * MXFP4_BLOCK_1X16), ka / kb the operands' tensor_exp. fp32 accumulation; the
  * factor 2^(ka + kb) is applied exactly to the fp32 sums; C stored as c_dtype
- * (fp32, or bf16 nearest-even) with leading dimension ldc.
+ * (fp32, or bf16 nearest-even) with leading dimension ldc. workspace /
+ * workspace_bytes as in mxfp4_gemm_ex, sized by
+ * mxfp4_gemm_workspace_size(M, N, K, 16) (six copies per K step instead of
+ * twelve; bit-identical result).
  *  Shapes: M % 256 == 0, N % 256 == 0, K % 256 == 0; |ka + kb| <= 126. */
 mxfp4_status nvfp4_gemm(const uint8_t* qa, const uint8_t* sa, int32_t ka, const uint8_t* qb,
                         const uint8_t* sb, int32_t kb, int64_t M, int64_t N, int64_t K, void* c,
-                        int32_t c_dtype, int64_t ldc, void* stream);
+                        int32_t c_dtype, int64_t ldc, void* workspace, size_t workspace_bytes,
+                        void* stream);
 
 /* The same GEMM with the quantizer fused into its epilogue ([News], para. 2:
  * the rotation and rounding run where the producing GEMM writes its output).

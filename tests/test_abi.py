@@ -93,9 +93,15 @@ def test_host_side_validation(L):
     assert L.mxfp4_gemm(None, good, good, good, 128, 256, 256, good, 256, None) == 1
     assert L.mxfp4_gemm(good, good, good, good, 128, 256, 256, P((1 << 20) + 4), 256, None) == 3
     # bf16 / fp32 C selection
-    assert L.mxfp4_gemm_ex(good, good, good, good, 128, 256, 256, good, 2, 256, None) == 1
-    assert L.mxfp4_gemm_ex(good, good, good, good, 100, 256, 256, good, 0, 256, None) == 2
-    assert L.mxfp4_gemm_ex(good, good, good, good, 128, 256, 256, good, 0, 260, None) == 3
+    assert L.mxfp4_gemm_ex(good, good, good, good, 128, 256, 256, good, 2, 256, None, 0, None) == 1
+    assert L.mxfp4_gemm_ex(good, good, good, good, 100, 256, 256, good, 0, 256, None, 0, None) == 2
+    assert L.mxfp4_gemm_ex(good, good, good, good, 128, 256, 256, good, 0, 260, None, 0, None) == 3
+    # misaligned workspace
+    assert L.mxfp4_gemm_ex(good, good, good, good, 256, 256, 256, good, 0, 256, P((1 << 20) + 8),
+                           1 << 20, None) == 3
+    assert L.mxfp4_gemm_workspace_size(256, 512, 1024, 32) == 4 * (256 + 512) * 1024 // 32
+    assert L.mxfp4_gemm_workspace_size(256, 512, 1024, 16) == 4 * (256 + 512) * 1024 // 16
+    assert L.mxfp4_gemm_workspace_size(256, 512, 1024, 8) == 0
     assert L.mxfp8_gemm(good, good, good, good, 256, 256, 256, good, 3, 256, None) == 1
     assert L.mxfp8_gemm(good, good, good, good, 128, 256, 128, good, 0, 256, None) == 2
     # NVFP4: tensor_exp only with 1x16 blocks, in range; E2M1 elements only
@@ -105,9 +111,9 @@ def test_host_side_validation(L):
     assert L.mxfp4_quantize(good, 0, 32, 32, 32, ctypes.byref(pe), good, good, None, None, None, None) == 1
     pe = mx.QuantParams(block=mx.BLOCK_1X16, elem_format=mx.FORMAT_E4M3)._c()
     assert L.mxfp4_quantize(good, 0, 32, 32, 32, ctypes.byref(pe), good, good, None, None, None, None) == 4
-    assert L.nvfp4_gemm(good, good, 0, good, good, 0, 256, 256, 128, good, 1, 256, None) == 2
-    assert L.nvfp4_gemm(good, good, 100, good, good, 30, 256, 256, 256, good, 1, 256, None) == 1
-    assert L.nvfp4_gemm(good, good, 0, good, good, 0, 256, 256, 256, good, 7, 256, None) == 1
+    assert L.nvfp4_gemm(good, good, 0, good, good, 0, 256, 256, 128, good, 1, 256, None, 0, None) == 2
+    assert L.nvfp4_gemm(good, good, 100, good, good, 30, 256, 256, 256, good, 1, 256, None, 0, None) == 1
+    assert L.nvfp4_gemm(good, good, 0, good, good, 0, 256, 256, 256, good, 7, 256, None, 0, None) == 1
     pq = mx.QuantParams()._c()
     assert L.mxfp4_gemm_quantize(good, good, good, good, 128, 256, 256, good, 5, 256,
                                  ctypes.byref(pq), good, good, None, None, None, None) == 1

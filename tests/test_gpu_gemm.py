@@ -141,3 +141,48 @@ def test_gemm_full_size_sampled_rows(M, N, K):
     ns = np.tile(np.linspace(0, N - 1, 64).astype(np.int64), len(rows))
     ref, absref = oracle.gemm_pairs(qa, sa, qb, sb, M, N, K, ms, ns)
     gemm_tolerance_check(c[ms, ns], ref, absref)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (256, 512, 768), (512, 768, 2304),
+                                   (1024, 1280, 4096), (16384, 8192, 28672)])
+def test_gemm_scale_images_bit_identical(M, N, K):
+    """The workspace path (scales rewritten as replicated images, 128x256b
+    tensor-memory copies) gives the same bits as the plain entry point, for
+    fp32 and bf16 C; also against the oracle on sampled rows."""
+    import gemm_pt_block_gb300 as mx
+
+    g = torch.Generator(device=DEV).manual_seed(M + K)
+    qa = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=DEV, generator=g)
+    qb = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=DEV, generator=g)
+    sa = torch.randint(118, 137, (M * K // 32,), dtype=torch.uint8, device=DEV, generator=g)
+    sb = torch.randint(118, 137, (N * K // 32,), dtype=torch.uint8, device=DEV, generator=g)
+    ws = torch.full((mx.gemm_workspace_size(M, N, K),), 0xAB, dtype=torch.uint8, device=DEV)
+    plain = mx.mxfp4_gemm(qa, sa, qb, sb, M, N, K, workspace=False)
+    img = mx.mxfp4_gemm(qa, sa, qb, sb, M, N, K, workspace=ws)
+    img16 = mx.mxfp4_gemm(qa, sa, qb, sb, M, N, K, workspace=ws, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    assert torch.equal(plain, img)
+    assert torch.equal(img16.view(torch.int16), plain.to(torch.bfloat16).view(torch.int16))
+    rows = np.array([0, 1, 129, M // 2 + 3, M - 1])
+    ms = np.repeat(rows, 16)
+    ns = np.tile(np.linspace(0, N - 1, 16).astype(np.int64), len(rows))
+    ref, absref = oracle.gemm_pairs(qa.cpu().numpy(), sa.cpu().numpy(), qb.cpu().numpy(),
+                                    sb.cpu().numpy(), M, N, K, ms, ns)
+    gemm_tolerance_check(img[torch.from_numpy(ms), torch.from_numpy(ns)].cpu().numpy(), ref, absref)
+
+
+def test_gemm_workspace_too_small_falls_back():
+    import gemm_pt_block_gb300 as mx
+
+    M, N, K = 256, 512, 512
+    g = torch.Generator(device=DEV).manual_seed(3)
+    qa = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=DEV, generator=g)
+    qb = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=DEV, generator=g)
+    sa = torch.randint(120, 135, (M * K // 32,), dtype=torch.uint8, device=DEV, generator=g)
+    sb = torch.randint(120, 135, (N * K // 32,), dtype=torch.uint8, device=DEV, generator=g)
+    small = torch.empty(mx.gemm_workspace_size(M, N, K) - 16, dtype=torch.uint8, device=DEV)
+    a = mx.mxfp4_gemm(qa, sa, qb, sb, M, N, K, workspace=small)
+    b = mx.mxfp4_gemm(qa, sa, qb, sb, M, N, K, workspace=False)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)

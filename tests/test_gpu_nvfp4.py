@@ -297,3 +297,25 @@ def test_dequantize_ex_every_format(fmt, layout):
     got = mx.mxfp4_dequantize(*_dev(q, sd), rows, cols, params=p)
     torch.cuda.synchronize()
     assert np.array_equal(got.cpu().numpy().astype(np.float64), want)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (512, 768, 2304), (16384, 8192, 28672)])
+def test_nvfp4_gemm_scale_images_bit_identical(M, N, K):
+    """nvfp4_gemm's workspace path (six 128x256b copies per K step instead of
+    twelve) gives the same bits as without a workspace."""
+    import gemm_pt_block_gb300 as mx
+
+    g = torch.Generator(device=DEV).manual_seed(M + N + K)
+    qa = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=DEV, generator=g)
+    qb = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=DEV, generator=g)
+    sa = torch.randint(40, 70, (M * K // 16,), dtype=torch.uint8, device=DEV, generator=g)
+    sb = torch.randint(40, 70, (N * K // 16,), dtype=torch.uint8, device=DEV, generator=g)
+    plain = mx.nvfp4_gemm(qa, sa, -3, qb, sb, 2, M, N, K, workspace=False)
+    img = mx.nvfp4_gemm(qa, sa, -3, qb, sb, 2, M, N, K)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    assert torch.equal(plain, img)
+    if M <= 512:
+        ref, absref = oracle.gemm_ref_nv(qa.cpu().numpy(), sa.cpu().numpy(), -3, qb.cpu().numpy(),
+                                         sb.cpu().numpy(), 2, M, N, K)
+        gemm_tolerance_check(img.cpu().numpy(), ref, absref)
