@@ -40,6 +40,7 @@ from .binding import (  # noqa: F401
     lib_path,
     mxfp4_dequantize,
     mxfp4_gemm,
+    mxfp4_gemm_noalloc,
     mxfp4_gemm_quantize,
     mxfp8_gemm,
     gemm_workspace_size,

@@ -124,6 +124,8 @@ def lib() -> ctypes.CDLL:
         sz = ctypes.c_size_t
         L.mxfp4_gemm_ex.restype = i32
         L.mxfp4_gemm_ex.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P, sz, P]
+        L.mxfp4_gemm_noalloc.restype = i32
+        L.mxfp4_gemm_noalloc.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
         L.mxfp4_gemm_workspace_size.restype = sz
         L.mxfp4_gemm_workspace_size.argtypes = [i64, i64, i64, i32]
         L.nvfp4_gemm.restype = i32
@@ -290,6 +292,19 @@ def mxfp4_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.T
     ws, nbytes = _workspace(workspace, M, N, K, 32, qa.device)
     _check(lib().mxfp4_gemm_ex(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), cdt,
                                ldc, _ptr(ws), nbytes, _stream(qa, stream)))
+    return c
+
+
+def mxfp4_gemm_noalloc(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
+                       M: int, N: int, K: int, *, c=None, ldc: int | None = None, stream=None):
+    """mxfp4_gemm on the scale-image path with the library's static scratch
+    (no workspace, no allocation); fp32 C."""
+    _check_operands(qa, sa, qb, sb)
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=qa.device)
+    ldc = c.stride(0) if ldc is None else ldc
+    _check(lib().mxfp4_gemm_noalloc(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), ldc,
+                                    _stream(qa, stream)))
     return c
 
 

@@ -214,6 +214,22 @@ mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                      nullptr, nullptr, 0, stream);
 }
 
+mxfp4_status mxfp4_gemm_noalloc(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                                const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
+                                int64_t ldc, void* stream) {
+  if (!c) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
+  if (M > 0 && N > 0 && K > 0 &&
+      mx::workspace_bytes(M, N, K, false) > (int64_t)mx::kStaticScratchBytes)
+    return fail(MXFP4_ERR_SHAPE,
+                "mxfp4_gemm_noalloc: scale images of %lld x %lld x %lld exceed the static scratch (%zu bytes)",
+                (long long)M, (long long)N, (long long)K, mx::kStaticScratchBytes);
+  void* ws = nullptr;
+  const cudaError_t e = mx::static_scratch(&ws);
+  if (e != cudaSuccess) return from_cuda(e, "mxfp4_gemm_noalloc: static scratch");
+  return gemm_common("mxfp4_gemm_noalloc", qa, sa, qb, sb, M, N, K, c, MXFP4_DTYPE_F32, ldc, nullptr,
+                     nullptr, ws, mx::kStaticScratchBytes, stream);
+}
+
 size_t mxfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t scale_block) {
   if (M <= 0 || N <= 0 || K <= 0 || (scale_block != 32 && scale_block != 16)) return 0;
   return (size_t)mx::workspace_bytes(M, N, K, scale_block == 16);

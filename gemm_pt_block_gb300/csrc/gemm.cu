@@ -902,6 +902,26 @@ int64_t workspace_bytes(int64_t M, int64_t N, int64_t K, bool nv) {
   return image_bytes(M, K, nv) + image_bytes(N, K, nv);
 }
 
+// The library's own scratch for mxfp4_gemm_noalloc: a static device array (one
+// per device context, no run-time allocation), its address looked up once per
+// device.
+__device__ __align__(256) uint8_t g_gemm_scratch[kStaticScratchBytes];
+
+cudaError_t static_scratch(void** p) {
+  static void* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev & 63]) {
+    e = cudaGetSymbolAddress(&addr[dev & 63], g_gemm_scratch);
+    if (e != cudaSuccess) return e;
+  }
+  *p = addr[dev & 63];
+  return cudaSuccess;
+}
+
 cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                         bool c_bf16, int64_t ldc, const OrientArgs* qout, const OrientArgs* qcol,

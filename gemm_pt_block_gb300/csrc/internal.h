@@ -48,6 +48,9 @@ cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t 
 // asked for, the CTA-pair GEMM reads its scales as replicated images built
 // there first (same results, fewer tensor-memory copies).
 int64_t workspace_bytes(int64_t M, int64_t N, int64_t K, bool nv);
+// Size and address (this device) of the library's static GEMM scratch.
+constexpr size_t kStaticScratchBytes = 96ull << 20;
+cudaError_t static_scratch(void** p);
 cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                         bool c_bf16, int64_t ldc, const OrientArgs* qout, const OrientArgs* qcol,

@@ -217,6 +217,17 @@ mxfp4_status mxfp4_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
                            int32_t c_dtype, int64_t ldc, void* workspace, size_t workspace_bytes,
                            void* stream);
 
+/* mxfp4_gemm through the scale-image path of mxfp4_gemm_ex without a caller
+ * workspace and without any allocation: the images go to a static device array
+ * of the library (96 MiB per device, set up when the library is loaded).
+ * Shapes whose images exceed it (4 * (M + N) * K / 32 bytes > 96 MiB) return
+ * MXFP4_ERR_SHAPE. The array is shared by every call on a device, so calls on
+ * different streams must not run concurrently. Result bit-identical to
+ * mxfp4_gemm. */
+mxfp4_status mxfp4_gemm_noalloc(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                                const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
+                                int64_t ldc, void* stream);
+
 /* Workspace bytes for mxfp4_gemm_ex (scale_block 32) or nvfp4_gemm
  * (scale_block 16): four times the scale bytes of both operands,
  * 4 * (M + N) * K / scale_block. 0 for non-positive sizes or another block. */
