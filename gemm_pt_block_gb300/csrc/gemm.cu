@@ -842,6 +842,15 @@ scale_images_kernel(const uint8_t* __restrict__ sa, uint8_t* __restrict__ ia, in
 // Bytes of one operand's scale images (four times its scale bytes).
 int64_t image_bytes(int64_t rows, int64_t K, bool nv) { return 4 * rows * (nv ? K / 16 : K / 32); }
 
+// The image path needs image indices (TMA coordinates) and the pre-pass grid
+// within 32 bits.
+bool images_fit(int64_t M, int64_t N, int64_t K, bool nv) {
+  const int64_t ntiles = nv ? K / 64 : K / 128;
+  const int64_t pieces = (image_bytes(M, K, nv) + image_bytes(N, K, nv)) / 16;
+  return (M / 128) * (ntiles / 2) < (1ll << 31) && (N / 256) * ntiles < (1ll << 31) &&
+         (pieces + 255) / 256 < (1ll << 31);
+}
+
 // Builds A's and B's images in ws (A first) and encodes their tensor maps.
 bool prepare_images(const uint8_t* sa, int64_t M, const uint8_t* sb, int64_t N, int64_t K, bool nv,
                     uint8_t* ws, CUtensorMap* tsa, CUtensorMap* tsb, cudaStream_t st) {
@@ -950,7 +959,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   if (M % 256 == 0) {
     // CTA pairs: 256 x 256 tiles.
     CUtensorMap tsa, tsb;
-    const bool img = ws != nullptr && !qout && !qcol &&
+    const bool img = ws != nullptr && !qout && !qcol && images_fit(M, N, K, false) &&
                      ws_bytes >= (size_t)(image_bytes(M, K, false) + image_bytes(N, K, false));
     (void)cudaGetLastError();  // drop a stale error left by an earlier call
     if (!make_code_map(&ta, qa, M, K / 2, pair::BM) || !make_code_map(&tb, qb, N, K / 2, pair::BNH) ||
@@ -1069,8 +1078,8 @@ cudaError_t launch_gemm_nv(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
   }
   ensure_context();
   CUtensorMap ta, tb, tsa, tsb;
-  const bool img =
-      ws != nullptr && ws_bytes >= (size_t)(image_bytes(M, K, true) + image_bytes(N, K, true));
+  const bool img = ws != nullptr && images_fit(M, N, K, true) &&
+                   ws_bytes >= (size_t)(image_bytes(M, K, true) + image_bytes(N, K, true));
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
   if (!make_code_map(&ta, qa, M, K / 2, pair::BM) || !make_code_map(&tb, qb, N, K / 2, pair::BNH) ||
       !(img ? prepare_images(sa, M, sb, N, K, true, static_cast<uint8_t*>(ws), &tsa, &tsb, st)
