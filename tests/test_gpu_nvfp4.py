@@ -319,3 +319,34 @@ def test_nvfp4_gemm_scale_images_bit_identical(M, N, K):
         ref, absref = oracle.gemm_ref_nv(qa.cpu().numpy(), sa.cpu().numpy(), -3, qb.cpu().numpy(),
                                          sb.cpu().numpy(), 2, M, N, K)
         gemm_tolerance_check(img.cpu().numpy(), ref, absref)
+
+
+def test_nvfp4_edge_cases():
+    """Zeros (S = 0: signed-zero codes), a strided input, an empty tensor,
+    tiny values under a large factor, and values that saturate the scale at 448."""
+    import gemm_pt_block_gb300 as mx
+
+    def both(x, p):
+        got = gpu_quantize(x.to(DEV), p, p)
+        want = oracle_quantize(oracle_input(x), p, p)
+        assert_same(got, want, "nvfp4 edge")
+
+    for mode in SCALES:
+        z = torch.zeros(64, 96, dtype=torch.bfloat16)
+        z[3, :16] = -0.0
+        both(z, oracle.Params(block=oracle.BLOCK_1X16, scale_mode=mode))
+        tiny = synth.normal(64, 96, 1e-30, 61).float()
+        both(tiny, oracle.Params(block=oracle.BLOCK_1X16, scale_mode=mode, tensor_exp=40))
+        big = synth.normal(64, 96, 1e4, 62).float()
+        both(big, oracle.Params(block=oracle.BLOCK_1X16, scale_mode=mode, rounding=oracle.ROUND_SR,
+                                seed=2, tensor_exp=-3))        # scales saturate at 448
+    # strided input: a column slice of a wider tensor
+    wide = _input(64, 160, "bf16", seed=63)
+    view = wide.to(DEV)[:, 32:128]
+    p = oracle.Params(block=oracle.BLOCK_1X16, scale_mode=oracle.SCALE_ROUNDUP, tensor_exp=_k(wide))
+    got = gpu_quantize(view, p, p)
+    want = oracle_quantize(oracle_input(wide[:, 32:128].contiguous()), p, p)
+    assert_same(got, want, "nvfp4 strided")
+    e = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
+    q, s, _, _ = mx.mxfp4_quantize(e, cuda_params(oracle.Params(block=oracle.BLOCK_1X16), 0))
+    assert q.shape == (0, 32) and s.shape == (0, 4)
