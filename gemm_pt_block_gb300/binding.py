@@ -135,7 +135,7 @@ def lib() -> ctypes.CDLL:
         L.mxfp4_gemm_quantize.restype = i32
         L.mxfp4_gemm_quantize.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64,
                                           ctypes.POINTER(_CParams), P, P,
-                                          ctypes.POINTER(_CParams), P, P, P]
+                                          ctypes.POINTER(_CParams), P, P, P, sz, P]
         L.hadamard32.restype = i32
         L.hadamard32.argtypes = [P, i32, i64, i64, i64, ctypes.c_uint32, i32, P, P]
         L.mxfp4_status_string.restype = ctypes.c_char_p
@@ -344,7 +344,7 @@ def mxfp4_gemm_quantize(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb
                         M: int, N: int, K: int, out: QuantParams | None = None, *,
                         col: QuantParams | None = None, with_c: bool = False, c=None,
                         out_dtype: torch.dtype = torch.float32, q_out=None, s_out=None,
-                        q_col=None, s_col=None, stream=None):
+                        q_col=None, s_col=None, workspace=None, stream=None):
     """GEMM whose epilogue quantizes C: row-wise with `out` and/or column-wise
     (C^T along M) with `col`. Returns (q_out, s_out, c) when only `out` is
     given, else (q_out, s_out, q_col, s_col, c) (None for an orientation not
@@ -365,6 +365,7 @@ def mxfp4_gemm_quantize(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb
     ldc = c.stride(0) if c is not None else N
     op = out._c() if out is not None else None
     cp = col._c() if col is not None else None
+    ws, nbytes = _workspace(workspace if col is None else False, M, N, K, 32, qa.device)
     _check(lib().mxfp4_gemm_quantize(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K,
                                      _ptr(c) if c is not None else None, cdt, ldc,
                                      ctypes.byref(op) if op is not None else None,
@@ -373,7 +374,7 @@ def mxfp4_gemm_quantize(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb
                                      ctypes.byref(cp) if cp is not None else None,
                                      _ptr(q_col if col is not None else None),
                                      _ptr(s_col if col is not None else None),
-                                     _stream(qa, stream)))
+                                     _ptr(ws), nbytes, _stream(qa, stream)))
     if col is None:
         return q_out, s_out, c
     return (q_out if out is not None else None, s_out if out is not None else None,

@@ -298,7 +298,8 @@ mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uin
                                  const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                                  int32_t c_dtype, int64_t ldc, const mxfp4_quant_params* row,
                                  uint8_t* q_row, uint8_t* s_row, const mxfp4_quant_params* col,
-                                 uint8_t* q_col, uint8_t* s_col, void* stream) {
+                                 uint8_t* q_col, uint8_t* s_col, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
   if (!row && !col)
     return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_gemm_quantize: row or col params are required");
   for (const mxfp4_quant_params* p : {row, col}) {
@@ -319,7 +320,7 @@ mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uin
     if (col && (st = check_params(col, q_col, s_col, N, M, "col", &co))) return st;
   }
   return gemm_common("mxfp4_gemm_quantize", qa, sa, qb, sb, M, N, K, c, c_dtype, ldc,
-                     row ? &ro : nullptr, col ? &co : nullptr, nullptr, 0, stream);
+                     row ? &ro : nullptr, col ? &co : nullptr, workspace, workspace_bytes, stream);
 }
 
 mxfp4_status hadamard32(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,

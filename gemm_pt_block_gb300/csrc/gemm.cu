@@ -526,7 +526,8 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                       float alpha, const __grid_constant__ OrientArgs qo,
                       const __grid_constant__ OrientArgs qc) {
   constexpr bool kF8 = kKind == kMxf8, kNv = kKind == kNvf4;
-  static_assert(!kImg || (kQ == 0 && !kF8), "scale images serve the plain MXFP4 / NVFP4 GEMMs");
+  static_assert(!kImg || (kQ != 2 && !kF8), "scale images serve the MXFP4 / NVFP4 GEMMs "
+                                             "without the column-wise epilogue");
   constexpr int kAImgs = kNv ? 2 : 1, kBImgs = kNv ? 4 : 2;   // images per stage
   constexpr int kStages = kImg ? (kNv ? NVI_STAGES : MXI_STAGES)
                                : (kNv ? NV_STAGES : (kQ == 2 ? QC_STAGES : STAGES));
@@ -897,6 +898,8 @@ DevInfo& dev_info(int dev) {
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::NV_SMEM_BYTES);
       cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<0, pair::kMxf4, true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::MXI_SMEM_BYTES);
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<1, pair::kMxf4, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, pair::MXI_SMEM_BYTES);
       cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<0, pair::kNvf4, true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::NVI_SMEM_BYTES);
     }
@@ -959,7 +962,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   if (M % 256 == 0) {
     // CTA pairs: 256 x 256 tiles.
     CUtensorMap tsa, tsb;
-    const bool img = ws != nullptr && !qout && !qcol && images_fit(M, N, K, false) &&
+    const bool img = ws != nullptr && !qcol && images_fit(M, N, K, false) &&
                      ws_bytes >= (size_t)(image_bytes(M, K, false) + image_bytes(N, K, false));
     (void)cudaGetLastError();  // drop a stale error left by an earlier call
     if (!make_code_map(&ta, qa, M, K / 2, pair::BM) || !make_code_map(&tb, qb, N, K / 2, pair::BNH) ||
@@ -973,7 +976,10 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
     const int grid = 2 * (num_tiles < pairs ? num_tiles : pairs);
     int64_t gm = kGroupBytes / (256 * (K / 2));
     gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
-    if (img)
+    if (img && qout)
+      pair::mxf4_gemm_pair_kernel<1, pair::kMxf4, true><<<grid, THREADS, pair::MXI_SMEM_BYTES, st>>>(
+          ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, qo, none);
+    else if (img)
       pair::mxf4_gemm_pair_kernel<0, pair::kMxf4, true><<<grid, THREADS, pair::MXI_SMEM_BYTES, st>>>(
           ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, qo, none);
     else if (qcol)

@@ -44,9 +44,9 @@ cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t 
 // qout / qcol: also quantize C row-wise / column-wise (C^T along M) in the
 // epilogue (nullptr: not produced; column-wise needs M % 256 == 0); with
 // either, c may be nullptr (no C output). ws: optional workspace of ws_bytes;
-// when it holds workspace_bytes(M, N, K) and neither quantized output is
-// asked for, the CTA-pair GEMM reads its scales as replicated images built
-// there first (same results, fewer tensor-memory copies).
+// when it holds workspace_bytes(M, N, K) and no column-wise output is asked
+// for, the CTA-pair GEMM reads its scales as replicated images built there
+// first (same results, fewer tensor-memory copies).
 int64_t workspace_bytes(int64_t M, int64_t N, int64_t K, bool nv);
 // Size and address (this device) of the library's static GEMM scratch.
 constexpr size_t kStaticScratchBytes = 96ull << 20;

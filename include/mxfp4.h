@@ -276,13 +276,15 @@ mxfp4_status nvfp4_gemm(const uint8_t* qa, const uint8_t* sa, int32_t ka, const 
  * by the element index m * N + n of C in both orientations. The codes come
  * from the fp32 sums even when C itself is stored as bf16 (c_dtype as in
  * mxfp4_gemm_ex). c may be NULL: then no C is written (c_dtype and ldc are
- * ignored), which saves its HBM traffic.
+ * ignored), which saves its HBM traffic. workspace / workspace_bytes as in
+ * mxfp4_gemm_ex (used for row-wise-only outputs; same bits either way).
  *  Shapes as mxfp4_gemm. q_row / q_col must be 16-byte aligned. */
 mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                                  const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                                  int32_t c_dtype, int64_t ldc, const mxfp4_quant_params* row,
                                  uint8_t* q_row, uint8_t* s_row, const mxfp4_quant_params* col,
-                                 uint8_t* q_col, uint8_t* s_col, void* stream);
+                                 uint8_t* q_col, uint8_t* s_col, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /* Stand-alone 32-point block rotation along cols ([News], para. 2):
  *  forward (inverse == 0): y = c * H * diag(s) * x per 32-block;

@@ -116,15 +116,15 @@ def test_host_side_validation(L):
     assert L.nvfp4_gemm(good, good, 0, good, good, 0, 256, 256, 256, good, 7, 256, None, 0, None) == 1
     pq = mx.QuantParams()._c()
     assert L.mxfp4_gemm_quantize(good, good, good, good, 128, 256, 256, good, 5, 256,
-                                 ctypes.byref(pq), good, good, None, None, None, None) == 1
+                                 ctypes.byref(pq), good, good, None, None, None, None, 0, None) == 1
     pnv = mx.QuantParams(block=mx.BLOCK_1X16)._c()
     assert L.mxfp4_gemm_quantize(good, good, good, good, 128, 256, 256, good, 1, 256,
-                                 ctypes.byref(pnv), good, good, None, None, None, None) == 4
+                                 ctypes.byref(pnv), good, good, None, None, None, None, 0, None) == 4
     # no orientation; column-wise output with M % 256 != 0
     assert L.mxfp4_gemm_quantize(good, good, good, good, 256, 256, 256, good, 1, 256,
-                                 None, None, None, None, None, None, None) == 1
+                                 None, None, None, None, None, None, None, 0, None) == 1
     assert L.mxfp4_gemm_quantize(good, good, good, good, 128, 256, 256, good, 1, 256,
-                                 None, None, None, ctypes.byref(pq), good, good, None) == 4
+                                 None, None, None, ctypes.byref(pq), good, good, None, 0, None) == 4
     # dequantize / hadamard32
     assert L.mxfp4_dequantize(good, good, 1, 64, 128, good, None) == 2
     assert L.mxfp4_dequantize(good, good, 2, 64, 128, good, None) == 1

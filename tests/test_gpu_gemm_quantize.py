@@ -195,3 +195,19 @@ def test_fused_columns_full_size_sampled():
         oq, os_ = oracle.quantize_cols(cn, op, c0, c0 + 32)
         assert np.array_equal(q_c[c0:c0 + 32].cpu().numpy(), oq)
         assert np.array_equal(s_c[c0:c0 + 32].cpu().numpy(), os_)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (512, 768, 2304)])
+def test_fused_row_output_same_with_and_without_workspace(M, N, K):
+    """Row-wise fused output on the scale-image path (workspace) and the plain
+    path: identical codes, scales and C."""
+    import gemm_pt_block_gb300 as mx
+
+    p = mx.QuantParams(mx.BLOCK_32X32, mx.SCALE_ROUNDUP, mx.ROUND_SR, mx.LAYOUT_MMA, True, MASK, 8, 1)
+    *_, t = _operands(M, N, K, 5 * M + K)
+    a = mx.mxfp4_gemm_quantize(*t, M, N, K, p, with_c=True)
+    b = mx.mxfp4_gemm_quantize(*t, M, N, K, p, with_c=True, workspace=False)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
