@@ -315,7 +315,21 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t par, uint32
 // NVFP4: the lean structure with the 1x16 E4M3-scale step).
 enum : int { kLean = 0, kGeneral = 1, kNv = 2 };
 
-template <typename InT, int kVar>
+// kProf: 0 reads the rounding and rotation flags at run time; 1..3 fix them at
+// compile time for a dual-orientation lean call (both outputs requested, no
+// row-wise rotation):
+//   1: rows nearest, columns nearest without rotation (weights);
+//   2: rows nearest, columns stochastic with rotation (activations);
+//   3: rows stochastic, columns stochastic with rotation (output gradients).
+// The fixed variants give the compiler straight-line code (the same bits).
+template <int kProf>
+struct TileProfile {
+  static constexpr bool fixed = kProf != 0;
+  static constexpr bool row_sr = kProf == 3, row_wht = false;
+  static constexpr bool col_sr = kProf >= 2, col_wht = kProf >= 2;
+};
+
+template <typename InT, int kVar, int kProf = 0>
 __global__ void __launch_bounds__(kTileThreads, 3)
 quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols,
                   uint32_t ntiles, FastDiv tiles_x, const __grid_constant__ OrientArgs orow,
@@ -394,6 +408,12 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
 
     if constexpr (kVar != kGeneral) {
       constexpr bool nv = kVar == kNv;
+      using Pf = TileProfile<kProf>;
+      const bool drow = Pf::fixed || do_row, dcol = Pf::fixed || do_col;
+      const bool rsr = Pf::fixed ? Pf::row_sr : (bool)orow.sr;
+      const bool rwht = Pf::fixed ? Pf::row_wht : (bool)orow.wht;
+      const bool csr = Pf::fixed ? Pf::col_sr : (bool)ocol.sr;
+      const bool cwht = Pf::fixed ? Pf::col_wht : (bool)ocol.wht;
       // ---- phase 1: rows ----
       if (ok) {
         const int rl = 32 * (warp & 1) + lane, cl = 32 * (warp >> 1);
@@ -402,18 +422,18 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
         float2 R[16];
         read_run(st, rl, cl, R, InT());
         uint32_t w[16];
-        if (do_col && ocol.sr) {
+        if (dcol && csr) {
           draws32(ocol.keys, ocol.stream, (uint64_t)(r * cols + c), w);
   #pragma unroll
           for (int i = 0; i < 4; ++i)
             *reinterpret_cast<uint4*>(tb + tile_off(rl, cl + 8 * i, uint16_t())) =
                 make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
-        if (do_row) {
-          if (orow.wht) hadamard32_lane(R, orow.sign_mask);
+        if (drow) {
+          if (rwht) hadamard32_lane(R, orow.sign_mask);
           float M = nv ? 0.0f : absmax32(R);    // NVFP4 takes its two 16-block maxima itself
           if (!nv && orow.block) M = warp_max(M);
-          if (orow.sr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
+          if (rsr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
           const int e = scale_run32<false, nv>(R, orow, M, w);
           if (valid) {
             store_run32<false>(orow, r, c, cols, R);
@@ -423,8 +443,8 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
       }
 
       // ---- phase 2: columns (quantization of x^T along rows) ----
-      if (do_col) {
-        if (ocol.sr) named_sync_consumers();   // the draws were written by other warps
+      if (dcol) {
+        if (csr) named_sync_consumers();   // the draws were written by other warps
         if (ok) {
           const int cl = 32 * (warp & 1) + lane, rl = 32 * (warp >> 1);
           const int64_t oc = C0 + cl, k0 = R0 + rl;
@@ -433,11 +453,11 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           uint32_t o[8];
           col_offsets(rl, cl, o, InT());
           read_col(st, o, R, InT());
-          if (ocol.wht) hadamard32_lane(R, ocol.sign_mask);
+          if (cwht) hadamard32_lane(R, ocol.sign_mask);
           float M = nv ? 0.0f : absmax32(R);
           if (!nv && ocol.block) M = warp_max(M);
           uint32_t w[16];
-          if (ocol.sr) {
+          if (csr) {
             uint32_t ob[8];   // the draw buffer is laid out like a bf16 tile
             col_offsets(rl, cl, ob, uint16_t());
   #pragma unroll
@@ -666,6 +686,12 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaFuncSetAttribute(quant_tile_kernel<InT, kNv>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          smem);
+    cudaFuncSetAttribute(quant_tile_kernel<InT, kLean, 1>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(quant_tile_kernel<InT, kLean, 2>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(quant_tile_kernel<InT, kLean, 3>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     attr_set[dev & 63] = true;
   }
   OrientArgs dummy{};
@@ -678,6 +704,16 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
   auto kern = (is_lean(row) && is_lean(col)) ? quant_tile_kernel<InT, kLean>
               : (is_nv(row) && is_nv(col))   ? quant_tile_kernel<InT, kNv>
                                              : quant_tile_kernel<InT, kGeneral>;
+  // Dual-orientation lean calls whose rounding / rotation flags match a fixed
+  // profile take that profile's kernel.
+  if (row && col && is_lean(row) && is_lean(col) && !row->wht) {
+    if (!row->sr && !col->sr && !col->wht)
+      kern = quant_tile_kernel<InT, kLean, 1>;
+    else if (!row->sr && col->sr && col->wht)
+      kern = quant_tile_kernel<InT, kLean, 2>;
+    else if (row->sr && col->sr && col->wht)
+      kern = quant_tile_kernel<InT, kLean, 3>;
+  }
   const unsigned grid = resident_ctas(quant_tile_kernel<InT, kLean>, tx * ty, smem, kTileThreads);
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
   kern<<<grid, kTileThreads, smem, st>>>(

@@ -350,3 +350,28 @@ def test_mxfp8_every_bf16_value_and_mma_layout():
                 "mxfp8 mma")
     with pytest.raises(mx.Mxfp4Error):
         mx.mxfp4_quantize(xm.to(DEV), mx.QuantParams(rounding=mx.ROUND_SR, elem_format=mx.FORMAT_E4M3))
+
+
+PROFILES = {   # (row rounding, row rotation, column rounding, column rotation)
+    "weights": (oracle.ROUND_RTN, False, oracle.ROUND_RTN, False),
+    "activations": (oracle.ROUND_RTN, False, oracle.ROUND_SR, True),
+    "gradients": (oracle.ROUND_SR, False, oracle.ROUND_SR, True),
+}
+
+
+@pytest.mark.parametrize("profile", sorted(PROFILES))
+@pytest.mark.parametrize("block,scale", list(itertools.product(BLOCKS, SCALES)))
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("same_stream", [True, False])
+def test_quantize_dual_profiles(profile, block, scale, dtype, same_stream):
+    """The dual-orientation recipes that take compile-time kernel profiles
+    (weights, activations, output gradients), ragged 160 x 352, against the
+    oracle; with and without shared draws between the orientations."""
+    rr, rw, cr, cw = PROFILES[profile]
+    x = _input(160, 352, dtype, seed=131 + block)
+    prow = oracle.Params(block=block, scale_mode=scale, rounding=rr, wht=rw, seed=11, sr_stream=3)
+    pcol = oracle.Params(block=block, scale_mode=scale, rounding=cr, wht=cw, wht_sign_mask=0x0BADF00D,
+                         seed=11, sr_stream=3 if same_stream else 4)
+    got = gpu_quantize(x.to(DEV), prow, pcol)
+    want = oracle_quantize(oracle_input(x), prow, pcol)
+    assert_same(got, want, profile)
