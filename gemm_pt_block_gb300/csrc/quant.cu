@@ -316,8 +316,8 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t par, uint32
 enum : int { kLean = 0, kGeneral = 1, kNv = 2 };
 
 // kProf: 0 reads the rounding and rotation flags at run time; 1..3 fix them at
-// compile time for a dual-orientation lean call (both outputs requested, no
-// row-wise rotation):
+// compile time for a dual-orientation lean or NVFP4 call (both outputs
+// requested, no row-wise rotation):
 //   1: rows nearest, columns nearest without rotation (weights);
 //   2: rows nearest, columns stochastic with rotation (activations);
 //   3: rows stochastic, columns stochastic with rotation (output gradients).
@@ -692,6 +692,12 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaFuncSetAttribute(quant_tile_kernel<InT, kLean, 3>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(quant_tile_kernel<InT, kNv, 1>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(quant_tile_kernel<InT, kNv, 2>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(quant_tile_kernel<InT, kNv, 3>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     attr_set[dev & 63] = true;
   }
   OrientArgs dummy{};
@@ -704,15 +710,17 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
   auto kern = (is_lean(row) && is_lean(col)) ? quant_tile_kernel<InT, kLean>
               : (is_nv(row) && is_nv(col))   ? quant_tile_kernel<InT, kNv>
                                              : quant_tile_kernel<InT, kGeneral>;
-  // Dual-orientation lean calls whose rounding / rotation flags match a fixed
-  // profile take that profile's kernel.
-  if (row && col && is_lean(row) && is_lean(col) && !row->wht) {
-    if (!row->sr && !col->sr && !col->wht)
-      kern = quant_tile_kernel<InT, kLean, 1>;
-    else if (!row->sr && col->sr && col->wht)
-      kern = quant_tile_kernel<InT, kLean, 2>;
-    else if (row->sr && col->sr && col->wht)
-      kern = quant_tile_kernel<InT, kLean, 3>;
+  // Dual-orientation lean or NVFP4 calls whose rounding / rotation flags match
+  // a fixed profile take that profile's kernel.
+  const bool lean2 = row && col && is_lean(row) && is_lean(col);
+  const bool nv2 = row && col && row->nv && col->nv;
+  if ((lean2 || nv2) && !row->wht) {
+    const int prof = (!row->sr && !col->sr && !col->wht) ? 1
+                     : (!row->sr && col->sr && col->wht) ? 2
+                     : (row->sr && col->sr && col->wht)  ? 3 : 0;
+    if (prof == 1) kern = lean2 ? quant_tile_kernel<InT, kLean, 1> : quant_tile_kernel<InT, kNv, 1>;
+    if (prof == 2) kern = lean2 ? quant_tile_kernel<InT, kLean, 2> : quant_tile_kernel<InT, kNv, 2>;
+    if (prof == 3) kern = lean2 ? quant_tile_kernel<InT, kLean, 3> : quant_tile_kernel<InT, kNv, 3>;
   }
   const unsigned grid = resident_ctas(quant_tile_kernel<InT, kLean>, tx * ty, smem, kTileThreads);
   (void)cudaGetLastError();  // drop a stale error left by an earlier call

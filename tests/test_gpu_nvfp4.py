@@ -350,3 +350,20 @@ def test_nvfp4_edge_cases():
     e = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
     q, s, _, _ = mx.mxfp4_quantize(e, cuda_params(oracle.Params(block=oracle.BLOCK_1X16), 0))
     assert q.shape == (0, 32) and s.shape == (0, 4)
+
+
+@pytest.mark.parametrize("rows_sr", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_nvfp4_dual_profiles(rows_sr, dtype):
+    """NVFP4 dual calls with the activation / gradient recipes (rows without
+    rotation, columns stochastic with rotation): the compile-time profiles."""
+    x = _input(160, 352, dtype, seed=141)
+    k = _k(x)
+    prow = oracle.Params(block=oracle.BLOCK_1X16, scale_mode=oracle.SCALE_ROUNDUP,
+                         rounding=oracle.ROUND_SR if rows_sr else oracle.ROUND_RTN, seed=12,
+                         sr_stream=2, tensor_exp=k)
+    pcol = oracle.Params(block=oracle.BLOCK_1X16, scale_mode=oracle.SCALE_ROUNDUP,
+                         rounding=oracle.ROUND_SR, wht=True, wht_sign_mask=0x600DCAFE, seed=12,
+                         sr_stream=2, tensor_exp=k)
+    assert_same(gpu_quantize(x.to(DEV), prow, pcol), oracle_quantize(oracle_input(x), prow, pcol),
+                "nvfp4 profile")
