@@ -14,6 +14,7 @@
 // truncation-free scaling, stochastic rounding; "The aha: transposition
 // scrambles the blocks": both orientations of one tensor).
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "mx_device.cuh"
@@ -330,7 +331,7 @@ struct TileProfile {
 };
 
 template <typename InT, int kVar, int kProf = 0>
-__global__ void __launch_bounds__(kTileThreads, 3)
+__global__ void __launch_bounds__(kTileThreads, kProf == 1 ? 4 : 3)
 quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols,
                   uint32_t ntiles, FastDiv tiles_x, const __grid_constant__ OrientArgs orow,
                   const __grid_constant__ OrientArgs ocol, int do_row, int do_col) {
@@ -641,18 +642,33 @@ inline unsigned blocks_for(int64_t threads) { return (unsigned)((threads + kThre
 // and kernel), never more than there are work items.
 template <typename K>
 unsigned resident_ctas(K kernel, int64_t items, int smem, int threads) {
-  static int per_sm[64] = {0};
-  static int sms[64] = {0};
+  struct Entry {
+    const void* fn;
+    int dev, per_sm, sms;
+  };
+  static Entry cache[64];
+  static int used = 0;
+  static std::mutex mu;
   int dev = 0;
   cudaGetDevice(&dev);
-  dev &= 63;
-  if (!per_sm[dev]) {
-    cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    int n = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
-    per_sm[dev] = n > 0 ? n : 1;
+  const void* fn = reinterpret_cast<const void*>(kernel);
+  int per_sm = 0, sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].fn == fn && cache[i].dev == dev) {
+        per_sm = cache[i].per_sm;
+        sms = cache[i].sms;
+      }
+    if (!per_sm) {
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      int n = 0;
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
+      per_sm = n > 0 ? n : 1;
+      if (used < 64) cache[used++] = Entry{fn, dev, per_sm, sms};
+    }
   }
-  const int64_t want = (int64_t)per_sm[dev] * sms[dev];
+  const int64_t want = (int64_t)per_sm * sms;
   return (unsigned)(items < want ? items : want);
 }
 
@@ -722,7 +738,7 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
     if (prof == 2) kern = lean2 ? quant_tile_kernel<InT, kLean, 2> : quant_tile_kernel<InT, kNv, 2>;
     if (prof == 3) kern = lean2 ? quant_tile_kernel<InT, kLean, 3> : quant_tile_kernel<InT, kNv, 3>;
   }
-  const unsigned grid = resident_ctas(quant_tile_kernel<InT, kLean>, tx * ty, smem, kTileThreads);
+  const unsigned grid = resident_ctas(kern, tx * ty, smem, kTileThreads);
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
   kern<<<grid, kTileThreads, smem, st>>>(
       tm, rows, cols, (uint32_t)(tx * ty), make_fastdiv((uint32_t)tx), row ? *row : dummy,
