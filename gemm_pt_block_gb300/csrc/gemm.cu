@@ -874,10 +874,10 @@ struct DevInfo {
 };
 
 DevInfo& dev_info(int dev) {
-  static DevInfo info[64];
+  static DevInfo info[kMaxDevices];
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
-  DevInfo& d = info[dev & 63];
+  DevInfo& d = info[dev];
   if (!d.attr_set) {
     cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
@@ -920,17 +920,18 @@ int64_t workspace_bytes(int64_t M, int64_t N, int64_t K, bool nv) {
 __device__ __align__(256) uint8_t g_gemm_scratch[kStaticScratchBytes];
 
 cudaError_t static_scratch(void** p) {
-  static void* addr[64] = {nullptr};
+  static void* addr[kMaxDevices] = {nullptr};
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev & 63]) {
-    e = cudaGetSymbolAddress(&addr[dev & 63], g_gemm_scratch);
+  if (!addr[dev]) {
+    e = cudaGetSymbolAddress(&addr[dev], g_gemm_scratch);
     if (e != cudaSuccess) return e;
   }
-  *p = addr[dev & 63];
+  *p = addr[dev];
   return cudaSuccess;
 }
 
@@ -948,6 +949,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   DevInfo& d = dev_info(dev);
   if (d.major != 10) {
     *why = "tcgen05 block-scaled MMA needs an sm_100-family (GB300 sm_103) device";
@@ -1038,6 +1040,7 @@ cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   DevInfo& d = dev_info(dev);
   if (d.major != 10) {
     *why = "tcgen05 block-scaled MMA needs an sm_100-family (GB300 sm_103) device";
@@ -1073,6 +1076,7 @@ cudaError_t launch_gemm_nv(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   DevInfo& d = dev_info(dev);
   if (d.major != 10) {
     *why = "tcgen05 block-scaled MMA needs an sm_100-family (GB300 sm_103) device";

@@ -49,6 +49,9 @@ cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t 
 // first (same results, fewer tensor-memory copies).
 int64_t workspace_bytes(int64_t M, int64_t N, int64_t K, bool nv);
 // Size and address (this device) of the library's static GEMM scratch.
+// Per-device caches (attributes, scratch addresses) cover device ordinals
+// 0 .. kMaxDevices - 1; a call on a higher ordinal returns cudaErrorInvalidDevice.
+constexpr int kMaxDevices = 64;
 constexpr size_t kStaticScratchBytes = 96ull << 20;
 cudaError_t static_scratch(void** p);
 cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,

@@ -672,6 +672,29 @@ unsigned resident_ctas(K kernel, int64_t items, int smem, int threads) {
   return (unsigned)(items < want ? items : want);
 }
 
+// Opts every tile-kernel instantiation of one input type into `smem` bytes of
+// dynamic shared memory, once per device.
+template <typename InT>
+void set_tile_smem_once(int dev, int smem) {
+  static bool done[kMaxDevices] = {false};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return;
+  const void* kernels[] = {
+      reinterpret_cast<const void*>(quant_tile_kernel<InT, kLean>),
+      reinterpret_cast<const void*>(quant_tile_kernel<InT, kGeneral>),
+      reinterpret_cast<const void*>(quant_tile_kernel<InT, kNv>),
+      reinterpret_cast<const void*>(quant_tile_kernel<InT, kLean, 1>),
+      reinterpret_cast<const void*>(quant_tile_kernel<InT, kLean, 2>),
+      reinterpret_cast<const void*>(quant_tile_kernel<InT, kLean, 3>),
+      reinterpret_cast<const void*>(quant_tile_kernel<InT, kNv, 1>),
+      reinterpret_cast<const void*>(quant_tile_kernel<InT, kNv, 2>),
+      reinterpret_cast<const void*>(quant_tile_kernel<InT, kNv, 3>)};
+  for (const void* k : kernels)
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  done[dev] = true;
+}
+
 template <typename InT>
 cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
                           const OrientArgs* row, const OrientArgs* col, cudaStream_t st) {
@@ -692,30 +715,11 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
                    sizeof(InT), x, rows, cols, ld, kTile, bf ? 64 : 32))
     return cudaErrorInvalidValue;
   constexpr int smem = kStages * kTile * kTile * sizeof(InT) + 2 * kTile * kTile * 2 + 256 + 1024;
-  static bool attr_set[64] = {false};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (!attr_set[dev & 63]) {
-    cudaFuncSetAttribute(quant_tile_kernel<InT, kLean>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         smem);
-    cudaFuncSetAttribute(quant_tile_kernel<InT, kGeneral>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(quant_tile_kernel<InT, kNv>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         smem);
-    cudaFuncSetAttribute(quant_tile_kernel<InT, kLean, 1>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(quant_tile_kernel<InT, kLean, 2>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(quant_tile_kernel<InT, kLean, 3>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(quant_tile_kernel<InT, kNv, 1>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(quant_tile_kernel<InT, kNv, 2>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(quant_tile_kernel<InT, kNv, 3>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attr_set[dev & 63] = true;
-  }
+  const cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return de;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  set_tile_smem_once<InT>(dev, smem);
   OrientArgs dummy{};
   const int64_t tx = (cols + kTile - 1) / kTile, ty = (rows + kTile - 1) / kTile;
   // The lean variant covers 1x32 / 32x32 E2M1 outputs, the NVFP4 one outputs
