@@ -102,6 +102,9 @@ def test_host_side_validation(L):
     assert L.mxfp4_gemm_workspace_size(256, 512, 1024, 32) == 4 * (256 + 512) * 1024 // 32
     assert L.mxfp4_gemm_workspace_size(256, 512, 1024, 16) == 4 * (256 + 512) * 1024 // 16
     assert L.mxfp4_gemm_workspace_size(256, 512, 1024, 8) == 0
+    # the static-scratch GEMM: images above its 96 MiB are refused before any device call
+    assert L.mxfp4_gemm_noalloc(good, good, good, good, 16384, 16384, 32768, good, 16384, None) == 2
+    assert L.mxfp4_gemm_noalloc(good, good, good, good, 256, 256, 256, None, 256, None) == 1
     assert L.mxfp8_gemm(good, good, good, good, 256, 256, 256, good, 3, 256, None) == 1
     assert L.mxfp8_gemm(good, good, good, good, 128, 256, 128, good, 0, 256, None) == 2
     # NVFP4: tensor_exp only with 1x16 blocks, in range; E2M1 elements only
