@@ -11,7 +11,8 @@ MXFP4", Abstract: Fprop, Dgrad and Wgrad):
 
 Each tensor is quantized once per pass in both orientations it needs (TIBQ,
 "The aha: transposition scrambles the blocks"); the backward pass reuses the
-column-wise X and W codes written by the forward pass. Gradients flow through
+column-wise X and W codes written by the forward pass. An orientation whose
+product will not run (no gradient wanted for X or W) is not produced. Gradients flow through
 the quantizers unchanged (straight-through). Rotating the Wgrad operands
 along T with the same random-sign mask leaves dW's expectation unchanged,
 since c H diag(s) is orthogonal (Tseng, "Training LLMs with MXFP4",
@@ -90,8 +91,11 @@ class _Mxfp4LinearFn(torch.autograd.Function):
             r = replace(r, x_col=replace(r.x_col, seed=r.x_col.seed + step),
                         dy_row=replace(r.dy_row, seed=r.dy_row.seed + step),
                         dy_col=replace(r.dy_col, seed=r.dy_col.seed + step))
-        xq, xs, xqc, xsc = mxfp4_quantize(x, r.x_row, r.x_col)
-        wq, ws, wqc, wsc = mxfp4_quantize(w, r.w_row, r.w_col)
+        # Column-wise codes only for the backward products that will run:
+        # X^T feeds Wgrad (dW), W^T feeds Dgrad (dX).
+        need_dx, need_dw = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        xq, xs, xqc, xsc = mxfp4_quantize(x, r.x_row, r.x_col if need_dw else None)
+        wq, ws, wqc, wsc = mxfp4_quantize(w, r.w_row, r.w_col if need_dx else None)
         y = mxfp4_gemm(xq, xs, wq, ws, T, F, D, out_dtype=out_dtype)
         ctx.save_for_backward(xqc, xsc, wqc, wsc)
         ctx.recipe, ctx.dims, ctx.dtypes = r, (T, D, F), (x.dtype, w.dtype)
@@ -102,13 +106,15 @@ class _Mxfp4LinearFn(torch.autograd.Function):
         xqc, xsc, wqc, wsc = ctx.saved_tensors
         T, D, F = ctx.dims
         r = ctx.recipe
+        need_dx, need_dw = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
         dy = dy.contiguous()
-        gq, gs, gqc, gsc = mxfp4_quantize(dy, r.dy_row, r.dy_col)
+        # dY row-wise feeds Dgrad, dY column-wise Wgrad; each element's draw
+        # is keyed by its source index, so either one alone has the same bits.
+        gq, gs, gqc, gsc = mxfp4_quantize(dy, r.dy_row if need_dx else None,
+                                          r.dy_col if need_dw else None)
         xdt, wdt = ctx.dtypes
-        dx = (mxfp4_gemm(gq, gs, wqc, wsc, T, D, F, out_dtype=xdt)
-              if ctx.needs_input_grad[0] else None)
-        dw = (mxfp4_gemm(gqc, gsc, xqc, xsc, F, D, T, out_dtype=wdt)
-              if ctx.needs_input_grad[1] else None)
+        dx = mxfp4_gemm(gq, gs, wqc, wsc, T, D, F, out_dtype=xdt) if need_dx else None
+        dw = mxfp4_gemm(gqc, gsc, xqc, xsc, F, D, T, out_dtype=wdt) if need_dw else None
         return dx, dw, None, None, None
 
 

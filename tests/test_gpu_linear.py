@@ -138,3 +138,36 @@ def test_linear_bf16_output_and_direct_bf16_gradients():
     assert torch.equal(y16.view(torch.int16), y32.to(torch.bfloat16).view(torch.int16))
     assert torch.equal(dx16.view(torch.int16), dx32.view(torch.int16))
     assert torch.equal(dw16.view(torch.int16), dw32.view(torch.int16))
+
+
+def test_linear_partial_gradients_match_full_run():
+    """With only W (or only X) wanting a gradient, or none (no_grad), the layer
+    skips the orientations whose products do not run; Y and the gradients it
+    does compute are bit-identical to the run that computes everything."""
+    import gemm_pt_block_gb300 as mx
+
+    T, D, F = 256, 512, 768
+    r = mx.recipe_2d_sr(synth.sign_mask(91), seed=11)
+    x = synth.student_t(T, D, 4.0, 4500).to(DEV)
+    w = synth.normal(F, D, 0.02, 4501).to(DEV)
+    g = synth.laplace(T, F, 1e-3, 4502).float().to(DEV)
+
+    def run(gx, gw):
+        xd, wd = x.clone().requires_grad_(gx), w.clone().requires_grad_(gw)
+        y = mx.mxfp4_linear(xd, wd, r)
+        if gx or gw:
+            y.backward(g)
+        torch.cuda.synchronize()
+        return y.detach(), xd.grad, wd.grad
+
+    y, dx, dw = run(True, True)
+    y_w, dx_w, dw_w = run(False, True)
+    y_x, dx_x, dw_x = run(True, False)
+    with torch.no_grad():
+        y_n = mx.mxfp4_linear(x, w, r)
+    torch.cuda.synchronize()
+    assert dx_w is None and dw_x is None
+    for yy in (y_w, y_x, y_n):
+        assert torch.equal(yy, y)
+    assert torch.equal(dw_w, dw)
+    assert torch.equal(dx_x, dx)
