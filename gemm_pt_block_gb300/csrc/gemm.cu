@@ -140,36 +140,61 @@ __device__ __forceinline__ uint32_t bf16x2(uint32_t lo, uint32_t hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Lanes 2i and 2i + 1 of a warp hold rows r and r + 1 (r even). For one
+// 32-byte segment of both rows (byte offset seg of each row), lo and hi are
+// this lane's two 16-byte halves of its own row's segment. The pair swaps
+// halves (the even lane passes its row's upper half, the odd lane its lower
+// half) so that each of the two stores writes a whole 32-byte sector of one
+// row: first row r (even lane bytes 0-15, odd lane 16-31), then row r + 1.
+// A warp store then fills 16 sectors instead of half-filling 32.
+__device__ __forceinline__ void store_row_pair(uint8_t* rowa, uint8_t* rowb, int64_t seg, uint4 lo,
+                                               uint4 hi, int odd) {
+  uint4 g;
+  g.x = __shfl_xor_sync(0xffffffffu, odd ? lo.x : hi.x, 1);
+  g.y = __shfl_xor_sync(0xffffffffu, odd ? lo.y : hi.y, 1);
+  g.z = __shfl_xor_sync(0xffffffffu, odd ? lo.z : hi.z, 1);
+  g.w = __shfl_xor_sync(0xffffffffu, odd ? lo.w : hi.w, 1);
+  *reinterpret_cast<uint4*>(rowa + seg + 16 * odd) = odd ? g : lo;
+  *reinterpret_cast<uint4*>(rowb + seg + 16 * odd) = odd ? hi : g;
+}
+
 // One epilogue thread's results: 128 consecutive fp32 values of row `row`
-// (columns c0 .. c0 + 127). They are stored to C when C is given (fp32, or
-// bf16 rounded to nearest-even when c_bf16), and with kQ (and a row-wise
-// output requested) they are also quantized row-wise (four 32-runs) from the
-// fp32 values, exactly as the quantizer would quantize that row of an fp32 C.
+// (columns c0 .. c0 + 127); lane l of the warp holds row r + l of the warp's
+// 32 rows (r a multiple of 32). They are stored to C when C is given (fp32, or bf16 rounded to nearest-even when
+// c_bf16; adjacent lanes pair up so that every store fills whole sectors), and
+// with kQ (and a row-wise output requested) they are also quantized row-wise
+// (four 32-runs) from the fp32 values, exactly as the quantizer would quantize
+// that row of an fp32 C. All 32 lanes of the warp take part.
 template <bool kQ>
 __device__ __forceinline__ void epilogue_out(const uint32_t (&r0)[64], const uint32_t (&r1)[64],
                                              void* C, int c_bf16, int64_t ldc, int64_t row,
                                              int64_t c0, int64_t N, const OrientArgs& qo) {
   if (!kQ || C != nullptr) {
+    const int odd = threadIdx.x & 1;
+    const int64_t esz = c_bf16 ? 2 : 4;
+    uint8_t* rowa = reinterpret_cast<uint8_t*>(C) + ((row - odd) * ldc + c0) * esz;
+    uint8_t* rowb = rowa + ldc * esz;
     if (c_bf16) {
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(C) + row * ldc + c0);
+      // 16 bf16 values (32 bytes) per segment: columns 16 m .. 16 m + 15.
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        dst[j] = make_uint4(bf16x2(r0[8 * j], r0[8 * j + 1]), bf16x2(r0[8 * j + 2], r0[8 * j + 3]),
-                            bf16x2(r0[8 * j + 4], r0[8 * j + 5]), bf16x2(r0[8 * j + 6], r0[8 * j + 7]));
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        dst[8 + j] = make_uint4(bf16x2(r1[8 * j], r1[8 * j + 1]), bf16x2(r1[8 * j + 2], r1[8 * j + 3]),
-                                bf16x2(r1[8 * j + 4], r1[8 * j + 5]), bf16x2(r1[8 * j + 6], r1[8 * j + 7]));
+      for (int m = 0; m < 8; ++m) {
+        const uint32_t* r = m < 4 ? r0 : r1;
+        const int o = (m & 3) * 16;
+        const uint4 lo = make_uint4(bf16x2(r[o], r[o + 1]), bf16x2(r[o + 2], r[o + 3]),
+                                    bf16x2(r[o + 4], r[o + 5]), bf16x2(r[o + 6], r[o + 7]));
+        const uint4 hi = make_uint4(bf16x2(r[o + 8], r[o + 9]), bf16x2(r[o + 10], r[o + 11]),
+                                    bf16x2(r[o + 12], r[o + 13]), bf16x2(r[o + 14], r[o + 15]));
+        store_row_pair(rowa, rowb, 32 * m, lo, hi, odd);
+      }
     } else {
-      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(C) + row * ldc + c0);
+      // 8 fp32 values (32 bytes) per segment: columns 8 m .. 8 m + 7.
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        dst[j] = make_float4(__uint_as_float(r0[4 * j]), __uint_as_float(r0[4 * j + 1]),
-                             __uint_as_float(r0[4 * j + 2]), __uint_as_float(r0[4 * j + 3]));
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        dst[16 + j] = make_float4(__uint_as_float(r1[4 * j]), __uint_as_float(r1[4 * j + 1]),
-                                  __uint_as_float(r1[4 * j + 2]), __uint_as_float(r1[4 * j + 3]));
+      for (int m = 0; m < 16; ++m) {
+        const uint32_t* r = m < 8 ? r0 : r1;
+        const int o = (m & 7) * 8;
+        store_row_pair(rowa, rowb, 32 * m, make_uint4(r[o], r[o + 1], r[o + 2], r[o + 3]),
+                       make_uint4(r[o + 4], r[o + 5], r[o + 6], r[o + 7]), odd);
+      }
     }
   }
   if (kQ && qo.q != nullptr) {
