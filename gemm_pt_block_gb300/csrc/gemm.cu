@@ -160,11 +160,12 @@ __device__ __forceinline__ void store_row_pair(uint8_t* rowa, uint8_t* rowb, int
 
 // One epilogue thread's results: 128 consecutive fp32 values of row `row`
 // (columns c0 .. c0 + 127); lane l of the warp holds row r + l of the warp's
-// 32 rows (r a multiple of 32). They are stored to C when C is given (fp32, or bf16 rounded to nearest-even when
-// c_bf16; adjacent lanes pair up so that every store fills whole sectors), and
-// with kQ (and a row-wise output requested) they are also quantized row-wise
-// (four 32-runs) from the fp32 values, exactly as the quantizer would quantize
-// that row of an fp32 C. All 32 lanes of the warp take part.
+// 32 rows (r a multiple of 32). They are stored to C when C is given (fp32,
+// or bf16 rounded to nearest-even when c_bf16; adjacent lanes pair up so that
+// every store fills whole sectors), and with kQ (and a row-wise output
+// requested) they are also quantized row-wise (four 32-runs) from the fp32
+// values, exactly as the quantizer would quantize that row of an fp32 C. All
+// 32 lanes of the warp take part.
 template <bool kQ>
 __device__ __forceinline__ void epilogue_out(const uint32_t (&r0)[64], const uint32_t (&r1)[64],
                                              void* C, int c_bf16, int64_t ldc, int64_t row,
