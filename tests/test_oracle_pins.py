@@ -56,16 +56,69 @@ def test_philox_known_answers():
         assert oracle.philox4x32_10(w[0:4], w[4:6]) == w[6:10]
 
 
-def test_sr_bits_mapping_slices_philox_output():
-    """Element i draws 16 bits from Philox(counter=(i>>3, stream), key=seed)."""
-    seed, stream = 0x0123456789ABCDEF, 7
-    for i in [0, 1, 2, 7, 8, 9, 15, 16, 1023, (1 << 35) + 13]:
-        g = i >> 3
-        out = oracle.philox4x32_10([g & 0xFFFFFFFF, g >> 32, stream, 0],
-                                   [seed & 0xFFFFFFFF, seed >> 32])
-        w = out[(i >> 1) & 3]
-        want = (w >> 16) if (i & 1) else (w & 0xFFFF)
-        assert oracle.sr_bits(seed, stream, i) == want
+def test_sr_bits_known_answers():
+    """Draws of elements 0..7 (seed 0, stream 0) are the 16-bit halves of the
+    published Philox4x32-10 known answer for counter 0, key 0, low half first
+    (golden file); this fixes the half and output-word order of the mapping."""
+    rows = _read_rows("sr_bits_kat.txt")
+    assert len(rows) == 8
+    for seed, stream, i, want in rows:
+        assert oracle.sr_bits(int(seed), int(stream), int(i)) == int(want, 16), (seed, stream, i)
+
+
+def _curand_host():
+    import ctypes
+    import ctypes.util
+
+    cands = [os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64", "libcurand.so"),
+             ctypes.util.find_library("curand")]
+    for c in cands:
+        if c:
+            try:
+                return ctypes.CDLL(c)
+            except OSError:
+                pass
+    pytest.skip("cuRAND host library not found")
+
+
+def _curand_philox_words(L, seed: int, group: int, n_groups: int):
+    """cuRAND's host Philox4x32-10 generator (CURAND_RNG_PSEUDO_PHILOX4_32_10,
+    default ordering) started at word offset 4 * group: it emits the four
+    output words of one Philox call per group g, whose counter is
+    (g >> 16 as a 64-bit low/high word pair, g & 0xFFFF, 0) and whose key is
+    (seed low word, seed high word)."""
+    import ctypes
+
+    gen = ctypes.c_void_p()
+    assert L.curandCreateGeneratorHost(ctypes.byref(gen), 161) == 0
+    try:
+        assert L.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+        assert L.curandSetGeneratorOffset(gen, ctypes.c_ulonglong(4 * group)) == 0
+        buf = np.zeros(4 * n_groups, dtype=np.uint32)
+        assert L.curandGenerate(gen, ctypes.c_void_p(buf.ctypes.data), ctypes.c_size_t(buf.size)) == 0
+    finally:
+        L.curandDestroyGenerator(gen)
+    return buf.reshape(n_groups, 4)
+
+
+def test_sr_bits_counter_and_key_layout_against_curand():
+    """The draw of element i under (seed, stream) comes from the Philox call
+    with counter (i >> 3 as a low/high word pair, stream, 0) and key (seed low,
+    seed high). cuRAND's host Philox generator, a library implementation, emits
+    exactly that call's words for group g = (i >> 3) << 16 | stream, so every
+    16-bit draw must be a half of its word (i >> 1) & 3 -- low half for even i
+    (the known-answer test above fixes the halves). Covers both counter words,
+    a non-zero stream word and both key words."""
+    L = _curand_host()
+    for seed in (0x0123456789ABCDEF, 5):
+        for stream in (0, 1, 0xBEEF):
+            for c in (0, 1, 77, (1 << 32) + 9, (3 << 40) + 12345):
+                w = _curand_philox_words(L, seed, (c << 16) | stream, 1)[0]
+                for j in range(8):
+                    i = 8 * c + j
+                    word = int(w[j >> 1])
+                    want = (word >> 16) if (j & 1) else (word & 0xFFFF)
+                    assert oracle.sr_bits(seed, stream, i) == want, (seed, stream, i)
 
 
 def test_mma_scale_offsets_golden():
@@ -307,6 +360,36 @@ def test_32x32_blocks_are_transposition_invariant():
         assert np.array_equal(sr[::32, :], sc[::32, :].T)
         # one scale per 32x32 tile
         assert np.all(sr.reshape(4, 32, 3) == sr.reshape(4, 32, 3)[:, :1, :])
+
+
+def _nibbles(q: np.ndarray) -> np.ndarray:
+    """[R, C/2] packed codes -> [R, C] codes (even element in the low nibble)."""
+    out = np.empty((q.shape[0], 2 * q.shape[1]), dtype=np.uint8)
+    out[:, 0::2] = q & 0xF
+    out[:, 1::2] = q >> 4
+    return out
+
+
+@pytest.mark.parametrize("seed,stream", [(0, 0), (0x9E3779B97F4A7C15, 3)])
+def test_32x32_blocks_with_stochastic_rounding_are_transposition_invariant(seed, stream):
+    """2D blocks without rotation stay transposition-invariant under stochastic
+    rounding: the code of x^T element (c, r) in the column-wise output equals the
+    code of x element (r, c) in the row-wise output (same block, same scale, and
+    the same draw, because both orientations key it by the source index
+    r * cols + c), and block (j, i) of the column scales equals block (i, j) of
+    the row scales. A non-square tensor, so a draw keyed by the transposed
+    index would differ."""
+    x = _bf16(synth.laplace(160, 96, 1e-3, seed=37, outlier_frac=0.01))
+    for mode in [oracle.SCALE_FLOOR, oracle.SCALE_ROUNDUP]:
+        p = oracle.Params(block=oracle.BLOCK_32X32, scale_mode=mode, rounding=oracle.ROUND_SR,
+                          seed=seed, sr_stream=stream)
+        qr, sr = oracle.quantize_rows(x, p)
+        qc, sc = oracle.quantize_cols(x, p)
+        assert np.array_equal(_nibbles(qc), _nibbles(qr).T)
+        assert np.array_equal(sc[::32, :], sr[::32, :].T)
+        # the draws matter: nearest rounding gives other codes somewhere
+        qn, _ = oracle.quantize_rows(x, oracle.Params(block=oracle.BLOCK_32X32, scale_mode=mode))
+        assert not np.array_equal(qn, qr)
 
 
 @pytest.mark.parametrize("mode", [oracle.SCALE_FLOOR, oracle.SCALE_ROUNDUP])
