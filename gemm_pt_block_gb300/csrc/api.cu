@@ -118,8 +118,10 @@ mxfp4_status mxfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int64_
   if (!row && !col) return fail(MXFP4_ERR_INVALID_ARG, "at least one of row / col params is required");
   mxfp4_status st = check_input(x, x_dtype, rows, cols, ld_x);
   if (st) return st;
-  if (rows > 0 && cols / 16 > (int64_t)0xFFFFFFFF / rows)
-    return fail(MXFP4_ERR_SHAPE, "tensor too large: rows * cols / 16 must be below 2^32");
+  // The row kernel counts 16-element units in 32 bits: units < 2^31 plus a
+  // grid stride < 2^31 keeps every index it forms below 2^32.
+  if (rows > 0 && cols / 16 > (int64_t)0x7FFFFFFF / rows)
+    return fail(MXFP4_ERR_SHAPE, "tensor too large: rows * cols / 16 must be below 2^31");
   const bool need_rows32 =
       col || (row && row->block != MXFP4_BLOCK_1X32 && row->block != MXFP4_BLOCK_1X16);
   if (need_rows32 && rows % 32 != 0)
@@ -179,6 +181,16 @@ mxfp4_status mxfp4_dequantize_ex(const uint8_t* q, const uint8_t* s, int32_t sca
 }
 
 namespace {
+// Shape rules of the MXFP4 GEMM entry points.
+mxfp4_status gemm_shape(const char* name, int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0)
+    return fail(MXFP4_ERR_SHAPE, "%s needs M %% 128 == 0, N %% 256 == 0, K %% 256 == 0 (got %lld, %lld, %lld)",
+                name, (long long)M, (long long)N, (long long)K);
+  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30) || (M / 128) * (N / 256) > (1ll << 30))
+    return fail(MXFP4_ERR_SHAPE, "%s dimensions too large", name);
+  return MXFP4_OK;
+}
+
 mxfp4_status gemm_common(const char* name, const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                          const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                          int32_t c_dtype, int64_t ldc, const mx::OrientArgs* qout,
@@ -187,11 +199,7 @@ mxfp4_status gemm_common(const char* name, const uint8_t* qa, const uint8_t* sa,
     return fail(MXFP4_ERR_INVALID_ARG, "%s: NULL pointer", name);
   if (c_dtype != MXFP4_DTYPE_BF16 && c_dtype != MXFP4_DTYPE_F32)
     return fail(MXFP4_ERR_INVALID_ARG, "%s: bad c_dtype %d", name, c_dtype);
-  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0)
-    return fail(MXFP4_ERR_SHAPE, "%s needs M %% 128 == 0, N %% 256 == 0, K %% 256 == 0 (got %lld, %lld, %lld)",
-                name, (long long)M, (long long)N, (long long)K);
-  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30) || (M / 128) * (N / 256) > (1ll << 30))
-    return fail(MXFP4_ERR_SHAPE, "%s dimensions too large", name);
+  if (mxfp4_status st = gemm_shape(name, M, N, K)) return st;
   if (c && ldc < N) return fail(MXFP4_ERR_SHAPE, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
   if (!aligned16(qa) || !aligned16(qb) || !aligned16(sa) || !aligned16(sb) || !aligned16(c) ||
       (c && ldc % 8 != 0))
@@ -218,8 +226,10 @@ mxfp4_status mxfp4_gemm_noalloc(const uint8_t* qa, const uint8_t* sa, const uint
                                 const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
                                 int64_t ldc, void* stream) {
   if (!c) return fail(MXFP4_ERR_INVALID_ARG, "NULL pointer");
-  if (M > 0 && N > 0 && K > 0 &&
-      mx::workspace_bytes(M, N, K, false) > (int64_t)mx::kStaticScratchBytes)
+  if (mxfp4_status st = gemm_shape("mxfp4_gemm_noalloc", M, N, K)) return st;
+  // Only the CTA-pair kernel (M % 256 == 0) reads scale images; the dimensions
+  // are validated above, so the image size cannot overflow.
+  if (M % 256 == 0 && mx::workspace_bytes(M, N, K, false) > (int64_t)mx::kStaticScratchBytes)
     return fail(MXFP4_ERR_SHAPE,
                 "mxfp4_gemm_noalloc: scale images of %lld x %lld x %lld exceed the static scratch (%zu bytes)",
                 (long long)M, (long long)N, (long long)K, mx::kStaticScratchBytes);

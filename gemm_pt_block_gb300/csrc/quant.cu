@@ -153,7 +153,8 @@ __device__ __forceinline__ uint2 quantize_halves(float2 (&R)[8], int upper, cons
 // 32-element block. Persistent grid-stride loop over `total` units (warp-
 // uniform trip count, so the pair shuffles always see both lanes), with the
 // next unit's input prefetched into registers while the current one is
-// processed.
+// processed. The host keeps total < 2^31 and the stride (grid * kThreads)
+// below 2^31, so base + stride and u + stride never wrap in 32 bits.
 template <typename InT>
 __global__ void __launch_bounds__(kThreads)
 quant_rows_1x32_kernel(const InT* __restrict__ x, uint32_t total, FastDiv halves, int64_t cols,
@@ -704,6 +705,7 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
     const int64_t total = rows * (cols >> 4);
     const unsigned grid =
         resident_ctas(quant_rows_1x32_kernel<InT>, (total + kThreads - 1) / kThreads, 0, kThreads);
+    if (total >= (1ll << 31) || (int64_t)grid * kThreads >= (1ll << 31)) return cudaErrorInvalidValue;
     (void)cudaGetLastError();  // drop a stale error left by an earlier call
     quant_rows_1x32_kernel<InT><<<grid, kThreads, 0, st>>>(
         x, (uint32_t)total, make_fastdiv((uint32_t)(cols >> 4)), cols, ld, *row);

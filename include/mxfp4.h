@@ -145,7 +145,8 @@ typedef struct {
  *  At least one of row / col must be non-NULL.
  *  Shapes: cols % 32 == 0; rows % 32 == 0 when col != NULL or either
  *  orientation uses 32x32 or 64x64 blocks; MMA scale layout needs the
- *  output's row count % 128 == 0 and its K % 128 == 0. Else MXFP4_ERR_SHAPE.
+ *  output's row count % 128 == 0 and its K % 128 == 0; rows * cols < 2^35
+ *  (rows * cols / 16 below 2^31). Else MXFP4_ERR_SHAPE.
  *  With MXFP4_BLOCK_1X16 the scale arrays are s_row [rows, cols/16] and
  *  s_col [cols, rows/16].
  *  With elem_format MXFP4_FORMAT_E4M3 the codes take one byte per element
@@ -217,13 +218,27 @@ mxfp4_status mxfp4_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
                            int32_t c_dtype, int64_t ldc, void* workspace, size_t workspace_bytes,
                            void* stream);
 
-/* mxfp4_gemm through the scale-image path of mxfp4_gemm_ex without a caller
- * workspace and without any allocation: the images go to a static device array
- * of the library (96 MiB per device, set up when the library is loaded).
- * Shapes whose images exceed it (4 * (M + N) * K / 32 bytes > 96 MiB) return
- * MXFP4_ERR_SHAPE. The array is shared by every call on a device, so calls on
- * different streams must not run concurrently. Result bit-identical to
- * mxfp4_gemm. */
+/* mxfp4_gemm for callers that cannot allocate device memory: code that runs
+ * where cudaMalloc is off limits: a framework that owns all device memory
+ * through its own pool, a host loop with latency bounds that must not wait on
+ * the driver's allocator, a plugin that is handed only its inputs and
+ * outputs. The pages have no counterpart: this is a property of the library,
+ * not of the method.
+ * It runs the scale-image path of mxfp4_gemm_ex with the workspace taken from
+ * a static device array of the library, 96 MiB, which every GPU that loads
+ * the library holds until the process exits. The call allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *  - The first call on a device looks up that device's address of the array
+ *    (cudaGetSymbolAddress, with the device current); make that first call
+ *    before any stream capture on the device.
+ *  - The array holds the scale images of the last call. Every call rewrites
+ *    all of the bytes it reads, so nothing needs clearing, but calls whose
+ *    GEMMs overlap on the GPU (different streams, or different host threads
+ *    on one device) race on the array and must be serialised by the caller.
+ *  - Shapes as mxfp4_gemm. With M % 256 == 0 the images take
+ *    4 * (M + N) * K / 32 bytes; above 96 MiB the call returns
+ *    MXFP4_ERR_SHAPE before touching the device (M % 256 == 128 uses no images).
+ *  - C is bit-identical to mxfp4_gemm's. */
 mxfp4_status mxfp4_gemm_noalloc(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                                 const uint8_t* sb, int64_t M, int64_t N, int64_t K, float* c,
                                 int64_t ldc, void* stream);

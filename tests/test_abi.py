@@ -80,6 +80,12 @@ def test_host_side_validation(L):
     # reserved field
     bad = _CParams(0, 0, 0, 0, 0, 0, 0, 0, 7)
     assert L.mxfp4_quantize(good, 0, 32, 32, 32, ctypes.byref(bad), good, good, None, None, None, None) == 1
+    # size limit of the 32-bit unit counter: rows * cols / 16 must stay below 2^31
+    assert L.mxfp4_quantize(good, 0, 65536, 524288, 524288, ctypes.byref(p), good, good,
+                            None, None, None, None) == 2
+    assert b"2^31" in L.mxfp4_last_error()
+    assert L.mxfp4_quantize(good, 0, 1 << 22, 1 << 17, 1 << 17, ctypes.byref(p), good, good,
+                            None, None, None, None) == 2
     # column output needs rows % 32
     assert L.mxfp4_quantize(good, 0, 48, 32, 32, None, None, None, ctypes.byref(p), good, good, None) == 2
     # tensor-core scale layout needs 128-row tiles
@@ -105,6 +111,13 @@ def test_host_side_validation(L):
     # the static-scratch GEMM: images above its 96 MiB are refused before any device call
     assert L.mxfp4_gemm_noalloc(good, good, good, good, 16384, 16384, 32768, good, 16384, None) == 2
     assert L.mxfp4_gemm_noalloc(good, good, good, good, 256, 256, 256, None, 256, None) == 1
+    assert L.mxfp4_gemm_noalloc(good, good, good, good, 12288, 12288, 32768 + 256, good, 12288,
+                                None) == 2
+    # dimensions are validated before the image size is formed (no overflow)
+    assert L.mxfp4_gemm_noalloc(good, good, good, good, 1 << 62, 1 << 62, 1 << 62, good, 1 << 62,
+                                None) == 2
+    assert b"too large" in L.mxfp4_last_error()
+    assert L.mxfp4_gemm_noalloc(good, good, good, good, 256, 384, 256, good, 384, None) == 2
     assert L.mxfp8_gemm(good, good, good, good, 256, 256, 256, good, 3, 256, None) == 1
     assert L.mxfp8_gemm(good, good, good, good, 128, 256, 128, good, 0, 256, None) == 2
     # NVFP4: tensor_exp only with 1x16 blocks, in range; E2M1 elements only
