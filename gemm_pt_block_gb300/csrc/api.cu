@@ -183,10 +183,10 @@ mxfp4_status mxfp4_dequantize_ex(const uint8_t* q, const uint8_t* s, int32_t sca
 namespace {
 // Shape rules of the MXFP4 GEMM entry points.
 mxfp4_status gemm_shape(const char* name, int64_t M, int64_t N, int64_t K) {
-  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0)
-    return fail(MXFP4_ERR_SHAPE, "%s needs M %% 128 == 0, N %% 256 == 0, K %% 256 == 0 (got %lld, %lld, %lld)",
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 128 != 0 || K % 128 != 0)
+    return fail(MXFP4_ERR_SHAPE, "%s needs M, N, K positive multiples of 128 (got %lld, %lld, %lld)",
                 name, (long long)M, (long long)N, (long long)K);
-  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30) || (M / 128) * (N / 256) > (1ll << 30))
+  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30) || (M / 128) * (N / 128) > (1ll << 30))
     return fail(MXFP4_ERR_SHAPE, "%s dimensions too large", name);
   return MXFP4_OK;
 }

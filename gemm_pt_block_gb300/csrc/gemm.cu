@@ -304,9 +304,16 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                                              ~static_cast<uintptr_t>(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_m = M / BM, num_n = N / BN, num_k = K / BK;
+  // N and K are multiples of 128: the last N tile may hold only 128 valid
+  // columns (B rows past N arrive zero-filled, their scales are not loaded and
+  // those columns are not stored) and the last K step only 128 valid K (its
+  // second half of the codes arrives zero-filled, its scale tiles are not
+  // loaded and its last two MMAs are not issued).
+  const int num_m = M / BM, num_n = (N + BN - 1) / BN, num_k = (K + BK - 1) / BK;
   const int num_tiles = num_m * num_n;
   const int64_t ktiles = K / 128;  // 512-byte scale tiles per 128-row band
+  const int64_t nbands = N / 128;  // 128-row bands of B
+  const bool k_half = (K % BK) != 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -346,15 +353,18 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           const uint32_t full = ptx::smem_u32(&ctl->full[stage]);
           if (!(ok = wait_bar(empty, phase ^ 1u, ctl))) break;
           const uint32_t st = ptx::smem_u32(smem + stage * STAGE_BYTES);
-          ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+          // A half K step (the last one when K % 256 == 128) takes one scale
+          // tile per band; a half N tile one band of B scales.
+          const uint32_t sf_bytes = (k_half && kb == num_k - 1) ? 512u : 1024u;
+          const int b_bands = 2 * nb + 1 < nbands ? 2 : 1;
+          ptx::mbar_arrive_expect_tx(full, A_BYTES + B_BYTES + sf_bytes * (1 + b_bands));
           ptx::tma_load_2d(st, &tmA, kb * BKB, mb * BM, full);
           ptx::tma_load_2d(st + A_BYTES, &tmB, kb * BKB, nb * BN, full);
           ptx::bulk_load(st + A_BYTES + B_BYTES, sa + ((int64_t)mb * ktiles + 2 * kb) * 512,
-                         SFA_BYTES, full);
-#pragma unroll
-          for (int t = 0; t < 2; ++t)
+                         sf_bytes, full);
+          for (int t = 0; t < b_bands; ++t)
             ptx::bulk_load(st + A_BYTES + B_BYTES + SFA_BYTES + t * 1024,
-                           sb + ((int64_t)(2 * nb + t) * ktiles + 2 * kb) * 512, 1024, full);
+                           sb + ((int64_t)(2 * nb + t) * ktiles + 2 * kb) * 512, sf_bytes, full);
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -395,8 +405,8 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
               ptx::tc_cp_32x128b_warpx4(tmem + SFB_COL + 8 * c + 4 * t,
                                         ptx::smem_desc(sfb_s + t * 1024 + c * 512, 0, 128, 0));
           }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          const int kmma = (k_half && kb == num_k - 1) ? 2 : 4;   // MMAs of K = 64
+          for (int k = 0; k < kmma; ++k) {
             const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
             const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
             ptx::mma_mxf4(tmem + ACC_COL, ad, bd, make_idesc((k & 1) * 2),
@@ -441,7 +451,8 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctl->acc_empty));
       acc_phase ^= 1u;
       const int64_t row = (int64_t)mb * BM + q * 32 + lane;
-      epilogue_out<kQ>(r0, r1, C, c_bf16, ldc, row, (int64_t)nb * BN + h * 128, N, qo);
+      const int64_t col0 = (int64_t)nb * BN + h * 128;
+      if (col0 < N) epilogue_out<kQ>(r0, r1, C, c_bf16, ldc, row, col0, N, qo);
     }
   }
 
@@ -568,7 +579,13 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
   const bool leader = rank == 0;
-  const int num_m = M / (2 * BM), num_n = N / BNP, num_k = K / (kF8 ? BK / 2 : BK);
+  // MXFP4 takes N and K multiples of 128: a last N tile with 128 valid
+  // columns (CTA 1's B rows and scale band arrive zero-filled; those columns
+  // are not stored) and a last K step with 128 valid K (the rest arrives
+  // zero-filled and its last two MMAs are not issued).
+  const int num_m = M / (2 * BM), num_n = (N + BNP - 1) / BNP;
+  const int num_k = kF8 ? K / (BK / 2) : (K + BK - 1) / BK;
+  const bool k_half = !kF8 && (K % BK) != 0;
   const int num_tiles = num_m * num_n;
   const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
   constexpr uint32_t kTx = kF8 ? 2u * (A_BYTES + B_BYTES + 512 + 1024)
@@ -623,9 +640,10 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
           ptx::tma_load_2d_pair(st, &tmA, kb * BKB, a_row, full_leader);
           ptx::tma_load_2d_pair(st + A_BYTES, &tmB, kb * BKB, b_row, full_leader);
           if constexpr (kImg) {
-            // A images: band * ntiles/2 + tile pair; B images: band pair * ntiles + tile.
+            // A images: band * ceil(ntiles / 2) + tile pair; B images: band pair *
+            // ntiles + tile.
             ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES, &tmSA, 0, 0,
-                                  (a_row / 128) * (ntiles / 2) + kAImgs * kb, full_leader);
+                                  (a_row / 128) * ((ntiles + 1) / 2) + kAImgs * kb, full_leader);
             ptx::tma_load_3d_pair(st + A_BYTES + B_BYTES + kSfaBytes, &tmSB, 0, 0,
                                   nb * ntiles + kBImgs * kb, full_leader);
           } else {
@@ -718,8 +736,8 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 ptx::tc_cp_pair_32x128b_warpx4(tmem + SFB_COL + 8 * c + 4 * t,
                                                ptx::smem_desc(sfb_s + t * 1024 + c * 512, 0, 128, 0));
             }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            const int kmma = (k_half && kb == num_k - 1) ? 2 : 4;   // MMAs of K = 64
+            for (int k = 0; k < kmma; ++k) {
               const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
               const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
               ptx::mma_mxf4_pair(tmem + ACC_COL, ad, bd, make_idesc((k & 1) * 2),
@@ -771,6 +789,7 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         }
       }
       const int64_t col0 = (int64_t)nb * BNP + h * 128;
+      if (col0 >= N) continue;          // the empty half of a last, 128-wide N tile
       if constexpr (kQ == 2) {
         uint8_t* xb = smem + kStages * kStageBytes + CTL_BYTES + (warp - 2) * kXposeBytes;
         epilogue_rowcol(r0, r1, C, c_bf16, ldc, row, col0, M, N, qo, qc,
@@ -841,13 +860,14 @@ bool make_image_map(CUtensorMap* m, const uint8_t* base, int64_t nimg, uint32_t 
 // [row j (8)][16 bytes], chunk c's bytes for row 8 g + j being that row's 16
 // bytes in the chunk's tile -- the 128-row x 32-byte matrix a 128x256b copy
 // reads, row r of which carries tile row r % 32. A-role images pair two
-// consecutive tiles of one band (index band * ntiles / 2 + tile / 2); B-role
-// images pair two bands at one tile (index band pair * ntiles + tile). One
-// thread copies one 16-byte piece.
+// consecutive tiles of one band (index band * ceil(ntiles / 2) + tile / 2);
+// B-role images pair two bands at one tile (index band pair * ntiles + tile).
+// A pair member past the last tile (odd ntiles) or the last band (odd band
+// count of B) is written as zeros. One thread copies one 16-byte piece.
 __global__ void __launch_bounds__(256)
 scale_images_kernel(const uint8_t* __restrict__ sa, uint8_t* __restrict__ ia, int64_t na,
                     const uint8_t* __restrict__ sb, uint8_t* __restrict__ ib, int64_t nb,
-                    int64_t ntiles) {
+                    int64_t ntiles, int64_t b_bands) {
   int64_t t = (int64_t)blockIdx.x * 256 + threadIdx.x;
   const bool bside = t >= na;
   if (bside) t -= na;
@@ -855,41 +875,47 @@ scale_images_kernel(const uint8_t* __restrict__ sa, uint8_t* __restrict__ ia, in
   const int64_t img = t >> 8;
   const int w = (int)(t & 255), g = (w >> 4) & 3, c = (w >> 3) & 1, j = w & 7;
   int64_t tile;
+  bool valid;
   if (!bside) {
-    const int64_t per = ntiles / 2, band = img / per;
-    tile = band * ntiles + 2 * (img - band * per) + c;
+    const int64_t per = (ntiles + 1) / 2, band = img / per, k = 2 * (img - band * per) + c;
+    tile = band * ntiles + k;
+    valid = k < ntiles;
   } else {
-    const int64_t q = img / ntiles;
-    tile = (2 * q + c) * ntiles + (img - q * ntiles);
+    const int64_t q = img / ntiles, band = 2 * q + c;
+    tile = band * ntiles + (img - q * ntiles);
+    valid = band < b_bands;
   }
-  const uint4 v = __ldg(reinterpret_cast<const uint4*>((bside ? sb : sa) + tile * 512 + (8 * g + j) * 16));
+  const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>((bside ? sb : sa) + tile * 512 + (8 * g + j) * 16))
+                        : make_uint4(0u, 0u, 0u, 0u);
   *reinterpret_cast<uint4*>((bside ? ib : ia) + t * 16) = v;
 }
 
-// Bytes of one operand's scale images (four times its scale bytes).
-int64_t image_bytes(int64_t rows, int64_t K, bool nv) { return 4 * rows * (nv ? K / 16 : K / 32); }
+// 512-byte scale tiles per 128-row band: K/128 (MXFP4), K/64 (NVFP4).
+int64_t scale_tiles(int64_t K, bool nv) { return nv ? K / 64 : K / 128; }
+// Image counts: A, (M / 128) bands x ceil(tiles / 2); B, ceil(N / 256) band pairs x tiles.
+int64_t a_images(int64_t M, int64_t K, bool nv) { return (M / 128) * ((scale_tiles(K, nv) + 1) / 2); }
+int64_t b_images(int64_t N, int64_t K, bool nv) { return ((N + 255) / 256) * scale_tiles(K, nv); }
+constexpr int64_t kImageBytes = 4096;
 
 // The image path needs image indices (TMA coordinates) and the pre-pass grid
 // within 32 bits.
 bool images_fit(int64_t M, int64_t N, int64_t K, bool nv) {
-  const int64_t ntiles = nv ? K / 64 : K / 128;
-  const int64_t pieces = (image_bytes(M, K, nv) + image_bytes(N, K, nv)) / 16;
-  return (M / 128) * (ntiles / 2) < (1ll << 31) && (N / 256) * ntiles < (1ll << 31) &&
+  const int64_t pieces = (a_images(M, K, nv) + b_images(N, K, nv)) * (kImageBytes / 16);
+  return a_images(M, K, nv) < (1ll << 31) && b_images(N, K, nv) < (1ll << 31) &&
          (pieces + 255) / 256 < (1ll << 31);
 }
 
 // Builds A's and B's images in ws (A first) and encodes their tensor maps.
 bool prepare_images(const uint8_t* sa, int64_t M, const uint8_t* sb, int64_t N, int64_t K, bool nv,
                     uint8_t* ws, CUtensorMap* tsa, CUtensorMap* tsb, cudaStream_t st) {
-  const int64_t ntiles = nv ? K / 64 : K / 128;
+  const int64_t ai = a_images(M, K, nv), bi = b_images(N, K, nv);
   uint8_t* ia = ws;
-  uint8_t* ib = ws + image_bytes(M, K, nv);
-  if (!make_image_map(tsa, ia, (M / 128) * (ntiles / 2), nv ? 2 : 1) ||
-      !make_image_map(tsb, ib, (N / 256) * ntiles, nv ? 4 : 2))
+  uint8_t* ib = ws + ai * kImageBytes;
+  if (!make_image_map(tsa, ia, ai, nv ? 2 : 1) || !make_image_map(tsb, ib, bi, nv ? 4 : 2))
     return false;
-  const int64_t na = image_bytes(M, K, nv) / 16, nb = image_bytes(N, K, nv) / 16;
+  const int64_t na = ai * (kImageBytes / 16), nb = bi * (kImageBytes / 16);
   scale_images_kernel<<<(unsigned)((na + nb + 255) / 256), 256, 0, st>>>(sa, ia, na, sb, ib, nb,
-                                                                          ntiles);
+                                                                          scale_tiles(K, nv), N / 128);
   return true;
 }
 
@@ -937,7 +963,7 @@ DevInfo& dev_info(int dev) {
 }  // namespace
 
 int64_t workspace_bytes(int64_t M, int64_t N, int64_t K, bool nv) {
-  return image_bytes(M, K, nv) + image_bytes(N, K, nv);
+  return (a_images(M, K, nv) + b_images(N, K, nv)) * kImageBytes;
 }
 
 // The library's own scratch for mxfp4_gemm_noalloc: a static device array (one
@@ -991,7 +1017,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
     // CTA pairs: 256 x 256 tiles.
     CUtensorMap tsa, tsb;
     const bool img = ws != nullptr && !qcol && images_fit(M, N, K, false) &&
-                     ws_bytes >= (size_t)(image_bytes(M, K, false) + image_bytes(N, K, false));
+                     ws_bytes >= (size_t)workspace_bytes(M, N, K, false);
     (void)cudaGetLastError();  // drop a stale error left by an earlier call
     if (!make_code_map(&ta, qa, M, K / 2, pair::BM) || !make_code_map(&tb, qb, N, K / 2, pair::BNH) ||
         !(img ? prepare_images(sa, M, sb, N, K, false, static_cast<uint8_t*>(ws), &tsa, &tsb, st)
@@ -999,7 +1025,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
       *why = "cuTensorMapEncodeTiled rejected the operand layout";
       return cudaErrorInvalidValue;
     }
-    const int num_tiles = (int)((M / 256) * (N / pair::BNP));
+    const int num_tiles = (int)((M / 256) * ((N + pair::BNP - 1) / pair::BNP));
     const int pairs = d.sms / 2;
     const int grid = 2 * (num_tiles < pairs ? num_tiles : pairs);
     int64_t gm = kGroupBytes / (256 * (K / 2));
@@ -1025,7 +1051,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
     *why = "cuTensorMapEncodeTiled rejected the operand layout";
     return cudaErrorInvalidValue;
   }
-  const int num_tiles = (int)((M / BM) * (N / BN));
+  const int num_tiles = (int)((M / BM) * ((N + BN - 1) / BN));
   const int grid = num_tiles < d.sms ? num_tiles : d.sms;
   int64_t gm = kGroupBytes / (BM * (K / 2));
   gm = gm < 8 ? 8 : (gm > 64 ? 64 : gm);
@@ -1115,7 +1141,7 @@ cudaError_t launch_gemm_nv(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
   ensure_context();
   CUtensorMap ta, tb, tsa, tsb;
   const bool img = ws != nullptr && images_fit(M, N, K, true) &&
-                   ws_bytes >= (size_t)(image_bytes(M, K, true) + image_bytes(N, K, true));
+                   ws_bytes >= (size_t)workspace_bytes(M, N, K, true);
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
   if (!make_code_map(&ta, qa, M, K / 2, pair::BM) || !make_code_map(&tb, qb, N, K / 2, pair::BNH) ||
       !(img ? prepare_images(sa, M, sb, N, K, true, static_cast<uint8_t*>(ws), &tsa, &tsb, st)

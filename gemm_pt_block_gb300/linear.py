@@ -74,9 +74,10 @@ def recipe_1d(sign_mask: int = 0, seed: int = 0) -> LinearRecipe:
 
 
 def _check_shapes(T: int, D: int, F: int) -> None:
-    # GEMM: M % 128, N % 256, K % 256 for (T,F,D), (T,D,F), (F,D,T).
-    if T % 256 or D % 256 or F % 256:
-        raise ValueError(f"MXFP4 linear needs T, D, F multiples of 256 (got {T}, {D}, {F})")
+    # GEMMs (T,F,D), (T,D,F), (F,D,T) need M, N, K multiples of 128; so does the
+    # tensor-core scale layout of every quantized operand.
+    if T % 128 or D % 128 or F % 128:
+        raise ValueError(f"MXFP4 linear needs T, D, F multiples of 128 (got {T}, {D}, {F})")
 
 
 class _Mxfp4LinearFn(torch.autograd.Function):

@@ -192,7 +192,10 @@ mxfp4_status mxfp4_dequantize_ex(const uint8_t* q, const uint8_t* s, int32_t sca
  * dimension ldc >= N. Fprop Y = X W^T is (A = X row-wise, B = W row-wise);
  * Dgrad dX = dY W is (A = dY row-wise, B = W column-wise); Wgrad dW = dY^T X is
  * (A = dY column-wise, B = X column-wise).
- *  Shapes: M % 128 == 0, N % 256 == 0, K % 256 == 0, all > 0.
+ *  Shapes: M, N and K positive multiples of 128, each at most 2^30. (The
+ *  kernels work on 256 x 256 output tiles and 256-deep K steps: a last tile
+ *  of 128 columns and a last K step of 128 are computed on zero-filled
+ *  operands and only the valid part is stored.)
  *  Runs on tcgen05 tensor cores (sm_103a); returns MXFP4_ERR_UNSUPPORTED on
  *  other devices. */
 mxfp4_status mxfp4_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
@@ -236,7 +239,8 @@ mxfp4_status mxfp4_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
  *    GEMMs overlap on the GPU (different streams, or different host threads
  *    on one device) race on the array and must be serialised by the caller.
  *  - Shapes as mxfp4_gemm. With M % 256 == 0 the images take
- *    4 * (M + N) * K / 32 bytes; above 96 MiB the call returns
+ *    mxfp4_gemm_workspace_size(M, N, K, 32) bytes (4 * (M + N) * K / 32 when
+ *    N and K are multiples of 256); above 96 MiB the call returns
  *    MXFP4_ERR_SHAPE before touching the device (M % 256 == 128 uses no images).
  *  - C is bit-identical to mxfp4_gemm's. */
 mxfp4_status mxfp4_gemm_noalloc(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
@@ -244,8 +248,10 @@ mxfp4_status mxfp4_gemm_noalloc(const uint8_t* qa, const uint8_t* sa, const uint
                                 int64_t ldc, void* stream);
 
 /* Workspace bytes for mxfp4_gemm_ex (scale_block 32) or nvfp4_gemm
- * (scale_block 16): four times the scale bytes of both operands,
- * 4 * (M + N) * K / scale_block. 0 for non-positive sizes or another block. */
+ * (scale_block 16): four times the scale bytes of both operands, with A's K
+ * and B's N rounded up to multiples of 256: 4 * (M * K' + N' * K) /
+ * scale_block (4 * (M + N) * K / scale_block when N and K are multiples of
+ * 256). 0 for non-positive sizes or another block. */
 size_t mxfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t scale_block);
 
 /* The MXFP8 counterpart of mxfp4_gemm ([TIBQ], "The fix, and its supporting

@@ -93,8 +93,9 @@ def test_host_side_validation(L):
     assert L.mxfp4_quantize(good, 0, 64, 128, 128, ctypes.byref(pm), good, good, None, None, None, None) == 2
     # GEMM shapes
     assert L.mxfp4_gemm(good, good, good, good, 100, 256, 256, good, 256, None) == 2
-    assert L.mxfp4_gemm(good, good, good, good, 128, 128, 256, good, 128, None) == 2
-    assert L.mxfp4_gemm(good, good, good, good, 128, 256, 128, good, 256, None) == 2
+    assert L.mxfp4_gemm(good, good, good, good, 128, 192, 256, good, 192, None) == 2
+    assert L.mxfp4_gemm(good, good, good, good, 128, 256, 192, good, 256, None) == 2
+    assert L.mxfp4_gemm(good, good, good, good, 128, 256, 0, good, 256, None) == 2
     assert L.mxfp4_gemm(good, good, good, good, 128, 256, 256, good, 100, None) == 2
     assert L.mxfp4_gemm(None, good, good, good, 128, 256, 256, good, 256, None) == 1
     assert L.mxfp4_gemm(good, good, good, good, 128, 256, 256, P((1 << 20) + 4), 256, None) == 3
@@ -117,7 +118,9 @@ def test_host_side_validation(L):
     assert L.mxfp4_gemm_noalloc(good, good, good, good, 1 << 62, 1 << 62, 1 << 62, good, 1 << 62,
                                 None) == 2
     assert b"too large" in L.mxfp4_last_error()
-    assert L.mxfp4_gemm_noalloc(good, good, good, good, 256, 384, 256, good, 384, None) == 2
+    assert L.mxfp4_gemm_noalloc(good, good, good, good, 256, 320, 256, good, 320, None) == 2
+    # workspace size: A's K and B's N rounded up to 256
+    assert L.mxfp4_gemm_workspace_size(256, 384, 640, 32) == 4 * (256 * 768 + 512 * 640) // 32
     assert L.mxfp8_gemm(good, good, good, good, 256, 256, 256, good, 3, 256, None) == 1
     assert L.mxfp8_gemm(good, good, good, good, 128, 256, 128, good, 0, 256, None) == 2
     # NVFP4: tensor_exp only with 1x16 blocks, in range; E2M1 elements only

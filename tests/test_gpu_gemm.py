@@ -51,9 +51,12 @@ def test_gemm_one_hot_rows_exact():
     assert np.array_equal(c.astype(np.float64), ref)
 
 
-def test_gemm_per_block_scales_exact():
-    """Unit scales except one block per row / column: checks each scale's slot."""
-    M, N, K = 256, 512, 1024
+@pytest.mark.parametrize("M,N,K", [(256, 512, 1024), (128, 384, 384), (256, 384, 640),
+                                   (384, 640, 1152)])
+def test_gemm_per_block_scales_exact(M, N, K):
+    """Unit scales except one block per row / column: checks each scale's slot,
+    including the last K step and last output tile of 128 when N or K is 128
+    more than a multiple of 256."""
     qa = synth.random_codes(M, K, 21)
     qb = synth.random_codes(N, K, 22)
     sa_rm = np.full((M, K // 32), 127, np.uint8)
@@ -68,8 +71,14 @@ def test_gemm_per_block_scales_exact():
     assert np.array_equal(c.astype(np.float64), ref)
 
 
+# Shapes whose N or K is 128 more than a multiple of 256 (a last output tile of
+# 128 columns, a last K step of 128) next to the aligned ones.
+ODD_SHAPES = [(128, 128, 128), (256, 128, 128), (128, 384, 384), (256, 384, 640), (384, 640, 1152),
+              (256, 256, 384), (256, 384, 256), (768, 1152, 1408)]
+
+
 @pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 768), (384, 768, 2304),
-                                   (2048, 4096, 512), (1280, 2560, 4096)])
+                                   (2048, 4096, 512), (1280, 2560, 4096)] + ODD_SHAPES)
 def test_gemm_random_within_tolerance(M, N, K):
     qa, qb = synth.random_codes(M, K, M + 1), synth.random_codes(N, K, N + 2)
     sa, sb = synth.random_scales(M, K, K + 3), synth.random_scales(N, K, K + 4)
@@ -144,7 +153,8 @@ def test_gemm_full_size_sampled_rows(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (256, 512, 768), (512, 768, 2304),
-                                   (1024, 1280, 4096), (16384, 8192, 28672)])
+                                   (1024, 1280, 4096), (16384, 8192, 28672), (256, 128, 128),
+                                   (256, 384, 640), (512, 640, 1152), (768, 1152, 1408)])
 def test_gemm_scale_images_bit_identical(M, N, K):
     """The workspace path (scales rewritten as replicated images, 128x256b
     tensor-memory copies) gives the same bits as the plain entry point, for
@@ -156,7 +166,10 @@ def test_gemm_scale_images_bit_identical(M, N, K):
     qb = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=DEV, generator=g)
     sa = torch.randint(118, 137, (M * K // 32,), dtype=torch.uint8, device=DEV, generator=g)
     sb = torch.randint(118, 137, (N * K // 32,), dtype=torch.uint8, device=DEV, generator=g)
-    ws = torch.full((mx.gemm_workspace_size(M, N, K),), 0xAB, dtype=torch.uint8, device=DEV)
+    nimg = mx.gemm_workspace_size(M, N, K)
+    ceil256 = lambda v: (v + 255) // 256 * 256
+    assert nimg == 4 * (M * ceil256(K) + ceil256(N) * K) // 32
+    ws = torch.full((nimg,), 0xAB, dtype=torch.uint8, device=DEV)
     plain = mx.mxfp4_gemm(qa, sa, qb, sb, M, N, K, workspace=False)
     img = mx.mxfp4_gemm(qa, sa, qb, sb, M, N, K, workspace=ws)
     img16 = mx.mxfp4_gemm(qa, sa, qb, sb, M, N, K, workspace=ws, out_dtype=torch.bfloat16)

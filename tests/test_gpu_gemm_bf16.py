@@ -44,7 +44,7 @@ def test_bf16_c_exact_products_round_like_the_oracle():
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 768), (384, 768, 2304),
-                                   (1280, 2560, 4096)])
+                                   (1280, 2560, 4096), (256, 384, 640), (384, 640, 1152)])
 def test_bf16_c_within_tolerance(M, N, K):
     import gemm_pt_block_gb300 as mx
 

@@ -18,7 +18,8 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 MASK = 0xC0FFEE11
 
-SHAPES = [(256, 512, 512), (384, 256, 768)]   # CTA-pair kernel; 1-CTA kernel (M % 256 = 128)
+# CTA-pair kernel; 1-CTA kernel (M % 256 = 128); N and K 128 past a multiple of 256
+SHAPES = [(256, 512, 512), (384, 256, 768), (256, 384, 640)]
 VARIANTS = list(itertools.product((0, 1), (0, 1), (0, 1), (False, True), (0, 1)))
 
 
@@ -70,7 +71,7 @@ def test_fused_rejects_bad_arguments():
     p = mx.QuantParams(mx.BLOCK_1X32, mx.SCALE_FLOOR, mx.ROUND_RTN, mx.LAYOUT_MMA)
     *_, t = _operands(256, 256, 256, 3)
     with pytest.raises(mx.Mxfp4Error):
-        mx.mxfp4_gemm_quantize(*t, 256, 384, 256, p)          # N % 256 != 0
+        mx.mxfp4_gemm_quantize(*t, 256, 320, 256, p)          # N % 128 != 0
     bad = mx.QuantParams(5, mx.SCALE_FLOOR, mx.ROUND_RTN, mx.LAYOUT_MMA)
     with pytest.raises(mx.Mxfp4Error):
         mx.mxfp4_gemm_quantize(*t, 256, 256, 256, bad)        # bad block
@@ -94,7 +95,7 @@ def test_fused_mxfp8_output(block):
 
 # ------------------------------------------------ column-wise (C^T along M) --
 
-COL_SHAPES = [(256, 512, 512), (512, 256, 768)]
+COL_SHAPES = [(256, 512, 512), (512, 256, 768), (256, 640, 384)]
 
 
 @pytest.mark.parametrize("M,N,K", COL_SHAPES)

@@ -30,7 +30,8 @@ def _cols(x, p):
     return q, oracle.scales_to_mma(s)
 
 
-@pytest.mark.parametrize("recipe_name,T,D,F", [("2d_sr", 256, 512, 768), ("1d", 512, 256, 256)])
+@pytest.mark.parametrize("recipe_name,T,D,F", [("2d_sr", 256, 512, 768), ("1d", 512, 256, 256),
+                                                ("2d_sr", 384, 640, 384), ("1d", 128, 384, 640)])
 def test_linear_forward_backward_match_oracle(recipe_name, T, D, F):
     import gemm_pt_block_gb300 as mx
 
@@ -83,8 +84,10 @@ def test_linear_module_bf16_and_fresh_draws_per_step():
 def test_linear_rejects_unsupported_shapes():
     import gemm_pt_block_gb300 as mx
 
-    with pytest.raises(ValueError):
-        mx.mxfp4_linear(torch.zeros(128, 256, device=DEV), torch.zeros(256, 256, device=DEV))
+    with pytest.raises(ValueError):      # T not a multiple of 128
+        mx.mxfp4_linear(torch.zeros(192, 256, device=DEV), torch.zeros(256, 256, device=DEV))
+    with pytest.raises(ValueError):      # F not a multiple of 128
+        mx.mxfp4_linear(torch.zeros(256, 256, device=DEV), torch.zeros(320, 256, device=DEV))
 
 
 def test_first_call_from_a_fresh_thread():
