@@ -134,6 +134,10 @@ def lib() -> ctypes.CDLL:
         L.orc_nv_scale_code.argtypes = [ctypes.c_float, ctypes.c_int, ctypes.c_int]
         L.orc_dequantize_nv_f64.restype = ctypes.c_int
         L.orc_dequantize_nv_f64.argtypes = [P, P, ctypes.c_int, i64, i64, ctypes.c_int, P]
+        L.orc_tensor_amax.restype = ctypes.c_float
+        L.orc_tensor_amax.argtypes = [P, ctypes.c_int, i64, i64, i64]
+        L.orc_nv_tensor_exp.restype = ctypes.c_int
+        L.orc_nv_tensor_exp.argtypes = [ctypes.c_float]
         L.orc_gemm_pairs_nv.restype = ctypes.c_int
         L.orc_gemm_pairs_nv.argtypes = [P, P, ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int,
                                         i64, i64, i64, i64, P, P, P, P]
@@ -206,6 +210,18 @@ def scale_exponent_fmt(M: float, mode: int, fmt: int) -> int:
 
 def round_sr(v: float, r16: int) -> int:
     return int(lib().orc_round_sr(ctypes.c_float(v), r16))
+
+
+def tensor_amax(x: np.ndarray) -> float:
+    """Largest |x| over a 2-D bf16-bits (uint16) or float32 array."""
+    x, dt, ld = _as_input(x)
+    rows, cols = x.shape
+    return float(lib().orc_tensor_amax(_ptr(x), dt, rows, cols, ld))
+
+
+def nv_tensor_exp(amax: float) -> int:
+    """NVFP4 per-tensor exponent: smallest k with 2688 * 2^k >= amax (0 for 0)."""
+    return int(lib().orc_nv_tensor_exp(ctypes.c_float(amax)))
 
 
 def nv_scale_code(M: float, k: int, mode: int) -> int:

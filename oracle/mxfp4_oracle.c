@@ -285,6 +285,29 @@ static float load_elem(const void* x, int dtype, int64_t ld, int64_t r, int64_t 
   return ((const float*)x)[r * ld + c];
 }
 
+/* Max-abs over the tensor [TIBQ, "Why FP4 training is the current frontier of
+ * precision reduction": block scales follow the max-abs; the per-tensor factor
+ * of 1x16 blocks follows the tensor's]: plain loop, fp32 compares. */
+float orc_tensor_amax(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld) {
+  float m = 0.0f;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      const float a = fabsf(load_elem(x, dtype, ld, r, c));
+      if (a > m) m = a;
+    }
+  return m;
+}
+
+/* Reading (the pages give no rule for the tensor factor): the smallest k in
+ * [-100, 100] with 2688 * 2^k >= amax, by direct search over k with exact
+ * fp64 powers of two; 100 if none is large enough; 0 for amax == 0. */
+int orc_nv_tensor_exp(float amax) {
+  if (amax == 0.0f) return 0;
+  for (int k = -100; k <= 100; ++k)
+    if (ldexp(2688.0, k) >= (double)amax) return k;
+  return 100;
+}
+
 /* Quantize output rows [i0, i1) of one orientation. In the row orientation
  * output row i is source row i and position k is source column k; in the
  * column orientation output row i is source column i and k is source row k.

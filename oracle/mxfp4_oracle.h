@@ -78,6 +78,16 @@ int orc_scale_exponent_fmt(float M, int scale_mode, int elem_format);
  * M / (6 * 2^k), ties to the even code, saturating at 448. */
 int orc_nv_scale_code(float M, int k, int scale_mode);
 
+/* Max-abs of x [rows, cols] (leading dim ld, elements): the largest |x[r][c]|,
+ * exact in fp32 (a maximum does not depend on the order). 0 when empty. */
+float orc_tensor_amax(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld);
+
+/* Per-tensor exponent k of the NVFP4 factor 2^k for a tensor whose max-abs is
+ * amax: the smallest integer k with 2688 * 2^k >= amax (2688 = 6 * 448, so the
+ * largest block scale amax / (6 * 2^k) fits E4M3's largest value), clamped to
+ * [-100, 100]; 0 for amax == 0. */
+int orc_nv_tensor_exp(float amax);
+
 /* Row-wise quantization of rows [r0, r1) of x [rows, cols] (leading dim ld,
  * elements), along cols. q: [(r1-r0), cols/2] bytes (E4M3: [(r1-r0), cols]),
  * s: [(r1-r0), cols/32] bytes (1x16 blocks: cols/16 E4M3 codes), both

@@ -836,3 +836,44 @@ def test_nvfp4_dequantize_and_gemm_pairs_exact():
         assert a[t] == sum(abs(Fraction(d[m, k]) * Fraction(db[n, k])) for k in range(cols))
     C, A = oracle.gemm_ref_nv(q, sm, -4, qb, oracle.scales_to_mma(sb), 3, rows, rows, cols)
     assert np.allclose(C[ms, ns], c, rtol=0, atol=1e-12 * a.max())
+
+
+# ------------------------------------------------ NVFP4 per-tensor factor --
+
+def test_tensor_amax_matches_numpy_max_abs():
+    """The max-abs over a tensor (bf16 bits and fp32, with a leading dimension
+    wider than the row) equals numpy's max of |x|, a library reduction."""
+    x = synth.laplace(96, 160, 1e-3, seed=71, outlier_frac=0.002)
+    xb = _bf16(x)
+    want = float(np.abs(x.float().numpy()).max())
+    assert oracle.tensor_amax(xb) == want
+    assert oracle.tensor_amax(x.float().numpy()) == want
+    wide = np.zeros((96, 192), dtype=np.float32)
+    wide[:, :160] = x.float().numpy()
+    wide[:, 160:] = 1e9                      # outside the view: must not count
+    assert oracle.tensor_amax(wide[:, :160]) == want
+    assert oracle.tensor_amax(np.zeros((32, 32), np.float32)) == 0.0
+    neg = -np.abs(x.float().numpy())
+    assert oracle.tensor_amax(neg) == want
+
+
+def test_nv_tensor_exp_closed_forms():
+    """k is the smallest integer with 2688 * 2^k >= amax: exactly 2688 * 2^j
+    gives j, the next fp32 above it j + 1, and every value in
+    (2688 * 2^(j-1), 2688 * 2^j] gives j; clamped to [-100, 100]; 0 for 0."""
+    for j in range(-60, 61, 7):
+        t = np.float32(2688.0 * 2.0 ** j)
+        assert oracle.nv_tensor_exp(float(t)) == j
+        assert oracle.nv_tensor_exp(float(np.nextafter(t, np.float32(np.inf)))) == j + 1
+        lo = np.float32(1344.0 * 2.0 ** j)
+        assert oracle.nv_tensor_exp(float(np.nextafter(lo, np.float32(np.inf)))) == j
+        assert oracle.nv_tensor_exp(float(lo)) == j - 1
+    assert oracle.nv_tensor_exp(0.0) == 0
+    assert oracle.nv_tensor_exp(float(np.float32(1e-40))) == -100      # subnormal: clamp
+    assert oracle.nv_tensor_exp(float(np.finfo(np.float32).max)) == 100
+    # the largest block scale then fits E4M3: amax / (6 * 2^k) <= 448
+    rng = np.random.default_rng(72)
+    for a in rng.uniform(-30, 30, 200):
+        amax = float(np.float32(2.0 ** a))
+        k = oracle.nv_tensor_exp(amax)
+        assert amax / (6.0 * 2.0 ** k) <= 448.0 < amax / (6.0 * 2.0 ** (k - 1))
