@@ -216,8 +216,8 @@ class Step:
         for q in spec.quants:
             self.inputs[q.name] = gen_input(q, device)
             prow, pcol = q.prow, q.pcol
-            if spec.nvfp4:   # per-tensor factor from the tensor's max-abs (set up once)
-                k = mx.nvfp4_tensor_exp(float(self.inputs[q.name].float().abs().max()))
+            if spec.nvfp4:   # per-tensor factor from the tensor's max-abs (on the device)
+                k = mx.nvfp4_tensor_exp(self.inputs[q.name])
                 prow = prow and replace(prow, tensor_exp=k)
                 pcol = pcol and replace(pcol, tensor_exp=k)
             self.params[q.name] = (prow, pcol)
@@ -230,6 +230,10 @@ class Step:
                 torch.empty(ns, dtype=u8, device=device) if q.pcol else None)
         for g in spec.gemms:
             self.outs[g.label] = torch.empty(g.M, g.N, device=device)
+        # NVFP4: each step also takes every tensor's max-abs on the device, the
+        # per-tensor factors of the next step (delayed scaling)
+        self.amax = {q.name: (torch.empty(1, device=device), torch.empty(1, dtype=torch.int32, device=device))
+                     for q in spec.quants} if spec.nvfp4 else {}
         # one workspace for the GEMMs' scale images (the largest the step needs)
         blk = 16 if spec.nvfp4 else 32
         self.ws = torch.empty(max([mx.gemm_workspace_size(g.M, g.N, g.K, blk) for g in spec.gemms],
@@ -244,8 +248,10 @@ class Step:
     def launches(self):
         """Kernel launches per step: one per quantize, two per GEMM (the scale
         images for the tensor-memory copies, then the GEMM) when it uses the
-        workspace, which every CTA-pair shape (M % 256 == 0) does."""
-        return len(self.spec.quants) + sum(2 if g.M % 256 == 0 else 1 for g in self.spec.gemms)
+        workspace, which every CTA-pair shape (M % 256 == 0) does; for NVFP4
+        two per tensor for its max-abs and exponent."""
+        return (len(self.spec.quants) + sum(2 if g.M % 256 == 0 else 1 for g in self.spec.gemms)
+                + 2 * len(self.amax))
 
     def operand(self, ref):
         q, s, qc, sc = self.bufs[ref[0]]
@@ -283,6 +289,8 @@ class Step:
             k += 1
             if events is not None:
                 events[k].record()
+        for name, (a, e) in self.amax.items():
+            mx.tensor_amax(inp[name], amax=a, tensor_exp=e)
 
 
 # ------------------------------------------------------------ utilities ---

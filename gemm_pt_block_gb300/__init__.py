@@ -15,6 +15,8 @@ Calls (same names as the C ABI):
                     epilogue; mxfp8_gemm (E4M3) and nvfp4_gemm (1x16 blocks,
                     E4M3 scales)
   hadamard32        stand-alone 32-point block rotation
+  mxfp4_tensor_amax device max-abs and NVFP4 per-tensor exponent
+                    (tensor_amax, nvfp4_tensor_exp)
 """
 from .binding import (  # noqa: F401
     BLOCK_1X32,
@@ -46,6 +48,7 @@ from .binding import (  # noqa: F401
     gemm_workspace_size,
     nvfp4_gemm,
     nvfp4_tensor_exp,
+    tensor_amax,
     mxfp4_quantize,
     scale_numel,
 )

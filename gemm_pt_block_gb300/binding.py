@@ -78,23 +78,6 @@ class QuantParams:
         return k // 16 if self.block == BLOCK_1X16 else k // 32
 
 
-def nvfp4_tensor_exp(amax: float) -> int:
-    """Per-tensor exponent k = ceil(log2(amax / 2688)) for NVFP4: the smallest k
-    whose largest block scale, amax / (6 * 2^k), fits E4M3's 448."""
-    import math
-
-    if not math.isfinite(amax):
-        raise ValueError("nvfp4_tensor_exp: the tensor's max-abs must be finite")
-    if not amax > 0:
-        return 0
-    k = math.ceil(math.log2(amax / 2688.0))
-    while amax > 2688.0 * 2.0 ** k:
-        k += 1
-    while k > -100 and amax <= 2688.0 * 2.0 ** (k - 1):
-        k -= 1
-    return max(-100, min(100, k))
-
-
 _lib = None
 
 
@@ -136,6 +119,8 @@ def lib() -> ctypes.CDLL:
         L.mxfp4_gemm_quantize.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64,
                                           ctypes.POINTER(_CParams), P, P,
                                           ctypes.POINTER(_CParams), P, P, P, sz, P]
+        L.mxfp4_tensor_amax.restype = i32
+        L.mxfp4_tensor_amax.argtypes = [P, i32, i64, i64, i64, P, P, P]
         L.hadamard32.restype = i32
         L.hadamard32.argtypes = [P, i32, i64, i64, i64, ctypes.c_uint32, i32, P, P]
         L.mxfp4_status_string.restype = ctypes.c_char_p
@@ -392,6 +377,30 @@ def hadamard32(x: torch.Tensor, sign_mask: int = 0, inverse: bool = False, *, y=
     _check(lib().hadamard32(_ptr(x), dt, rows, cols, ld, sign_mask & 0xFFFFFFFF, int(bool(inverse)),
                             _ptr(y), _stream(x, stream)))
     return y
+
+
+def tensor_amax(x: torch.Tensor, *, amax=None, tensor_exp=None, stream=None):
+    """Device max |x| and NVFP4 per-tensor exponent (the smallest k with
+    2688 * 2^k >= max |x|): returns (amax, tensor_exp) as one-element CUDA
+    tensors (float32, int32), filled asynchronously on the stream."""
+    _cuda2d(x, "x")
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("x must be bfloat16 or float32")
+    dt = DTYPE_BF16 if x.dtype == torch.bfloat16 else DTYPE_F32
+    rows, cols = x.shape
+    ld = x.stride(0) if rows > 1 else cols
+    amax = torch.empty(1, dtype=torch.float32, device=x.device) if amax is None else amax
+    tensor_exp = torch.empty(1, dtype=torch.int32, device=x.device) if tensor_exp is None else tensor_exp
+    _check(lib().mxfp4_tensor_amax(_ptr(x), dt, rows, cols, ld, _ptr(amax), _ptr(tensor_exp),
+                                   _stream(x, stream)))
+    return amax, tensor_exp
+
+
+def nvfp4_tensor_exp(x: torch.Tensor, stream=None) -> int:
+    """The NVFP4 per-tensor exponent of x from tensor_amax, read back to the
+    host (synchronizes the stream)."""
+    _, k = tensor_amax(x, stream=stream)
+    return int(k.item())
 
 
 def device_status(stream=None) -> int:

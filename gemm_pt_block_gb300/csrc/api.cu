@@ -346,6 +346,18 @@ mxfp4_status hadamard32(const void* x, int32_t x_dtype, int64_t rows, int64_t co
                    "hadamard32 launch");
 }
 
+mxfp4_status mxfp4_tensor_amax(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
+                               int64_t ld_x, float* amax, int32_t* tensor_exp, void* stream) {
+  mxfp4_status st = check_input(x, x_dtype, rows, cols, ld_x);
+  if (st) return st;
+  if (!amax) return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_tensor_amax: amax is NULL");
+  if ((reinterpret_cast<uintptr_t>(amax) & 3u) || (reinterpret_cast<uintptr_t>(tensor_exp) & 3u))
+    return fail(MXFP4_ERR_ALIGN, "mxfp4_tensor_amax: amax / tensor_exp must be 4-byte aligned");
+  return from_cuda(mx::launch_amax(x, x_dtype == MXFP4_DTYPE_F32, rows, cols, ld_x, amax, tensor_exp,
+                                   static_cast<cudaStream_t>(stream)),
+                   "mxfp4_tensor_amax launch");
+}
+
 mxfp4_status mxfp4_device_status(void* stream) {
   uint32_t err = 0;
   cudaError_t e = mx::read_device_error(static_cast<cudaStream_t>(stream), &err);

@@ -34,6 +34,7 @@
 
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -254,7 +255,7 @@ __device__ __forceinline__ void col_chunk(const float2 (&v)[16], float* tb, uint
   }
   __syncwarp();   // the buffers are rewritten by the next chunk
   const int64_t n = n0 + lane;
-  if (qc.wht) hadamard32_lane(R, qc.sign_mask);
+  if (qc.wht) hadamard32_lane(R, qc.sign_mask, qc.sgn);
   float Mx = absmax32(R);
   if (qc.block) Mx = warp_max(Mx);
   const int e = scale_run32<true, false>(R, qc, Mx, w);
@@ -388,8 +389,13 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         if (!(ok = wait_bar(ptx::smem_u32(&ctl->acc_empty), acc_phase ^ 1u, ctl))) break;
         ptx::tc_fence_after();
-        for (int kb = 0; kb < num_k; ++kb) {
-          if (!(ok = wait_bar(ptx::smem_u32(&ctl->full[stage]), phase, ctl))) break;
+        // One K step with kMmas MMAs of K = 64: four, or two for a last,
+        // 128-deep step. The full steps run in a loop of their own and the
+        // half step after it, so the hot loop has no branch between MMAs
+        // (one there measurably slows the issue).
+        auto kstep = [&](int kb, auto nmma) -> bool {
+          [[maybe_unused]] constexpr int kMmas = decltype(nmma)::value;
+          if (!(ok = wait_bar(ptx::smem_u32(&ctl->full[stage]), phase, ctl))) return false;
           ptx::tc_fence_after();
           const uint32_t st = ptx::smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sfa_s = st + A_BYTES + B_BYTES;
@@ -405,8 +411,8 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
               ptx::tc_cp_32x128b_warpx4(tmem + SFB_COL + 8 * c + 4 * t,
                                         ptx::smem_desc(sfb_s + t * 1024 + c * 512, 0, 128, 0));
           }
-          const int kmma = (k_half && kb == num_k - 1) ? 2 : 4;   // MMAs of K = 64
-          for (int k = 0; k < kmma; ++k) {
+#pragma unroll
+          for (int k = 0; k < kMmas; ++k) {
             const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
             const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
             ptx::mma_mxf4(tmem + ACC_COL, ad, bd, make_idesc((k & 1) * 2),
@@ -418,7 +424,12 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             stage = 0;
             phase ^= 1u;
           }
-        }
+          return true;
+        };
+        const int num_kf = k_half ? num_k - 1 : num_k;
+        for (int kb = 0; kb < num_kf; ++kb)
+          if (!kstep(kb, std::integral_constant<int, 4>{})) break;
+        if (ok && k_half) kstep(num_kf, std::integral_constant<int, 2>{});
         if (!ok) break;
         ptx::tc_commit(ptx::smem_u32(&ctl->acc_full));
         acc_phase ^= 1u;
@@ -673,8 +684,13 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       for (int tile = pair_id; ok && tile < num_tiles; tile += num_pairs) {
         if (!(ok = wait_bar(ptx::smem_u32(&ctl->acc_empty), acc_phase ^ 1u, ctl))) break;
         ptx::tc_fence_after();
-        for (int kb = 0; kb < num_k; ++kb) {
-          if (!(ok = wait_bar(ptx::smem_u32(&ctl->full[stage]), phase, ctl))) break;
+        // One K step; kMmas (MXFP4 only) is four, or two for a last, 128-deep
+        // step. The full steps run in a loop of their own and the half step
+        // after it, so the hot loop has no branch between MMAs (one there
+        // measurably slows the issue).
+        auto kstep = [&](int kb, auto nmma) -> bool {
+          [[maybe_unused]] constexpr int kMmas = decltype(nmma)::value;
+          if (!(ok = wait_bar(ptx::smem_u32(&ctl->full[stage]), phase, ctl))) return false;
           ptx::tc_fence_after();
           const uint32_t st = ptx::smem_u32(smem + stage * kStageBytes);
           const uint32_t sfa_s = st + A_BYTES + B_BYTES;
@@ -736,8 +752,8 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 ptx::tc_cp_pair_32x128b_warpx4(tmem + SFB_COL + 8 * c + 4 * t,
                                                ptx::smem_desc(sfb_s + t * 1024 + c * 512, 0, 128, 0));
             }
-            const int kmma = (k_half && kb == num_k - 1) ? 2 : 4;   // MMAs of K = 64
-            for (int k = 0; k < kmma; ++k) {
+#pragma unroll
+            for (int k = 0; k < kMmas; ++k) {
               const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
               const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
               ptx::mma_mxf4_pair(tmem + ACC_COL, ad, bd, make_idesc((k & 1) * 2),
@@ -750,7 +766,12 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             stage = 0;
             phase ^= 1u;
           }
-        }
+          return true;
+        };
+        const int num_kf = k_half ? num_k - 1 : num_k;
+        for (int kb = 0; kb < num_kf; ++kb)
+          if (!kstep(kb, std::integral_constant<int, 4>{})) break;
+        if (ok && k_half) kstep(num_kf, std::integral_constant<int, 2>{});
         if (!ok) break;
         ptx::tc_commit_pair_multicast(ptx::smem_u32(&ctl->acc_full), 0x3);
         acc_phase ^= 1u;

@@ -28,9 +28,10 @@ struct OrientArgs {
   uint32_t sm_half[2];  // sign bits of local elements, lane holding block half 0 / 1
   uint32_t sm_inter[2]; // sign bits of local elements, lane holding even / odd block elements
   uint32_t xw[2][8];    // sign bits placed on bf16 word pairs (bits 15 and 31), per half
+  float sgn[32];        // rotation signs s_i as factors +-1 (all +1 without rotation)
 };
 
-// Fills keys, sm_* and xw from seed and sign_mask.
+// Fills keys, sm_*, xw and sgn from seed and sign_mask.
 void prepare_orient(OrientArgs* o);
 
 // All launchers return the cudaError_t of the launch.
@@ -41,6 +42,10 @@ cudaError_t launch_dequantize(const uint8_t* q, const uint8_t* s, bool mma_layou
                               int64_t cols, int fmt, float p2k, float* out, cudaStream_t st);
 cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t cols, int64_t ld,
                               uint32_t sign_mask, bool inverse, float* y, cudaStream_t st);
+// Max |x| into *amax (device) and, when tensor_exp is non-NULL, the NVFP4
+// per-tensor exponent derived from it (device int).
+cudaError_t launch_amax(const void* x, bool f32_in, int64_t rows, int64_t cols, int64_t ld,
+                        float* amax, int32_t* tensor_exp, cudaStream_t st);
 // qout / qcol: also quantize C row-wise / column-wise (C^T along M) in the
 // epilogue (nullptr: not produced; column-wise needs M % 256 == 0); with
 // either, c may be nullptr (no C output). ws: optional workspace of ws_bytes;

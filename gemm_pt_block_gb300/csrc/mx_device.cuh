@@ -31,11 +31,18 @@ struct PhiloxKeys {
   uint32_t k0[10], k1[10];
 };
 
+// Both 32-bit halves of the 64-bit product a * b in one instruction.
+__device__ __forceinline__ void mul_wide(uint32_t a, uint32_t b, uint32_t& lo, uint32_t& hi) {
+  asm("{.reg .u64 t;\n\tmul.wide.u32 t, %2, %3;\n\tmov.b64 {%0, %1}, t;}"
+      : "=r"(lo), "=r"(hi) : "r"(a), "r"(b));
+}
+
 __device__ __forceinline__ U4 philox4x32_10(U4 c, const PhiloxKeys& k) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    uint32_t lo0, hi0, lo1, hi1;
+    mul_wide(0xD2511F53u, c.x, lo0, hi0);
+    mul_wide(0xCD9E8D57u, c.z, lo1, hi1);
     c = U4{hi1 ^ c.y ^ k.k0[r], lo1, hi0 ^ c.w ^ k.k1[r], lo0};
   }
   return c;
@@ -203,17 +210,18 @@ __device__ __forceinline__ void stage32(float2 (&R)[16], int h) {
 }
 
 // y = c * H * diag(s) * x for one block held by one lane, butterflies in the
-// order h = 1, 2, 4, 8, 16, c applied last.
-__device__ __forceinline__ void hadamard32_lane(float2 (&R)[16], uint32_t sign_mask) {
+// order h = 1, 2, 4, 8, 16, c applied last. The signs come as the factors
+// sgn[i] = s_i = +-1 (kernel parameters, built on the host from the mask), so
+// that no per-element bit extraction is needed; sign_mask != 0 says some are -1.
+__device__ __forceinline__ void hadamard32_lane(float2 (&R)[16], uint32_t sign_mask,
+                                                const float (&sgn)[32]) {
   if (sign_mask) {
     // Stage h = 1 with the signs folded in: (s0 x0 + s1 x1, s0 x0 - s1 x1),
     // each an exact product and one rounded sum (s = +-1).
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      const float s0 = __uint_as_float(0x3F800000u | (((sign_mask >> (2 * k)) & 1u) << 31));
-      const float s1 = __uint_as_float(0x3F800000u | (((sign_mask >> (2 * k + 1)) & 1u) << 31));
-      const float t = __fmul_rn(R[k].y, s1);
-      R[k] = make_float2(__fmaf_rn(R[k].x, s0, t), __fmaf_rn(R[k].x, s0, -t));
+      const float t = __fmul_rn(R[k].y, sgn[2 * k + 1]);
+      R[k] = make_float2(__fmaf_rn(R[k].x, sgn[2 * k], t), __fmaf_rn(R[k].x, sgn[2 * k], -t));
     }
   } else {
     stage32(R, 1);

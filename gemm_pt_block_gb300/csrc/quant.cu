@@ -33,6 +33,7 @@ void prepare_orient(OrientArgs* o) {
     k1 += 0xBB67AE85u;
   }
   const uint32_t m = o->wht ? o->sign_mask : 0u;
+  for (int i = 0; i < 32; ++i) o->sgn[i] = ((m >> i) & 1u) ? -1.0f : 1.0f;
   for (int u = 0; u < 2; ++u) {
     o->sm_half[u] = (m >> (16 * u)) & 0xFFFFu;
     // Column-orientation lanes hold block elements 4 (j / 2) + 2 u + (j % 2).
@@ -432,7 +433,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
                 make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
         if (drow) {
-          if (rwht) hadamard32_lane(R, orow.sign_mask);
+          if (rwht) hadamard32_lane(R, orow.sign_mask, orow.sgn);
           float M = nv ? 0.0f : absmax32(R);    // NVFP4 takes its two 16-block maxima itself
           if (!nv && orow.block) M = warp_max(M);
           if (rsr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
@@ -455,7 +456,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           uint32_t o[8];
           col_offsets(rl, cl, o, InT());
           read_col(st, o, R, InT());
-          if (cwht) hadamard32_lane(R, ocol.sign_mask);
+          if (cwht) hadamard32_lane(R, ocol.sign_mask, ocol.sgn);
           float M = nv ? 0.0f : absmax32(R);
           if (!nv && ocol.block) M = warp_max(M);
           uint32_t w[16];
@@ -466,7 +467,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
             for (int k = 0; k < 16; ++k) {
               const uint32_t a = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k) & 7] + 1024 * (k >> 2));
               const uint32_t b = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k + 1) & 7] + 1024 * (k >> 2));
-              w[k] = a | (b << 16);
+              w[k] = __byte_perm(a, b, 0x5410);
             }
           }
           const int e = scale_run32<false, nv>(R, ocol, M, w);
@@ -497,7 +498,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
                   make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
           }
           if (do_row) {
-            if (orow.wht) hadamard32_lane(R, orow.sign_mask);
+            if (orow.wht) hadamard32_lane(R, orow.sign_mask, orow.sgn);
             M = absmax32(R);
             if (orow.block) M = warp_max(M);
           }
@@ -525,7 +526,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           uint32_t o[8];
           col_offsets(rl, cl, o, InT());
           read_col(st, o, R, InT());
-          if (ocol.wht) hadamard32_lane(R, ocol.sign_mask);
+          if (ocol.wht) hadamard32_lane(R, ocol.sign_mask, ocol.sgn);
           M = absmax32(R);
           if (ocol.block) M = warp_max(M);
         }
@@ -539,7 +540,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
             for (int k = 0; k < 16; ++k) {
               const uint32_t a = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k) & 7] + 1024 * (k >> 2));
               const uint32_t b = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k + 1) & 7] + 1024 * (k >> 2));
-              w[k] = a | (b << 16);
+              w[k] = __byte_perm(a, b, 0x5410);
             }
           }
           const int e = scale_run32(R, ocol, M, w);
@@ -635,6 +636,62 @@ dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int
   float4* o = reinterpret_cast<float4*>(out + r * cols + c0);
 #pragma unroll
   for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+// ------------------------------------------------------- tensor max-abs ---
+// Max |x| over a [rows, cols] tensor, as the bit pattern of a non-negative
+// fp32 (such patterns order like the values), into *amax_bits, which the
+// host zeroes first. CTAs stride over rows; a row's 16-byte vectors (8 bf16
+// or 4 fp32) are spread over the CTA's threads; warp and CTA maxima, then one
+// atomicMax per CTA.
+template <typename InT>
+__global__ void __launch_bounds__(kThreads)
+amax_kernel(const InT* __restrict__ x, int64_t rows, int64_t vecs, int64_t ld,
+            uint32_t* __restrict__ amax_bits) {
+  uint32_t m = 0;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint4* row = reinterpret_cast<const uint4*>(x + r * ld);
+    for (int64_t v = threadIdx.x; v < vecs; v += kThreads) {
+      const uint4 q = __ldg(row + v);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (sizeof(InT) == 2) {
+          m = max(m, max(w[i] & 0x7FFF0000u, (w[i] << 16) & 0x7FFF0000u));
+        } else {
+          m = max(m, w[i] & 0x7FFFFFFFu);
+        }
+      }
+    }
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  __shared__ uint32_t part[kThreads / 32];
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < kThreads / 32 ? part[threadIdx.x] : 0u;
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (threadIdx.x == 0 && m) atomicMax(amax_bits, m);
+  }
+}
+
+// NVFP4 per-tensor exponent from the max-abs: the smallest k with
+// 2688 * 2^k >= amax, clamped to [-100, 100], 0 for amax = 0. For a normal
+// amax = (1 + f) 2^E: 2688 * 2^(E - 11) = 1.3125 * 2^E covers it iff
+// f <= 0.3125 (fraction bits <= 0x280000), else k = E - 10.
+__global__ void nv_tensor_exp_kernel(const uint32_t* __restrict__ amax_bits, int32_t* __restrict__ k) {
+  const uint32_t b = *amax_bits;
+  int32_t e;
+  if (b == 0u) {
+    e = 0;
+  } else if (b < 0x00800000u) {
+    e = -100;
+  } else {
+    const int32_t E = (int32_t)(b >> 23) - 127;
+    e = (b & 0x7FFFFFu) <= 0x280000u ? E - 11 : E - 10;
+    e = max(-100, min(100, e));
+  }
+  *k = e;
 }
 
 inline unsigned blocks_for(int64_t threads) { return (unsigned)((threads + kThreads - 1) / kThreads); }
@@ -758,6 +815,28 @@ cudaError_t launch_quantize(const void* x, bool f32_in, int64_t rows, int64_t co
                             const OrientArgs* row, const OrientArgs* col, cudaStream_t st) {
   return f32_in ? quantize_impl(static_cast<const float*>(x), rows, cols, ld, row, col, st)
                 : quantize_impl(static_cast<const uint16_t*>(x), rows, cols, ld, row, col, st);
+}
+
+cudaError_t launch_amax(const void* x, bool f32_in, int64_t rows, int64_t cols, int64_t ld,
+                        float* amax, int32_t* tensor_exp, cudaStream_t st) {
+  uint32_t* bits = reinterpret_cast<uint32_t*>(amax);
+  cudaError_t e = cudaMemsetAsync(bits, 0, sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  (void)cudaGetLastError();  // drop a stale error left by an earlier call
+  if (rows > 0 && cols > 0) {
+    const int64_t want = rows < (1ll << 31) ? rows : (1ll << 31) - 1;
+    if (f32_in) {
+      const unsigned grid = resident_ctas(amax_kernel<float>, want, 0, kThreads);
+      amax_kernel<float><<<grid, kThreads, 0, st>>>(static_cast<const float*>(x), rows, cols / 4,
+                                                    ld, bits);
+    } else {
+      const unsigned grid = resident_ctas(amax_kernel<uint16_t>, want, 0, kThreads);
+      amax_kernel<uint16_t><<<grid, kThreads, 0, st>>>(static_cast<const uint16_t*>(x), rows,
+                                                       cols / 8, ld, bits);
+    }
+  }
+  if (tensor_exp) nv_tensor_exp_kernel<<<1, 1, 0, st>>>(bits, tensor_exp);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t cols, int64_t ld,

@@ -96,7 +96,7 @@ __device__ __forceinline__ void store_run32(const OrientArgs& o, int64_t orow, i
 // rows, one per lane, for 32x32 blocks), scale, round, pack, store.
 __device__ __forceinline__ void quantize_run32(float2 (&R)[16], int64_t row, int64_t c0, int64_t cols,
                                                const OrientArgs& o) {
-  if (o.wht) hadamard32_lane(R, o.sign_mask);
+  if (o.wht) hadamard32_lane(R, o.sign_mask, o.sgn);
   float M = absmax32(R);
   if (o.block) M = warp_max(M);
   uint32_t w[16];

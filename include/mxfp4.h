@@ -316,6 +316,25 @@ mxfp4_status hadamard32(const void* x, int32_t x_dtype, int64_t rows, int64_t co
                         int64_t ld_x, uint32_t sign_mask, int32_t inverse, float* y,
                         void* stream);
 
+/* The per-tensor factor of the 1x16 block format ([TIBQ], "Why FP4 training
+ * is the current frontier of precision reduction": NVFP4 blocks whose scale
+ * follows the block max-abs, under a tensor-wide factor): computed on the
+ * device so a training step can carry it to the next step without a host
+ * round trip.
+ *  x          [rows, cols] bf16 or fp32 (x_dtype), leading dimension ld_x;
+ *             shape and alignment rules as mxfp4_quantize (cols % 32 == 0).
+ *  amax       device pointer to one float (4-byte aligned): receives the
+ *             largest |x| (0 for an empty tensor).
+ *  tensor_exp device pointer to one int32 or NULL: receives the smallest k
+ *             with 2688 * 2^k >= amax (2688 = 6 * 448: the largest block
+ *             scale amax / (6 * 2^k) then fits E4M3), clamped to [-100, 100],
+ *             0 when amax is 0 -- the tensor_exp mxfp4_quantize takes for
+ *             MXFP4_BLOCK_1X16.
+ * Enqueued on `stream` (a memset of *amax, the reduction, and a one-thread
+ * kernel for tensor_exp). Inputs must be finite. */
+mxfp4_status mxfp4_tensor_amax(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
+                               int64_t ld_x, float* amax, int32_t* tensor_exp, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* mxfp4_status_string(mxfp4_status s);
 

@@ -23,9 +23,8 @@ WHTS = [(False, 0), (True, 0), (True, 0x9E3779B9)]
 
 
 def _k(x: torch.Tensor) -> int:
-    import gemm_pt_block_gb300 as mx
-
-    return mx.nvfp4_tensor_exp(float(x.float().abs().max()))
+    """The tensor's NVFP4 exponent as the oracle defines it."""
+    return oracle.nv_tensor_exp(oracle.tensor_amax(oracle_input(x.cpu())))
 
 
 def _input(rows, cols, dtype, seed, scale=1.0):
