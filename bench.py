@@ -336,14 +336,15 @@ class ClockSampler:
               "clocks_event_reasons.sw_power_cap")
     NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: int = 100):
         self.index, self.proc, self.lines = index, None, []
+        self.interval_ms = interval_ms
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
             time.sleep(0.3)
@@ -379,9 +380,13 @@ class ClockSampler:
             for n, v in zip(self.NAMES, parts[3:7]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+        # samples taken under load: power at least half of the largest seen
+        loaded = [c for c, w in zip(sm, power) if power and w >= 0.5 * max(power)]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
                 "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None}
+                "power_w_max": max(power) if power else None,
+                "sm_mhz_loaded": statistics.median(loaded) if loaded else None,
+                "samples_loaded": len(loaded)}
 
 
 def source_digest(path: str) -> str:
@@ -856,6 +861,79 @@ def run_2d(args):
     return 0
 
 
+def run_ceiling(args):
+    """Context for the GEMM's roofline: the three 70B-layer GEMM shapes, timed
+    alone with CUDA events as a short burst (20 launches) and a sustained run
+    (1500 launches, ~2 s) with the SM clock, power and power-cap flag sampled
+    every 50 ms; and cuBLAS's block-scaled FP4 GEMM (torch._scaled_mm with
+    NVFP4 operands: E2M1, E4M3 scales per 16, bf16 out; MXFP4 where this torch
+    supports it) on the same shapes, as a measured achievable rate. One JSON
+    line per measurement."""
+    import torch
+    import gemm_pt_block_gb300 as mx
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+
+    def clocked(fn, n):
+        torch.cuda.synchronize()
+        with ClockSampler(0, interval_ms=50) as clk:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n, clk.summary()
+
+    spec = make_spec("70b-layer")
+    st = Step(spec, dev)
+    st.run()
+    torch.cuda.synchronize()
+    for g in spec.gemms:
+        qa, sa = st.operand(g.a)
+        qb, sb = st.operand(g.b)
+        fn = lambda: mx.mxfp4_gemm(qa, sa, qb, sb, g.M, g.N, g.K, c=st.outs[g.label], workspace=st.ws)
+        for n in (20, 1500):
+            ms, clk = clocked(fn, n)
+            print(json.dumps({"ceiling": "mxfp4_gemm (this library, fp32 C)", "gemm": g.label,
+                              "M": g.M, "N": g.N, "K": g.K, "launches": n, "ms": ms,
+                              "tflops": 2.0 * g.M * g.N * g.K / (ms / 1e3) / 1e12, "clocks": clk}),
+                  flush=True)
+    del st
+    torch.cuda.empty_cache()
+    fp4 = getattr(torch, "float4_e2m1fn_x2", None)
+    for g in spec.gemms:
+        M, N, K = g.M, g.N, g.K
+        for kind in ("nvfp4", "mxfp4"):
+            try:
+                if fp4 is None:
+                    raise RuntimeError("this torch has no float4_e2m1fn_x2")
+                a = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=dev).view(fp4)
+                b = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev).view(fp4)
+                if kind == "nvfp4":
+                    s_a = (torch.rand(M * K // 16, device=dev) + 0.5).to(torch.float8_e4m3fn)
+                    s_b = (torch.rand(N * K // 16, device=dev) + 0.5).to(torch.float8_e4m3fn)
+                else:
+                    s_a = torch.randint(120, 134, (M * K // 32,), dtype=torch.uint8,
+                                        device=dev).view(torch.float8_e8m0fnu)
+                    s_b = torch.randint(120, 134, (N * K // 32,), dtype=torch.uint8,
+                                        device=dev).view(torch.float8_e8m0fnu)
+                fn = lambda: torch._scaled_mm(a, b.t(), s_a, s_b, out_dtype=torch.bfloat16)
+                fn()
+                for n in (20, 1500):
+                    ms, clk = clocked(fn, n)
+                    print(json.dumps({"ceiling": f"cuBLAS {kind} (torch._scaled_mm, bf16 C)",
+                                      "gemm": g.label, "M": M, "N": N, "K": K, "launches": n,
+                                      "ms": ms, "tflops": 2.0 * M * N * K / (ms / 1e3) / 1e12,
+                                      "clocks": clk}), flush=True)
+                del a, b, s_a, s_b
+            except Exception as e:   # the torch build may not offer this scaling
+                print(json.dumps({"ceiling": f"cuBLAS {kind} (torch._scaled_mm)", "gemm": g.label,
+                                  "unavailable": repr(e).splitlines()[0][:200]}), flush=True)
+    return 0
+
+
 def run_sweep(args):
     """Quantizer throughput over the square sweep (algorithmic bytes / time,
     against the measured HBM copy peak). Between timed launches a 512 MB
@@ -951,6 +1029,9 @@ def main():
                          "random-sign rotation}) and both dual-orientation block types; one JSON "
                          "line per point (L2 flushed between launches)")
     ap.add_argument("--oracle-sample", type=int, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--ceiling", action="store_true",
+                    help="time the 70B GEMM shapes alone (burst and sustained, with clocks) and "
+                         "cuBLAS's block-scaled FP4 GEMM on the same shapes; one JSON line each")
     ap.add_argument("--op", default=None,
                     help="profiling aid: allocate and time only this operation of the workload's "
                          "step (a quantizer name such as dY, or a GEMM label such as Fprop); prints "
@@ -966,6 +1047,8 @@ def main():
         return run_op(args)
     if args.sweep:
         return run_sweep(args)
+    if args.ceiling:
+        return run_ceiling(args)
 
     import torch
 
