@@ -24,7 +24,7 @@ _SRC = os.path.join(_HERE, "mxfp4_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle_mxfp4.so")
 
 BLOCK_1X32, BLOCK_32X32, BLOCK_64X64, BLOCK_1X16 = 0, 1, 2, 3
-FORMAT_E2M1, FORMAT_E4M3 = 0, 1
+FORMAT_E2M1, FORMAT_E4M3, FORMAT_E5M2 = 0, 1, 2
 SCALE_FLOOR, SCALE_ROUNDUP = 0, 1
 ROUND_RTN, ROUND_SR = 0, 1
 LAYOUT_ROWMAJOR, LAYOUT_MMA = 0, 1
@@ -72,7 +72,7 @@ class Params:
     wht_sign_mask: int = 0
     seed: int = 0
     sr_stream: int = 0
-    elem_format: int = 0        # FORMAT_E2M1 (MXFP4) or FORMAT_E4M3 (MXFP8)
+    elem_format: int = 0        # FORMAT_E2M1 (MXFP4), FORMAT_E4M3 or FORMAT_E5M2 (MXFP8)
     tensor_exp: int = 0         # BLOCK_1X16 (NVFP4): per-tensor factor 2^tensor_exp
 
     def _c(self) -> _Params:
@@ -116,6 +116,12 @@ def lib() -> ctypes.CDLL:
         L.orc_scale_exponent_fmt.argtypes = [ctypes.c_float, ctypes.c_int, ctypes.c_int]
         L.orc_dequantize_e4m3_f64.restype = ctypes.c_int
         L.orc_dequantize_e4m3_f64.argtypes = [P, P, ctypes.c_int, i64, i64, P]
+        L.orc_dequantize_fp8_f64.restype = ctypes.c_int
+        L.orc_dequantize_fp8_f64.argtypes = [P, P, ctypes.c_int, i64, i64, ctypes.c_int, P]
+        L.orc_e5m2_value.restype = ctypes.c_float
+        L.orc_e5m2_value.argtypes = [ctypes.c_int]
+        L.orc_round_e5m2_rtn.restype = ctypes.c_int
+        L.orc_round_e5m2_rtn.argtypes = [ctypes.c_float]
         for fn in (L.orc_quantize_rows, L.orc_quantize_cols):
             fn.restype = ctypes.c_int
             fn.argtypes = [P, ctypes.c_int, i64, i64, i64, ctypes.POINTER(_Params), i64, i64, P, P]
@@ -204,6 +210,14 @@ def round_e4m3_rtn(v: float) -> int:
     return int(lib().orc_round_e4m3_rtn(ctypes.c_float(v)))
 
 
+def e5m2_value(code: int) -> float:
+    return float(lib().orc_e5m2_value(code))
+
+
+def round_e5m2_rtn(v: float) -> int:
+    return int(lib().orc_round_e5m2_rtn(ctypes.c_float(v)))
+
+
 def scale_exponent_fmt(M: float, mode: int, fmt: int) -> int:
     return int(lib().orc_scale_exponent_fmt(ctypes.c_float(M), mode, fmt))
 
@@ -236,7 +250,8 @@ def quantize_rows(x: np.ndarray, p: Params, r0: int = 0, r1: int | None = None):
     x, dt, ld = _as_input(x)
     rows, cols = x.shape
     r1 = rows if r1 is None else r1
-    q = np.zeros((r1 - r0, cols if p.elem_format == FORMAT_E4M3 else cols // 2), dtype=np.uint8)
+    q = np.zeros((r1 - r0, cols if p.elem_format in (FORMAT_E4M3, FORMAT_E5M2) else cols // 2),
+                 dtype=np.uint8)
     s = np.zeros((r1 - r0, p.scale_cols(cols)), dtype=np.uint8)
     cp = p._c()
     rc = lib().orc_quantize_rows(_ptr(x), dt, rows, cols, ld, ctypes.byref(cp), r0, r1, _ptr(q), _ptr(s))
@@ -250,7 +265,8 @@ def quantize_cols(x: np.ndarray, p: Params, c0: int = 0, c1: int | None = None):
     x, dt, ld = _as_input(x)
     rows, cols = x.shape
     c1 = cols if c1 is None else c1
-    q = np.zeros((c1 - c0, rows if p.elem_format == FORMAT_E4M3 else rows // 2), dtype=np.uint8)
+    q = np.zeros((c1 - c0, rows if p.elem_format in (FORMAT_E4M3, FORMAT_E5M2) else rows // 2),
+                 dtype=np.uint8)
     s = np.zeros((c1 - c0, p.scale_cols(rows)), dtype=np.uint8)
     cp = p._c()
     rc = lib().orc_quantize_cols(_ptr(x), dt, rows, cols, ld, ctypes.byref(cp), c0, c1, _ptr(q), _ptr(s))
@@ -276,9 +292,9 @@ def dequantize(q: np.ndarray, s: np.ndarray, rows: int, cols: int,
                layout: int = LAYOUT_ROWMAJOR, f64: bool = False, fmt: int = FORMAT_E2M1) -> np.ndarray:
     q = np.ascontiguousarray(q, dtype=np.uint8)
     s = np.ascontiguousarray(s, dtype=np.uint8)
-    if fmt == FORMAT_E4M3:
+    if fmt in (FORMAT_E4M3, FORMAT_E5M2):
         out = np.zeros((rows, cols), dtype=np.float64)
-        if lib().orc_dequantize_e4m3_f64(_ptr(q), _ptr(s), layout, rows, cols, _ptr(out)):
+        if lib().orc_dequantize_fp8_f64(_ptr(q), _ptr(s), layout, rows, cols, fmt, _ptr(out)):
             raise ValueError("oracle dequantize: bad shape")
         return out if f64 else out.astype(np.float32)
     out = np.zeros((rows, cols), dtype=np.float64 if f64 else np.float32)

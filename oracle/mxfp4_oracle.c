@@ -144,8 +144,11 @@ void orc_wht32(const float in[32], uint32_t sign_mask, int inverse, float out[32
  * stored byte is e + 127 (0xFF, the E8M0 NaN, is never produced).
  * Computed with exact fp64 frexp/ldexp. */
 int orc_scale_exponent_fmt(float M, int scale_mode, int elem_format) {
-  const int emax = elem_format == ORC_FORMAT_E4M3 ? 8 : 2;         /* exponent of the largest element */
-  const double vmax = elem_format == ORC_FORMAT_E4M3 ? 448.0 : 6.0; /* largest element value */
+  /* exponent and value of the largest element: E2M1 6 = 1.5 * 2^2, E4M3
+   * 448 = 1.75 * 2^8, E5M2 57344 = 1.75 * 2^15 */
+  const int emax = elem_format == ORC_FORMAT_E4M3 ? 8 : (elem_format == ORC_FORMAT_E5M2 ? 15 : 2);
+  const double vmax = elem_format == ORC_FORMAT_E4M3 ? 448.0
+                      : (elem_format == ORC_FORMAT_E5M2 ? 57344.0 : 6.0);
   int e;
   if (!(M > 0.0f)) {
     e = -127;
@@ -189,6 +192,36 @@ int orc_round_e4m3_rtn(float v) {
   double bestd = a;
   for (int k = 1; k < 127; ++k) {                   /* the finite non-negative codes */
     const double d = fabs(a - (double)orc_e4m3_value(k));
+    if (d < bestd || (d == bestd && (k % 2) == 0 && (best % 2) != 0)) {
+      best = k;
+      bestd = d;
+    }
+  }
+  return (signbit(v) ? 0x80 : 0) | best;
+}
+
+/* -------------------------------------------------------------- E5M2 ---- */
+/* The other OCP FP8 element format of the same MX family: sign, 5 exponent
+ * bits (bias 15), 2 mantissa bits; exponent field 31 holds infinities
+ * (mantissa 0) and NaNs; subnormals m/4 * 2^-14; largest finite 57344. */
+float orc_e5m2_value(int code) {
+  const int sgn = (code >> 7) & 1, E = (code >> 2) & 31, m = code & 3;
+  double v;
+  if (E == 31) v = m ? NAN : INFINITY;
+  else if (E == 0) v = ldexp((double)m, -16);
+  else v = ldexp(1.0 + m / 4.0, E - 15);
+  return (float)(sgn ? -v : v);
+}
+
+/* Nearest finite E5M2 code, ties to the even code, saturating at 57344, sign
+ * kept: direct search over the 124 finite non-negative codes. */
+int orc_round_e5m2_rtn(float v) {
+  double a = fabs((double)v);
+  if (a > 57344.0) a = 57344.0;
+  int best = 0;
+  double bestd = a;
+  for (int k = 1; k < 124; ++k) {
+    const double d = fabs(a - (double)orc_e5m2_value(k));
     if (d < bestd || (d == bestd && (k % 2) == 0 && (best % 2) != 0)) {
       best = k;
       bestd = d;
@@ -331,10 +364,11 @@ static int quantize_orient(const void* x, int dtype, int64_t rows, int64_t cols,
   /* g output rows by bw values of k share one scale */
   const int g = p->block == ORC_BLOCK_64X64 ? 64 : (p->block == ORC_BLOCK_32X32 ? 32 : 1);
   const int bw = p->block == ORC_BLOCK_64X64 ? 64 : 32;
-  const int e4m3 = p->elem_format == ORC_FORMAT_E4M3;
+  /* 8-bit elements (MXFP8): E4M3 or E5M2, one byte each */
+  const int fp8 = p->elem_format == ORC_FORMAT_E4M3 || p->elem_format == ORC_FORMAT_E5M2;
   if (K % bw != 0 || i0 < 0 || i1 > nout || i0 > i1) return -1;
-  if (p->elem_format != ORC_FORMAT_E2M1 && !e4m3) return -1;
-  if (e4m3 && p->rounding != ORC_ROUND_RTN) return -1;   /* nearest only for MXFP8 */
+  if (p->elem_format != ORC_FORMAT_E2M1 && !fp8) return -1;
+  if (fp8 && p->rounding != ORC_ROUND_RTN) return -1;   /* nearest only for MXFP8 */
   if (g > 1 && (nout % g != 0 || i0 % g != 0 || i1 % g != 0)) return -1;
   const int64_t nkb = K / 32;
   const int64_t ngroups = (i1 - i0) / g;
@@ -374,8 +408,9 @@ static int quantize_orient(const void* x, int dtype, int64_t rows, int64_t cols,
           const int64_t k = kb0 * bw + j;
           const float v = y[t][j] * inv_scale;
           int code;
-          if (e4m3) {
-            q[orow * K + k] = (uint8_t)orc_round_e4m3_rtn(v);
+          if (fp8) {
+            q[orow * K + k] = (uint8_t)(p->elem_format == ORC_FORMAT_E5M2 ? orc_round_e5m2_rtn(v)
+                                                                         : orc_round_e4m3_rtn(v));
             continue;
           }
           if (p->rounding == ORC_ROUND_SR) {
@@ -531,17 +566,26 @@ int orc_dequantize_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t r
   return 0;
 }
 
-int orc_dequantize_e4m3_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
-                            int64_t cols, double* out) {
+int orc_dequantize_fp8_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
+                           int64_t cols, int elem_format, double* out) {
   if (deq_check(layout, rows, cols)) return -1;
+  if (elem_format != ORC_FORMAT_E4M3 && elem_format != ORC_FORMAT_E5M2) return -1;
   const int64_t nkb = cols / 32;
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t c = 0; c < cols; ++c) {
       const uint8_t sb = (layout == ORC_LAYOUT_MMA) ? s[orc_mma_scale_offset(r, c / 32, rows, nkb)]
                                                     : s[r * nkb + c / 32];
-      out[r * cols + c] = sb == 0xFF ? NAN : ldexp((double)orc_e4m3_value(q[r * cols + c]), (int)sb - 127);
+      const int code = q[r * cols + c];
+      const double v = elem_format == ORC_FORMAT_E5M2 ? (double)orc_e5m2_value(code)
+                                                      : (double)orc_e4m3_value(code);
+      out[r * cols + c] = sb == 0xFF ? NAN : ldexp(v, (int)sb - 127);
     }
   return 0;
+}
+
+int orc_dequantize_e4m3_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
+                            int64_t cols, double* out) {
+  return orc_dequantize_fp8_f64(q, s, layout, rows, cols, ORC_FORMAT_E4M3, out);
 }
 
 /* NVFP4 reconstruction: E2M1(code) * E4M3(scale) * 2^tensor_exp. */

@@ -26,7 +26,7 @@ enum { ORC_SCALE_FLOOR = 0, ORC_SCALE_ROUNDUP = 1 };
 enum { ORC_ROUND_RTN = 0, ORC_ROUND_SR = 1 };
 enum { ORC_LAYOUT_ROWMAJOR = 0, ORC_LAYOUT_MMA = 1 };
 enum { ORC_DTYPE_BF16 = 0, ORC_DTYPE_F32 = 1 };
-enum { ORC_FORMAT_E2M1 = 0, ORC_FORMAT_E4M3 = 1 };
+enum { ORC_FORMAT_E2M1 = 0, ORC_FORMAT_E4M3 = 1, ORC_FORMAT_E5M2 = 2 };
 
 typedef struct {
   int block;              /* ORC_BLOCK_* */
@@ -37,7 +37,7 @@ typedef struct {
   uint32_t wht_sign_mask; /* bit i set => sign -1 on element i of a block */
   uint64_t seed;          /* Philox key */
   uint32_t sr_stream;     /* Philox counter word 2 */
-  int elem_format;        /* ORC_FORMAT_*: E2M1 (MXFP4) or E4M3 (MXFP8, nearest only) */
+  int elem_format;        /* ORC_FORMAT_*: E2M1 (MXFP4), E4M3 or E5M2 (MXFP8, nearest only) */
   int tensor_exp;         /* 1x16 (NVFP4) only: per-tensor factor 2^tensor_exp; else 0 */
 } orc_params;
 
@@ -66,9 +66,16 @@ int orc_round_sr(float v, uint32_t r16);
 float orc_e4m3_value(int code);
 int orc_round_e4m3_rtn(float v);
 
+/* OCP FP8 E5M2 (sign, 5 exponent bits with bias 15, 2 mantissa bits;
+ * S.11111.00 infinite, S.11111.xx NaN otherwise, largest finite 57344):
+ * code -> value, and the nearest finite code to v (ties to the even code,
+ * saturating at 57344, sign kept). */
+float orc_e5m2_value(int code);
+int orc_round_e5m2_rtn(float v);
+
 /* Scale exponent for an element format: floor: floor(log2 M) - emax (emax 2
- * for E2M1, 8 for E4M3); round-up: the smallest e with max * 2^e >= M (max 6
- * or 448). orc_scale_exponent is the E2M1 case. */
+ * for E2M1, 8 for E4M3, 15 for E5M2); round-up: the smallest e with
+ * max * 2^e >= M (max 6, 448 or 57344). orc_scale_exponent is the E2M1 case. */
 int orc_scale_exponent_fmt(float M, int scale_mode, int elem_format);
 
 /* NVFP4 block scale: the E4M3 code (0 .. 126) of the scale S of a 1x16 block
@@ -114,7 +121,10 @@ int orc_dequantize_f32(const uint8_t* q, const uint8_t* s, int layout, int64_t r
                        int64_t cols, float* out);
 int orc_dequantize_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
                        int64_t cols, double* out);
-/* The same for E4M3 codes q [rows, cols] (one byte per element). */
+/* The same for 8-bit codes q [rows, cols] (one byte per element) of
+ * elem_format ORC_FORMAT_E4M3 or ORC_FORMAT_E5M2; the E4M3 form kept too. */
+int orc_dequantize_fp8_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
+                           int64_t cols, int elem_format, double* out);
 int orc_dequantize_e4m3_f64(const uint8_t* q, const uint8_t* s, int layout, int64_t rows,
                             int64_t cols, double* out);
 

@@ -637,6 +637,89 @@ def test_mxfp8_quantize_by_elementwise_definition():
         oracle.quantize_rows(xb, oracle.Params(rounding=oracle.ROUND_SR, elem_format=oracle.FORMAT_E4M3))
 
 
+def test_e5m2_decode_matches_torch_float8_e5m2():
+    """All 256 E5M2 codes decode like PyTorch's float8_e5m2 (OCP FP8 E5M2:
+    bias 15, S.11111.00 infinite, other S.11111.xx NaN, largest finite 57344)."""
+    import torch
+
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e5m2).float().numpy()
+    for c in range(256):
+        got = oracle.e5m2_value(c)
+        if np.isnan(ref[c]):
+            assert math.isnan(got), c
+        else:
+            assert got == ref[c], c
+
+
+def test_e5m2_nearest_even_matches_torch_and_saturates():
+    """Within the finite range the nearest-even code equals PyTorch's cast;
+    above 57344 the oracle saturates to the largest finite code (the cast
+    would give infinity there)."""
+    import torch
+
+    vals = [oracle.e5m2_value(c) for c in range(124)]          # 0 .. 57344
+    pts = []
+    for a, b in zip(vals[:-1], vals[1:]):
+        mid = (a + b) / 2
+        pts += [a, mid, np.nextafter(np.float32(mid), np.float32(0)),
+                np.nextafter(np.float32(mid), np.float32(1e9)), b]
+    rng = np.random.default_rng(74)
+    pts += list(rng.uniform(0, 57344, 4000).astype(np.float32))
+    pts += list((2.0 ** rng.uniform(-17, -14, 1000)).astype(np.float32))   # subnormal range
+    x = np.array(pts, dtype=np.float32)
+    x = np.concatenate([x, -x])
+    ref = torch.from_numpy(x).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    for v, r in zip(x, ref):
+        assert oracle.round_e5m2_rtn(float(v)) == int(r), float(v)
+    for v in (57344.0, 60000.0, 61439.0, 1e6, 3.0e38):
+        assert oracle.round_e5m2_rtn(v) == 0x7B
+        assert oracle.round_e5m2_rtn(-v) == 0xFB
+
+
+def test_e5m2_scale_exponent_definitions():
+    rng = np.random.default_rng(75)
+    for M in list(2.0 ** rng.uniform(-100, 100, 300)) + [57344.0, 57345.0, 114688.0, 1.0, 0.75]:
+        M = float(np.float32(M))
+        fl = math.floor(math.log2(Fraction(M)))
+        while Fraction(2) ** (fl + 1) <= Fraction(M):
+            fl += 1
+        while Fraction(2) ** fl > Fraction(M):
+            fl -= 1
+        ef = oracle.scale_exponent_fmt(M, oracle.SCALE_FLOOR, oracle.FORMAT_E5M2)
+        eu = oracle.scale_exponent_fmt(M, oracle.SCALE_ROUNDUP, oracle.FORMAT_E5M2)
+        assert ef == max(-127, min(127, fl - 15))
+        assert 57344 * Fraction(2) ** eu >= Fraction(M) > 57344 * Fraction(2) ** (eu - 1)
+
+
+def test_mxfp8_e5m2_quantize_by_elementwise_definition():
+    """1x32 and 32x32 blocks with E5M2 elements: e from the block max (pinned
+    exponent), each byte the nearest E5M2 code of x / 2^e (pinned rounding);
+    both orientations."""
+    rows, cols = 64, 96
+    xb = _bf16(synth.laplace(rows, cols, 1e-3, seed=76, outlier_frac=0.01))
+    xv = (xb.view(np.uint16).astype(np.uint32) << 16).view(np.float32).reshape(rows, cols)
+    for block, g in ((oracle.BLOCK_1X32, 1), (oracle.BLOCK_32X32, 32)):
+        for mode in (oracle.SCALE_FLOOR, oracle.SCALE_ROUNDUP):
+            p = oracle.Params(block=block, scale_mode=mode, elem_format=oracle.FORMAT_E5M2)
+            q, s = oracle.quantize_rows(xb, p)
+            assert q.shape == (rows, cols)
+            for r0 in range(0, rows, g):
+                for kb in range(cols // 32):
+                    blk = xv[r0:r0 + g, 32 * kb:32 * kb + 32]
+                    e = oracle.scale_exponent_fmt(float(np.max(np.abs(blk))), mode, oracle.FORMAT_E5M2)
+                    assert np.all(s[r0:r0 + g, kb] == e + 127)
+                    for i in range(g):
+                        for j in range(32):
+                            want = oracle.round_e5m2_rtn(float(blk[i, j]) * 2.0 ** -e)
+                            assert q[r0 + i, 32 * kb + j] == want
+            d = oracle.dequantize(q, s, rows, cols, fmt=oracle.FORMAT_E5M2, f64=True)
+            assert np.all(np.isfinite(d))
+            qc, sc = oracle.quantize_cols(xb, p)
+            qt, st = oracle.quantize_rows(np.ascontiguousarray(xb.T), p)
+            assert np.array_equal(qc, qt) and np.array_equal(sc, st)
+
+
 # ------------------------------------------------------- NVFP4 (1x16, E4M3) --
 
 def _e4m3_grid_round(t: Fraction, up: bool) -> Fraction:
