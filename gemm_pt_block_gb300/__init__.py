@@ -27,6 +27,7 @@ from .binding import (  # noqa: F401
     DTYPE_F32,
     FORMAT_E2M1,
     FORMAT_E4M3,
+    FORMAT_E5M2,
     LAYOUT_MMA,
     LAYOUT_ROWMAJOR,
     ROUND_RTN,

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libmxfp4.so"
 
 BLOCK_1X32, BLOCK_32X32, BLOCK_64X64, BLOCK_1X16 = 0, 1, 2, 3
-FORMAT_E2M1, FORMAT_E4M3 = 0, 1
+FORMAT_E2M1, FORMAT_E4M3, FORMAT_E5M2 = 0, 1, 2
 SCALE_FLOOR, SCALE_ROUNDUP = 0, 1
 ROUND_RTN, ROUND_SR = 0, 1
 LAYOUT_ROWMAJOR, LAYOUT_MMA = 0, 1
@@ -60,7 +60,7 @@ class QuantParams:
     wht_sign_mask: int = 0
     seed: int = 0
     sr_stream: int = 0
-    elem_format: int = 0          # FORMAT_E2M1 (MXFP4) or FORMAT_E4M3 (MXFP8)
+    elem_format: int = 0          # FORMAT_E2M1 (MXFP4), FORMAT_E4M3 or FORMAT_E5M2 (MXFP8)
     tensor_exp: int = 0           # BLOCK_1X16 (NVFP4): per-tensor factor 2^tensor_exp
 
     def _c(self) -> _CParams:
@@ -71,7 +71,7 @@ class QuantParams:
 
     def code_cols(self, k: int) -> int:
         """Bytes of codes per output row for K elements."""
-        return k if self.elem_format == FORMAT_E4M3 else k // 2
+        return k if self.elem_format in (FORMAT_E4M3, FORMAT_E5M2) else k // 2
 
     def scale_cols(self, k: int) -> int:
         """Scale bytes per output row for K elements (one per block along K)."""
@@ -115,6 +115,8 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_gemm.argtypes = [P, P, i32, P, P, i32, i64, i64, i64, P, i32, i64, P, sz, P]
         L.mxfp8_gemm.restype = i32
         L.mxfp8_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P]
+        L.mxfp8_gemm_ex.restype = i32
+        L.mxfp8_gemm_ex.argtypes = [P, P, P, P, i64, i64, i64, ctypes.c_uint32, P, i32, i64, P]
         L.mxfp4_gemm_quantize.restype = i32
         L.mxfp4_gemm_quantize.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64,
                                           ctypes.POINTER(_CParams), P, P,
@@ -295,16 +297,22 @@ def mxfp4_gemm_noalloc(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb:
 
 def mxfp8_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.Tensor,
                M: int, N: int, K: int, *, c=None, ldc: int | None = None,
-               out_dtype: torch.dtype = torch.float32, stream=None):
-    """C[M, N] = deq(A) deq(B)^T for MXFP8 operands: E4M3 codes [M, K] / [N, K],
-    E8M0 scales in tensor-core layout; C fp32 or bf16 as in mxfp4_gemm."""
+               out_dtype: torch.dtype = torch.float32, elem_format: int = FORMAT_E4M3,
+               stream=None):
+    """C[M, N] = deq(A) deq(B)^T for MXFP8 operands: E4M3 (or, with
+    elem_format=FORMAT_E5M2, E5M2) codes [M, K] / [N, K], E8M0 scales in
+    tensor-core layout; C fp32 or bf16 as in mxfp4_gemm."""
     _check_operands(qa, sa, qb, sb)
     cdt = _c_dtype(c, out_dtype)
     if c is None:
         c = torch.empty((M, N), dtype=out_dtype, device=qa.device)
     ldc = c.stride(0) if ldc is None else ldc
-    _check(lib().mxfp8_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), cdt, ldc,
-                            _stream(qa, stream)))
+    if elem_format == FORMAT_E4M3:
+        _check(lib().mxfp8_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), cdt, ldc,
+                                _stream(qa, stream)))
+    else:
+        _check(lib().mxfp8_gemm_ex(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, elem_format,
+                                   _ptr(c), cdt, ldc, _stream(qa, stream)))
     return c
 
 

@@ -54,9 +54,10 @@ mxfp4_status check_params(const mxfp4_quant_params* p, uint8_t* q, uint8_t* s, i
   if (p->scale_layout != MXFP4_LAYOUT_ROWMAJOR && p->scale_layout != MXFP4_LAYOUT_MMA)
     return fail(MXFP4_ERR_INVALID_ARG, "%s: bad scale_layout %d", name, p->scale_layout);
   if (p->wht != 0 && p->wht != 1) return fail(MXFP4_ERR_INVALID_ARG, "%s: wht must be 0/1", name);
-  if (p->elem_format != MXFP4_FORMAT_E2M1 && p->elem_format != MXFP4_FORMAT_E4M3)
+  if (p->elem_format != MXFP4_FORMAT_E2M1 && p->elem_format != MXFP4_FORMAT_E4M3 &&
+      p->elem_format != MXFP4_FORMAT_E5M2)
     return fail(MXFP4_ERR_INVALID_ARG, "%s: bad elem_format %u", name, p->elem_format);
-  if (p->elem_format == MXFP4_FORMAT_E4M3 && p->rounding == MXFP4_ROUND_SR)
+  if (p->elem_format != MXFP4_FORMAT_E2M1 && p->rounding == MXFP4_ROUND_SR)
     return fail(MXFP4_ERR_UNSUPPORTED, "%s: stochastic rounding is available for E2M1 only", name);
   if (p->scale_layout == MXFP4_LAYOUT_MMA && (out_rows % 128 != 0 || k % 128 != 0))
     return fail(MXFP4_ERR_SHAPE,
@@ -70,7 +71,8 @@ mxfp4_status check_params(const mxfp4_quant_params* p, uint8_t* q, uint8_t* s, i
   o->sr = p->rounding == MXFP4_ROUND_SR;
   o->mma_layout = p->scale_layout == MXFP4_LAYOUT_MMA;
   o->wht = p->wht;
-  o->e4m3 = p->elem_format == MXFP4_FORMAT_E4M3;
+  o->e4m3 = p->elem_format == MXFP4_FORMAT_E4M3 || p->elem_format == MXFP4_FORMAT_E5M2;
+  o->e5m2 = p->elem_format == MXFP4_FORMAT_E5M2;
   o->sign_mask = p->wht_sign_mask;
   o->seed = p->seed;
   o->stream = p->sr_stream;
@@ -168,14 +170,15 @@ mxfp4_status mxfp4_dequantize_ex(const uint8_t* q, const uint8_t* s, int32_t sca
   if (block != MXFP4_BLOCK_1X32 && block != MXFP4_BLOCK_32X32 && block != MXFP4_BLOCK_64X64 &&
       block != MXFP4_BLOCK_1X16)
     return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_dequantize_ex: bad block %d", block);
-  if (elem_format != MXFP4_FORMAT_E2M1 && elem_format != MXFP4_FORMAT_E4M3)
+  if (elem_format != MXFP4_FORMAT_E2M1 && elem_format != MXFP4_FORMAT_E4M3 &&
+      elem_format != MXFP4_FORMAT_E5M2)
     return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_dequantize_ex: bad elem_format %u", elem_format);
   const bool nv = block == MXFP4_BLOCK_1X16;
   if (nv && elem_format != MXFP4_FORMAT_E2M1)
     return fail(MXFP4_ERR_UNSUPPORTED, "mxfp4_dequantize_ex: 1x16 blocks take E2M1 elements");
   if (nv ? (tensor_exp < -100 || tensor_exp > 100) : tensor_exp != 0)
     return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_dequantize_ex: bad tensor_exp %d", tensor_exp);
-  const int fmt = nv ? 2 : (elem_format == MXFP4_FORMAT_E4M3 ? 1 : 0);
+  const int fmt = nv ? 2 : (elem_format == MXFP4_FORMAT_E4M3 ? 1 : (elem_format == MXFP4_FORMAT_E5M2 ? 3 : 0));
   return dequantize_common("mxfp4_dequantize_ex", q, s, scale_layout, fmt, tensor_exp, rows, cols,
                            out, stream);
 }
@@ -254,10 +257,13 @@ mxfp4_status mxfp4_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
                      workspace, workspace_bytes, stream);
 }
 
-mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
-                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
-                        int32_t c_dtype, int64_t ldc, void* stream) {
+namespace {
+mxfp4_status mxfp8_common(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                          const uint8_t* sb, int64_t M, int64_t N, int64_t K, uint32_t elem_format,
+                          void* c, int32_t c_dtype, int64_t ldc, void* stream) {
   if (!qa || !sa || !qb || !sb || !c) return fail(MXFP4_ERR_INVALID_ARG, "mxfp8_gemm: NULL pointer");
+  if (elem_format != MXFP4_FORMAT_E4M3 && elem_format != MXFP4_FORMAT_E5M2)
+    return fail(MXFP4_ERR_INVALID_ARG, "mxfp8_gemm: elem_format %u is not E4M3 or E5M2", elem_format);
   if (c_dtype != MXFP4_DTYPE_BF16 && c_dtype != MXFP4_DTYPE_F32)
     return fail(MXFP4_ERR_INVALID_ARG, "mxfp8_gemm: bad c_dtype %d", c_dtype);
   if (M <= 0 || N <= 0 || K <= 0 || M % 256 != 0 || N % 256 != 0 || K % 128 != 0)
@@ -269,11 +275,26 @@ mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   if (!aligned16(qa) || !aligned16(qb) || !aligned16(sa) || !aligned16(sb) || !aligned16(c) || ldc % 8 != 0)
     return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");
   const char* why = "";
-  cudaError_t e = mx::launch_gemm_f8(qa, sa, qb, sb, M, N, K, c, c_dtype == MXFP4_DTYPE_BF16, ldc,
+  cudaError_t e = mx::launch_gemm_f8(qa, sa, qb, sb, M, N, K, elem_format == MXFP4_FORMAT_E5M2, c,
+                                     c_dtype == MXFP4_DTYPE_BF16, ldc,
                                      static_cast<cudaStream_t>(stream), &why);
   if (e == cudaErrorNotSupported) return fail(MXFP4_ERR_UNSUPPORTED, "%s", why);
   if (e == cudaErrorInvalidValue && why[0]) return fail(MXFP4_ERR_ALIGN, "%s", why);
   return from_cuda(e, "mxfp8_gemm");
+}
+}  // namespace
+
+mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                        const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                        int32_t c_dtype, int64_t ldc, void* stream) {
+  return mxfp8_common(qa, sa, qb, sb, M, N, K, MXFP4_FORMAT_E4M3, c, c_dtype, ldc, stream);
+}
+
+mxfp4_status mxfp8_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                           const uint8_t* sb, int64_t M, int64_t N, int64_t K,
+                           uint32_t elem_format, void* c, int32_t c_dtype, int64_t ldc,
+                           void* stream) {
+  return mxfp8_common(qa, sa, qb, sb, M, N, K, elem_format, c, c_dtype, ldc, stream);
 }
 
 mxfp4_status nvfp4_gemm(const uint8_t* qa, const uint8_t* sa, int32_t ka, const uint8_t* qb,

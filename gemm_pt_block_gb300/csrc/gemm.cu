@@ -511,7 +511,7 @@ constexpr int NV_SMEM_BYTES = NV_STAGES * NV_STAGE_BYTES + CTL_BYTES + 1024;
 constexpr uint32_t SFB_COL_NV = SFA_COL + 16;   // A: 4 tiles x 4 columns, B: 4 x 8
 static_assert(NV_STAGE_BYTES % 1024 == 0 && NV_STAGES <= STAGES, "NVFP4 ring");
 static_assert(SFB_COL_NV + 32 <= TMEM_COLS, "NVFP4 scale columns");
-enum : int { kMxf4 = 0, kMxf8 = 1, kNvf4 = 2 };
+enum : int { kMxf4 = 0, kMxf8 = 1, kNvf4 = 2, kMxf8e5 = 3 };
 // Column-wise epilogue quantization: per epilogue warp a 32 x 33 fp32 value
 // buffer and a 32 x 17 word draw buffer, after five stages.
 constexpr int QC_STAGES = 5;
@@ -542,11 +542,11 @@ __device__ __forceinline__ uint32_t make_idesc_nv() {
   return (1u << 7) | (1u << 10) | ((uint32_t)(BNP >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
 }
 
-// kF8: kind::mxf8f6f4 with E4M3 operands (type code 0) instead of kind::mxf4's
-// E2M1 (type code 1).
-template <bool kF8 = false>
+// kF8: kind::mxf8f6f4 with E4M3 operands (type code 0), or E5M2 operands
+// (type code 1) with kE5, instead of kind::mxf4's E2M1 (type code 1).
+template <bool kF8 = false, bool kE5 = false>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
-  const uint32_t t = kF8 ? 0u : 1u;
+  const uint32_t t = kF8 ? (kE5 ? 1u : 0u) : 1u;
   return (sf_id << 4) | (t << 7) | (t << 10) | ((uint32_t)(BNP >> 3) << 17) | (1u << 23) |
          ((uint32_t)(256 >> 4) << 24) | (sf_id << 29);
 }
@@ -574,7 +574,7 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                       void* __restrict__ C, int c_bf16, int64_t ldc, int M, int N, int K, int group_m,
                       float alpha, const __grid_constant__ OrientArgs qo,
                       const __grid_constant__ OrientArgs qc) {
-  constexpr bool kF8 = kKind == kMxf8, kNv = kKind == kNvf4;
+  constexpr bool kF8 = kKind == kMxf8 || kKind == kMxf8e5, kNv = kKind == kNvf4;
   static_assert(!kImg || (kQ != 2 && !kF8), "scale images serve the MXFP4 / NVFP4 GEMMs "
                                              "without the column-wise epilogue");
   constexpr int kAImgs = kNv ? 2 : 1, kBImgs = kNv ? 4 : 2;   // images per stage
@@ -780,7 +780,7 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             for (int k = 0; k < 4; ++k) {
               const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
               const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
-              ptx::mma_mxf8_pair(tmem + ACC_COL, ad, bd, make_idesc<true>(k), tmem + SFA_COL,
+              ptx::mma_mxf8_pair(tmem + ACC_COL, ad, bd, make_idesc<true, kKind == kMxf8e5>(k), tmem + SFA_COL,
                                  tmem + SFB_COL, (kb | k) != 0);
             }
           } else {
@@ -1007,6 +1007,8 @@ DevInfo& dev_info(int dev) {
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::QC_SMEM_BYTES);
       cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<0, pair::kMxf8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
+      cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<0, pair::kMxf8e5>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
       cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<0, pair::kNvf4>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, pair::NV_SMEM_BYTES);
       cudaFuncSetAttribute(pair::mxf4_gemm_pair_kernel<0, pair::kMxf4, true>,
@@ -1148,7 +1150,7 @@ cudaError_t launch_wait_probe(cudaStream_t st) {
 }
 
 cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
-                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, bool e5m2, void* c,
                            bool c_bf16, int64_t ldc, cudaStream_t st, const char** why) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1177,8 +1179,12 @@ cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
   gm = gm < 4 ? 4 : (gm > 32 ? 32 : gm);
   const OrientArgs none{};
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
-  pair::mxf4_gemm_pair_kernel<0, pair::kMxf8><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
-      ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, none, none);
+  if (e5m2)
+    pair::mxf4_gemm_pair_kernel<0, pair::kMxf8e5><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
+        ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, none, none);
+  else
+    pair::mxf4_gemm_pair_kernel<0, pair::kMxf8><<<grid, THREADS, pair::SMEM_BYTES, st>>>(
+        ta, tb, tsa, tsb, c, (int)c_bf16, ldc, (int)M, (int)N, (int)K, (int)gm, 1.0f, none, none);
   return cudaGetLastError();
 }
 

@@ -15,7 +15,8 @@ struct OrientArgs {
   int32_t sr;           // 0: nearest-even, 1: stochastic
   int32_t mma_layout;   // scale array layout: 0 row-major, 1 tensor-core tiles
   int32_t wht;          // rotate 32-runs along the quantization axis first
-  int32_t e4m3;         // element format: 0 E2M1 (MXFP4), 1 E4M3 (MXFP8)
+  int32_t e4m3;         // element format: 0 E2M1 (MXFP4), 1 one byte per element (MXFP8)
+  int32_t e5m2;         // with e4m3 set: 0 E4M3 elements, 1 E5M2 elements
   int32_t nv;           // 1x16 blocks with E4M3 scales (NVFP4); block is then 0
   float nv_p2k;         // NVFP4: 2^tensor_exp
   float nv_zmul;        // NVFP4: 2^-tensor_exp / 6 rounded to fp32 (first guess only)
@@ -37,7 +38,8 @@ void prepare_orient(OrientArgs* o);
 // All launchers return the cudaError_t of the launch.
 cudaError_t launch_quantize(const void* x, bool f32_in, int64_t rows, int64_t cols, int64_t ld,
                             const OrientArgs* row, const OrientArgs* col, cudaStream_t st);
-// fmt: 0 MXFP4, 1 MXFP8 (E4M3 codes), 2 NVFP4 (E4M3 scales per 16, times p2k).
+// fmt: 0 MXFP4, 1 MXFP8 (E4M3 codes), 2 NVFP4 (E4M3 scales per 16, times p2k),
+// 3 MXFP8 with E5M2 codes.
 cudaError_t launch_dequantize(const uint8_t* q, const uint8_t* s, bool mma_layout, int64_t rows,
                               int64_t cols, int fmt, float p2k, float* out, cudaStream_t st);
 cudaError_t launch_hadamard32(const void* x, bool f32_in, int64_t rows, int64_t cols, int64_t ld,
@@ -67,10 +69,11 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
 cudaError_t read_quant_error(uint32_t* err);
 // Reads and clears the device error words (synchronizes st).
 cudaError_t read_device_error(cudaStream_t st, uint32_t* err);
-// MXFP8 GEMM (E4M3 codes [M, K], [N, K] bytes; E8M0 scales in the tensor-core
-// layout): CTA pairs, M % 256 == 0, N % 256 == 0, K % 128 == 0.
+// MXFP8 GEMM (E4M3, or E5M2 with e5m2, codes [M, K], [N, K] bytes, both
+// operands the same format; E8M0 scales in the tensor-core layout): CTA pairs,
+// M % 256 == 0, N % 256 == 0, K % 128 == 0.
 cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
-                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
+                           const uint8_t* sb, int64_t M, int64_t N, int64_t K, bool e5m2, void* c,
                            bool c_bf16, int64_t ldc, cudaStream_t st, const char** why);
 // NVFP4 GEMM (E2M1 codes [M, K/2], [N, K/2]; E4M3 scales per 16 in the
 // tensor-core layout with K/16 scale columns): C = alpha * sum, alpha a power

@@ -256,13 +256,15 @@ __device__ __forceinline__ float warp_max(float m) {
 //  M zero or subnormal: e = -127. Clamped to [-127, 126] (126 is the largest
 //  value a finite fp32 M can give).
 // For MXFP8 (E4M3 elements, largest 448 = 1.75 * 2^8) the same with 8 in place
-// of 2 and the round-up threshold f > 3/4 (fraction > 0x600000).
-__device__ __forceinline__ int scale_exponent(float M, bool roundup, bool e4m3 = false) {
+// of 2 and the round-up threshold f > 3/4 (fraction > 0x600000); E5M2
+// elements (largest 57344 = 1.75 * 2^15) with 15 in place of 2.
+__device__ __forceinline__ int scale_exponent(float M, bool roundup, bool fp8 = false,
+                                              bool e5m2 = false) {
   const uint32_t b = __float_as_uint(M);
   const int bexp = (int)(b >> 23) & 0xFF;
-  // E2M1: emax 2, 6 = 1.5 * 2^2; E4M3: emax 8, 448 = 1.75 * 2^8.
-  const uint32_t over = e4m3 ? 0x600000u : 0x400000u;
-  int e = bexp - (e4m3 ? 135 : 129) + ((roundup && (b & 0x7FFFFFu) > over) ? 1 : 0);
+  // E2M1: emax 2, 6 = 1.5 * 2^2; E4M3: emax 8; E5M2: emax 15 (both 1.75 * 2^emax).
+  const uint32_t over = fp8 ? 0x600000u : 0x400000u;
+  int e = bexp - (fp8 ? (e5m2 ? 142 : 135) : 129) + ((roundup && (b & 0x7FFFFFu) > over) ? 1 : 0);
   e = bexp == 0 ? -127 : e;
   return max(-127, min(126, e));
 }
@@ -309,8 +311,24 @@ __device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v
   return r;
 }
 
-// 8 pairs -> 16 E4M3 bytes.
-__device__ __forceinline__ uint4 encode16_e4m3(const float2* V) {
+// OCP FP8 E5M2 elements: nearest-even with saturation at 57344 (the IEEE
+// conversion cvt.rn.satfinite), sign kept; 4 values -> 4 bytes.
+__device__ __forceinline__ uint32_t e5m2x4(float v0, float v1, float v2, float v3) {
+  uint32_t r;
+  asm("{.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};}"
+      : "=r"(r)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+  return r;
+}
+
+// 8 pairs -> 16 E4M3 bytes, or E5M2 bytes when e5m2.
+__device__ __forceinline__ uint4 encode16_fp8(const float2* V, bool e5m2) {
+  if (e5m2)
+    return make_uint4(e5m2x4(V[0].x, V[0].y, V[1].x, V[1].y), e5m2x4(V[2].x, V[2].y, V[3].x, V[3].y),
+                      e5m2x4(V[4].x, V[4].y, V[5].x, V[5].y), e5m2x4(V[6].x, V[6].y, V[7].x, V[7].y));
   return make_uint4(e4m3x4(V[0].x, V[0].y, V[1].x, V[1].y), e4m3x4(V[2].x, V[2].y, V[3].x, V[3].y),
                     e4m3x4(V[4].x, V[4].y, V[5].x, V[5].y), e4m3x4(V[6].x, V[6].y, V[7].x, V[7].y));
 }

@@ -138,7 +138,7 @@ __device__ __forceinline__ uint2 quantize_halves(float2 (&R)[8], int upper, cons
     return encode16(R);
   }
   const float M = reduce(pair_absmax(R));
-  const int e = scale_exponent(M, o.roundup, o.e4m3);
+  const int e = scale_exponent(M, o.roundup, o.e4m3, o.e5m2);
   scale_all(R, inv_scale(e));
   if (o.sr) {
     uint32_t w[8];
@@ -184,7 +184,7 @@ quant_rows_1x32_kernel(const InT* __restrict__ x, uint32_t total, FastDiv halves
                                               [](float m) { return m; }, &e);
     if (valid) {
       if (o.e4m3)
-        *reinterpret_cast<uint4*>(o.q + (int64_t)r * cols + c0) = encode16_e4m3(R);
+        *reinterpret_cast<uint4*>(o.q + (int64_t)r * cols + c0) = encode16_fp8(R, o.e5m2);
       else
         *reinterpret_cast<uint2*>(o.q + (int64_t)r * (cols >> 1) + (c0 >> 1)) = packed;
       if (o.nv)
@@ -593,6 +593,20 @@ __device__ __forceinline__ float e4m3_decode(uint32_t b) {
   return (b & 0x80u) ? -v : v;
 }
 
+// Full E5M2 byte -> value, exact: exponent field 31 is infinity (mantissa 0)
+// or NaN; field 0 the subnormals m 2^-16; else (1 + m/4) 2^(E - 15).
+__device__ __forceinline__ float e5m2_decode(uint32_t b) {
+  const uint32_t E = (b >> 2) & 31u, m = b & 3u;
+  float v;
+  if (E == 31u)
+    v = __uint_as_float(m ? 0x7FC00000u : 0x7F800000u);
+  else if (E == 0u)
+    v = __fmul_rn((float)m, 1.52587890625e-05f);
+  else
+    v = __uint_as_float(((E + 112u) << 23) | (m << 21));
+  return (b & 0x80u) ? -v : v;
+}
+
 // E8M0 byte -> 2^(byte - 127); 0xFF is NaN.
 __device__ __forceinline__ float e8m0_decode(uint32_t sb) {
   return sb == 255u ? __uint_as_float(0x7FC00000u)
@@ -604,7 +618,8 @@ __device__ __forceinline__ float e8m0_decode(uint32_t sb) {
 // (an E2M1 or E4M3 value times a power of two or an E4M3 scale).
 //  kFmt 0: MXFP4 (E2M1 codes, E8M0 scale per 32);
 //  kFmt 1: MXFP8 (E4M3 codes, one byte each, E8M0 scale per 32);
-//  kFmt 2: NVFP4 (E2M1 codes, E4M3 scale per 16, times p2k = 2^tensor_exp).
+//  kFmt 2: NVFP4 (E2M1 codes, E4M3 scale per 16, times p2k = 2^tensor_exp);
+//  kFmt 3: MXFP8 with E5M2 codes, one byte each, E8M0 scale per 32.
 template <int kFmt>
 __global__ void __launch_bounds__(kThreads)
 dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int mma_layout,
@@ -619,11 +634,14 @@ dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int
   const uint32_t sb = __ldg(s + so);
   const float scale = kFmt == 2 ? __fmul_rn(e4m3_decode(sb), p2k) : e8m0_decode(sb);
   float v[16];
-  if constexpr (kFmt == 1) {
+  if constexpr (kFmt == 1 || kFmt == 3) {
     const uint4 w = __ldg(reinterpret_cast<const uint4*>(q + r * cols + c0));
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(e4m3_decode((ws[j >> 2] >> (8 * (j & 3))) & 0xFFu), scale);
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t b = (ws[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+      v[j] = __fmul_rn(kFmt == 3 ? e5m2_decode(b) : e4m3_decode(b), scale);
+    }
   } else {
     const uint2 w = __ldg(reinterpret_cast<const uint2*>(q + r * (cols >> 1) + (c0 >> 1)));
 #pragma unroll
@@ -869,6 +887,8 @@ cudaError_t launch_dequantize(const uint8_t* q, const uint8_t* s, bool mma_layou
   const unsigned nb = blocks_for(rows * (cols >> 4));
   if (fmt == 1)
     dequant_kernel<1><<<nb, kThreads, 0, st>>>(q, s, mma_layout, rows, cols, p2k, out);
+  else if (fmt == 3)
+    dequant_kernel<3><<<nb, kThreads, 0, st>>>(q, s, mma_layout, rows, cols, p2k, out);
   else if (fmt == 2)
     dequant_kernel<2><<<nb, kThreads, 0, st>>>(q, s, mma_layout, rows, cols, p2k, out);
   else

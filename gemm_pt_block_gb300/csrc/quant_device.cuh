@@ -65,7 +65,7 @@ __device__ __forceinline__ int scale_run32(float2 (&R)[16], const OrientArgs& o,
     }
     return (int)(a.code | (b.code << 8));
   }
-  const int e = scale_exponent(M, o.roundup, kAnyFormat && o.e4m3);
+  const int e = scale_exponent(M, o.roundup, kAnyFormat && o.e4m3, kAnyFormat && o.e5m2);
   const float2 is = make_float2(inv_scale(e), inv_scale(e));
 #pragma unroll
   for (int k = 0; k < 16; ++k) R[k] = f2mul(R[k], is);
@@ -77,14 +77,14 @@ __device__ __forceinline__ int scale_run32(float2 (&R)[16], const OrientArgs& o,
 }
 
 // Encode a scaled 32-run of output row `orow`, K positions k0 .. k0 + 31, and
-// store it: E2M1 two per byte ([rows, K/2]) or E4M3 one per byte ([rows, K]).
+// store it: E2M1 two per byte ([rows, K/2]) or E4M3 / E5M2 one per byte ([rows, K]).
 template <bool kAnyFormat = true>
 __device__ __forceinline__ void store_run32(const OrientArgs& o, int64_t orow, int64_t k0,
                                             int64_t K, const float2 (&R)[16]) {
   if (kAnyFormat && o.e4m3) {
     uint4* d = reinterpret_cast<uint4*>(o.q + orow * K + k0);
-    d[0] = encode16_e4m3(&R[0]);
-    d[1] = encode16_e4m3(&R[8]);
+    d[0] = encode16_fp8(&R[0], o.e5m2);
+    d[1] = encode16_fp8(&R[8], o.e5m2);
   } else {
     *reinterpret_cast<uint4*>(o.q + orow * (K >> 1) + (k0 >> 1)) = encode32(R);
   }

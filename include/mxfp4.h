@@ -60,11 +60,11 @@ enum { MXFP4_SCALE_FLOOR = 0, MXFP4_SCALE_ROUNDUP = 1 };
 enum { MXFP4_ROUND_RTN = 0, MXFP4_ROUND_SR = 1 };
 enum { MXFP4_LAYOUT_ROWMAJOR = 0, MXFP4_LAYOUT_MMA = 1 };
 enum { MXFP4_DTYPE_BF16 = 0, MXFP4_DTYPE_F32 = 1 };
-/* Element format of the codes: E2M1 (MXFP4, two codes per byte) or E4M3
- * (MXFP8, OCP FP8 E4M3, one code per byte) [TIBQ, "The fix, and its
- * supporting cast": MXFP8 for queries and keys]. Both share the E8M0 block
- * scale and its layouts. */
-enum { MXFP4_FORMAT_E2M1 = 0, MXFP4_FORMAT_E4M3 = 1 };
+/* Element format of the codes: E2M1 (MXFP4, two codes per byte), or MXFP8
+ * with one code per byte, E4M3 or E5M2 (the two OCP FP8 formats) [TIBQ, "The
+ * fix, and its supporting cast": MXFP8 for queries and keys]. All share the
+ * E8M0 block scale and its layouts. */
+enum { MXFP4_FORMAT_E2M1 = 0, MXFP4_FORMAT_E4M3 = 1, MXFP4_FORMAT_E5M2 = 2 };
 
 /* Quantization parameters of one output orientation.
  *  block        MXFP4_BLOCK_1X32: 32 consecutive elements along the
@@ -113,7 +113,7 @@ enum { MXFP4_FORMAT_E2M1 = 0, MXFP4_FORMAT_E4M3 = 1 };
  *               c = fp32(1/sqrt(32)) applied last as one rounded multiply.
  *  wht_sign_mask bit i set => s_i = -1 (0 = the deterministic rotation).
  *  seed, sr_stream  Philox key and counter word 2 (used by MXFP4_ROUND_SR).
- *  elem_format  MXFP4_FORMAT_E2M1 or MXFP4_FORMAT_E4M3.
+ *  elem_format  MXFP4_FORMAT_E2M1, MXFP4_FORMAT_E4M3 or MXFP4_FORMAT_E5M2.
  *  tensor_exp   MXFP4_BLOCK_1X16 only (else it must be 0): the exponent k of
  *               the per-tensor factor 2^k, in [-100, 100]. Choosing
  *               k = ceil(log2(amax / 2688)) for the tensor's max-abs amax keeps
@@ -129,7 +129,7 @@ typedef struct {
   uint32_t wht_sign_mask;
   uint64_t seed;
   uint32_t sr_stream;
-  uint32_t elem_format; /* MXFP4_FORMAT_E2M1 (0) or MXFP4_FORMAT_E4M3 (1) */
+  uint32_t elem_format; /* MXFP4_FORMAT_E2M1 (0), MXFP4_FORMAT_E4M3 (1) or MXFP4_FORMAT_E5M2 (2) */
   int32_t tensor_exp;   /* MXFP4_BLOCK_1X16: per-tensor factor 2^tensor_exp */
 } mxfp4_quant_params;
 
@@ -149,11 +149,12 @@ typedef struct {
  *  (rows * cols / 16 below 2^31). Else MXFP4_ERR_SHAPE.
  *  With MXFP4_BLOCK_1X16 the scale arrays are s_row [rows, cols/16] and
  *  s_col [cols, rows/16].
- *  With elem_format MXFP4_FORMAT_E4M3 the codes take one byte per element
- *  (q_row [rows, cols], q_col [cols, rows]), the scale is chosen for the
- *  largest E4M3 value 448 (floor: floor(log2 M) - 8; round-up: the smallest
- *  e with 448 * 2^e >= M) and the rounding is nearest-even with saturation
- *  (stochastic rounding: MXFP4_ERR_UNSUPPORTED).
+ *  With elem_format MXFP4_FORMAT_E4M3 or MXFP4_FORMAT_E5M2 the codes take one
+ *  byte per element (q_row [rows, cols], q_col [cols, rows]), the scale is
+ *  chosen for the format's largest value, 448 for E4M3 and 57344 for E5M2
+ *  (floor: floor(log2 M) - 8 or - 15; round-up: the smallest e with
+ *  max * 2^e >= M) and the rounding is nearest-even with saturation at that
+ *  value (stochastic rounding: MXFP4_ERR_UNSUPPORTED).
  *  Inputs must be finite, and with the rotation on every rotated value must
  *  be finite too (|x| < 2^122 suffices); otherwise the codes are unspecified. */
 mxfp4_status mxfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
@@ -172,8 +173,9 @@ mxfp4_status mxfp4_dequantize(const uint8_t* q, const uint8_t* s, int32_t scale_
 /* Reconstruction for every format mxfp4_quantize writes, described by the
  * block, elem_format and tensor_exp it was quantized with:
  *  E2M1 with 1x32 / 32x32 / 64x64 blocks: as mxfp4_dequantize;
- *  MXFP4_FORMAT_E4M3 (MXFP8): q [rows, cols] one E4M3 byte per element,
- *    out = E4M3(byte) * 2^(scale - 127);
+ *  MXFP4_FORMAT_E4M3 / MXFP4_FORMAT_E5M2 (MXFP8): q [rows, cols] one byte
+ *    per element, out = E4M3(byte) or E5M2(byte) times 2^(scale - 127) (E5M2
+ *    infinity and NaN bytes decode as such);
  *  MXFP4_BLOCK_1X16 (NVFP4): q [rows, cols/2], s one E4M3 byte per 16
  *    elements ([rows, cols/16] or the tensor-core layout with cols/16 scale
  *    columns), out = E2M1(code) * E4M3(scale) * 2^tensor_exp.
@@ -263,6 +265,15 @@ size_t mxfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t scale_
 mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                         int32_t c_dtype, int64_t ldc, void* stream);
+
+/* mxfp8_gemm with the element format named: elem_format MXFP4_FORMAT_E4M3
+ * (as mxfp8_gemm) or MXFP4_FORMAT_E5M2 (both operands E5M2 codes, as
+ * mxfp4_quantize writes them for that format; kind::mxf8f6f4 with E5M2
+ * operands); other values MXFP4_ERR_INVALID_ARG. Shapes and C as mxfp8_gemm. */
+mxfp4_status mxfp8_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                           const uint8_t* sb, int64_t M, int64_t N, int64_t K,
+                           uint32_t elem_format, void* c, int32_t c_dtype, int64_t ldc,
+                           void* stream);
 
 /* Block-scaled NVFP4 GEMM (the 1 x 16 block format of [TIBQ], "Why FP4
  * training is the current frontier of precision reduction"):

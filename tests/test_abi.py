@@ -123,6 +123,13 @@ def test_host_side_validation(L):
     assert L.mxfp4_gemm_workspace_size(256, 384, 640, 32) == 4 * (256 * 768 + 512 * 640) // 32
     assert L.mxfp8_gemm(good, good, good, good, 256, 256, 256, good, 3, 256, None) == 1
     assert L.mxfp8_gemm(good, good, good, good, 128, 256, 128, good, 0, 256, None) == 2
+    assert L.mxfp8_gemm_ex(good, good, good, good, 256, 256, 128, 0, good, 0, 256, None) == 1
+    assert L.mxfp8_gemm_ex(good, good, good, good, 256, 256, 128, 3, good, 0, 256, None) == 1
+    assert L.mxfp8_gemm_ex(good, good, good, good, 128, 256, 128, 2, good, 0, 256, None) == 2
+    pe5 = mx.QuantParams(rounding=mx.ROUND_SR, elem_format=mx.FORMAT_E5M2)._c()
+    assert L.mxfp4_quantize(good, 0, 32, 32, 32, ctypes.byref(pe5), good, good, None, None, None, None) == 4
+    pe3 = _CParams(0, 0, 0, 0, 0, 0, 0, 0, 3)
+    assert L.mxfp4_quantize(good, 0, 32, 32, 32, ctypes.byref(pe3), good, good, None, None, None, None) == 1
     # NVFP4: tensor_exp only with 1x16 blocks, in range; E2M1 elements only
     pe = mx.QuantParams(tensor_exp=1)._c()
     assert L.mxfp4_quantize(good, 0, 32, 32, 32, ctypes.byref(pe), good, good, None, None, None, None) == 1
