@@ -85,6 +85,55 @@ def lib_path() -> str:
     return os.path.join(HERE, _LIB_NAME)
 
 
+def load_library(path: str) -> ctypes.CDLL:
+    """Loads a build of the library at `path` and declares its C signatures
+    (the regular libmxfp4.so, or the bounds-checking libmxfp4_bc.so that the
+    tests use)."""
+    L = ctypes.CDLL(path)
+    P, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    L.mxfp4_quantize.restype = i32
+    L.mxfp4_quantize.argtypes = [P, i32, i64, i64, i64, ctypes.POINTER(_CParams), P, P,
+                                 ctypes.POINTER(_CParams), P, P, P]
+    L.mxfp4_dequantize.restype = i32
+    L.mxfp4_dequantize.argtypes = [P, P, i32, i64, i64, P, P]
+    L.mxfp4_dequantize_ex.restype = i32
+    L.mxfp4_dequantize_ex.argtypes = [P, P, i32, i32, ctypes.c_uint32, i32, i64, i64, P, P]
+    L.mxfp4_gemm.restype = i32
+    L.mxfp4_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
+    sz = ctypes.c_size_t
+    L.mxfp4_gemm_ex.restype = i32
+    L.mxfp4_gemm_ex.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P, sz, P]
+    L.mxfp4_gemm_noalloc.restype = i32
+    L.mxfp4_gemm_noalloc.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
+    L.mxfp4_gemm_workspace_size.restype = sz
+    L.mxfp4_gemm_workspace_size.argtypes = [i64, i64, i64, i32]
+    L.nvfp4_gemm.restype = i32
+    L.nvfp4_gemm.argtypes = [P, P, i32, P, P, i32, i64, i64, i64, P, i32, i64, P, sz, P]
+    L.mxfp8_gemm.restype = i32
+    L.mxfp8_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P]
+    L.mxfp8_gemm_ex.restype = i32
+    L.mxfp8_gemm_ex.argtypes = [P, P, P, P, i64, i64, i64, ctypes.c_uint32, P, i32, i64, P]
+    L.mxfp4_gemm_quantize.restype = i32
+    L.mxfp4_gemm_quantize.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64,
+                                      ctypes.POINTER(_CParams), P, P,
+                                      ctypes.POINTER(_CParams), P, P, P, sz, P]
+    L.mxfp4_tensor_amax.restype = i32
+    L.mxfp4_tensor_amax.argtypes = [P, i32, i64, i64, i64, P, P, P]
+    L.hadamard32.restype = i32
+    L.hadamard32.argtypes = [P, i32, i64, i64, i64, ctypes.c_uint32, i32, P, P]
+    L.mxfp4_status_string.restype = ctypes.c_char_p
+    L.mxfp4_status_string.argtypes = [i32]
+    L.mxfp4_last_error.restype = ctypes.c_char_p
+    L.mxfp4_last_error.argtypes = []
+    L.mxfp4_device_status.restype = i32
+    L.mxfp4_device_status.argtypes = [P]
+    L.mxfp4_selftest_wait_timeout.restype = i32
+    L.mxfp4_selftest_wait_timeout.argtypes = [P]
+    L.mxfp4_bounds_check_shrink.restype = i32
+    L.mxfp4_bounds_check_shrink.argtypes = [i64]
+    return L
+
+
 def lib() -> ctypes.CDLL:
     """Loads libmxfp4.so (built by gemm_pt_block_gb300.build). Raises if absent."""
     global _lib
@@ -93,47 +142,7 @@ def lib() -> ctypes.CDLL:
         if not os.path.exists(path):
             raise RuntimeError(f"{path} is not built; run gemm_pt_block_gb300.build.build() "
                                "(there is no fallback implementation)")
-        L = ctypes.CDLL(path)
-        P, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
-        L.mxfp4_quantize.restype = i32
-        L.mxfp4_quantize.argtypes = [P, i32, i64, i64, i64, ctypes.POINTER(_CParams), P, P,
-                                     ctypes.POINTER(_CParams), P, P, P]
-        L.mxfp4_dequantize.restype = i32
-        L.mxfp4_dequantize.argtypes = [P, P, i32, i64, i64, P, P]
-        L.mxfp4_dequantize_ex.restype = i32
-        L.mxfp4_dequantize_ex.argtypes = [P, P, i32, i32, ctypes.c_uint32, i32, i64, i64, P, P]
-        L.mxfp4_gemm.restype = i32
-        L.mxfp4_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
-        sz = ctypes.c_size_t
-        L.mxfp4_gemm_ex.restype = i32
-        L.mxfp4_gemm_ex.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P, sz, P]
-        L.mxfp4_gemm_noalloc.restype = i32
-        L.mxfp4_gemm_noalloc.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P]
-        L.mxfp4_gemm_workspace_size.restype = sz
-        L.mxfp4_gemm_workspace_size.argtypes = [i64, i64, i64, i32]
-        L.nvfp4_gemm.restype = i32
-        L.nvfp4_gemm.argtypes = [P, P, i32, P, P, i32, i64, i64, i64, P, i32, i64, P, sz, P]
-        L.mxfp8_gemm.restype = i32
-        L.mxfp8_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64, P]
-        L.mxfp8_gemm_ex.restype = i32
-        L.mxfp8_gemm_ex.argtypes = [P, P, P, P, i64, i64, i64, ctypes.c_uint32, P, i32, i64, P]
-        L.mxfp4_gemm_quantize.restype = i32
-        L.mxfp4_gemm_quantize.argtypes = [P, P, P, P, i64, i64, i64, P, i32, i64,
-                                          ctypes.POINTER(_CParams), P, P,
-                                          ctypes.POINTER(_CParams), P, P, P, sz, P]
-        L.mxfp4_tensor_amax.restype = i32
-        L.mxfp4_tensor_amax.argtypes = [P, i32, i64, i64, i64, P, P, P]
-        L.hadamard32.restype = i32
-        L.hadamard32.argtypes = [P, i32, i64, i64, i64, ctypes.c_uint32, i32, P, P]
-        L.mxfp4_status_string.restype = ctypes.c_char_p
-        L.mxfp4_status_string.argtypes = [i32]
-        L.mxfp4_last_error.restype = ctypes.c_char_p
-        L.mxfp4_last_error.argtypes = []
-        L.mxfp4_device_status.restype = i32
-        L.mxfp4_device_status.argtypes = [P]
-        L.mxfp4_selftest_wait_timeout.restype = i32
-        L.mxfp4_selftest_wait_timeout.argtypes = [P]
-        _lib = L
+        _lib = load_library(path)
     return _lib
 
 

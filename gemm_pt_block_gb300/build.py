@@ -17,6 +17,10 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmxfp4.so")
+# The bounds-checking build (every kernel store checked against its output's
+# extent; for tests): its own objects and library.
+BUILD_BC = os.path.join(HERE, "_build_bc")
+LIB_BC = os.path.join(HERE, "libmxfp4_bc.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-ftz=false", "-prec-div=true",
@@ -41,16 +45,19 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False,
+          bounds_check: bool = False) -> str:
+    build_dir, lib_out = (BUILD_BC, LIB_BC) if bounds_check else (BUILD, LIB)
+    flags = ["-DMXFP4_BOUNDS_CHECK"] if bounds_check else []
+    os.makedirs(build_dir, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "mxfp4.h")]
     objs, jobs = [], []
     for unit, extra in UNITS.items():
         src = os.path.join(CSRC, unit)
-        obj = os.path.join(BUILD, unit.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, unit.replace(".cu", ".o"))
         objs.append(obj)
         if force or ptxas_v or _stale(obj, [src, __file__] + hdrs):
-            cmd = [nvcc(), *ARCH, *COMMON, *extra, "-c", src, "-o", obj]
+            cmd = [nvcc(), *ARCH, *COMMON, *flags, *extra, "-c", src, "-o", obj]
             if ptxas_v:
                 cmd.insert(1, "-Xptxas=-v")
             jobs.append(cmd)
@@ -67,15 +74,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
                 sys.stderr.write(r.stdout + r.stderr)
             if r.returncode:
                 raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".{os.getpid()}.tmp"
+    if force or jobs or _stale(lib_out, objs):
+        tmp = lib_out + f".{os.getpid()}.tmp"
         cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("nvcc link failed")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_out)
+    return lib_out
 
 
 if __name__ == "__main__":

@@ -12,6 +12,9 @@
 namespace {
 
 thread_local char g_last_error[512] = "";
+// Bounds-checking builds: bytes taken off every output extent this thread's
+// later calls check against (mxfp4_bounds_check_shrink).
+thread_local int64_t g_extent_shrink = 0;
 
 mxfp4_status fail(mxfp4_status s, const char* fmt, ...) {
   va_list ap;
@@ -78,6 +81,9 @@ mxfp4_status check_params(const mxfp4_quant_params* p, uint8_t* q, uint8_t* s, i
   o->stream = p->sr_stream;
   o->q = q;
   o->s = s;
+  const int64_t qb = out_rows * (o->e4m3 ? k : k / 2), sb = out_rows * (nv ? k / 16 : k / 32);
+  o->q_bytes = (uint64_t)(qb > g_extent_shrink ? qb - g_extent_shrink : 0);
+  o->s_bytes = (uint64_t)(sb > g_extent_shrink ? sb - g_extent_shrink : 0);
   mx::prepare_orient(o);
   return MXFP4_OK;
 }
@@ -107,6 +113,7 @@ const char* mxfp4_status_string(mxfp4_status s) {
     case MXFP4_ERR_UNSUPPORTED: return "MXFP4_ERR_UNSUPPORTED";
     case MXFP4_ERR_CUDA: return "MXFP4_ERR_CUDA";
     case MXFP4_ERR_TIMEOUT: return "MXFP4_ERR_TIMEOUT";
+    case MXFP4_ERR_BOUNDS: return "MXFP4_ERR_BOUNDS";
   }
   return "MXFP4_ERR_UNKNOWN";
 }
@@ -385,7 +392,20 @@ mxfp4_status mxfp4_device_status(void* stream) {
   if (e != cudaSuccess) return from_cuda(e, "mxfp4_device_status");
   if (err == MXFP4_ERR_TIMEOUT)
     return fail(MXFP4_ERR_TIMEOUT, "a bounded device-side wait in the GEMM ran out");
+  if (err == MXFP4_ERR_BOUNDS)
+    return fail(MXFP4_ERR_BOUNDS, "a kernel store fell outside its output (skipped)");
   return err ? fail(static_cast<mxfp4_status>(err), "device error word %u", err) : MXFP4_OK;
+}
+
+mxfp4_status mxfp4_bounds_check_shrink(int64_t bytes) {
+#ifdef MXFP4_BOUNDS_CHECK
+  if (bytes < 0) return fail(MXFP4_ERR_INVALID_ARG, "mxfp4_bounds_check_shrink: negative bytes");
+  g_extent_shrink = bytes;
+  return MXFP4_OK;
+#else
+  (void)bytes;
+  return fail(MXFP4_ERR_UNSUPPORTED, "mxfp4_bounds_check_shrink: not a bounds-checking build");
+#endif
 }
 
 mxfp4_status mxfp4_selftest_wait_timeout(void* stream) {

@@ -38,6 +38,14 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+
+namespace mx {
+namespace {
+__device__ uint32_t g_gemm_error;
+}  // namespace
+}  // namespace mx
+#define MX_BOUNDS_FAIL() atomicExch(&::mx::g_gemm_error, ::mx::kErrBounds)
+
 #include "quant_device.cuh"
 #include "tma_host.h"
 
@@ -69,8 +77,6 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int64_t kGroupBytes = 24ll << 20;
 
 static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
-
-__device__ uint32_t g_gemm_error;
 
 // Barriers and flags of one CTA; S = pipeline depth of the kernel using it.
 template <int S>
@@ -149,15 +155,16 @@ __device__ __forceinline__ uint32_t bf16x2(uint32_t lo, uint32_t hi) {
 // half) so that each of the two stores writes a whole 32-byte sector of one
 // row: first row r (even lane bytes 0-15, odd lane 16-31), then row r + 1.
 // A warp store then fills 16 sectors instead of half-filling 32.
+// (cbase, cbytes: C's extent, checked in bounds-checking builds.)
 __device__ __forceinline__ void store_row_pair(uint8_t* rowa, uint8_t* rowb, int64_t seg, uint4 lo,
-                                               uint4 hi, int odd) {
+                                               uint4 hi, int odd, const void* cbase, uint64_t cbytes) {
   uint4 g;
   g.x = __shfl_xor_sync(0xffffffffu, odd ? lo.x : hi.x, 1);
   g.y = __shfl_xor_sync(0xffffffffu, odd ? lo.y : hi.y, 1);
   g.z = __shfl_xor_sync(0xffffffffu, odd ? lo.z : hi.z, 1);
   g.w = __shfl_xor_sync(0xffffffffu, odd ? lo.w : hi.w, 1);
-  *reinterpret_cast<uint4*>(rowa + seg + 16 * odd) = odd ? g : lo;
-  *reinterpret_cast<uint4*>(rowb + seg + 16 * odd) = odd ? hi : g;
+  put(reinterpret_cast<uint4*>(rowa + seg + 16 * odd), odd ? g : lo, cbase, cbytes);
+  put(reinterpret_cast<uint4*>(rowb + seg + 16 * odd), odd ? hi : g, cbase, cbytes);
 }
 
 // One epilogue thread's results: 128 consecutive fp32 values of row `row`
@@ -171,7 +178,8 @@ __device__ __forceinline__ void store_row_pair(uint8_t* rowa, uint8_t* rowb, int
 template <bool kQ>
 __device__ __forceinline__ void epilogue_out(const uint32_t (&r0)[64], const uint32_t (&r1)[64],
                                              void* C, int c_bf16, int64_t ldc, int64_t row,
-                                             int64_t c0, int64_t N, const OrientArgs& qo) {
+                                             int64_t c0, int64_t N, const OrientArgs& qo,
+                                             uint64_t c_bytes) {
   if (!kQ || C != nullptr) {
     const int odd = threadIdx.x & 1;
     const int64_t esz = c_bf16 ? 2 : 4;
@@ -187,7 +195,7 @@ __device__ __forceinline__ void epilogue_out(const uint32_t (&r0)[64], const uin
                                     bf16x2(r[o + 4], r[o + 5]), bf16x2(r[o + 6], r[o + 7]));
         const uint4 hi = make_uint4(bf16x2(r[o + 8], r[o + 9]), bf16x2(r[o + 10], r[o + 11]),
                                     bf16x2(r[o + 12], r[o + 13]), bf16x2(r[o + 14], r[o + 15]));
-        store_row_pair(rowa, rowb, 32 * m, lo, hi, odd);
+        store_row_pair(rowa, rowb, 32 * m, lo, hi, odd, C, c_bytes);
       }
     } else {
       // 8 fp32 values (32 bytes) per segment: columns 8 m .. 8 m + 7.
@@ -196,7 +204,7 @@ __device__ __forceinline__ void epilogue_out(const uint32_t (&r0)[64], const uin
         const uint32_t* r = m < 8 ? r0 : r1;
         const int o = (m & 7) * 8;
         store_row_pair(rowa, rowb, 32 * m, make_uint4(r[o], r[o + 1], r[o + 2], r[o + 3]),
-                       make_uint4(r[o + 4], r[o + 5], r[o + 6], r[o + 7]), odd);
+                       make_uint4(r[o + 4], r[o + 5], r[o + 6], r[o + 7]), odd, C, c_bytes);
       }
     }
   }
@@ -271,10 +279,10 @@ __device__ __forceinline__ void epilogue_rowcol(const uint32_t (&r0)[64], const 
                                                 void* C, int c_bf16, int64_t ldc, int64_t row,
                                                 int64_t c0, int64_t M, int64_t N,
                                                 const OrientArgs& qo, const OrientArgs& qc,
-                                                float* tb, uint32_t* db, int lane) {
+                                                float* tb, uint32_t* db, int lane, uint64_t c_bytes) {
   if (C != nullptr) {
     const OrientArgs none{};
-    epilogue_out<false>(r0, r1, C, c_bf16, ldc, row, c0, N, none);
+    epilogue_out<false>(r0, r1, C, c_bf16, ldc, row, c0, N, none, c_bytes);
   }
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
@@ -464,7 +472,9 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       acc_phase ^= 1u;
       const int64_t row = (int64_t)mb * BM + q * 32 + lane;
       const int64_t col0 = (int64_t)nb * BN + h * 128;
-      if (col0 < N) epilogue_out<kQ>(r0, r1, C, c_bf16, ldc, row, col0, N, qo);
+      if (col0 < N)
+        epilogue_out<kQ>(r0, r1, C, c_bf16, ldc, row, col0, N, qo,
+                         ((uint64_t)(M - 1) * ldc + N) * (c_bf16 ? 2u : 4u));
     }
   }
 
@@ -854,9 +864,11 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       if constexpr (kQ == 2) {
         uint8_t* xb = smem + kStages * kStageBytes + CTL_BYTES + (warp - 2) * kXposeBytes;
         epilogue_rowcol(r0, r1, C, c_bf16, ldc, row, col0, M, N, qo, qc,
-                        reinterpret_cast<float*>(xb), reinterpret_cast<uint32_t*>(xb + 4224), lane);
+                        reinterpret_cast<float*>(xb), reinterpret_cast<uint32_t*>(xb + 4224), lane,
+                        ((uint64_t)(M - 1) * ldc + N) * (c_bf16 ? 2u : 4u));
       } else {
-        epilogue_out<kQ != 0>(r0, r1, C, c_bf16, ldc, row, col0, N, qo);
+        epilogue_out<kQ != 0>(r0, r1, C, c_bf16, ldc, row, col0, N, qo,
+                              ((uint64_t)(M - 1) * ldc + N) * (c_bf16 ? 2u : 4u));
       }
     }
   }
@@ -928,7 +940,7 @@ bool make_image_map(CUtensorMap* m, const uint8_t* base, int64_t nimg, uint32_t 
 __global__ void __launch_bounds__(256)
 scale_images_kernel(const uint8_t* __restrict__ sa, uint8_t* __restrict__ ia, int64_t na,
                     const uint8_t* __restrict__ sb, uint8_t* __restrict__ ib, int64_t nb,
-                    int64_t ntiles, int64_t b_bands) {
+                    int64_t ntiles, int64_t b_bands, uint64_t ws_bytes) {
   int64_t t = (int64_t)blockIdx.x * 256 + threadIdx.x;
   const bool bside = t >= na;
   if (bside) t -= na;
@@ -948,7 +960,7 @@ scale_images_kernel(const uint8_t* __restrict__ sa, uint8_t* __restrict__ ia, in
   }
   const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>((bside ? sb : sa) + tile * 512 + (8 * g + j) * 16))
                         : make_uint4(0u, 0u, 0u, 0u);
-  *reinterpret_cast<uint4*>((bside ? ib : ia) + t * 16) = v;
+  put(reinterpret_cast<uint4*>((bside ? ib : ia) + t * 16), v, ia, ws_bytes);
 }
 
 // 512-byte scale tiles per 128-row band: K/128 (MXFP4), K/64 (NVFP4).
@@ -968,7 +980,8 @@ bool images_fit(int64_t M, int64_t N, int64_t K, bool nv) {
 
 // Builds A's and B's images in ws (A first) and encodes their tensor maps.
 bool prepare_images(const uint8_t* sa, int64_t M, const uint8_t* sb, int64_t N, int64_t K, bool nv,
-                    uint8_t* ws, CUtensorMap* tsa, CUtensorMap* tsb, cudaStream_t st) {
+                    uint8_t* ws, size_t ws_bytes, CUtensorMap* tsa, CUtensorMap* tsb,
+                    cudaStream_t st) {
   const int64_t ai = a_images(M, K, nv), bi = b_images(N, K, nv);
   uint8_t* ia = ws;
   uint8_t* ib = ws + ai * kImageBytes;
@@ -976,7 +989,8 @@ bool prepare_images(const uint8_t* sa, int64_t M, const uint8_t* sb, int64_t N, 
     return false;
   const int64_t na = ai * (kImageBytes / 16), nb = bi * (kImageBytes / 16);
   scale_images_kernel<<<(unsigned)((na + nb + 255) / 256), 256, 0, st>>>(sa, ia, na, sb, ib, nb,
-                                                                          scale_tiles(K, nv), N / 128);
+                                                                          scale_tiles(K, nv), N / 128,
+                                                                          (uint64_t)ws_bytes);
   return true;
 }
 
@@ -1083,7 +1097,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                      ws_bytes >= (size_t)workspace_bytes(M, N, K, false);
     (void)cudaGetLastError();  // drop a stale error left by an earlier call
     if (!make_code_map(&ta, qa, M, K / 2, pair::BM) || !make_code_map(&tb, qb, N, K / 2, pair::BNH) ||
-        !(img ? prepare_images(sa, M, sb, N, K, false, static_cast<uint8_t*>(ws), &tsa, &tsb, st)
+        !(img ? prepare_images(sa, M, sb, N, K, false, static_cast<uint8_t*>(ws), ws_bytes, &tsa, &tsb, st)
               : (make_scale_map(&tsa, sa, M, K, 1) && make_scale_map(&tsb, sb, N, K, 2)))) {
       *why = "cuTensorMapEncodeTiled rejected the operand layout";
       return cudaErrorInvalidValue;
@@ -1211,7 +1225,7 @@ cudaError_t launch_gemm_nv(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
                    ws_bytes >= (size_t)workspace_bytes(M, N, K, true);
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
   if (!make_code_map(&ta, qa, M, K / 2, pair::BM) || !make_code_map(&tb, qb, N, K / 2, pair::BNH) ||
-      !(img ? prepare_images(sa, M, sb, N, K, true, static_cast<uint8_t*>(ws), &tsa, &tsb, st)
+      !(img ? prepare_images(sa, M, sb, N, K, true, static_cast<uint8_t*>(ws), ws_bytes, &tsa, &tsb, st)
             : (make_scale_map(&tsa, sa, M, K, 1, 4, 64) && make_scale_map(&tsb, sb, N, K, 2, 4, 64)))) {
     *why = "cuTensorMapEncodeTiled rejected the operand layout";
     return cudaErrorInvalidValue;

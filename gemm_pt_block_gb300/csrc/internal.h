@@ -30,7 +30,12 @@ struct OrientArgs {
   uint32_t sm_inter[2]; // sign bits of local elements, lane holding even / odd block elements
   uint32_t xw[2][8];    // sign bits placed on bf16 word pairs (bits 15 and 31), per half
   float sgn[32];        // rotation signs s_i as factors +-1 (all +1 without rotation)
+  uint64_t q_bytes;     // extent of q and s in bytes (checked in bounds-checking builds)
+  uint64_t s_bytes;
 };
+
+// Device error word value of a store outside its output (bounds-checking builds).
+constexpr uint32_t kErrBounds = 7;
 
 // Fills keys, sm_*, xw and sgn from seed and sign_mask.
 void prepare_orient(OrientArgs* o);

@@ -18,6 +18,14 @@
 
 #include "internal.h"
 #include "mx_device.cuh"
+
+namespace mx {
+namespace {
+__device__ uint32_t g_quant_error;
+}  // namespace
+}  // namespace mx
+#define MX_BOUNDS_FAIL() atomicExch(&::mx::g_quant_error, ::mx::kErrBounds)
+
 #include "quant_device.cuh"
 #include "ptx.cuh"
 #include "tma_host.h"
@@ -184,11 +192,13 @@ quant_rows_1x32_kernel(const InT* __restrict__ x, uint32_t total, FastDiv halves
                                               [](float m) { return m; }, &e);
     if (valid) {
       if (o.e4m3)
-        *reinterpret_cast<uint4*>(o.q + (int64_t)r * cols + c0) = encode16_fp8(R, o.e5m2);
+        put(reinterpret_cast<uint4*>(o.q + (int64_t)r * cols + c0), encode16_fp8(R, o.e5m2), o.q,
+            o.q_bytes);
       else
-        *reinterpret_cast<uint2*>(o.q + (int64_t)r * (cols >> 1) + (c0 >> 1)) = packed;
+        put(reinterpret_cast<uint2*>(o.q + (int64_t)r * (cols >> 1) + (c0 >> 1)), packed, o.q,
+            o.q_bytes);
       if (o.nv)
-        o.s[scale_offset(o, r, c0 >> 4, cols >> 4)] = (uint8_t)e;
+        put(o.s + scale_offset(o, r, c0 >> 4, cols >> 4), (uint8_t)e, o.s, o.s_bytes);
       else if (!upper)
         store_scale(o, r, c0 >> 5, cols >> 5, e);
     }
@@ -216,8 +226,6 @@ constexpr int kStages = 3;
 constexpr int kConsumers = 128;
 constexpr int kTileThreads = kConsumers + 32;
 constexpr uint64_t kQuantWaitNs = 2000000000ull;
-
-__device__ uint32_t g_quant_error;
 
 // Byte offset of element (r, c) in a 64 x 64 tile as TMA lays it out with the
 // 128-byte swizzle: 128-byte rows, 16-byte chunk j of row r at chunk j ^ (r % 8).
@@ -581,7 +589,9 @@ hadamard32_kernel(const InT* __restrict__ x, int64_t rows, int64_t cols, int64_t
   if (valid) {
     float4* out = reinterpret_cast<float4*>(y + r * cols + c0);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) out[i] = make_float4(R[2 * i].x, R[2 * i].y, R[2 * i + 1].x, R[2 * i + 1].y);
+    for (int i = 0; i < 4; ++i)
+      put(out + i, make_float4(R[2 * i].x, R[2 * i].y, R[2 * i + 1].x, R[2 * i + 1].y), y,
+          (uint64_t)(rows * cols) * 4);
   }
 }
 
@@ -653,7 +663,9 @@ dequant_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int
   }
   float4* o = reinterpret_cast<float4*>(out + r * cols + c0);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  for (int i = 0; i < 4; ++i)
+    put(o + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]), out,
+        (uint64_t)(rows * cols) * 4);
 }
 
 // ------------------------------------------------------- tensor max-abs ---

@@ -6,7 +6,32 @@
 #include "internal.h"
 #include "mx_device.cuh"
 
+// Each translation unit that includes this header defines MX_BOUNDS_FAIL()
+// (raise its device error word to kErrBounds) first.
+#ifndef MX_BOUNDS_FAIL
+#error "define MX_BOUNDS_FAIL() before including quant_device.cuh"
+#endif
+
 namespace mx {
+
+// Store v at p. Builds with MXFP4_BOUNDS_CHECK first check that the store lies
+// inside [base, base + bytes), the extent the boundary computed for the output;
+// a store outside it is skipped and raises the device error word.
+template <typename T>
+__device__ __forceinline__ void put(T* p, const T& v, const void* base, uint64_t bytes) {
+#ifdef MXFP4_BOUNDS_CHECK
+  const uint8_t* b = static_cast<const uint8_t*>(base);
+  const uint8_t* a = reinterpret_cast<const uint8_t*>(p);
+  if (a < b || a + sizeof(T) > b + bytes) {
+    MX_BOUNDS_FAIL();
+    return;
+  }
+#else
+  (void)base;
+  (void)bytes;
+#endif
+  *p = v;
+}
 
 __device__ __forceinline__ int64_t scale_offset(const OrientArgs& o, int64_t orow, int64_t kb,
                                                 int64_t nkb) {
@@ -16,7 +41,7 @@ __device__ __forceinline__ int64_t scale_offset(const OrientArgs& o, int64_t oro
 // E8M0 scale 2^e of block kb of output row orow (nkb blocks per row).
 __device__ __forceinline__ void store_scale(const OrientArgs& o, int64_t orow, int64_t kb,
                                             int64_t nkb, int e) {
-  o.s[scale_offset(o, orow, kb, nkb)] = (uint8_t)(e + 127);
+  put(o.s + scale_offset(o, orow, kb, nkb), (uint8_t)(e + 127), o.s, o.s_bytes);
 }
 
 // The scales of the 32-run at K positions k0 .. k0 + 31 of output row orow as
@@ -26,7 +51,8 @@ template <bool kNvfp4 = true>
 __device__ __forceinline__ void store_run_scales(const OrientArgs& o, int64_t orow, int64_t k0,
                                                  int64_t K, int e) {
   if (kNvfp4 && o.nv)
-    *reinterpret_cast<uint16_t*>(o.s + scale_offset(o, orow, k0 >> 4, K >> 4)) = (uint16_t)e;
+    put(reinterpret_cast<uint16_t*>(o.s + scale_offset(o, orow, k0 >> 4, K >> 4)), (uint16_t)e, o.s,
+        o.s_bytes);
   else
     store_scale(o, orow, k0 >> 5, K >> 5, e);
 }
@@ -83,10 +109,10 @@ __device__ __forceinline__ void store_run32(const OrientArgs& o, int64_t orow, i
                                             int64_t K, const float2 (&R)[16]) {
   if (kAnyFormat && o.e4m3) {
     uint4* d = reinterpret_cast<uint4*>(o.q + orow * K + k0);
-    d[0] = encode16_fp8(&R[0], o.e5m2);
-    d[1] = encode16_fp8(&R[8], o.e5m2);
+    put(d, encode16_fp8(&R[0], o.e5m2), o.q, o.q_bytes);
+    put(d + 1, encode16_fp8(&R[8], o.e5m2), o.q, o.q_bytes);
   } else {
-    *reinterpret_cast<uint4*>(o.q + orow * (K >> 1) + (k0 >> 1)) = encode32(R);
+    put(reinterpret_cast<uint4*>(o.q + orow * (K >> 1) + (k0 >> 1)), encode32(R), o.q, o.q_bytes);
   }
 }
 

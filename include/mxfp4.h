@@ -52,7 +52,9 @@ typedef enum {
   MXFP4_ERR_ALIGN = 3,       /* pointer or leading dimension misaligned */
   MXFP4_ERR_UNSUPPORTED = 4, /* device is not sm_103 / sm_100 family */
   MXFP4_ERR_CUDA = 5,        /* CUDA runtime / driver error at launch */
-  MXFP4_ERR_TIMEOUT = 6      /* a bounded device-side wait ran out */
+  MXFP4_ERR_TIMEOUT = 6,     /* a bounded device-side wait ran out */
+  MXFP4_ERR_BOUNDS = 7       /* a kernel store fell outside its output (only
+                                builds with MXFP4_BOUNDS_CHECK detect it) */
 } mxfp4_status;
 
 enum { MXFP4_BLOCK_1X32 = 0, MXFP4_BLOCK_32X32 = 1, MXFP4_BLOCK_64X64 = 2, MXFP4_BLOCK_1X16 = 3 };
@@ -356,6 +358,17 @@ const char* mxfp4_last_error(void);
  * GEMM kernel set when they run out (MXFP4_OK if none). Synchronizes `stream`
  * first. */
 mxfp4_status mxfp4_device_status(void* stream);
+
+/* Diagnostic of the bounds-checking build (the pages have no counterpart).
+ * A library built with MXFP4_BOUNDS_CHECK checks every store of its kernels
+ * against the extent the call computed for that output (codes, scales, C,
+ * rotated or reconstructed values, scale images); a store outside it is
+ * skipped and mxfp4_device_status then returns MXFP4_ERR_BOUNDS. This call
+ * makes the code and scale extents of later calls on the calling thread
+ * `bytes` smaller (0 restores them), so a test can watch the check fire while
+ * every store that does happen stays inside its real buffer. The regular
+ * library returns MXFP4_ERR_UNSUPPORTED. */
+mxfp4_status mxfp4_bounds_check_shrink(int64_t bytes);
 
 /* Diagnostic for the library's own failure reporting (the pages have no
  * counterpart). Enqueues on `stream` a one-thread kernel that waits on a

@@ -53,9 +53,11 @@ def test_header_compiles_as_c():
 
 
 def test_status_strings(L):
-    names = [L.mxfp4_status_string(i).decode() for i in range(7)]
+    names = [L.mxfp4_status_string(i).decode() for i in range(8)]
     assert names == ["MXFP4_OK", "MXFP4_ERR_INVALID_ARG", "MXFP4_ERR_SHAPE", "MXFP4_ERR_ALIGN",
-                     "MXFP4_ERR_UNSUPPORTED", "MXFP4_ERR_CUDA", "MXFP4_ERR_TIMEOUT"]
+                     "MXFP4_ERR_UNSUPPORTED", "MXFP4_ERR_CUDA", "MXFP4_ERR_TIMEOUT",
+                     "MXFP4_ERR_BOUNDS"]
+    assert L.mxfp4_bounds_check_shrink(16) == 4      # the regular library refuses the diagnostic
 
 
 def test_host_side_validation(L):

@@ -57,7 +57,7 @@ def _scale_bytes(rows, k, p):
 
 
 def _code_bytes(rows, k, p):
-    return rows * (k if p.elem_format == oracle.FORMAT_E4M3 else k // 2)
+    return rows * (k if p.elem_format in (oracle.FORMAT_E4M3, oracle.FORMAT_E5M2) else k // 2)
 
 
 QUANT_CASES = [
@@ -74,6 +74,10 @@ QUANT_CASES = [
      oracle.Params(block=oracle.BLOCK_32X32, rounding=oracle.ROUND_SR, seed=4), 1),
     (192, 320, oracle.Params(block=oracle.BLOCK_64X64), oracle.Params(block=oracle.BLOCK_64X64), 0),
     (160, 352, None, oracle.Params(elem_format=oracle.FORMAT_E4M3), 0),
+    (150, 352, oracle.Params(elem_format=oracle.FORMAT_E5M2, rounding=oracle.ROUND_SR, seed=5),
+     None, 0),
+    (256, 384, oracle.Params(elem_format=oracle.FORMAT_E5M2, block=oracle.BLOCK_32X32),
+     oracle.Params(elem_format=oracle.FORMAT_E5M2, block=oracle.BLOCK_32X32), 1),
     (160, 352, oracle.Params(block=oracle.BLOCK_1X16, tensor_exp=-3),
      oracle.Params(block=oracle.BLOCK_1X16, tensor_exp=-3, rounding=oracle.ROUND_SR), 0),
 ]
