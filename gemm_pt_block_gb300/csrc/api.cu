@@ -191,7 +191,7 @@ mxfp4_status mxfp4_dequantize_ex(const uint8_t* q, const uint8_t* s, int32_t sca
 }
 
 namespace {
-// Shape rules of the MXFP4 GEMM entry points.
+// Shape rules of the GEMM entry points (MXFP4, MXFP8, NVFP4).
 mxfp4_status gemm_shape(const char* name, int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 128 != 0 || K % 128 != 0)
     return fail(MXFP4_ERR_SHAPE, "%s needs M, N, K positive multiples of 128 (got %lld, %lld, %lld)",
@@ -273,11 +273,7 @@ mxfp4_status mxfp8_common(const uint8_t* qa, const uint8_t* sa, const uint8_t* q
     return fail(MXFP4_ERR_INVALID_ARG, "mxfp8_gemm: elem_format %u is not E4M3 or E5M2", elem_format);
   if (c_dtype != MXFP4_DTYPE_BF16 && c_dtype != MXFP4_DTYPE_F32)
     return fail(MXFP4_ERR_INVALID_ARG, "mxfp8_gemm: bad c_dtype %d", c_dtype);
-  if (M <= 0 || N <= 0 || K <= 0 || M % 256 != 0 || N % 256 != 0 || K % 128 != 0)
-    return fail(MXFP4_ERR_SHAPE, "mxfp8_gemm needs M %% 256 == 0, N %% 256 == 0, K %% 128 == 0 (got %lld, %lld, %lld)",
-                (long long)M, (long long)N, (long long)K);
-  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30))
-    return fail(MXFP4_ERR_SHAPE, "mxfp8_gemm dimensions too large");
+  if (mxfp4_status st = gemm_shape("mxfp8_gemm", M, N, K)) return st;
   if (ldc < N) return fail(MXFP4_ERR_SHAPE, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
   if (!aligned16(qa) || !aligned16(qb) || !aligned16(sa) || !aligned16(sb) || !aligned16(c) || ldc % 8 != 0)
     return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");
@@ -313,11 +309,7 @@ mxfp4_status nvfp4_gemm(const uint8_t* qa, const uint8_t* sa, int32_t ka, const 
     return fail(MXFP4_ERR_INVALID_ARG, "nvfp4_gemm: bad c_dtype %d", c_dtype);
   if (ka < -100 || ka > 100 || kb < -100 || kb > 100 || ka + kb < -126 || ka + kb > 126)
     return fail(MXFP4_ERR_INVALID_ARG, "nvfp4_gemm: tensor exponents %d, %d out of range", ka, kb);
-  if (M <= 0 || N <= 0 || K <= 0 || M % 256 != 0 || N % 256 != 0 || K % 256 != 0)
-    return fail(MXFP4_ERR_SHAPE, "nvfp4_gemm needs M %% 256 == 0, N %% 256 == 0, K %% 256 == 0 (got %lld, %lld, %lld)",
-                (long long)M, (long long)N, (long long)K);
-  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30))
-    return fail(MXFP4_ERR_SHAPE, "nvfp4_gemm dimensions too large");
+  if (mxfp4_status st = gemm_shape("nvfp4_gemm", M, N, K)) return st;
   if (ldc < N) return fail(MXFP4_ERR_SHAPE, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
   if (!aligned16(qa) || !aligned16(qb) || !aligned16(sa) || !aligned16(sb) || !aligned16(c) || ldc % 8 != 0)
     return fail(MXFP4_ERR_ALIGN, "operands must be 16-byte aligned and ldc %% 8 == 0");

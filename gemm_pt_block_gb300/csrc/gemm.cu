@@ -601,11 +601,13 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
   const bool leader = rank == 0;
-  // MXFP4 takes N and K multiples of 128: a last N tile with 128 valid
-  // columns (CTA 1's B rows and scale band arrive zero-filled; those columns
-  // are not stored) and a last K step with 128 valid K (the rest arrives
-  // zero-filled and its last two MMAs are not issued).
-  const int num_m = M / (2 * BM), num_n = (N + BNP - 1) / BNP;
+  // M, N and K are multiples of 128: a last M tile with 128 valid rows (CTA
+  // 1's A rows and scales arrive zero-filled and its epilogue stores nothing),
+  // a last N tile with 128 valid columns (CTA 1's B rows and scale band arrive
+  // zero-filled; those columns are not stored) and, for E2M1 operands, a last
+  // K step with 128 valid K (the rest arrives zero-filled and its last two
+  // MMAs are not issued; an FP8 K step is 128 deep).
+  const int num_m = (M + 2 * BM - 1) / (2 * BM), num_n = (N + BNP - 1) / BNP;
   const int num_k = kF8 ? K / (BK / 2) : (K + BK - 1) / BK;
   const bool k_half = !kF8 && (K % BK) != 0;
   const int num_tiles = num_m * num_n;
@@ -763,7 +765,7 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             // Four K tiles, one per MMA: A's tile k to SFA_COL + 4 k, B's band t
             // of tile k to kSfbCol + 8 k + 4 t; each MMA reads whole words.
 #pragma unroll
-            for (int k = 0; k < 4 && !kImg; ++k) {
+            for (int k = 0; k < kMmas && !kImg; ++k) {
               ptx::tc_cp_pair_32x128b_warpx4(tmem + SFA_COL + 4 * k,
                                              ptx::smem_desc(sfa_s + k * 512, 0, 128, 0));
 #pragma unroll
@@ -772,7 +774,7 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                                                ptx::smem_desc(sfb_s + t * 2048 + k * 512, 0, 128, 0));
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < kMmas; ++k) {
               const uint64_t ad = ptx::smem_desc(st + k * 32, 16, 1024, 2);
               const uint64_t bd = ptx::smem_desc(st + A_BYTES + k * 32, 16, 1024, 2);
               ptx::mma_nvf4_pair(tmem + ACC_COL, ad, bd, make_idesc_nv(), tmem + SFA_COL + 4 * k,
@@ -851,6 +853,7 @@ mxf4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(acc_empty_leader);
       acc_phase ^= 1u;
+      if ((int64_t)mb * 2 * BM + rank * BM >= M) continue;   // the empty half of a last M tile
       const int64_t row = (int64_t)mb * 2 * BM + rank * BM + q * 32 + lane;
       if constexpr (kNv) {   // exact: alpha is a power of two
 #pragma unroll
@@ -1186,7 +1189,7 @@ cudaError_t launch_gemm_f8(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
     *why = "cuTensorMapEncodeTiled rejected the operand layout";
     return cudaErrorInvalidValue;
   }
-  const int num_tiles = (int)((M / 256) * (N / pair::BNP));
+  const int num_tiles = (int)(((M + 255) / 256) * ((N + pair::BNP - 1) / pair::BNP));
   const int pairs = d.sms / 2;
   const int grid = 2 * (num_tiles < pairs ? num_tiles : pairs);
   int64_t gm = kGroupBytes / (256 * K);
@@ -1230,7 +1233,7 @@ cudaError_t launch_gemm_nv(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
     *why = "cuTensorMapEncodeTiled rejected the operand layout";
     return cudaErrorInvalidValue;
   }
-  const int num_tiles = (int)((M / 256) * (N / pair::BNP));
+  const int num_tiles = (int)(((M + 255) / 256) * ((N + pair::BNP - 1) / pair::BNP));
   const int pairs = d.sms / 2;
   const int grid = 2 * (num_tiles < pairs ? num_tiles : pairs);
   int64_t gm = kGroupBytes / (256 * (K / 2));

@@ -252,10 +252,11 @@ mxfp4_status mxfp4_gemm_noalloc(const uint8_t* qa, const uint8_t* sa, const uint
                                 int64_t ldc, void* stream);
 
 /* Workspace bytes for mxfp4_gemm_ex (scale_block 32) or nvfp4_gemm
- * (scale_block 16): four times the scale bytes of both operands, with A's K
- * and B's N rounded up to multiples of 256: 4 * (M * K' + N' * K) /
- * scale_block (4 * (M + N) * K / scale_block when N and K are multiples of
- * 256). 0 for non-positive sizes or another block. */
+ * (scale_block 16): four times the scale bytes of both operands, with B's N
+ * rounded up to a multiple of 256 and (scale_block 32) A's K rounded up to a
+ * multiple of 256: 4 * (M * K' + N' * K) / scale_block (4 * (M + N) * K /
+ * scale_block when N and K are multiples of 256). 0 for non-positive sizes
+ * or another block. */
 size_t mxfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t scale_block);
 
 /* The MXFP8 counterpart of mxfp4_gemm ([TIBQ], "The fix, and its supporting
@@ -263,7 +264,10 @@ size_t mxfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t scale_
  * (MXFP4_FORMAT_E4M3, one byte per element), sa / sb E8M0 scales per 32
  * elements in MXFP4_LAYOUT_MMA, C [M, N] = sum_k deqA[m, k] deqB[n, k] in fp32,
  * stored as c_dtype (fp32, or bf16 nearest-even) as in mxfp4_gemm_ex.
- *  Shapes: M % 256 == 0, N % 256 == 0, K % 128 == 0. */
+ *  Shapes as mxfp4_gemm: M, N and K positive multiples of 128, each at most
+ *  2^30 (the K step of one-byte codes is 128 deep; a last 128-row or
+ *  128-column tile is computed on zero-filled operands and only its valid
+ *  part is stored). */
 mxfp4_status mxfp8_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, void* c,
                         int32_t c_dtype, int64_t ldc, void* stream);
@@ -288,7 +292,8 @@ mxfp4_status mxfp8_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
  * workspace_bytes as in mxfp4_gemm_ex, sized by
  * mxfp4_gemm_workspace_size(M, N, K, 16) (six copies per K step instead of
  * twelve; bit-identical result).
- *  Shapes: M % 256 == 0, N % 256 == 0, K % 256 == 0; |ka + kb| <= 126. */
+ *  Shapes as mxfp4_gemm: M, N and K positive multiples of 128, each at most
+ *  2^30; |ka + kb| <= 126. */
 mxfp4_status nvfp4_gemm(const uint8_t* qa, const uint8_t* sa, int32_t ka, const uint8_t* qb,
                         const uint8_t* sb, int32_t kb, int64_t M, int64_t N, int64_t K, void* c,
                         int32_t c_dtype, int64_t ldc, void* workspace, size_t workspace_bytes,

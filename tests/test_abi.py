@@ -123,11 +123,12 @@ def test_host_side_validation(L):
     assert L.mxfp4_gemm_noalloc(good, good, good, good, 256, 320, 256, good, 320, None) == 2
     # workspace size: A's K and B's N rounded up to 256
     assert L.mxfp4_gemm_workspace_size(256, 384, 640, 32) == 4 * (256 * 768 + 512 * 640) // 32
+    assert L.mxfp4_gemm_workspace_size(384, 384, 384, 16) == 4 * (384 * 384 + 512 * 384) // 16
     assert L.mxfp8_gemm(good, good, good, good, 256, 256, 256, good, 3, 256, None) == 1
-    assert L.mxfp8_gemm(good, good, good, good, 128, 256, 128, good, 0, 256, None) == 2
+    assert L.mxfp8_gemm(good, good, good, good, 64, 256, 128, good, 0, 256, None) == 2
     assert L.mxfp8_gemm_ex(good, good, good, good, 256, 256, 128, 0, good, 0, 256, None) == 1
     assert L.mxfp8_gemm_ex(good, good, good, good, 256, 256, 128, 3, good, 0, 256, None) == 1
-    assert L.mxfp8_gemm_ex(good, good, good, good, 128, 256, 128, 2, good, 0, 256, None) == 2
+    assert L.mxfp8_gemm_ex(good, good, good, good, 256, 192, 128, 2, good, 0, 256, None) == 2
     pe5 = mx.QuantParams(rounding=mx.ROUND_SR, elem_format=mx.FORMAT_E5M2)._c()
     assert L.mxfp4_quantize(good, 0, 32, 32, 32, ctypes.byref(pe5), good, good, None, None, None, None) == 4
     pe3 = _CParams(0, 0, 0, 0, 0, 0, 0, 0, 3)
@@ -139,7 +140,7 @@ def test_host_side_validation(L):
     assert L.mxfp4_quantize(good, 0, 32, 32, 32, ctypes.byref(pe), good, good, None, None, None, None) == 1
     pe = mx.QuantParams(block=mx.BLOCK_1X16, elem_format=mx.FORMAT_E4M3)._c()
     assert L.mxfp4_quantize(good, 0, 32, 32, 32, ctypes.byref(pe), good, good, None, None, None, None) == 4
-    assert L.nvfp4_gemm(good, good, 0, good, good, 0, 256, 256, 128, good, 1, 256, None, 0, None) == 2
+    assert L.nvfp4_gemm(good, good, 0, good, good, 0, 256, 256, 96, good, 1, 256, None, 0, None) == 2
     assert L.nvfp4_gemm(good, good, 100, good, good, 30, 256, 256, 256, good, 1, 256, None, 0, None) == 1
     assert L.nvfp4_gemm(good, good, 0, good, good, 0, 256, 256, 256, good, 7, 256, None, 0, None) == 1
     pq = mx.QuantParams()._c()

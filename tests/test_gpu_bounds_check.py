@@ -101,31 +101,32 @@ def test_gemm_stores_stay_inside(bc_lib, M, N, K, c_dtype, images):
     assert torch.equal(want, got)
 
 
-@pytest.mark.parametrize("M,N,K", [(512, 768, 1024), (256, 384, 640)])
+@pytest.mark.parametrize("M,N,K", [(512, 768, 1024), (256, 384, 640), (384, 640, 1152)])
 def test_fused_epilogue_and_other_gemms_stay_inside(bc_lib, M, N, K):
     import gemm_pt_block_gb300 as mx
 
     t = _operands(M, N, K, 5)
     p = mx.QuantParams(rounding=mx.ROUND_SR, wht=True, wht_sign_mask=0x1234, seed=6,
                        scale_layout=mx.LAYOUT_MMA)
-    for fn in (lambda: mx.mxfp4_gemm_quantize(*t, M, N, K, p, col=p, with_c=True),
+    colp = p if M % 256 == 0 else None     # the column-wise epilogue needs the CTA-pair kernel
+    for fn in (lambda: mx.mxfp4_gemm_quantize(*t, M, N, K, p, col=colp, with_c=True),
                lambda: mx.mxfp4_gemm_quantize(*t, M, N, K, p, out_dtype=torch.bfloat16, with_c=True),
                lambda: mx.mxfp4_gemm_noalloc(*t, M, N, K)):
         want, got, status = _both(bc_lib, fn)
         assert status == 0
         assert _equal(want, got)
-    if N % 256 == 0 and K % 256 == 0:
-        tn = (t[0], torch.randint(40, 70, (M * K // 16,), dtype=torch.uint8, device=DEV),
-              t[2], torch.randint(40, 70, (N * K // 16,), dtype=torch.uint8, device=DEV))
-        fn = lambda: mx.nvfp4_gemm(tn[0], tn[1], -1, tn[2], tn[3], 2, M, N, K)
+    tn = (t[0], torch.randint(40, 70, (M * K // 16,), dtype=torch.uint8, device=DEV),
+          t[2], torch.randint(40, 70, (N * K // 16,), dtype=torch.uint8, device=DEV))
+    for ws in (None, False):
+        fn = lambda: mx.nvfp4_gemm(tn[0], tn[1], -1, tn[2], tn[3], 2, M, N, K, workspace=ws)
         want, got, status = _both(bc_lib, fn)
         assert status == 0 and torch.equal(want, got)
-        q8a = torch.randint(0, 120, (M, K), dtype=torch.uint8, device=DEV)
-        q8b = torch.randint(0, 120, (N, K), dtype=torch.uint8, device=DEV)
-        for fmt in (mx.FORMAT_E4M3, mx.FORMAT_E5M2):
-            fn = lambda: mx.mxfp8_gemm(q8a, t[1], q8b, t[3], M, N, K, elem_format=fmt)
-            want, got, status = _both(bc_lib, fn)
-            assert status == 0 and torch.equal(want, got)
+    q8a = torch.randint(0, 120, (M, K), dtype=torch.uint8, device=DEV)
+    q8b = torch.randint(0, 120, (N, K), dtype=torch.uint8, device=DEV)
+    for fmt in (mx.FORMAT_E4M3, mx.FORMAT_E5M2):
+        fn = lambda: mx.mxfp8_gemm(q8a, t[1], q8b, t[3], M, N, K, elem_format=fmt)
+        want, got, status = _both(bc_lib, fn)
+        assert status == 0 and torch.equal(want, got)
 
 
 def test_dequantize_rotation_and_amax_stay_inside(bc_lib):

@@ -140,6 +140,39 @@ def test_gemm_writes_only_c_rows_up_to_n(M, N, K, c_dtype, images):
     assert torch.equal(c[:, :N], want)
 
 
+@pytest.mark.parametrize("M,N,K", [(128, 384, 384), (384, 640, 1152), (256, 128, 128)])
+@pytest.mark.parametrize("kind", ["nvfp4", "nvfp4-images", "mxfp8", "mxfp8-e5m2"])
+def test_nvfp4_and_mxfp8_gemms_write_only_c(M, N, K, kind):
+    """The NVFP4 and MXFP8 GEMMs on shapes with a last M, N or K tile of 128:
+    nothing outside C's first N columns (and the NVFP4 workspace) is written."""
+    import gemm_pt_block_gb300 as mx
+
+    ldc = N + 40
+    g = torch.Generator(device=DEV).manual_seed(M + N + K)
+    nv = kind.startswith("nvfp4")
+    kb = K // 2 if nv else K
+    qa = torch.randint(0, 120, (M, kb), dtype=torch.uint8, device=DEV, generator=g)
+    qb = torch.randint(0, 120, (N, kb), dtype=torch.uint8, device=DEV, generator=g)
+    lo, hi = (40, 70) if nv else (120, 135)
+    per = 16 if nv else 32
+    sa = torch.randint(lo, hi, (M * K // per,), dtype=torch.uint8, device=DEV, generator=g)
+    sb = torch.randint(lo, hi, (N * K // per,), dtype=torch.uint8, device=DEV, generator=g)
+    ws_bytes = mx.gemm_workspace_size(M, N, K, 16) if kind == "nvfp4-images" else 0
+    ar = Arena([M * ldc * 4, max(ws_bytes, 16)])
+    c = ar.region(0, torch.float32, (M, ldc), writable=[(m * ldc * 4, (m * ldc + N) * 4) for m in range(M)])
+    if nv:
+        ws = ar.region(1, torch.uint8, (ws_bytes,)) if ws_bytes else False
+        mx.nvfp4_gemm(qa, sa, -2, qb, sb, 1, M, N, K, c=c, ldc=ldc, workspace=ws)
+        want = mx.nvfp4_gemm(qa, sa, -2, qb, sb, 1, M, N, K, workspace=False)
+    else:
+        fmt = mx.FORMAT_E5M2 if kind.endswith("e5m2") else mx.FORMAT_E4M3
+        mx.mxfp8_gemm(qa, sa, qb, sb, M, N, K, c=c, ldc=ldc, elem_format=fmt)
+        want = mx.mxfp8_gemm(qa, sa, qb, sb, M, N, K, elem_format=fmt)
+    ar.check(f"{kind} {M}x{N}x{K}")
+    assert mx.device_status() == 0
+    assert torch.equal(c[:, :N], want)
+
+
 @pytest.mark.parametrize("col", [False, True])
 @pytest.mark.parametrize("M,N,K", [(512, 768, 1024), (256, 384, 640)])
 def test_fused_epilogue_quantizer_writes_only_its_outputs(col, M, N, K):

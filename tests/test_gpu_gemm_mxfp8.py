@@ -45,7 +45,8 @@ def test_mxfp8_gemm_all_ones_exact():
     assert np.all(c == K)
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (256, 512, 384), (512, 768, 1024), (1024, 1280, 2048)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (256, 512, 384), (512, 768, 1024), (1024, 1280, 2048),
+                                   (128, 128, 128), (128, 384, 384), (384, 640, 1152), (640, 384, 256)])
 def test_mxfp8_gemm_random_within_tolerance(M, N, K):
     qa, qb = _codes(M, K, M + 1), _codes(N, K, N + 2)
     sa, sa_rm = _scales(M, K, K + 3)
@@ -87,4 +88,6 @@ def test_mxfp8_gemm_rejects_bad_shapes():
 
     z = torch.zeros(128 * 128, dtype=torch.uint8, device=DEV)
     with pytest.raises(mx.Mxfp4Error):
-        mx.mxfp8_gemm(z, z, z, z, 128, 256, 128)      # M % 256 != 0
+        mx.mxfp8_gemm(z, z, z, z, 64, 128, 128)       # M % 128 != 0
+    with pytest.raises(mx.Mxfp4Error):
+        mx.mxfp8_gemm(z, z, z, z, 128, 128, 96)       # K % 128 != 0

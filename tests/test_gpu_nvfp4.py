@@ -185,7 +185,8 @@ def test_nvfp4_gemm_per_block_scales_exact():
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (256, 512, 768), (512, 768, 2304),
-                                   (1024, 1280, 4096)])
+                                   (1024, 1280, 4096), (128, 128, 128), (128, 384, 384),
+                                   (384, 640, 1152), (640, 384, 640)])
 def test_nvfp4_gemm_random_within_tolerance(M, N, K):
     import gemm_pt_block_gb300 as mx
 
@@ -298,7 +299,8 @@ def test_dequantize_ex_every_format(fmt, layout):
     assert np.array_equal(got.cpu().numpy().astype(np.float64), want)
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (512, 768, 2304), (16384, 8192, 28672)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (512, 768, 2304), (16384, 8192, 28672),
+                                   (128, 384, 384), (384, 640, 1152)])
 def test_nvfp4_gemm_scale_images_bit_identical(M, N, K):
     """nvfp4_gemm's workspace path (six 128x256b copies per K step instead of
     twelve) gives the same bits as without a workspace."""
