@@ -340,9 +340,6 @@ mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uin
       return fail(MXFP4_ERR_UNSUPPORTED,
                   "mxfp4_gemm_quantize: 1x16 (NVFP4) output is not fused; quantize C separately");
   }
-  if (col && M % 256 != 0)
-    return fail(MXFP4_ERR_UNSUPPORTED,
-                "mxfp4_gemm_quantize: column-wise output needs M %% 256 == 0 (CTA-pair kernel)");
   mx::OrientArgs ro{}, co{};
   if (M > 0 && N > 0) {
     mxfp4_status st;

@@ -1074,10 +1074,6 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   const OrientArgs none{};
   const OrientArgs& qo = qout ? *qout : none;
   const OrientArgs& qc = qcol ? *qcol : none;
-  if (qcol && M % 256 != 0) {
-    *why = "column-wise quantization in the GEMM epilogue needs M % 256 == 0 (CTA pairs)";
-    return cudaErrorNotSupported;
-  }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1093,8 +1089,10 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
   }
   ensure_context();
   CUtensorMap ta, tb;
-  if (M % 256 == 0) {
-    // CTA pairs: 256 x 256 tiles.
+  if (M % 256 == 0 || qcol) {
+    // CTA pairs: 256 x 256 tiles (the column-wise epilogue runs only there; a
+    // last M tile of 128 rows leaves CTA 1 of its pair without output). The
+    // 1-CTA kernel below takes the other shapes with M % 256 == 128.
     CUtensorMap tsa, tsb;
     const bool img = ws != nullptr && !qcol && images_fit(M, N, K, false) &&
                      ws_bytes >= (size_t)workspace_bytes(M, N, K, false);
@@ -1105,7 +1103,7 @@ cudaError_t launch_gemm(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
       *why = "cuTensorMapEncodeTiled rejected the operand layout";
       return cudaErrorInvalidValue;
     }
-    const int num_tiles = (int)((M / 256) * ((N + pair::BNP - 1) / pair::BNP));
+    const int num_tiles = (int)(((M + 255) / 256) * ((N + pair::BNP - 1) / pair::BNP));
     const int pairs = d.sms / 2;
     const int grid = 2 * (num_tiles < pairs ? num_tiles : pairs);
     int64_t gm = kGroupBytes / (256 * (K / 2));

@@ -125,7 +125,7 @@ def mxfp4_linear(x: torch.Tensor, w: torch.Tensor, recipe: LinearRecipe | None =
     bf16), gradients in their inputs' dtypes.
 
     x [T, D] and w [F, D] are bf16 or fp32 CUDA tensors; T, D, F must be
-    multiples of 256. `step` offsets the stochastic-rounding seeds so each
+    multiples of 128. `step` offsets the stochastic-rounding seeds so each
     training step draws fresh bits."""
     for t, n in ((x, "x"), (w, "w")):
         if t.dtype not in (torch.bfloat16, torch.float32):

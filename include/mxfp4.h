@@ -307,8 +307,7 @@ mxfp4_status nvfp4_gemm(const uint8_t* qa, const uint8_t* sa, int32_t ka, const 
  *  row  if non-NULL, along N: q_row [M, N/2], s_row ([M, N/32] or
  *       MXFP4_LAYOUT_MMA);
  *  col  if non-NULL, C^T along M (the orientation the next layer's Wgrad
- *       consumes): q_col [N, M/2], s_col ([N, M/32] or MXFP4_LAYOUT_MMA);
- *       needs M % 256 == 0 (else MXFP4_ERR_UNSUPPORTED).
+ *       consumes): q_col [N, M/2], s_col ([N, M/32] or MXFP4_LAYOUT_MMA).
  * At least one of row / col must be non-NULL. Any block (except 64x64 and
  * 1x16: MXFP4_ERR_UNSUPPORTED), scale mode, rounding, rotation, element
  * format and scale layout mxfp4_quantize accepts; stochastic draws are keyed

@@ -149,11 +149,11 @@ def test_host_side_validation(L):
     pnv = mx.QuantParams(block=mx.BLOCK_1X16)._c()
     assert L.mxfp4_gemm_quantize(good, good, good, good, 128, 256, 256, good, 1, 256,
                                  ctypes.byref(pnv), good, good, None, None, None, None, 0, None) == 4
-    # no orientation; column-wise output with M % 256 != 0
+    # no orientation; column-wise NVFP4 output (not fused)
     assert L.mxfp4_gemm_quantize(good, good, good, good, 256, 256, 256, good, 1, 256,
                                  None, None, None, None, None, None, None, 0, None) == 1
     assert L.mxfp4_gemm_quantize(good, good, good, good, 128, 256, 256, good, 1, 256,
-                                 None, None, None, ctypes.byref(pq), good, good, None, 0, None) == 4
+                                 None, None, None, ctypes.byref(pnv), good, good, None, 0, None) == 4
     # dequantize / hadamard32
     assert L.mxfp4_dequantize(good, good, 1, 64, 128, good, None) == 2
     assert L.mxfp4_dequantize(good, good, 2, 64, 128, good, None) == 1

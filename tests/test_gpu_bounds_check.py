@@ -108,8 +108,7 @@ def test_fused_epilogue_and_other_gemms_stay_inside(bc_lib, M, N, K):
     t = _operands(M, N, K, 5)
     p = mx.QuantParams(rounding=mx.ROUND_SR, wht=True, wht_sign_mask=0x1234, seed=6,
                        scale_layout=mx.LAYOUT_MMA)
-    colp = p if M % 256 == 0 else None     # the column-wise epilogue needs the CTA-pair kernel
-    for fn in (lambda: mx.mxfp4_gemm_quantize(*t, M, N, K, p, col=colp, with_c=True),
+    for fn in (lambda: mx.mxfp4_gemm_quantize(*t, M, N, K, p, col=p, with_c=True),
                lambda: mx.mxfp4_gemm_quantize(*t, M, N, K, p, out_dtype=torch.bfloat16, with_c=True),
                lambda: mx.mxfp4_gemm_noalloc(*t, M, N, K)):
         want, got, status = _both(bc_lib, fn)

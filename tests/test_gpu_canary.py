@@ -174,7 +174,7 @@ def test_nvfp4_and_mxfp8_gemms_write_only_c(M, N, K, kind):
 
 
 @pytest.mark.parametrize("col", [False, True])
-@pytest.mark.parametrize("M,N,K", [(512, 768, 1024), (256, 384, 640)])
+@pytest.mark.parametrize("M,N,K", [(512, 768, 1024), (256, 384, 640), (384, 640, 1152)])
 def test_fused_epilogue_quantizer_writes_only_its_outputs(col, M, N, K):
     import gemm_pt_block_gb300 as mx
 
