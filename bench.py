@@ -699,6 +699,47 @@ def copy_bandwidth(device, nbytes: int = 1 << 30, reps: int = 3) -> dict:
             "both_gbs": 2 * nbytes / (t_both / 1e3) / 1e9}
 
 
+def measure_graph(st, steps: int):
+    """The same step captured once into a CUDA graph and replayed: launch
+    overhead paid once per step instead of once per call. The library's
+    per-device caches (kernel attributes, occupancy) are filled by an eager
+    step first; the captured calls then enqueue only kernel launches (and, for
+    NVFP4, async memsets). Outputs of the replay equal the eager step's."""
+    import torch
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        st.run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    want = {k: v.clone() for k, v in st.outs.items()}
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(g):
+            st.run()
+    except RuntimeError as e:     # report, do not fail the benchmark
+        return {"unavailable": str(e).splitlines()[0][:200]}
+    for o in st.outs.values():
+        o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    same = all(torch.equal(want[k], st.outs[k]) for k in want)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return {"value": sum(st.spec.gemm_flops()) / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": ms, "steps": steps, "outputs_equal_eager": same,
+            "what": "the step captured once in a CUDA graph (torch.cuda.graph) and replayed"}
+
+
 def measure_linear(spec: Spec, st: "Step", steps: int):
     """The same layer step through the autograd op (mxfp4_linear forward +
     backward on the step's X, W and dY, recipe taken from the workload), timed
@@ -1167,6 +1208,7 @@ def main():
         "gpu_launches": st.launches * args.steps,
         "clocks": clocks,
     }
+    line["graph"] = measure_graph(st, max(3, args.steps))
     if not args.no_e2e:
         line["e2e"] = measure_e2e(st, max(1, min(args.steps, 10)), ws)
     if len(spec.gemms) == 3 and not spec.nvfp4 and not args.no_e2e:

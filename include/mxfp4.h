@@ -20,6 +20,13 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Work is enqueued asynchronously on it; the return value reports argument
  *    validation and launch errors only. Calls are thread-safe.
+ *  - The first call of an entry point on a device fills per-device caches
+ *    (kernel attributes, occupancy). Later calls of mxfp4_quantize,
+ *    mxfp4_gemm, mxfp4_gemm_ex, mxfp4_gemm_quantize, nvfp4_gemm, mxfp8_gemm
+ *    and mxfp4_tensor_amax with caller-supplied outputs and workspaces enqueue
+ *    only kernel launches and asynchronous memsets on the stream, so a
+ *    sequence of them can be captured into a CUDA graph and replayed (tested:
+ *    the replay gives the eager results bit for bit).
  *  - Tensors are row-major with a leading dimension in elements. Packed E2M1
  *    codes hold two elements per byte: the even index in the low nibble, the
  *    odd index in the high nibble; code = sign << 3 | magnitude index into
