@@ -718,8 +718,9 @@ def measure_graph(st, steps: int):
     try:
         with torch.cuda.graph(g):
             st.run()
-    except RuntimeError as e:     # report, do not fail the benchmark
-        return {"unavailable": str(e).splitlines()[0][:200]}
+    except Exception as e:        # report, do not fail the benchmark
+        torch.cuda.synchronize()
+        return {"unavailable": (str(e).splitlines() or [repr(e)])[0][:200]}
     for o in st.outs.values():
         o.zero_()
     g.replay()
