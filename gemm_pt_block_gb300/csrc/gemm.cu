@@ -455,7 +455,7 @@ mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       int mb, nb;
       tile_coords(tile, num_m, num_n, group_m, mb, nb);
-      // One lane waits; the verdict is broadcast so the warp stays converged
+      // One lane waits; its result is broadcast so the warp stays converged
       // for the .sync.aligned tensor-memory loads.
       int ok = 0;
       if (lane == 0) ok = wait_bar(ptx::smem_u32(&ctl->acc_full), acc_phase, ctl, true);

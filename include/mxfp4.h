@@ -235,7 +235,7 @@ mxfp4_status mxfp4_gemm_ex(const uint8_t* qa, const uint8_t* sa, const uint8_t* 
 /* mxfp4_gemm for callers that cannot allocate device memory: code that runs
  * where cudaMalloc is off limits: a framework that owns all device memory
  * through its own pool, a host loop with latency bounds that must not wait on
- * the driver's allocator, a plugin that is handed only its inputs and
+ * the CUDA allocator, a plugin that is handed only its inputs and
  * outputs. The pages have no counterpart: this is a property of the library,
  * not of the method.
  * It runs the scale-image path of mxfp4_gemm_ex with the workspace taken from
