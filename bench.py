@@ -593,7 +593,9 @@ def measure_e2e(st: Step, steps: int, ws: int):
     out_ready, out_free = [ev(), ev()], [ev(), ev()]
     used = [False, False]
 
-    def one(i):
+    marks = []
+
+    def one(i, mark=False):
         b = i % 2
         with torch.cuda.stream(s_in):
             if used[b]:
@@ -612,6 +614,10 @@ def measure_e2e(st: Step, steps: int, ws: int):
             for k in host_out[b]:
                 host_out[b][k].copy_(dev_out[b][k], non_blocking=True)
             out_free[b].record(s_out)
+            if mark:                       # end of this step's copy-out
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(s_out)
+                marks.append(e)
         used[b] = True
 
     # A first copy from or into freshly pinned host memory runs several times
@@ -631,10 +637,17 @@ def measure_e2e(st: Step, steps: int, ws: int):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(s_in)
     for i in range(steps):
-        one(i)
+        one(i, mark=True)
     stop.record(s_out)
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop) / steps
+    # Per-step intervals between the ends of consecutive copy-outs (the first
+    # also holds the pipeline fill). Steps far above the median are pauses of
+    # the host copies on the GPU machine (seen after many pinned allocations by
+    # earlier processes); `value` keeps them.
+    iv = [start.elapsed_time(marks[0])] + [marks[j].elapsed_time(marks[j + 1])
+                                           for j in range(len(marks) - 1)]
+    med = statistics.median(iv[1:]) if len(iv) > 1 else iv[0]
     dev = next(iter(st.outs.values())).device
     ms = max_over_ranks(ms, ws, dev)
     flops = sum(st.spec.gemm_flops())
@@ -648,7 +661,10 @@ def measure_e2e(st: Step, steps: int, ws: int):
     return {"value": job_rate(flops, ws, ms) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "pipelined": "copy-in, compute and copy-out on three streams, two buffer slots",
-            "copy_roofline": bw, "frac_of_copy_bound": bound / ms}
+            "copy_roofline": bw, "frac_of_copy_bound": bound / ms,
+            "step_ms_median": med, "step_ms_max": max(iv[1:] or iv),
+            "stalled_steps": sum(1 for t in iv[1:] if t > 2 * med),
+            "frac_of_copy_bound_median_step": bound / med}
 
 
 def copy_bandwidth(device, nbytes: int = 1 << 30, reps: int = 3) -> dict:
