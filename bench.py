@@ -154,7 +154,7 @@ def make_spec(name: str) -> Spec:
     if name == TWO_D:
         s = Spec(name, "2D-block consistency: W [4096,4096] N(0,0.02) bf16; 32x32 blocks, round-up "
                        "scales, nearest-even, no rotation; W and W^T quantized in one pass")
-        p = P(mx.BLOCK_32X32, mx.SCALE_ROUNDUP, mx.ROUND_RTN, mx.LAYOUT_ROWMAJOR)
+        p = P(mx.BLOCK_32X32, mx.SCALE_ROUNDUP, mx.ROUND_RTN, mx.LAYOUT_MMA)
         s.quants = [QuantOp("W", 4096, 4096, ("normal", 0.02), 1001, p, p)]
         return s
     if name == "tiny":
@@ -866,7 +866,9 @@ def run_2d(args):
     L2); then checked in the same run: the column-wise codes and scales are
     exactly the transposes of the row-wise ones, and the same tensor in 1x32
     blocks gives the fraction of elements whose row-wise and column-wise scales
-    differ (zero for 32x32 blocks)."""
+    differ (zero for 32x32 blocks). Scales are written in the tensor-core
+    layout the GEMM consumes and read back into row-major order for the
+    checks."""
     import torch
     import gemm_pt_block_gb300 as mx
 
@@ -900,15 +902,23 @@ def run_2d(args):
     def codes(t):
         return torch.stack([t & 15, t >> 4], dim=-1).reshape(t.shape[0], -1)
 
-    def scale_map(s):                       # per-element scale of a [rows, K/32] array
-        return s.repeat_interleave(32, dim=1)
+    def rowmajor(s, rows):                  # tensor-core layout -> [rows, K/32]
+        nkb = s.numel() // rows
+        r = torch.arange(rows, device=s.device).view(-1, 1)
+        kb = torch.arange(nkb, device=s.device).view(1, -1)
+        off = (((r // 128) * (nkb // 4) + kb // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4
+               + kb % 4)
+        return s.reshape(-1)[off]
+
+    def scale_map(s, k):                    # per-element scale, [rows, k]
+        return rowmajor(s, s.numel() * 32 // k).repeat_interleave(32, dim=1)
 
     same_codes = torch.equal(codes(out[0]), codes(out[2]).T)
-    srow, scol = scale_map(out[1]), scale_map(out[3])
+    srow, scol = scale_map(out[1], q.cols), scale_map(out[3], q.rows)
     same_scales = torch.equal(srow, scol.T)
     p1 = replace(q.prow, block=mx.BLOCK_1X32)
     o1 = mx.mxfp4_quantize(x, p1, p1)
-    mism_1x32 = (scale_map(o1[1]) != scale_map(o1[3]).T).double().mean().item()
+    mism_1x32 = (scale_map(o1[1], q.cols) != scale_map(o1[3], q.rows).T).double().mean().item()
     mism_32x32 = (srow != scol.T).double().mean().item()
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
