@@ -225,6 +225,7 @@ constexpr int kTile = 64;
 constexpr int kStages = 3;
 constexpr int kConsumers = 128;
 constexpr int kTileThreads = kConsumers + 32;
+constexpr uint32_t kCodeTileBytes = kTile * kTile / 2;   // one orientation's E2M1 codes of a tile
 constexpr uint64_t kQuantWaitNs = 2000000000ull;
 
 // Byte offset of element (r, c) in a 64 x 64 tile as TMA lays it out with the
@@ -344,14 +345,28 @@ template <typename InT, int kVar, int kProf = 0>
 __global__ void __launch_bounds__(kTileThreads, kProf == 1 ? 4 : 3)
 quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols,
                   uint32_t ntiles, FastDiv tiles_x, const __grid_constant__ OrientArgs orow,
-                  const __grid_constant__ OrientArgs ocol, int do_row, int do_col) {
+                  const __grid_constant__ OrientArgs ocol, int do_row, int do_col,
+                  const __grid_constant__ CUtensorMap tmqr, const __grid_constant__ CUtensorMap tmqc) {
   constexpr uint32_t kStageBytes = kTile * kTile * sizeof(InT);
   constexpr uint32_t kBitsBytes = kTile * kTile * 2;
+  // The nearest-only profile (weights) stages each tile's E2M1 codes in
+  // shared memory and writes them with one tensor store per orientation (64
+  // rows of 32 bytes: whole sectors) instead of a 16-byte store per lane on a
+  // row of its own: W of the 70B layer 0.169 -> 0.140 ms. The stochastic
+  // profiles, bound by instruction issue, measured 1-2 % slower with it (the
+  // extra barrier and staging), so they keep the per-lane stores, as do
+  // bounds-checking builds (each store checked).
+#ifdef MXFP4_BOUNDS_CHECK
+  constexpr bool kTmaCodes = false;
+#else
+  constexpr bool kTmaCodes = kVar != kGeneral && kProf == 1;
+#endif
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   uint8_t* tbits0 = sm + kStages * kStageBytes;   // two draw buffers, swizzled like bf16 tiles
-  uint64_t* full = reinterpret_cast<uint64_t*>(tbits0 + 2 * kBitsBytes);
+  uint8_t* stage0 = tbits0 + 2 * kBitsBytes;       // code staging [tile parity][orientation][64][32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(stage0 + 4 * kCodeTileBytes);
   uint64_t* empty = full + kStages;
   uint32_t* abort_flag = reinterpret_cast<uint32_t*>(empty + kStages);
 
@@ -411,6 +426,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
     const int s = (int)(j % kStages);
     const uint8_t* st = sm + s * kStageBytes;
     uint8_t* tb = tbits0 + (j & 1) * kBitsBytes;
+    uint8_t* stg = stage0 + (j & 1) * 2 * kCodeTileBytes;   // row codes, then column codes
     int ok = 0;
     if (lane == 0) ok = wait_or_abort(ptx::smem_u32(&full[s]), (j / kStages) & 1u, abort_flag);
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -446,7 +462,10 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           if (!nv && orow.block) M = warp_max(M);
           if (rsr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
           const int e = scale_run32<false, nv>(R, orow, M, w);
-          if (valid) {
+          if constexpr (kTmaCodes) {
+            *reinterpret_cast<uint4*>(stg + rl * 32 + (warp >> 1) * 16) = encode32(R);
+            if (valid) store_run_scales<nv>(orow, r, c, cols, e);
+          } else if (valid) {
             store_run32<false>(orow, r, c, cols, R);
             store_run_scales<nv>(orow, r, c, cols, e);
           }
@@ -479,10 +498,31 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
             }
           }
           const int e = scale_run32<false, nv>(R, ocol, M, w);
-          if (valid) {
+          if constexpr (kTmaCodes) {
+            *reinterpret_cast<uint4*>(stg + kCodeTileBytes + cl * 32 + (warp >> 1) * 16) = encode32(R);
+            if (valid) store_run_scales<nv>(ocol, oc, k0, rows, e);
+          } else if (valid) {
             store_run32<false>(ocol, oc, k0, rows, R);
             store_run_scales<nv>(ocol, oc, k0, rows, e);
           }
+        }
+      }
+
+      if constexpr (kTmaCodes) {
+        // Every consumer's staged codes reach the tensor-store (async) proxy;
+        // thread 0 first waits until the previous tile's stores have read
+        // their staging buffer (the one the next tile writes), then issues
+        // this tile's stores. Out-of-range rows and columns of a ragged tile
+        // are clipped by the tensor maps.
+        ptx::fence_proxy_async();
+        if (t == 0) ptx::bulk_wait_read<0>();
+        named_sync_consumers();
+        if (t == 0 && ok) {
+          if (drow) ptx::tma_store_2d(&tmqr, (int32_t)(C0 >> 1), (int32_t)R0, ptx::smem_u32(stg));
+          if (dcol)
+            ptx::tma_store_2d(&tmqc, (int32_t)(R0 >> 1), (int32_t)C0,
+                              ptx::smem_u32(stg + kCodeTileBytes));
+          ptx::bulk_commit();
         }
       }
     } else {
@@ -561,6 +601,9 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[s]));
+  }
+  if constexpr (kTmaCodes) {
+    if (t == 0) ptx::bulk_wait<0>();   // the last stores are complete before the CTA exits
   }
 }
 
@@ -803,7 +846,8 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
   if (!make_tma_2d(&tm, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                    sizeof(InT), x, rows, cols, ld, kTile, bf ? 64 : 32))
     return cudaErrorInvalidValue;
-  constexpr int smem = kStages * kTile * kTile * sizeof(InT) + 2 * kTile * kTile * 2 + 256 + 1024;
+  constexpr int smem = kStages * kTile * kTile * sizeof(InT) + 2 * kTile * kTile * 2 +
+                       4 * kCodeTileBytes + 256 + 1024;
   int dev = 0;
   const cudaError_t de = cudaGetDevice(&dev);
   if (de != cudaSuccess) return de;
@@ -831,11 +875,23 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
     if (prof == 2) kern = lean2 ? quant_tile_kernel<InT, kLean, 2> : quant_tile_kernel<InT, kNv, 2>;
     if (prof == 3) kern = lean2 ? quant_tile_kernel<InT, kLean, 3> : quant_tile_kernel<InT, kNv, 3>;
   }
+  // Tensor maps of the E2M1 code outputs, written by the weights profile's
+  // tile stores (64 rows x 32 bytes); unused by the other variants and by
+  // bounds-checking builds, which store per lane.
+  CUtensorMap tqr{}, tqc{};
+#ifndef MXFP4_BOUNDS_CHECK
+  if (kern == quant_tile_kernel<InT, kLean, 1> || kern == quant_tile_kernel<InT, kNv, 1>) {
+    if (row && !make_byte_store_map(&tqr, row->q, rows, cols / 2, kTile, 32))
+      return cudaErrorInvalidValue;
+    if (col && !make_byte_store_map(&tqc, col->q, cols, rows / 2, kTile, 32))
+      return cudaErrorInvalidValue;
+  }
+#endif
   const unsigned grid = resident_ctas(kern, tx * ty, smem, kTileThreads);
   (void)cudaGetLastError();  // drop a stale error left by an earlier call
   kern<<<grid, kTileThreads, smem, st>>>(
       tm, rows, cols, (uint32_t)(tx * ty), make_fastdiv((uint32_t)tx), row ? *row : dummy,
-      col ? *col : dummy, row != nullptr, col != nullptr);
+      col ? *col : dummy, row != nullptr, col != nullptr, tqr, tqc);
   return cudaGetLastError();
 }
 

@@ -55,4 +55,21 @@ inline bool make_tma_2d(CUtensorMap* m, CUtensorMapDataType dt, uint32_t elem_by
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Byte array [rows, row_bytes] (row_bytes % 16 == 0, base 16-byte aligned)
+// written by tiled stores of box_rows x box_bytes boxes, unswizzled: the box's
+// image in shared memory is row-major. Stores are clipped at the edges.
+inline bool make_byte_store_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes,
+                                uint32_t box_rows, uint32_t box_bytes) {
+  auto fn = tma_encode_fn();
+  if (!fn) return false;
+  ensure_context();
+  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {box_bytes, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace mx
