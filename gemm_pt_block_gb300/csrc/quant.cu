@@ -349,17 +349,18 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
                   const __grid_constant__ CUtensorMap tmqr, const __grid_constant__ CUtensorMap tmqc) {
   constexpr uint32_t kStageBytes = kTile * kTile * sizeof(InT);
   constexpr uint32_t kBitsBytes = kTile * kTile * 2;
-  // The nearest-only profile (weights) stages each tile's E2M1 codes in
+  // The nearest-only MXFP4 profile (weights) stages each tile's E2M1 codes in
   // shared memory and writes them with one tensor store per orientation (64
   // rows of 32 bytes: whole sectors) instead of a 16-byte store per lane on a
   // row of its own: W of the 70B layer 0.169 -> 0.140 ms. The stochastic
-  // profiles, bound by instruction issue, measured 1-2 % slower with it (the
-  // extra barrier and staging), so they keep the per-lane stores, as do
-  // bounds-checking builds (each store checked).
+  // profiles and the NVFP4 weights profile (two scales per 32-run) measured
+  // 1-6 % slower with it (the extra barrier and staging cost more than the
+  // stores save), so they keep the per-lane stores, as do bounds-checking
+  // builds (each store checked).
 #ifdef MXFP4_BOUNDS_CHECK
   constexpr bool kTmaCodes = false;
 #else
-  constexpr bool kTmaCodes = kVar != kGeneral && kProf == 1;
+  constexpr bool kTmaCodes = kVar == kLean && kProf == 1;
 #endif
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -875,12 +876,12 @@ cudaError_t quantize_impl(const InT* x, int64_t rows, int64_t cols, int64_t ld,
     if (prof == 2) kern = lean2 ? quant_tile_kernel<InT, kLean, 2> : quant_tile_kernel<InT, kNv, 2>;
     if (prof == 3) kern = lean2 ? quant_tile_kernel<InT, kLean, 3> : quant_tile_kernel<InT, kNv, 3>;
   }
-  // Tensor maps of the E2M1 code outputs, written by the weights profile's
-  // tile stores (64 rows x 32 bytes); unused by the other variants and by
-  // bounds-checking builds, which store per lane.
+  // Tensor maps of the E2M1 code outputs, written by the MXFP4 weights
+  // profile's tile stores (64 rows x 32 bytes); unused by the other variants
+  // and by bounds-checking builds, which store per lane.
   CUtensorMap tqr{}, tqc{};
 #ifndef MXFP4_BOUNDS_CHECK
-  if (kern == quant_tile_kernel<InT, kLean, 1> || kern == quant_tile_kernel<InT, kNv, 1>) {
+  if (kern == quant_tile_kernel<InT, kLean, 1>) {
     if (row && !make_byte_store_map(&tqr, row->q, rows, cols / 2, kTile, 32))
       return cudaErrorInvalidValue;
     if (col && !make_byte_store_map(&tqc, col->q, cols, rows / 2, kTile, 32))
