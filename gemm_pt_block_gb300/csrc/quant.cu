@@ -217,8 +217,12 @@ quant_rows_1x32_kernel(const InT* __restrict__ x, uint32_t total, FastDiv halves
 //    warp reduction; it writes the row-wise output (16 bytes per lane) and,
 //    for stochastic rounding of the column orientation, the draws keyed by
 //    source index (computed once when both orientations share seed and stream).
-//    Phase 2: warp w owns columns 32(w%2) + lane of rows 32(w/2) ..: the same
-//    with a lane holding a whole column run; 16 bytes per lane.
+//    Phase 2: a lane holds a whole column run. With stochastic column
+//    rounding warp w owns columns 32(w/2) + lane of rows 32(w%2) .., the same
+//    32 x 32 block, so the shared draws it reads are the ones it wrote (a warp
+//    barrier, not a CTA one); otherwise columns 32(w%2) + lane of rows
+//    32(w/2) .. (the 64 x 64 general variant keeps this mapping and a CTA
+//    barrier).
 // Bank conflicts: row reads of 8 rows hit 8 different swizzled chunks; column
 // reads of 32 lanes read one 64-byte row segment.
 constexpr int kTile = 64;
@@ -464,7 +468,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           if (rsr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
           const int e = scale_run32<false, nv>(R, orow, M, w);
           if constexpr (kTmaCodes) {
-            *reinterpret_cast<uint4*>(stg + rl * 32 + (warp >> 1) * 16) = encode32(R);
+            *reinterpret_cast<uint4*>(stg + rl * 32 + (cl >> 5) * 16) = encode32(R);
             if (valid) store_run_scales<nv>(orow, r, c, cols, e);
           } else if (valid) {
             store_run32<false>(orow, r, c, cols, R);
@@ -475,9 +479,13 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
 
       // ---- phase 2: columns (quantization of x^T along rows) ----
       if (dcol) {
-        if (csr) named_sync_consumers();   // the draws were written by other warps
+        // With column draws each warp quantizes the same 32x32 block in both
+        // phases, so the draws it reads are the ones it wrote in phase 1 (a
+        // warp barrier suffices); without them it takes the other block of
+        // its column half, measured 1.5 % faster for the weights profile.
+        if (csr) __syncwarp();
         if (ok) {
-          const int cl = 32 * (warp & 1) + lane, rl = 32 * (warp >> 1);
+          const int cl = 32 * (csr ? warp >> 1 : warp & 1) + lane, rl = 32 * (csr ? warp & 1 : warp >> 1);
           const int64_t oc = C0 + cl, k0 = R0 + rl;
           const bool valid = oc < cols && k0 < rows;
           float2 R[16];
@@ -500,7 +508,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           }
           const int e = scale_run32<false, nv>(R, ocol, M, w);
           if constexpr (kTmaCodes) {
-            *reinterpret_cast<uint4*>(stg + kCodeTileBytes + cl * 32 + (warp >> 1) * 16) = encode32(R);
+            *reinterpret_cast<uint4*>(stg + kCodeTileBytes + cl * 32 + (rl >> 5) * 16) = encode32(R);
             if (valid) store_run_scales<nv>(ocol, oc, k0, rows, e);
           } else if (valid) {
             store_run32<false>(ocol, oc, k0, rows, R);
