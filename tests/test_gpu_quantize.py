@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from _util import assert_same, gpu_quantize, oracle_input, oracle_quantize
+from _util import assert_same, cuda_params, gpu_quantize, oracle_input, oracle_quantize
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -207,6 +207,46 @@ def test_transposition_invariance_on_gpu():
             return np.stack([lo, hi], axis=-1).reshape(qq.shape[0], -1)
         assert np.array_equal(unpack(q), unpack(qc).T)
         assert np.array_equal(np.repeat(s, 32, 1), np.repeat(sc, 32, 1).T)
+
+
+@pytest.mark.parametrize("rnd", ROUNDS)
+def test_transposition_invariance_full_2d_config(rnd):
+    """The 2D-block configuration at full size (W [4096, 4096] N(0, 0.02),
+    32x32 blocks, round-up scales, tensor-core scale layout; nearest rounding
+    runs the weights profile, whose codes leave by tile stores): column-wise
+    codes and scales are exactly the transposes of the row-wise ones, and the
+    same tensor in 1x32 blocks has different row- and column-wise scales for a
+    large share of its elements. A row band is checked against the oracle."""
+    import gemm_pt_block_gb300 as mx
+
+    x = synth.normal(4096, 4096, 0.02, seed=1001)
+    p = oracle.Params(block=oracle.BLOCK_32X32, scale_mode=oracle.SCALE_ROUNDUP, rounding=rnd, seed=8)
+    q, s, qc, sc = mx.mxfp4_quantize(x.to(DEV), cuda_params(p, 1), cuda_params(p, 1))
+    q, s, qc, sc = (t.cpu().numpy() for t in (q, s, qc, sc))
+
+    def unpack(qq):
+        return np.stack([qq & 15, qq >> 4], axis=-1).reshape(qq.shape[0], -1)
+
+    def rowmajor(ss, rows):                   # tensor-core layout -> [rows, nkb]
+        nkb = ss.size // rows
+        idx = np.arange(rows * nkb, dtype=np.int64).reshape(rows, nkb)
+        perm = sum(oracle.scales_to_mma(((idx >> (8 * b)) & 255).astype(np.uint8)).astype(np.int64) << (8 * b)
+                   for b in range(3))             # row-major index of each layout position
+        out = np.empty(rows * nkb, dtype=np.uint8)
+        out[perm] = ss.reshape(-1)
+        return out.reshape(rows, nkb)
+
+    assert np.array_equal(unpack(q), unpack(qc).T)
+    srow, scol = rowmajor(s, 4096), rowmajor(sc, 4096)
+    assert np.array_equal(np.repeat(srow, 32, 1), np.repeat(scol, 32, 1).T)
+    band = oracle_input(x[:64])
+    oq, os_ = oracle.quantize_rows(band, p)
+    assert np.array_equal(q[:64], oq) and np.array_equal(srow[:64], os_)
+    p1 = oracle.Params(block=oracle.BLOCK_1X32, scale_mode=oracle.SCALE_ROUNDUP, rounding=rnd, seed=8)
+    _, s1, _, sc1 = mx.mxfp4_quantize(x.to(DEV), cuda_params(p1, 1), cuda_params(p1, 1))
+    r1, c1 = rowmajor(s1.cpu().numpy(), 4096), rowmajor(sc1.cpu().numpy(), 4096)
+    mism = np.mean(np.repeat(r1, 32, 1) != np.repeat(c1, 32, 1).T)
+    assert 0.3 < mism < 0.7
 
 
 def test_hadamard32_matches_oracle_and_fused_path():
