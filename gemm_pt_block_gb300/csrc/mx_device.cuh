@@ -60,6 +60,15 @@ __device__ __forceinline__ void draws16(const PhiloxKeys& k, uint32_t stream, ui
   w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
 }
 
+// The same for elements 8 g0 .. 8 g0 + 15 when g0 fits in 32 bits.
+__device__ __forceinline__ void draws16_g(const PhiloxKeys& k, uint32_t stream, uint32_t g0,
+                                          uint32_t (&w)[8]) {
+  const U4 a = philox4x32_10(U4{g0, 0u, stream, 0u}, k);
+  const U4 b = philox4x32_10(U4{g0 + 1u, 0u, stream, 0u}, k);
+  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
 // ------------------------------------------------------- packed fp32 ops ---
 __device__ __forceinline__ float2 f2add(float2 a, float2 b) {
   float2 r;

@@ -126,10 +126,10 @@ __device__ __forceinline__ constexpr bool is_bf16() { return sizeof(InT) == 2; }
 // Row-orientation processing of the 16 elements a lane holds (block half
 // `upper` of a 1x32 run): rotation, block max (optionally reduced further by
 // `reduce`), scale, rounding. Returns the packed codes; *e receives the
-// exponent. i0 = source index of the first element (for the random draws).
+// exponent. g0 = source index of the first element / 8 (for the random draws).
 template <typename InT, typename Reduce>
 __device__ __forceinline__ uint2 quantize_halves(float2 (&R)[8], int upper, const OrientArgs& o,
-                                                 uint64_t i0, Reduce reduce, int* e_out) {
+                                                 uint32_t g0, Reduce reduce, int* e_out) {
   if (o.wht) {
     if (!is_bf16<InT>() && o.sm_half[upper]) apply_signs(R, o.sm_half[upper]);
     hadamard_halves(R, upper);
@@ -139,7 +139,7 @@ __device__ __forceinline__ uint2 quantize_halves(float2 (&R)[8], int upper, cons
     scale_all(R, sc.rcp);
     if (o.sr) {
       uint32_t w[8];
-      draws16(o.keys, o.stream, i0, w);
+      draws16_g(o.keys, o.stream, g0, w);
       sr16(R, w);
     }
     *e_out = (int)sc.code;
@@ -150,7 +150,7 @@ __device__ __forceinline__ uint2 quantize_halves(float2 (&R)[8], int upper, cons
   scale_all(R, inv_scale(e));
   if (o.sr) {
     uint32_t w[8];
-    draws16(o.keys, o.stream, i0, w);
+    draws16_g(o.keys, o.stream, g0, w);
     sr16(R, w);
   }
   *e_out = e;
@@ -188,8 +188,8 @@ quant_rows_1x32_kernel(const InT* __restrict__ x, uint32_t total, FastDiv halves
     float2 R[8];
     unpack(cur, R, o.xw[upper], signs);
     int e;
-    const uint2 packed = quantize_halves<InT>(R, upper, o, (uint64_t)((int64_t)r * cols + c0),
-                                              [](float m) { return m; }, &e);
+    // unit u is elements 16 u .. 16 u + 15 of the row-major tensor
+    const uint2 packed = quantize_halves<InT>(R, upper, o, u << 1, [](float m) { return m; }, &e);
     if (valid) {
       if (o.e4m3)
         put(reinterpret_cast<uint4*>(o.q + (int64_t)r * cols + c0), encode16_fp8(R, o.e5m2), o.q,
@@ -198,9 +198,10 @@ quant_rows_1x32_kernel(const InT* __restrict__ x, uint32_t total, FastDiv halves
         put(reinterpret_cast<uint2*>(o.q + (int64_t)r * (cols >> 1) + (c0 >> 1)), packed, o.q,
             o.q_bytes);
       if (o.nv)
-        put(o.s + scale_offset(o, r, c0 >> 4, cols >> 4), (uint8_t)e, o.s, o.s_bytes);
+        put(o.s + scale_offset32(o, r, (uint32_t)(c0 >> 4), (uint32_t)(cols >> 4)), (uint8_t)e, o.s,
+            o.s_bytes);
       else if (!upper)
-        store_scale(o, r, c0 >> 5, cols >> 5, e);
+        store_scale32(o, r, (uint32_t)(c0 >> 5), (uint32_t)(cols >> 5), e);
     }
   }
 }
@@ -455,7 +456,7 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
         read_run(st, rl, cl, R, InT());
         uint32_t w[16];
         if (dcol && csr) {
-          draws32(ocol.keys, ocol.stream, (uint64_t)(r * cols + c), w);
+          draws32_g(ocol.keys, ocol.stream, (uint32_t)r * (uint32_t)(cols >> 3) + (uint32_t)(c >> 3), w);
   #pragma unroll
           for (int i = 0; i < 4; ++i)
             *reinterpret_cast<uint4*>(tb + tile_off(rl, cl + 8 * i, uint16_t())) =
@@ -465,14 +466,14 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           if (rwht) hadamard32_lane(R, orow.sign_mask, orow.sgn);
           float M = nv ? 0.0f : absmax32(R);    // NVFP4 takes its two 16-block maxima itself
           if (!nv && orow.block) M = warp_max(M);
-          if (rsr && !share) draws32(orow.keys, orow.stream, (uint64_t)(r * cols + c), w);
+          if (rsr && !share) draws32_g(orow.keys, orow.stream, (uint32_t)r * (uint32_t)(cols >> 3) + (uint32_t)(c >> 3), w);
           const int e = scale_run32<false, nv>(R, orow, M, w);
           if constexpr (kTmaCodes) {
             *reinterpret_cast<uint4*>(stg + rl * 32 + (cl >> 5) * 16) = encode32(R);
-            if (valid) store_run_scales<nv>(orow, r, c, cols, e);
+            if (valid) store_run_scales32<nv>(orow, (uint32_t)r, (uint32_t)c, (uint32_t)cols, e);
           } else if (valid) {
             store_run32<false>(orow, r, c, cols, R);
-            store_run_scales<nv>(orow, r, c, cols, e);
+            store_run_scales32<nv>(orow, (uint32_t)r, (uint32_t)c, (uint32_t)cols, e);
           }
         }
       }
@@ -509,10 +510,10 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           const int e = scale_run32<false, nv>(R, ocol, M, w);
           if constexpr (kTmaCodes) {
             *reinterpret_cast<uint4*>(stg + kCodeTileBytes + cl * 32 + (rl >> 5) * 16) = encode32(R);
-            if (valid) store_run_scales<nv>(ocol, oc, k0, rows, e);
+            if (valid) store_run_scales32<nv>(ocol, (uint32_t)oc, (uint32_t)k0, (uint32_t)rows, e);
           } else if (valid) {
             store_run32<false>(ocol, oc, k0, rows, R);
-            store_run_scales<nv>(ocol, oc, k0, rows, e);
+            store_run_scales32<nv>(ocol, (uint32_t)oc, (uint32_t)k0, (uint32_t)rows, e);
           }
         }
       }
