@@ -579,6 +579,8 @@ def measure_e2e(st: Step, steps: int, ws: int):
     copies measured no faster: the copy bandwidth is the limit.)"""
     import torch
 
+    dev0 = next(iter(st.outs.values())).device
+    bw_before = copy_bandwidth(dev0)
     host_in = {k: v.cpu().pin_memory() for k, v in st.inputs.items()}
     dev_in = [{k: torch.empty_like(v) for k, v in st.inputs.items()} for _ in range(2)]
     dev_out = [{k: torch.empty_like(v) for k, v in st.outs.items()} for _ in range(2)]
@@ -652,7 +654,11 @@ def measure_e2e(st: Step, steps: int, ws: int):
     ms = max_over_ranks(ms, ws, dev)
     flops = sum(st.spec.gemm_flops())
     del dev_in, dev_out, host_out, host_in
-    bw = copy_bandwidth(dev)
+    # The copy rates, measured before and after the timed steps (best of five
+    # each time): the host copies pause at times on the GPU machine, and a probe
+    # caught in a pause would understate the bound.
+    bw_after = copy_bandwidth(dev)
+    bw = {k: max(bw_before[k], bw_after[k]) if k.endswith("_gbs") else bw_after[k] for k in bw_after}
     # Copy bound of one step: each direction at its own rate, and both together
     # at the combined rate while they overlap.
     bound = 1e3 * max(h2d / (bw["h2d_gbs"] * 1e9), d2h / (bw["d2h_gbs"] * 1e9),
@@ -667,7 +673,7 @@ def measure_e2e(st: Step, steps: int, ws: int):
             "frac_of_copy_bound_median_step": bound / med}
 
 
-def copy_bandwidth(device, nbytes: int = 1 << 30, reps: int = 3) -> dict:
+def copy_bandwidth(device, nbytes: int = 1 << 30, reps: int = 5) -> dict:
     """Raw pinned-host <-> device copy rates on this machine, in the same run: one
     nbytes cudaMemcpyAsync host->device, one device->host, and both at once on
     two streams (best of `reps` each, CUDA events)."""
