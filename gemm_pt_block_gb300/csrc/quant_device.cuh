@@ -146,12 +146,14 @@ __device__ __forceinline__ int scale_run32(float2 (&R)[16], const OrientArgs& o,
 template <bool kAnyFormat = true>
 __device__ __forceinline__ void store_run32(const OrientArgs& o, int64_t orow, int64_t k0,
                                             int64_t K, const float2 (&R)[16]) {
+  // orow and K are below 2^31 for every caller: one widening multiply.
   if (kAnyFormat && o.e4m3) {
-    uint4* d = reinterpret_cast<uint4*>(o.q + orow * K + k0);
+    uint4* d = reinterpret_cast<uint4*>(o.q + (uint64_t)(uint32_t)orow * (uint32_t)K + k0);
     put(d, encode16_fp8(&R[0], o.e5m2), o.q, o.q_bytes);
     put(d + 1, encode16_fp8(&R[8], o.e5m2), o.q, o.q_bytes);
   } else {
-    put(reinterpret_cast<uint4*>(o.q + orow * (K >> 1) + (k0 >> 1)), encode32(R), o.q, o.q_bytes);
+    put(reinterpret_cast<uint4*>(o.q + (uint64_t)(uint32_t)orow * (uint32_t)(K >> 1) + (k0 >> 1)),
+        encode32(R), o.q, o.q_bytes);
   }
 }
 
