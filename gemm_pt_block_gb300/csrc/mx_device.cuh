@@ -251,10 +251,12 @@ __device__ __forceinline__ float absmax32(const float2 (&R)[16]) {
   return m;
 }
 
+// Maximum over the warp in one instruction (exact, like the shuffle tree it
+// replaces; the quantizer's maxima are finite and >= 0).
 __device__ __forceinline__ float warp_max(float m) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  return m;
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(m));
+  return r;
 }
 
 // ----------------------------------------------------------------- scale ---
