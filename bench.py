@@ -17,8 +17,13 @@ quantization time included), TFLOP/s summed over ranks; the parts (GEMM
 TFLOP/s against the dense FP4 peak, quantizer GB/s against the HBM peak) are
 reported alongside, with the roofline of the dominant kernel.
 
+At N = 1 the default run then measures the pages' other configurations
+briefly (`other_configs`: the tiny layer, the 2D-block consistency check,
+the Llama-3.1-8B-shaped MLP step and the square sweep), outside the headline's
+timed region.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-       [--workload NAME] [--no-cpu-baseline] [--no-e2e]
+       [--workload NAME] [--no-cpu-baseline] [--no-e2e] [--no-configs]
 """
 from __future__ import annotations
 
@@ -854,6 +859,90 @@ def run_op(args):
     return 0
 
 
+def measure_step_config(name: str, steps: int, device) -> dict:
+    """A training-step configuration other than the headline, measured after
+    it. Before each step a 512 MB buffer is rewritten and read back (cold L2:
+    the tiny step would otherwise run from L2). The step time is a CUDA-graph
+    replay of the whole step (no host launch gaps, which would dominate the
+    tiny step); the per-launch times come from eager steps with CUDA events
+    around each launch. Medians over `steps` steps after 3 warm-up steps."""
+    import torch
+
+    spec = make_spec(name)
+    st = Step(spec, device)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    for _ in range(3):
+        st.run()
+    torch.cuda.synchronize()
+    per = [[] for _ in range(st.ops)]
+    for _ in range(steps):
+        flush_l2(flush)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(st.ops + 1)]
+        st.run(events=ev)
+        torch.cuda.synchronize()
+        for j in range(st.ops):
+            per[j].append(ev[j].elapsed_time(ev[j + 1]))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st.run()
+    g.replay()
+    whole = []
+    for _ in range(steps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        whole.append(e0.elapsed_time(e1))
+    import gemm_pt_block_gb300 as mx
+    if mx.device_status() != 0:
+        raise RuntimeError("a bounded device-side wait ran out")
+    ms = [statistics.median(t) for t in per]
+    nq = len(spec.quants)
+    labels, qwork, gwork = spec.labels(), spec.quant_bytes(), spec.gemm_flops()
+    peaks, src = _peaks()
+    fp4 = peaks.get("bf16_tflops", FALLBACK["bf16_tflops"]) * FP4_OVER_BF16
+    hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    step_ms = statistics.median(whole)
+    gt = sum(gwork) / (sum(ms[nq:]) / 1e3) / 1e12
+    qg = sum(qwork) / (sum(ms[:nq]) / 1e3) / 1e9
+    return {"workload": spec.desc, "value": sum(gwork) / (step_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": step_ms, "steps": steps,
+            "gemm": {"tflops": gt, "frac_of_fp4_peak": gt / fp4, "ms": dict(zip(labels[nq:], ms[nq:]))},
+            "quantize": {"gbs": qg, "frac_of_hbm": qg / hbm, "ms": dict(zip(labels[:nq], ms[:nq]))},
+            "timing": "graph replay of the step (value, ms_per_step) and eager per-launch CUDA events "
+                      "(parts), L2 flushed before each step; peaks as in the headline (" + src + ")"}
+
+
+def measure_configs(steps: int, device) -> dict:
+    """The pages' other configurations, measured briefly after the headline
+    step so that one benchmark line carries all five: the tiny layer (X, W
+    [512, 1024], outlier columns, Y = Xq Wq^T), the 2D-block consistency
+    check (W [4096, 4096] dual 32x32 in one pass, with its checks), the
+    Llama-3.1-8B-shaped MLP up-projection step, and the square sweep (the
+    quantizer variants and the n^3 GEMM, n = 1024..16384), the sweep's points
+    condensed to fractions of their rooflines."""
+    out = {"tiny": measure_step_config("tiny", steps, device)}
+    two = measure_2d(steps, 3)
+    out["2d-blocks"] = {k: two[k] for k in ("value", "unit", "ms_per_step", "steps", "checks")}
+    out["2d-blocks"].update(workload=two["config"]["workload"], frac_of_hbm=two["roofline"]["frac"],
+                            l2=two["config"]["l2"])
+    out["8b-mlp-up"] = measure_step_config("8b-mlp-up", steps, device)
+    pts = []
+    sweep_points(3, pts.append)
+    quant, gemm = {}, {}
+    for p in pts:
+        if "gbs" in p:
+            quant.setdefault(p["sweep"], {})[str(p["n"])] = round(p["frac_of_hbm"], 3)
+        else:
+            gemm[str(p["n"])] = {"tflops": round(p["tflops"], 1), "frac_of_fp4_peak": round(p["frac_of_fp4_peak"], 3)}
+    out["sweep"] = {"quantize_frac_of_hbm": quant, "gemm_n3": gemm,
+                    "what": "square bf16 inputs ~ t(3); per point the median of 3 launches, L2 flushed "
+                            "before each; `bench.py --sweep` prints every point in full"}
+    return out
+
+
 def flush_l2(buf):
     """Cold-L2 start for the next launch: rewrite a buffer larger than L2, then
     read it back, so none of the next launch's inputs are in L2 and the
@@ -866,6 +955,18 @@ def flush_l2(buf):
 
 
 def run_2d(args):
+    """`--workload 2d-blocks`: prints measure_2d's line; fails if the 32x32
+    blocks are not transposition-invariant."""
+    line = measure_2d(args.steps, args.warmup)
+    print(json.dumps(line), flush=True)
+    c = line["checks"]
+    if not (c["codes_transposition_invariant"] and c["scales_transposition_invariant"]
+            and c["scale_mismatch_fraction_32x32"] == 0.0):
+        raise RuntimeError("32x32 blocks are not transposition-invariant")
+    return 0
+
+
+def measure_2d(steps: int, warmup: int) -> dict:
     """The 2D-block consistency workload: W [4096, 4096] ~ N(0, 0.02) quantized
     in 32x32 blocks (round-up scales, nearest-even) in both orientations in one
     pass, timed with L2 flushed before each launch (W is 33.5 MB, smaller than
@@ -886,11 +987,11 @@ def run_2d(args):
     out = mx.mxfp4_quantize(x, q.prow, q.pcol)
     kw = dict(q_row=out[0], s_row=out[1], q_col=out[2], s_col=out[3])
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         mx.mxfp4_quantize(x, q.prow, q.pcol, **kw)
     times = []
     with ClockSampler(0) as clk:
-        for _ in range(args.steps):
+        for _ in range(steps):
             flush_l2(flush)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -927,8 +1028,8 @@ def run_2d(args):
     mism_1x32 = (scale_map(o1[1], q.cols) != scale_map(o1[3], q.rows).T).double().mean().item()
     mism_32x32 = (srow != scol.T).double().mean().item()
     line = {
-        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": steps,
+        "warmup": max(warmup, 3), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e2m1", "data": "synthetic",
         "config": bench_config(spec, 1),
         "roofline": {"bound": "hbm", "kernel": "quant_tile_kernel (weights profile)", "achieved": gbs,
@@ -938,12 +1039,9 @@ def run_2d(args):
                    "scales_transposition_invariant": same_scales,
                    "scale_mismatch_fraction_32x32": mism_32x32,
                    "scale_mismatch_fraction_1x32": mism_1x32},
-        "gpu_launches": args.steps, "clocks": clk.summary(),
+        "gpu_launches": steps, "clocks": clk.summary(),
     }
-    print(json.dumps(line), flush=True)
-    if not (same_codes and same_scales and mism_32x32 == 0.0):
-        raise RuntimeError("32x32 blocks are not transposition-invariant")
-    return 0
+    return line
 
 
 def run_ceiling(args):
@@ -1020,10 +1118,17 @@ def run_ceiling(args):
 
 
 def run_sweep(args):
+    """`--sweep`: one JSON line per point of sweep_points."""
+    sweep_points(max(args.steps, 3), lambda d: print(json.dumps(d), flush=True))
+    return 0
+
+
+def sweep_points(steps: int, emit) -> None:
     """Quantizer throughput over the square sweep (algorithmic bytes / time,
-    against the measured HBM copy peak). Between timed launches a 512 MB
-    buffer is rewritten and read back (flush_l2) so every launch starts with a
-    cold L2."""
+    against the measured HBM copy peak), then the n^3 GEMM at each n; `emit`
+    receives one dict per point. Between timed launches a 512 MB buffer is
+    rewritten and read back (flush_l2) so every launch starts with a cold
+    L2."""
     import torch
     import gemm_pt_block_gb300 as mx
     import synth
@@ -1032,7 +1137,6 @@ def run_sweep(args):
     peaks, src = _peaks()
     hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
-    steps = max(args.steps, 3)
     for n in sorted(SQUARES.values()):
         x = synth.dev_student_t(n, n, 3.0, 1004, "cuda")
         mask = synth.sign_mask(1004)
@@ -1064,9 +1168,8 @@ def run_sweep(args):
             ms = statistics.median(times)
             byts = n * n * (2 + ((prow is not None) + (pcol is not None)) * (0.5 + 1 / 32))
             gbs = byts / (ms / 1e3) / 1e9
-            print(json.dumps({"sweep": name, "n": n, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm,
-                              "hbm_peak_source": src, "l2": "flushed (512 MB rewrite and read-back) before each launch"}),
-                  flush=True)
+            emit({"sweep": name, "n": n, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm,
+                  "hbm_peak_source": src, "l2": "flushed (512 MB rewrite and read-back) before each launch"})
             del out, kw
         # the n^3 GEMM on 1x32 floor nearest-even operands (A, B ~ t(3))
         pg = P(mx.BLOCK_1X32, mx.SCALE_FLOOR, mx.ROUND_RTN, mx.LAYOUT_MMA)
@@ -1090,14 +1193,13 @@ def run_sweep(args):
         ms = statistics.median(times)
         tflops = 2.0 * n ** 3 / (ms / 1e3) / 1e12
         fp4 = peaks.get("bf16_tflops", FALLBACK["bf16_tflops"]) * FP4_OVER_BF16
-        print(json.dumps({"sweep": "gemm n^3 (1x32 floor nearest-even operands, scale images)", "n": n,
-                          "ms": ms, "tflops": tflops, "frac_of_fp4_peak": tflops / fp4,
-                          "fp4_peak_source": f"derived: {src} bf16_tflops x {FP4_OVER_BF16:g}",
-                          "l2": "flushed (512 MB rewrite and read-back) before each launch"}), flush=True)
+        emit({"sweep": "gemm n^3 (1x32 floor nearest-even operands, scale images)", "n": n,
+              "ms": ms, "tflops": tflops, "frac_of_fp4_peak": tflops / fp4,
+              "fp4_peak_source": f"derived: {src} bf16_tflops x {FP4_OVER_BF16:g}",
+              "l2": "flushed (512 MB rewrite and read-back) before each launch"})
         del qa, sa, qb, sb, c, ws, x
     if mx.device_status() != 0:
         raise RuntimeError("a bounded device-side wait ran out")
-    return 0
 
 
 def main():
@@ -1109,6 +1211,9 @@ def main():
     ap.add_argument("--workload", default="70b-layer", choices=WORKLOADS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations (tiny, 2d-blocks, 8b-mlp-up, sweep) that the "
+                         "default run measures after the headline step")
     ap.add_argument("--sweep", action="store_true",
                     help="quantizer sweep on square bf16 inputs n = 1024..16384: eight row-wise "
                          "variants ({RTN, SR} x {1x32 floor, 32x32 round-up} x {no rotation, "
@@ -1249,6 +1354,10 @@ def main():
         line["e2e"] = measure_e2e(st, min(max(args.steps, 20), 40), ws)
     if len(spec.gemms) == 3 and not spec.nvfp4 and not args.no_e2e:
         line["autograd_linear"] = measure_linear(spec, st, max(1, min(args.steps, 5)))
+    if ws == 1 and args.workload == "70b-layer" and not args.no_configs:
+        del st
+        torch.cuda.empty_cache()
+        line["other_configs"] = measure_configs(max(3, min(args.steps, 10)), device)
     if not args.no_cpu_baseline and rank == 0 and ws == 1:
         sample = OracleSample(spec, 4096)
         dt = sample.run()
