@@ -411,8 +411,15 @@ __device__ __forceinline__ uint2 encode16(const float2 (&V)[8]) {
                     e2m1x8(V[4].x, V[4].y, V[5].x, V[5].y, V[6].x, V[6].y, V[7].x, V[7].y));
 }
 
-// Stochastic rounding of two scaled values v whose draws are the 16-bit
-// halves r of w (element 0 low). With a = |v| in [lo, lo + st) on the E2M1
+// The draws of w as the floats 2^23 + r (element 0's r in the low half).
+__device__ __forceinline__ float2 draw_floats(uint32_t w) {
+  return make_float2(__uint_as_float(0x4B000000u | (w & 0xFFFFu)),
+                     __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7432)));
+}
+
+// Stochastic rounding of two scaled values v whose draws r come as
+// f = draw_floats(w) (the 16-bit halves of w, element 0 low). With a = |v|
+// in [lo, lo + st) on the E2M1
 // grid, the value goes up iff r < 2^16 (a - lo) / st, i.e. iff a - lo > th
 // with th = r * st * 2^-16; equivalently the result is the smallest multiple
 // of st that is >= a - th (lo is a multiple of st, and a - th > lo - st).
@@ -420,8 +427,8 @@ __device__ __forceinline__ uint2 encode16(const float2 (&V)[8]) {
 //   st = max(1, 2^E(a)) / 2 (E = unbiased exponent; 1/2 below 1); the grid
 //     points of [lo, lo + st] are multiples of st, and values in (6, 8) that
 //     reach 8 saturate to 6 in the E2M1 conversion as they round down to 6;
-//   -r * 2^-17 is exact, formed as fma(2^23 + r, -2^-17, 64) from a float
-//     2^23 + r assembled from r's bits (r has 16 bits);
+//   -r * 2^-17 is exact, formed as fma(2^23 + r, -2^-17, 64) from f
+//     (r has 16 bits);
 //   x = a - th, taken with one rounding as fma(2 st, -r * 2^-17, a) (the
 //     product is exact: 2 st is a power of two), is exact for a >= 1/2 (both
 //     are multiples of ulp(a) within one binade of x) and otherwise has the
@@ -431,20 +438,21 @@ __device__ __forceinline__ uint2 encode16(const float2 (&V)[8]) {
 // The rounding works on |v|; v's sign bit is put back on the result (a
 // negative value that rounds to zero gives -0). Returns the chosen grid
 // values, whose E2M1 conversion is then exact.
-__device__ __forceinline__ float2 sr_pair(float2 v, uint32_t w) {
+__device__ __forceinline__ float2 sr_pair(float2 v, float2 f) {
   const uint32_t b0 = __float_as_uint(v.x), b1 = __float_as_uint(v.y);
   const float2 a = make_float2(fabsf(v.x), fabsf(v.y));
   const float2 st2 = make_float2(fmaxf(__uint_as_float(b0 & 0x7F800000u), 1.0f),
                                  fmaxf(__uint_as_float(b1 & 0x7F800000u), 1.0f));
   const float2 C = f2mul(st2, make_float2(6291456.0f, 6291456.0f));        // 3 * 2^21
-  const float2 f = make_float2(__uint_as_float(0x4B000000u | (w & 0xFFFFu)),
-                               __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7432)));
   const float2 nr = f2fma(f, make_float2(-7.62939453125e-6f, -7.62939453125e-6f), make_float2(64.0f, 64.0f));
   const float2 x = f2fma(st2, nr, a);
   const float2 q = f2sub(f2add_rp(x, C), C);
   return make_float2(__uint_as_float(__float_as_uint(q.x) | (b0 & 0x80000000u)),
                      __uint_as_float(__float_as_uint(q.y) | (b1 & 0x80000000u)));
 }
+
+// The same with the draws as the word w.
+__device__ __forceinline__ float2 sr_pair(float2 v, uint32_t w) { return sr_pair(v, draw_floats(w)); }
 
 // SR of 16 scaled values; word k of w holds the draws of pair R[k].
 __device__ __forceinline__ void sr16(float2 (&V)[8], const uint32_t (&w)[8]) {

@@ -496,7 +496,9 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
           if (cwht) hadamard32_lane(R, ocol.sign_mask, ocol.sgn);
           float M = nv ? 0.0f : absmax32(R);
           if (!nv && ocol.block) M = warp_max(M);
-          uint32_t w[16];
+          // The draws of column elements (rl + 2k, rl + 2k + 1), each 16-bit
+          // draw read straight into its float 2^23 + r.
+          float2 F[16];
           if (csr) {
             uint32_t ob[8];   // the draw buffer is laid out like a bf16 tile
             col_offsets(rl, cl, ob, uint16_t());
@@ -504,10 +506,10 @@ quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t
             for (int k = 0; k < 16; ++k) {
               const uint32_t a = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k) & 7] + 1024 * (k >> 2));
               const uint32_t b = *reinterpret_cast<const uint16_t*>(tb + ob[(2 * k + 1) & 7] + 1024 * (k >> 2));
-              w[k] = __byte_perm(a, b, 0x5410);
+              F[k] = make_float2(__uint_as_float(0x4B000000u | a), __uint_as_float(0x4B000000u | b));
             }
           }
-          const int e = scale_run32<false, nv>(R, ocol, M, w);
+          const int e = scale_run32<false, nv>(R, ocol, M, F);
           if constexpr (kTmaCodes) {
             *reinterpret_cast<uint4*>(stg + kCodeTileBytes + cl * 32 + (rl >> 5) * 16) = encode32(R);
             if (valid) store_run_scales32<nv>(ocol, (uint32_t)oc, (uint32_t)k0, (uint32_t)rows, e);

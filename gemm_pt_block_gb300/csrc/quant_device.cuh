@@ -111,10 +111,11 @@ __device__ __forceinline__ void draws32(const PhiloxKeys& k, uint32_t stream, ui
 // when asked; nearest rounding happens in the conversion). Returns e, or for
 // NVFP4 (whose two 16-blocks take their own maxima and E4M3 scales) the two
 // scale codes, first block in the low byte. kAnyFormat = false compiles the
-// E2M1 / E8M0 case only; kNvfp4 = false leaves NVFP4 out.
-template <bool kAnyFormat = true, bool kNvfp4 = kAnyFormat>
+// E2M1 / E8M0 case only; kNvfp4 = false leaves NVFP4 out. The draws come as
+// words (D = uint32_t, two 16-bit draws each) or as draw_floats pairs.
+template <bool kAnyFormat = true, bool kNvfp4 = kAnyFormat, typename D = uint32_t>
 __device__ __forceinline__ int scale_run32(float2 (&R)[16], const OrientArgs& o, float M,
-                                           const uint32_t (&w)[16]) {
+                                           const D (&w)[16]) {
   if (kNvfp4 && o.nv) {
     const NvScale a = nv_scale(absmax16(&R[0]), o.roundup, o.nv_p2k, o.nv_zmul);
     const NvScale b = nv_scale(absmax16(&R[8]), o.roundup, o.nv_p2k, o.nv_zmul);
