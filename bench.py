@@ -883,15 +883,22 @@ def measure_step_config(name: str, steps: int, device) -> dict:
         for j in range(st.ops):
             per[j].append(ev[j].elapsed_time(ev[j + 1]))
     g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        st.run()
-    g.replay()
+    try:
+        with torch.cuda.graph(g):
+            st.run()
+        replay = g.replay
+        how = "graph replay of the step (value, ms_per_step)"
+    except Exception:              # time the eager step instead; say so
+        torch.cuda.synchronize()
+        replay = st.run
+        how = "eager step (graph capture failed) for value and ms_per_step"
+    replay()
     whole = []
     for _ in range(steps):
         flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        g.replay()
+        replay()
         e1.record()
         torch.cuda.synchronize()
         whole.append(e0.elapsed_time(e1))
@@ -911,8 +918,8 @@ def measure_step_config(name: str, steps: int, device) -> dict:
             "ms_per_step": step_ms, "steps": steps,
             "gemm": {"tflops": gt, "frac_of_fp4_peak": gt / fp4, "ms": dict(zip(labels[nq:], ms[nq:]))},
             "quantize": {"gbs": qg, "frac_of_hbm": qg / hbm, "ms": dict(zip(labels[:nq], ms[:nq]))},
-            "timing": "graph replay of the step (value, ms_per_step) and eager per-launch CUDA events "
-                      "(parts), L2 flushed before each step; peaks as in the headline (" + src + ")"}
+            "timing": how + " and eager per-launch CUDA events (parts), L2 flushed before each "
+                      "step; peaks as in the headline (" + src + ")"}
 
 
 def measure_configs(steps: int, device) -> dict:
