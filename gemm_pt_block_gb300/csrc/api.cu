@@ -88,11 +88,18 @@ mxfp4_status check_params(const mxfp4_quant_params* p, uint8_t* q, uint8_t* s, i
   return MXFP4_OK;
 }
 
+// Element counts above 2^40 (2 TB of bf16) cannot be resident on one GPU;
+// rejecting them first keeps every size product below int64's range.
+constexpr int64_t kMaxElems = (int64_t)1 << 40;
+
+bool too_large(int64_t rows, int64_t cols) { return rows > 0 && cols > kMaxElems / rows; }
+
 mxfp4_status check_input(const void* x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld) {
-  if (!x && rows * cols > 0) return fail(MXFP4_ERR_INVALID_ARG, "x is NULL");
   if (dtype != MXFP4_DTYPE_BF16 && dtype != MXFP4_DTYPE_F32)
     return fail(MXFP4_ERR_INVALID_ARG, "bad x_dtype %d", dtype);
   if (rows < 0 || cols < 0) return fail(MXFP4_ERR_SHAPE, "negative dimension");
+  if (too_large(rows, cols)) return fail(MXFP4_ERR_SHAPE, "tensor too large (more than 2^40 elements)");
+  if (!x && rows * cols > 0) return fail(MXFP4_ERR_INVALID_ARG, "x is NULL");
   if (cols % 32 != 0) return fail(MXFP4_ERR_SHAPE, "cols (%lld) must be a multiple of 32", (long long)cols);
   if (ld < cols) return fail(MXFP4_ERR_SHAPE, "ld_x (%lld) < cols (%lld)", (long long)ld, (long long)cols);
   if (!aligned16(x) || ld % 8 != 0)
@@ -149,12 +156,13 @@ namespace {
 mxfp4_status dequantize_common(const char* name, const uint8_t* q, const uint8_t* s,
                                int32_t scale_layout, int fmt, int32_t tensor_exp, int64_t rows,
                                int64_t cols, float* out, void* stream) {
-  if ((!q || !s || !out) && rows * cols > 0) return fail(MXFP4_ERR_INVALID_ARG, "%s: NULL pointer", name);
   if (scale_layout != MXFP4_LAYOUT_ROWMAJOR && scale_layout != MXFP4_LAYOUT_MMA)
     return fail(MXFP4_ERR_INVALID_ARG, "%s: bad scale_layout %d", name, scale_layout);
   if (rows < 0 || cols < 0 || cols % 32 != 0)
     return fail(MXFP4_ERR_SHAPE, "%s: cols (%lld) must be a non-negative multiple of 32", name,
                 (long long)cols);
+  if (too_large(rows, cols)) return fail(MXFP4_ERR_SHAPE, "%s: tensor too large (more than 2^40 elements)", name);
+  if ((!q || !s || !out) && rows * cols > 0) return fail(MXFP4_ERR_INVALID_ARG, "%s: NULL pointer", name);
   if (scale_layout == MXFP4_LAYOUT_MMA && (rows % 128 != 0 || cols % 128 != 0))
     return fail(MXFP4_ERR_SHAPE, "%s: tensor-core scale layout needs rows and cols %% 128 == 0", name);
   if (!aligned16(q) || !aligned16(out))

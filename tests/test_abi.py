@@ -88,6 +88,14 @@ def test_host_side_validation(L):
     assert b"2^31" in L.mxfp4_last_error()
     assert L.mxfp4_quantize(good, 0, 1 << 22, 1 << 17, 1 << 17, ctypes.byref(p), good, good,
                             None, None, None, None) == 2
+    # dimensions whose product would overflow int64 are rejected as shapes
+    # before any pointer or size arithmetic
+    huge = 1 << 40
+    assert L.mxfp4_quantize(None, 0, huge, huge, huge, ctypes.byref(p), None, None,
+                            None, None, None, None) == 2
+    assert b"too large" in L.mxfp4_last_error()
+    assert L.mxfp4_dequantize(None, None, 0, huge, huge, None, None) == 2
+    assert L.hadamard32(None, 0, huge, huge, huge, 0, 0, None, None) == 2
     # column output needs rows % 32
     assert L.mxfp4_quantize(good, 0, 48, 32, 32, None, None, None, ctypes.byref(p), good, good, None) == 2
     # tensor-core scale layout needs 128-row tiles
