@@ -175,7 +175,8 @@ mxfp4_status mxfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int64_
  * of precision reduction"): out[r, c] = E2M1(code) * 2^(byte - 127) in fp32;
  * scale byte 0xFF (E8M0 NaN) gives NaN.
  *  q [rows, cols/2], s in scale_layout, out [rows, cols] fp32 (dense).
- *  cols % 32 == 0 (MMA layout: rows % 128 == 0, cols % 128 == 0). */
+ *  cols % 32 == 0 (MMA layout: rows % 128 == 0, cols % 128 == 0), at most
+ *  2^40 elements; else MXFP4_ERR_SHAPE. */
 mxfp4_status mxfp4_dequantize(const uint8_t* q, const uint8_t* s, int32_t scale_layout,
                               int64_t rows, int64_t cols, float* out, void* stream);
 
@@ -334,7 +335,8 @@ mxfp4_status mxfp4_gemm_quantize(const uint8_t* qa, const uint8_t* sa, const uin
 /* Stand-alone 32-point block rotation along cols ([News], para. 2):
  *  forward (inverse == 0): y = c * H * diag(s) * x per 32-block;
  *  inverse (inverse == 1): y = diag(s) * c * H * x.
- *  x [rows, cols] bf16/fp32 with ld_x; y [rows, cols] fp32 dense; cols % 32 == 0.
+ *  x [rows, cols] bf16/fp32 with ld_x; y [rows, cols] fp32 dense; cols % 32 == 0
+ *  and at most 2^40 elements (else MXFP4_ERR_SHAPE).
  *  The forward rotation is bit-identical to the one mxfp4_quantize fuses. */
 mxfp4_status hadamard32(const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
                         int64_t ld_x, uint32_t sign_mask, int32_t inverse, float* y,
@@ -346,7 +348,8 @@ mxfp4_status hadamard32(const void* x, int32_t x_dtype, int64_t rows, int64_t co
  * device so a training step can carry it to the next step without a host
  * round trip.
  *  x          [rows, cols] bf16 or fp32 (x_dtype), leading dimension ld_x;
- *             shape and alignment rules as mxfp4_quantize (cols % 32 == 0).
+ *             cols % 32 == 0, at most 2^40 elements (else MXFP4_ERR_SHAPE);
+ *             16-byte aligned with ld_x % 8 == 0 (else MXFP4_ERR_ALIGN).
  *  amax       device pointer to one float (4-byte aligned): receives the
  *             largest |x| (0 for an empty tensor).
  *  tensor_exp device pointer to one int32 or NULL: receives the smallest k
