@@ -25,6 +25,7 @@ DTYPE_BF16, DTYPE_F32 = 0, 1
 _STATUS = {
     0: "MXFP4_OK", 1: "MXFP4_ERR_INVALID_ARG", 2: "MXFP4_ERR_SHAPE", 3: "MXFP4_ERR_ALIGN",
     4: "MXFP4_ERR_UNSUPPORTED", 5: "MXFP4_ERR_CUDA", 6: "MXFP4_ERR_TIMEOUT",
+    7: "MXFP4_ERR_BOUNDS",
 }
 
 
