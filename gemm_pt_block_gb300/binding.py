@@ -1,8 +1,9 @@
 """ctypes marshalling for libmxfp4.so: torch tensors in, pointers and sizes out.
 
 Nothing here computes: each function checks that tensors live on a CUDA
-device with the expected dtype and contiguity, allocates outputs the caller did
-not pass, and forwards raw pointers plus the current CUDA stream to the C ABI.
+device with the expected dtype, contiguity and size (the C ABI takes raw
+pointers and cannot check extents), allocates outputs the caller did not
+pass, and forwards raw pointers plus the current CUDA stream to the C ABI.
 """
 from __future__ import annotations
 
@@ -172,6 +173,40 @@ def scale_numel(rows: int, k: int, block: int = BLOCK_1X32) -> int:
     return rows * (k // 16 if block == BLOCK_1X16 else k // 32)
 
 
+def _buffer(t: torch.Tensor, numel: int, dtype: torch.dtype, name: str) -> None:
+    """A caller-supplied buffer the library reads or writes as `numel` dense
+    elements of `dtype`: on a CUDA device, contiguous and large enough (the C
+    ABI takes raw pointers and cannot check extents itself)."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements; {numel} are needed")
+
+
+def _matrix_out(c: torch.Tensor, M: int, N: int, ldc: int, name: str = "c") -> None:
+    """C [M, N] with row stride ldc inside c's storage, unit column stride."""
+    if not c.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if c.dim() != 2 or c.shape[0] < M or c.shape[1] < N or (N > 1 and c.stride(1) != 1):
+        raise ValueError(f"{name} must be 2-D, at least [{M}, {N}], with unit column stride")
+    if ldc < N:
+        raise ValueError(f"ldc ({ldc}) < N ({N})")
+    es = c.element_size()
+    room = c.untyped_storage().nbytes() - c.storage_offset() * es
+    if M > 0 and N > 0 and ((M - 1) * ldc + N) * es > room:
+        raise ValueError(f"{name}'s storage is too small for [{M}, {N}] with ldc {ldc}")
+
+
+def _operand(q: torch.Tensor, s: torch.Tensor, rows: int, K: int, code_bytes: int, scale_div: int,
+             name: str) -> None:
+    _buffer(q, rows * K * code_bytes // 2, torch.uint8, "q" + name)
+    _buffer(s, rows * (K // scale_div), torch.uint8, "s" + name)
+
+
 def _scales_out(rows: int, k: int, p: QuantParams, dev) -> torch.Tensor:
     if p.scale_layout == LAYOUT_MMA:
         return torch.empty(scale_numel(rows, k, p.block), dtype=torch.uint8, device=dev)
@@ -203,6 +238,12 @@ def mxfp4_quantize(x: torch.Tensor, row: QuantParams | None = None, col: QuantPa
     if col is not None:
         q_col = torch.empty((cols, col.code_cols(rows)), dtype=torch.uint8, device=dev) if q_col is None else q_col
         s_col = _scales_out(cols, rows, col, dev) if s_col is None else s_col
+    if row is not None:
+        _buffer(q_row, rows * row.code_cols(cols), torch.uint8, "q_row")
+        _buffer(s_row, scale_numel(rows, cols, row.block), torch.uint8, "s_row")
+    if col is not None:
+        _buffer(q_col, cols * col.code_cols(rows), torch.uint8, "q_col")
+        _buffer(s_col, scale_numel(cols, rows, col.block), torch.uint8, "s_col")
     rp = row._c() if row is not None else None
     cp = col._c() if col is not None else None
     _check(lib().mxfp4_quantize(
@@ -224,7 +265,11 @@ def mxfp4_dequantize(q: torch.Tensor, s: torch.Tensor, rows: int, cols: int,
     its scale_layout is used when given."""
     if not q.is_cuda or not s.is_cuda:
         raise ValueError("q and s must be CUDA tensors")
+    p = QuantParams() if params is None else params
+    _buffer(q, rows * p.code_cols(cols), torch.uint8, "q")
+    _buffer(s, scale_numel(rows, cols, p.block), torch.uint8, "s")
     out = torch.empty((rows, cols), dtype=torch.float32, device=q.device) if out is None else out
+    _buffer(out, rows * cols, torch.float32, "out")
     if params is None:
         _check(lib().mxfp4_dequantize(_ptr(q), _ptr(s), scale_layout, rows, cols, _ptr(out),
                                       _stream(q, stream)))
@@ -278,10 +323,13 @@ def mxfp4_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.T
     images (mxfp4_gemm_ex; same result, faster), a CUDA tensor supplies it,
     False calls the plain mxfp4_gemm entry point (fp32 C) without one."""
     _check_operands(qa, sa, qb, sb)
+    _operand(qa, sa, M, K, 1, 32, "a")
+    _operand(qb, sb, N, K, 1, 32, "b")
     cdt = _c_dtype(c, out_dtype)
     if c is None:
         c = torch.empty((M, N), dtype=out_dtype, device=qa.device)
     ldc = c.stride(0) if ldc is None else ldc
+    _matrix_out(c, M, N, ldc)
     if workspace is False and cdt == DTYPE_F32:
         _check(lib().mxfp4_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), ldc,
                                 _stream(qa, stream)))
@@ -297,9 +345,14 @@ def mxfp4_gemm_noalloc(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb:
     """mxfp4_gemm on the scale-image path with the library's static scratch
     (no workspace, no allocation); fp32 C."""
     _check_operands(qa, sa, qb, sb)
+    _operand(qa, sa, M, K, 1, 32, "a")
+    _operand(qb, sb, N, K, 1, 32, "b")
     if c is None:
         c = torch.empty((M, N), dtype=torch.float32, device=qa.device)
+    if c.dtype != torch.float32:
+        raise TypeError("c must be float32")
     ldc = c.stride(0) if ldc is None else ldc
+    _matrix_out(c, M, N, ldc)
     _check(lib().mxfp4_gemm_noalloc(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), ldc,
                                     _stream(qa, stream)))
     return c
@@ -313,10 +366,13 @@ def mxfp8_gemm(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb: torch.T
     elem_format=FORMAT_E5M2, E5M2) codes [M, K] / [N, K], E8M0 scales in
     tensor-core layout; C fp32 or bf16 as in mxfp4_gemm."""
     _check_operands(qa, sa, qb, sb)
+    _operand(qa, sa, M, K, 2, 32, "a")
+    _operand(qb, sb, N, K, 2, 32, "b")
     cdt = _c_dtype(c, out_dtype)
     if c is None:
         c = torch.empty((M, N), dtype=out_dtype, device=qa.device)
     ldc = c.stride(0) if ldc is None else ldc
+    _matrix_out(c, M, N, ldc)
     if elem_format == FORMAT_E4M3:
         _check(lib().mxfp8_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c), cdt, ldc,
                                 _stream(qa, stream)))
@@ -333,10 +389,13 @@ def nvfp4_gemm(qa: torch.Tensor, sa: torch.Tensor, ka: int, qb: torch.Tensor, sb
     [N, K/2], E4M3 scales per 16 in tensor-core layout, ka / kb their tensor_exp.
     `workspace` as in mxfp4_gemm (False: none)."""
     _check_operands(qa, sa, qb, sb)
+    _operand(qa, sa, M, K, 1, 16, "a")
+    _operand(qb, sb, N, K, 1, 16, "b")
     cdt = _c_dtype(c, out_dtype)
     if c is None:
         c = torch.empty((M, N), dtype=out_dtype, device=qa.device)
     ldc = c.stride(0) if ldc is None else ldc
+    _matrix_out(c, M, N, ldc)
     ws, nbytes = _workspace(workspace, M, N, K, 16, qa.device)
     _check(lib().nvfp4_gemm(_ptr(qa), _ptr(sa), ka, _ptr(qb), _ptr(sb), kb, M, N, K, _ptr(c), cdt,
                             ldc, _ptr(ws), nbytes, _stream(qa, stream)))
@@ -365,7 +424,17 @@ def mxfp4_gemm_quantize(qa: torch.Tensor, sa: torch.Tensor, qb: torch.Tensor, sb
     if col is not None:
         q_col = torch.empty((N, col.code_cols(M)), dtype=torch.uint8, device=qa.device) if q_col is None else q_col
         s_col = _scales_out(N, M, col, qa.device) if s_col is None else s_col
+    _operand(qa, sa, M, K, 1, 32, "a")
+    _operand(qb, sb, N, K, 1, 32, "b")
+    if out is not None:
+        _buffer(q_out, M * out.code_cols(N), torch.uint8, "q_out")
+        _buffer(s_out, scale_numel(M, N, out.block), torch.uint8, "s_out")
+    if col is not None:
+        _buffer(q_col, N * col.code_cols(M), torch.uint8, "q_col")
+        _buffer(s_col, scale_numel(N, M, col.block), torch.uint8, "s_col")
     ldc = c.stride(0) if c is not None else N
+    if c is not None:
+        _matrix_out(c, M, N, ldc)
     op = out._c() if out is not None else None
     cp = col._c() if col is not None else None
     ws, nbytes = _workspace(workspace if col is None else False, M, N, K, 32, qa.device)
@@ -392,6 +461,7 @@ def hadamard32(x: torch.Tensor, sign_mask: int = 0, inverse: bool = False, *, y=
     rows, cols = x.shape
     ld = x.stride(0) if rows > 1 else cols
     y = torch.empty((rows, cols), dtype=torch.float32, device=x.device) if y is None else y
+    _buffer(y, rows * cols, torch.float32, "y")
     _check(lib().hadamard32(_ptr(x), dt, rows, cols, ld, sign_mask & 0xFFFFFFFF, int(bool(inverse)),
                             _ptr(y), _stream(x, stream)))
     return y
@@ -409,6 +479,8 @@ def tensor_amax(x: torch.Tensor, *, amax=None, tensor_exp=None, stream=None):
     ld = x.stride(0) if rows > 1 else cols
     amax = torch.empty(1, dtype=torch.float32, device=x.device) if amax is None else amax
     tensor_exp = torch.empty(1, dtype=torch.int32, device=x.device) if tensor_exp is None else tensor_exp
+    _buffer(amax, 1, torch.float32, "amax")
+    _buffer(tensor_exp, 1, torch.int32, "tensor_exp")
     _check(lib().mxfp4_tensor_amax(_ptr(x), dt, rows, cols, ld, _ptr(amax), _ptr(tensor_exp),
                                    _stream(x, stream)))
     return amax, tensor_exp

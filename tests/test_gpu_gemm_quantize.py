@@ -70,8 +70,11 @@ def test_fused_rejects_bad_arguments():
 
     p = mx.QuantParams(mx.BLOCK_1X32, mx.SCALE_FLOOR, mx.ROUND_RTN, mx.LAYOUT_MMA)
     *_, t = _operands(256, 256, 256, 3)
+    z = torch.zeros(1 << 20, dtype=torch.uint8, device=DEV)   # room for N = 320
     with pytest.raises(mx.Mxfp4Error):
-        mx.mxfp4_gemm_quantize(*t, 256, 320, 256, p)          # N % 128 != 0
+        mx.mxfp4_gemm_quantize(t[0], t[1], z, z, 256, 320, 256, p)   # N % 128 != 0
+    with pytest.raises(ValueError):                           # B smaller than N = 320 rows
+        mx.mxfp4_gemm_quantize(*t, 256, 320, 256, p)
     bad = mx.QuantParams(5, mx.SCALE_FLOOR, mx.ROUND_RTN, mx.LAYOUT_MMA)
     with pytest.raises(mx.Mxfp4Error):
         mx.mxfp4_gemm_quantize(*t, 256, 256, 256, bad)        # bad block

@@ -14,6 +14,8 @@ at its first failure has run every other test already.
 """
 from __future__ import annotations
 
+import ctypes
+
 import pytest
 import torch
 
@@ -68,10 +70,17 @@ def test_noalloc_without_images_is_not_limited_by_the_scratch():
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     import gemm_pt_block_gb300 as mx
 
+    # Through the C ABI directly: the library must refuse these shapes before
+    # it touches any buffer (the binding would already refuse the tiny ones).
     z = torch.zeros(16, dtype=torch.uint8, device=DEV)
     c = torch.empty(16, dtype=torch.float32, device=DEV)
+    L = mx.lib()
+    P = ctypes.c_void_p
     for M, N, K in ((12288, 12288, 32768 + 256), (32768, 32768, 32768)):
         assert 4 * (M + N) * K // 32 > SCRATCH
-        with pytest.raises(mx.Mxfp4Error) as e:
-            mx.mxfp4_gemm_noalloc(z, z, z, z, M, N, K, c=c, ldc=N)
-        assert e.value.status == 2
+        st = L.mxfp4_gemm_noalloc(P(z.data_ptr()), P(z.data_ptr()), P(z.data_ptr()), P(z.data_ptr()),
+                                  M, N, K, P(c.data_ptr()), N,
+                                  P(torch.cuda.current_stream().cuda_stream))
+        assert st == 2, L.mxfp4_last_error()
+    with pytest.raises(ValueError):                 # the binding checks extents first
+        mx.mxfp4_gemm_noalloc(z, z, z, z, 12288, 12288, 32768 + 256, c=c, ldc=12288)
